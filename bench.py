@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Benchmark of the VLA forward recurrence on GB300.
+
+One step = one vla_forward call over one batch of synthetic inputs (all of
+the recurrence: key normalisation, Sherman-Morrison update, unit gate, state
+write, ELU+1 readout, final state).  Prints ONE JSON line on rank 0.
+
+Default workload: the long stream, B=1 H=16 T=65536 d_h=64, bf16 inputs, fp32
+state, u scaled by 0.5, lambda0=1.  Its inputs (537 MB) and output (134 MB)
+exceed the 129 MB L2, so no flush is needed between steps; smaller
+workloads are flushed by writing a 256 MB buffer between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                  [--kernel auto|seq|chunk] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs its own batch of the same shape
+(independent (batch, head) units, no collective on the data path; weak
+scaling); value = all units / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "VLA forward tokens·heads/sec at d_h=64 and % of roofline on 1 GB300"
+UNIT = "tokens*heads/s"
+L2_BYTES = 129 * 1024 * 1024
+N_SM = 152
+SM_MAX_GHZ = 2.070
+# FP32 SIMT peak: 152 SMs x 128 FP32 lanes x 2 flop per FMA x max SM clock.
+FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
+
+# DRAM traffic per launch of the dominant kernel, from the ncu captures
+# summarised under profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
+# keyed by (kernel, workload).  Reported only while the kernel source still
+# hashes to the value it was captured from; otherwise null.
+TRAFFIC = {}
+
+
+def kernel_src_hash(kernel_name: str) -> str:
+    fn = {"seq": "vla_seq.cu", "chunk": "vla_chunk.cu"}[kernel_name]
+    path = os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", fn)
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", "vla_internal.cuh")):
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def algorithmic_work(B, H, T, d, io_bytes):
+    """Per-launch algorithmic flops and bytes of the recurrence.
+
+    flops: 12 d^2 + 16 d per token-head (A u, A k_hat, S k_hat, S phi(q)
+    matrix-vector products; the rank-1 updates of A and S; O(d) norms, phi,
+    divisions).  bytes: q, k, v, u read and o written (5 d io_bytes per
+    token-head) plus S_T and A_T written (8 d^2 per head).
+    """
+    units = B * H * T
+    flops = units * (12 * d * d + 16 * d)
+    byts = units * 5 * d * io_bytes + B * H * 8 * d * d
+    return flops, byts
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None, interval_ms: int = 100):
+        self.bus_id = bus_id
+        self.proc = None
+        self.interval_ms = interval_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", str(self.interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            time.sleep(0.4)
+        except Exception as e:  # pragma: no cover
+            log("clock sampling unavailable:", e)
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:  # pragma: no cover
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.bus_id and parts[0].lower()[-12:] != self.bus_id.lower()[-12:]:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+def bus_id_of(dev_index):
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        return "%08x:%02x:%02x.0" % (getattr(p, "pci_domain_id"), getattr(p, "pci_bus_id"),
+                                      getattr(p, "pci_device_id"))
+    except Exception:
+        return None
+
+
+def make_host_inputs(cfg_name, rank, overrides):
+    from synthetic import make_config
+    kw = dict(overrides)
+    if rank:
+        from synthetic.generator import CONFIGS
+        kw["seed"] = CONFIGS[cfg_name]["seed"] + 7919 * rank
+    return make_config(cfg_name, **kw)
+
+
+def to_torch_host(x, pin=True):
+    import torch
+    out = []
+    for n in "qkvu":
+        a = getattr(x, n)
+        if x.dtype == "bf16":
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+        out.append(t.pin_memory() if pin else t)
+    return out
+
+
+def oracle_sample(x, max_heads=64):
+    """The oracle (as it stands) on the first heads of the workload, full T."""
+    import oracle
+    B, H, T, d = x.q.shape
+    nh = min(B * H, max_heads)
+    flat = lambda a: a.reshape((B * H, T, d))[:nh]  # noqa: E731
+    args = [flat(x.as_f64(n)) for n in "qkvu"]
+    threads = min(oracle.default_threads(), nh)
+    t0 = time.perf_counter()
+    ref = oracle.forward(*args, x.lambda0, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return ref, nh, threads, dt
+
+
+def run_reference(args):
+    """--impl reference: the fp64 oracle timed on the host cores, one bounded
+    sample of the workload per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from synthetic.generator import CONFIGS
+    x = make_host_inputs(args.config, 0, parse_overrides(args))
+    B, H, T, d = x.q.shape
+    for _ in range(args.warmup):
+        oracle_sample(x, args.ref_heads)
+    times = []
+    nh = threads = 0
+    for _ in range(args.steps):
+        _, nh, threads, dt = oracle_sample(x, args.ref_heads)
+        times.append(dt)
+    ms = 1e3 * float(np.mean(times))
+    value = nh * T / (ms / 1e3)
+    sample = "first %d of %d (b,h) units, all %d tokens, d_h=%d, per step" % (nh, B * H, T, d)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(args.config, x, "oracle"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block(name, x, kernel):
+    B, H, T, d = x.q.shape
+    io_bytes = 2 if x.dtype == "bf16" else 4
+    in_bytes = 4 * B * H * T * d * io_bytes
+    return {"workload": "%s: B=%d H=%d T=%d d_h=%d %s inputs, fp32 state, lambda0=%g" % (
+        name, B, H, T, d, x.dtype, x.lambda0), "B": B, "H": H, "T": T, "d_h": d,
+        "io_dtype": x.dtype, "lambda0": x.lambda0, "kernel": kernel,
+        "l2": ("inputs larger than L2 (%d MB)" % (in_bytes >> 20)) if in_bytes > L2_BYTES
+        else "L2 flushed (256 MB write) between timed steps"}
+
+
+def parse_overrides(args):
+    ov = {}
+    for item in args.set or []:
+        k, v = item.split("=", 1)
+        ov[k] = type_of(v)
+    return ov
+
+
+def type_of(v):
+    for f in (int, float):
+        try:
+            return f(v)
+        except ValueError:
+            pass
+    return v
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="long")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "seq", "chunk"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--set", action="append", help="workload override, e.g. T=4096")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--ref-heads", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        log("note: fewer than 3 warm-up steps")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import rls_associative_memory_gb300 as vla
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kernel = {"auto": vla.VLA_KERNEL_AUTO, "seq": vla.VLA_KERNEL_SEQ, "chunk": vla.VLA_KERNEL_CHUNK}[args.kernel]
+
+    t_gen = time.perf_counter()
+    x = make_host_inputs(args.config, rank, parse_overrides(args))
+    B, H, T, d = x.q.shape
+    log("inputs %s generated in %.1fs" % (x.q.shape, time.perf_counter() - t_gen))
+    io_bytes = 2 if x.dtype == "bf16" else 4
+    hq, hk, hv, hu = to_torch_host(x)
+    q, k, v, u = (t.to(dev) for t in (hq, hk, hv, hu))
+    resolved = kernel if kernel != vla.VLA_KERNEL_AUTO else vla.vla_select_kernel(B, H, T, d)
+    kname = {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk"}[resolved]
+    o = torch.empty_like(q)
+    S_T = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    A_T = torch.empty_like(S_T)
+    n_T = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    need = vla.vla_workspace_bytes(B, H, T, d, vla.VLA_BF16 if x.dtype == "bf16" else vla.VLA_F32, resolved)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    in_bytes = 4 * B * H * T * d * io_bytes
+    flush = in_bytes <= L2_BYTES
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        vla.vla_forward(q, k, v, u, x.lambda0, o=o, S_T=S_T, A_T=A_T, n_T=n_T, kernel=resolved,
+                        workspace=ws if need else None, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = vla.vla_device_status(stream)
+    if st != vla.VLA_OK:
+        raise RuntimeError("device status after warm-up: " + vla.vla_status_str(st))
+
+    sampler = ClockSampler(bus_id_of(dev.index)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        if flush:
+            scratch.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    st = vla.vla_device_status(stream)
+    if st != vla.VLA_OK:
+        raise RuntimeError("device status after timed steps: " + vla.vla_status_str(st))
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = float(np.mean(step_ms))
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    units = B * H * T
+    value = world * units / (ms / 1e3)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hS = torch.empty(S_T.shape, dtype=torch.float32).pin_memory()
+        hA = torch.empty(A_T.shape, dtype=torch.float32).pin_memory()
+        hn = torch.empty(n_T.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            for dst, src in ((q, hq), (k, hk), (v, hv), (u, hu)):
+                dst.copy_(src, non_blocking=True)
+            step()
+            for dst, src in ((ho, o), (hS, S_T), (hA, A_T), (hn, n_T)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if dist:
+            dist.barrier()
+        for i in range(args.steps):
+            es[i].record(stream)
+            e2e_step()
+            ee[i].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(es, ee)]))
+        if dist:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = 4 * units * d * io_bytes
+        d2h = units * d * io_bytes + B * H * (2 * d * d + d) * 4
+        e2e = {"value": world * units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    # ---- roofline of the dominant kernel ----
+    flops, byts = algorithmic_work(B, H, T, d, io_bytes)
+    kernel_ms = ms  # one kernel launch per step for the sequential path
+    achieved_tf = flops / (kernel_ms / 1e3) / 1e12
+    tr = TRAFFIC.get((kname, args.config))
+    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash(kname) else None
+    roofline = {"bound": "alu", "achieved": achieved_tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": achieved_tf / FP32_PEAK_TFLOPS, "traffic": traffic,
+                "kernel": "vla::seq_kernel<%d,%s>" % (d, "bf16" if x.dtype == "bf16" else "f32"),
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop/FMA x 2.070 GHz",
+                "algorithmic_flops": flops, "algorithmic_bytes": byts,
+                "hbm_frac_of_measured": (byts / (kernel_ms / 1e3) / 1e9) / measured_hbm_gbs()}
+
+    cpu = None
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        ref, nh, threads, dt = oracle_sample(x, args.ref_heads)
+        cpu = {"value": nh * T / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "first %d of %d (b,h) units, all %d tokens (%.1f s)" % (nh, B * H, T, dt),
+               "host_cores": os.cpu_count()}
+        flat = lambda a: a.reshape((B * H,) + tuple(a.shape[2:]))[:nh]  # noqa: E731
+        got = {"o": flat(o.float().cpu().numpy()), "S_T": flat(S_T.cpu().numpy()),
+               "A_T": flat(A_T.cpu().numpy()), "n_T": flat(n_T.cpu().numpy())}
+        parity = {key: float(np.linalg.norm((got[key] - ref[key]).ravel()) / np.linalg.norm(ref[key].ravel()))
+                  for key in got}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": config_block(args.config, x, kname), "roofline": roofline, "e2e": e2e,
+                "gpu_launches": args.steps * launches_per_step(kname), "clocks": clocks,
+                "cpu_baseline": cpu, "parity_rel_fro": parity, "wall_s_timed": wall}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def launches_per_step(kname):
+    return {"seq": 1}.get(kname, 1)
+
+
+def measured_hbm_gbs():
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+    except Exception:
+        return 6800.0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

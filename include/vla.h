@@ -1,0 +1,119 @@
+/*
+ * vla.h -- C ABI of libvla, the GB300 (sm_103a) forward recurrence of
+ * Variational Linear Attention (VLA).
+ *
+ * Operation (per batch b, head h, token t = 1..T; d = d_h):
+ *   k_hat_t = k_t / max(|k_t|, eps)                         section 2.3 (unit key)
+ *   z_t     = A_{t-1} u_t
+ *   A_t     = A_{t-1} - z_t z_t^T / (1 + u_t^T z_t)        sections 2.2, 2.3 step 1
+ *   alpha_t = A_t k_hat_t / max(|A_t k_hat_t|, eps)         section 2.3 step 2
+ *   S_t     = S_{t-1} + (v_t - S_{t-1} k_hat_t) alpha_t^T   section 2.3 step 3
+ *   n_t     = n_{t-1} + phi(k_hat_t),  phi(x) = ELU(x) + 1
+ *   o_t     = S_t phi(q_t) / (phi(q_t)^T n_t + eps)          section 2.3 (readout)
+ * with eps = 1e-6.  Sections are those of "Variational Linear Attention:
+ * Stable Associative Memory for Long-Context Transformers" (web summaries);
+ * z_t = A_{t-1} u_t, A_0 = I / lambda0, the readout denominator and eps are
+ * this library's readings of what those pages leave open.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or synchronises inside vla_forward.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).
+ *   - Device pointers must be 16-byte aligned (bulk-copy requirement).
+ *   - Layouts are C-contiguous: q, k, v, u, o are [B, H, T, d];
+ *     S, A are [B, H, d, d] fp32 row-major, S[i][j] maps key coordinate j
+ *     to value coordinate i, A symmetric; n is [B, H, d] fp32.
+ *   - Return value 0 is success; negative values are VLA_ERR_* codes.  No
+ *     C++ exception crosses this boundary.
+ */
+#ifndef VLA_H
+#define VLA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define VLA_OK 0
+#define VLA_ERR_ARG (-1)             /* null required pointer, negative size, bad lambda0/dtype/kernel */
+#define VLA_ERR_UNSUPPORTED_DIM (-2) /* d_h not in {32, 64, 128} */
+#define VLA_ERR_ALIGN (-3)           /* a pointer is not 16-byte aligned */
+#define VLA_ERR_WORKSPACE (-4)       /* workspace missing or smaller than vla_workspace_bytes() */
+#define VLA_ERR_CUDA (-5)            /* a CUDA runtime call failed; see vla_last_cuda_error() */
+#define VLA_ERR_TIMEOUT (-6)         /* a bounded device-side wait gave up (vla_device_status) */
+
+/* I/O element types of q, k, v, u and o */
+#define VLA_F32 0
+#define VLA_BF16 1
+
+/* kernel selection */
+#define VLA_KERNEL_AUTO 0  /* pick by shape */
+#define VLA_KERNEL_SEQ 1   /* one CTA per (b, h), token-sequential, no workspace */
+#define VLA_KERNEL_CHUNK 2 /* chunk-parallel over T, needs workspace */
+
+/*
+ * vla_forward -- run the recurrence over T tokens for all B*H units.
+ *
+ * q, k, v, u   [B,H,T,d] io_dtype, read only.  Required when B*H*T > 0.
+ * io_dtype     VLA_F32 or VLA_BF16.
+ * lambda0      > 0 and finite; A_0 = I / lambda0 when A0 is NULL.
+ * B, H, T      >= 0.  T = 0 copies the initial state to the outputs.
+ * d_h          32, 64 or 128.
+ * S0, A0, n0   optional initial state ([B,H,d,d], [B,H,d,d], [B,H,d] fp32);
+ *              NULL means 0, I/lambda0 and 0.  S0 == S_T, A0 == A_T and
+ *              n0 == n_T are allowed (in-place streaming); other overlaps
+ *              between inputs and outputs are not.
+ * o            [B,H,T,d] io_dtype, written.
+ * S_T, A_T     [B,H,d,d] fp32, written (required).
+ * n_T          [B,H,d] fp32, written when non-NULL.
+ * kernel       VLA_KERNEL_AUTO / _SEQ / _CHUNK.
+ * chunk        chunk length for VLA_KERNEL_CHUNK (0 = library default).
+ * workspace    device scratch of at least vla_workspace_bytes(...) bytes
+ *              (may be NULL when that is 0).  Contents on entry are ignored.
+ * stream       cudaStream_t as void*.
+ * Returns VLA_OK or a VLA_ERR_* code; on error nothing has been launched.
+ */
+int vla_forward(const void *q, const void *k, const void *v, const void *u, int io_dtype,
+                float lambda0, int B, int H, int T, int d_h, const float *S0, const float *A0,
+                const float *n0, void *o, float *S_T, float *A_T, float *n_T, int kernel,
+                int chunk, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes vla_forward needs for these arguments (0 for the
+ * sequential kernel).  Returns 0 for invalid arguments as well. */
+size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk);
+
+/* Which kernel VLA_KERNEL_AUTO resolves to for this shape (VLA_KERNEL_SEQ or
+ * VLA_KERNEL_CHUNK), or a VLA_ERR_* code for invalid arguments. */
+int vla_select_kernel(int B, int H, int T, int d_h);
+
+/* Static, human-readable text for a status code. */
+const char *vla_status_str(int status);
+
+/* The cudaError_t value of the last failed CUDA call on this host thread
+ * (0 if none). */
+int vla_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears the device error word that
+ * bounded waits set on expiry.  Returns VLA_OK, VLA_ERR_TIMEOUT, or
+ * VLA_ERR_CUDA. */
+int vla_device_status(void *stream);
+
+/* Test hook for the failure path: mode 1 makes the next vla_forward launches
+ * of the sequential kernel wait for an input tile that is never requested,
+ * so that the bounded wait (limit `wait_limit_ns`, clamped to [1e5, 1e10])
+ * expires and sets the device error word; mode 0 restores normal operation
+ * and the default one-second limit.  Host state only; returns VLA_OK or
+ * VLA_ERR_ARG. */
+int vla_debug_inject(int mode, long long wait_limit_ns);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int vla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VLA_H */

@@ -1,0 +1,159 @@
+"""ctypes binding of libvla (include/vla.h).  Argument marshalling only.
+
+The functions here carry the C names.  ``vla_forward`` accepts torch CUDA
+tensors, allocates missing outputs and the workspace with torch (device
+memory is PyTorch's job here), and passes raw device pointers and the
+current CUDA stream to the C entry point.  Every step of the recurrence runs
+in the library's kernels; there is no CPU fallback, and a missing or
+unloadable library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+from . import build as _build
+
+VLA_OK = 0
+VLA_ERR_ARG = -1
+VLA_ERR_UNSUPPORTED_DIM = -2
+VLA_ERR_ALIGN = -3
+VLA_ERR_WORKSPACE = -4
+VLA_ERR_CUDA = -5
+VLA_ERR_TIMEOUT = -6
+
+VLA_F32 = 0
+VLA_BF16 = 1
+
+VLA_KERNEL_AUTO = 0
+VLA_KERNEL_SEQ = 1
+VLA_KERNEL_CHUNK = 2
+
+# every symbol include/vla.h declares, with (restype, argtypes)
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_SIGS = {
+    "vla_forward": (_i, [_vp, _vp, _vp, _vp, _i, ctypes.c_float, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
+                         _vp, _vp, _vp, _i, _i, _vp, ctypes.c_size_t, _vp]),
+    "vla_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
+    "vla_select_kernel": (_i, [_i, _i, _i, _i]),
+    "vla_status_str": (ctypes.c_char_p, [_i]),
+    "vla_last_cuda_error": (_i, []),
+    "vla_device_status": (_i, [_vp]),
+    "vla_debug_inject": (_i, [_i, ctypes.c_longlong]),
+    "vla_version": (_i, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class VLAError(RuntimeError):
+    def __init__(self, status: int, where: str = "vla_forward"):
+        self.status = status
+        msg = lib().vla_status_str(status).decode()
+        if status == VLA_ERR_CUDA:
+            msg += " (cudaError %d)" % lib().vla_last_cuda_error()
+        super().__init__("%s failed: %s [%d]" % (where, msg, status))
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded CDLL (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError("libvla.so was not built")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def vla_status_str(status: int) -> str:
+    return lib().vla_status_str(int(status)).decode()
+
+
+def vla_workspace_bytes(B, H, T, d_h, io_dtype=VLA_BF16, kernel=VLA_KERNEL_AUTO, chunk=0) -> int:
+    return int(lib().vla_workspace_bytes(B, H, T, d_h, io_dtype, kernel, chunk))
+
+
+def vla_select_kernel(B, H, T, d_h) -> int:
+    return int(lib().vla_select_kernel(B, H, T, d_h))
+
+
+def vla_device_status(stream=None) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(lib().vla_device_status(ctypes.c_void_p(s.cuda_stream)))
+
+
+def vla_debug_inject(mode: int, wait_limit_ns: int = 0) -> int:
+    return int(lib().vla_debug_inject(int(mode), int(wait_limit_ns)))
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def vla_forward(q, k, v, u, lambda0: float, S0=None, A0=None, n0=None, o=None, S_T=None, A_T=None,
+                n_T=None, kernel: int = VLA_KERNEL_AUTO, chunk: int = 0, workspace=None,
+                stream=None, want_n: bool = True):
+    """Run the VLA forward recurrence on the GPU.
+
+    q, k, v, u: contiguous CUDA tensors ``[B, H, T, d]``, all float32 or all
+    bfloat16.  S0, A0 ``[B, H, d, d]`` and n0 ``[B, H, d]`` float32, optional.
+    Returns ``(o, S_T, A_T, n_T)``; ``n_T`` is None when ``want_n`` is False
+    and no ``n_T`` buffer was passed.  Launches asynchronously on ``stream``
+    (default: torch's current stream).
+    """
+    import torch
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, d]")
+    B, H, T, d = q.shape
+    for t in (k, v, u):
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError("q, k, v, u must share shape, dtype and device")
+    for t in (q, k, v, u):
+        if not t.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+    if not q.is_cuda:
+        raise ValueError("inputs must be CUDA tensors")
+    if q.dtype == torch.float32:
+        io = VLA_F32
+    elif q.dtype == torch.bfloat16:
+        io = VLA_BF16
+    else:
+        raise ValueError("io dtype must be float32 or bfloat16")
+    dev = q.device
+    if o is None:
+        o = torch.empty_like(q)
+    if S_T is None:
+        S_T = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    if A_T is None:
+        A_T = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    if n_T is None and want_n:
+        n_T = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    need = vla_workspace_bytes(B, H, T, d, io, kernel, chunk)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    rc = lib().vla_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(u), io, float(lambda0), B, H, T, d,
+                           _ptr(S0), _ptr(A0), _ptr(n0), _ptr(o), _ptr(S_T), _ptr(A_T), _ptr(n_T),
+                           int(kernel), int(chunk), _ptr(workspace), ws_bytes,
+                           ctypes.c_void_p(s.cuda_stream))
+    if rc != VLA_OK:
+        raise VLAError(rc)
+    return o, S_T, A_T, n_T

@@ -1,0 +1,164 @@
+// vla_api.cu -- the extern "C" boundary of libvla: argument validation,
+// kernel selection, launch on the caller's stream, status reporting.
+//
+// Nothing here allocates or synchronises except vla_device_status (which
+// synchronises the given stream by contract).
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/vla.h"
+#include "vla_internal.cuh"
+
+namespace {
+
+__device__ int g_vla_dev_err;  // device error word, set by bounded waits on expiry
+
+thread_local int t_last_cuda_error = 0;
+
+long long g_wait_limit_ns = 1000000000LL;  // 1 s bound on every device-side wait
+int g_inject = 0;
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return VLA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int *device_err_word() {
+    // Per device: the symbol's address in the current device's context.
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_vla_dev_err) != cudaSuccess) return nullptr;
+    return static_cast<int *>(ptr);
+}
+
+int check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int kernel) {
+    if (B < 0 || H < 0 || T < 0) return VLA_ERR_ARG;
+    if (io_dtype != VLA_F32 && io_dtype != VLA_BF16) return VLA_ERR_ARG;
+    if (!(lambda0 > 0.f) || !isfinite(lambda0)) return VLA_ERR_ARG;
+    if (kernel != VLA_KERNEL_AUTO && kernel != VLA_KERNEL_SEQ && kernel != VLA_KERNEL_CHUNK)
+        return VLA_ERR_ARG;
+    if (d_h != 32 && d_h != 64 && d_h != 128) return VLA_ERR_UNSUPPORTED_DIM;
+    // element offsets are computed in size_t; counts themselves must fit the kernels' int math
+    if ((long long)B * H > 0x7fffffffLL) return VLA_ERR_ARG;
+    if ((long long)T * d_h > 0x7fffffffLL) return VLA_ERR_ARG;
+    return VLA_OK;
+}
+
+int resolve_kernel(int B, int H, int T, int d_h, int kernel) {
+    (void)B; (void)H; (void)T; (void)d_h;
+    if (kernel == VLA_KERNEL_AUTO) return VLA_KERNEL_SEQ;
+    return kernel;
+}
+
+}  // namespace
+
+extern "C" {
+
+int vla_version(void) { return 100; }
+
+const char *vla_status_str(int status) {
+    switch (status) {
+        case VLA_OK: return "ok";
+        case VLA_ERR_ARG: return "invalid argument";
+        case VLA_ERR_UNSUPPORTED_DIM: return "unsupported head dimension (d_h must be 32, 64 or 128)";
+        case VLA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case VLA_ERR_WORKSPACE: return "workspace missing or too small";
+        case VLA_ERR_CUDA: return "CUDA runtime error (see vla_last_cuda_error)";
+        case VLA_ERR_TIMEOUT: return "a bounded device-side wait expired";
+        default: return "unknown status";
+    }
+}
+
+int vla_last_cuda_error(void) { return t_last_cuda_error; }
+
+int vla_select_kernel(int B, int H, int T, int d_h) {
+    const int rc = check_common(VLA_F32, 1.f, B, H, T, d_h, VLA_KERNEL_AUTO);
+    if (rc != VLA_OK) return rc;
+    return resolve_kernel(B, H, T, d_h, VLA_KERNEL_AUTO);
+}
+
+size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk) {
+    if (check_common(io_dtype, 1.f, B, H, T, d_h, kernel) != VLA_OK) return 0;
+    (void)chunk;
+    const int kk = resolve_kernel(B, H, T, d_h, kernel);
+    if (kk == VLA_KERNEL_SEQ) return 0;
+    return 0;
+}
+
+int vla_debug_inject(int mode, long long wait_limit_ns) {
+    if (mode != 0 && mode != 1) return VLA_ERR_ARG;
+    g_inject = mode;
+    if (mode == 0) {
+        g_wait_limit_ns = 1000000000LL;
+    } else {
+        long long l = wait_limit_ns;
+        if (l < 100000LL) l = 100000LL;
+        if (l > 10000000000LL) l = 10000000000LL;
+        g_wait_limit_ns = l;
+    }
+    return VLA_OK;
+}
+
+int vla_device_status(void *stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int host = 0;
+    e = cudaMemcpyFromSymbol(&host, g_vla_dev_err, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (host != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_vla_dev_err, &zero, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e);
+        return VLA_ERR_TIMEOUT;
+    }
+    return VLA_OK;
+}
+
+int vla_forward(const void *q, const void *k, const void *v, const void *u, int io_dtype, float lambda0,
+                int B, int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o,
+                float *S_T, float *A_T, float *n_T, int kernel, int chunk, void *workspace,
+                size_t ws_bytes, void *stream) {
+    int rc = check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
+    if (rc != VLA_OK) return rc;
+    if (chunk < 0) return VLA_ERR_ARG;
+    const long long BH = (long long)B * H;
+    if (BH > 0) {
+        if (!S_T || !A_T) return VLA_ERR_ARG;
+        if (T > 0 && (!q || !k || !v || !u || !o)) return VLA_ERR_ARG;
+    }
+    const void *ptrs[] = {q, k, v, u, o, S0, A0, n0, S_T, A_T, n_T, workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return VLA_ERR_ALIGN;
+    const int kk = resolve_kernel(B, H, T, d_h, kernel);
+    const size_t need = vla_workspace_bytes(B, H, T, d_h, io_dtype, kk, chunk);
+    if (need > 0 && (!workspace || ws_bytes < need)) return VLA_ERR_WORKSPACE;
+    if (BH == 0) return VLA_OK;
+
+    int *err = device_err_word();
+    if (!err) return cuda_fail(cudaGetLastError());
+
+    vla::FwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.u = u; p.o = o;
+    p.S0 = S0; p.A0 = A0; p.n0 = n0;
+    p.S_T = S_T; p.A_T = A_T; p.n_T = n_T;
+    p.BH = (int)BH; p.T = T; p.d = d_h;
+    p.io_bf16 = (io_dtype == VLA_BF16);
+    p.lambda0 = lambda0;
+    p.err = err;
+    p.wait_limit_ns = g_wait_limit_ns;
+    p.inject = g_inject;
+    p.ws = workspace; p.ws_bytes = ws_bytes; p.chunk = chunk;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    switch (kk) {
+        case VLA_KERNEL_SEQ: e = vla::launch_seq(p, st); break;
+        default: return VLA_ERR_ARG;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return VLA_OK;
+}
+
+}  // extern "C"

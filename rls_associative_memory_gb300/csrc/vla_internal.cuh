@@ -1,0 +1,138 @@
+// vla_internal.cuh -- shared declarations of libvla's translation units:
+// launch parameter block, launcher prototypes and the sm_100-family PTX
+// helpers (mbarrier, bulk async copy, bounded waits) the kernels use.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vla {
+
+constexpr float kEps = 1e-6f;  // key norm, gate norm and readout denominator guard
+
+// Device error word values (written with atomicExch, read by vla_device_status).
+constexpr int kDevErrTimeout = 1;
+
+struct FwdParams {
+    const void *q, *k, *v, *u;  // [BH, T, d] io dtype
+    void *o;                    // [BH, T, d] io dtype
+    const float *S0, *A0, *n0;  // optional initial state
+    float *S_T, *A_T, *n_T;     // final state (n_T optional)
+    int BH, T, d;
+    int io_bf16;                // 1: bf16 I/O, 0: fp32 I/O
+    float lambda0;
+    int *err;                   // device error word
+    long long wait_limit_ns;    // bound on every device-side wait
+    int inject;                 // test hook: 1 = never request the first input tile
+    void *ws;                   // workspace (chunked kernel)
+    size_t ws_bytes;
+    int chunk;                  // chunk length (chunked kernel)
+};
+
+// Sequential kernel: one CTA per (b, h).  Returns a cudaError_t.
+cudaError_t launch_seq(const FwdParams &p, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for phase `parity` of `bar`, giving up after limit_ns.  Returns true
+// on success; on expiry sets the device error word and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long limit_ns,
+                                                  int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((long long)(globaltimer_ns() - t0) > limit_ns) {
+            atomicExch(err, kDevErrTimeout);
+            return false;
+        }
+    }
+}
+
+// 1-D bulk async copy global -> shared, completion counted on `bar` in bytes.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// phi(x) = ELU(x) + 1: x + 1 for x > 0, exp(x) otherwise.
+__device__ __forceinline__ float phi_elu1(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+template <typename IO>
+__device__ __forceinline__ float io_to_f32(IO x);
+template <>
+__device__ __forceinline__ float io_to_f32<float>(float x) {
+    return x;
+}
+template <>
+__device__ __forceinline__ float io_to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+
+template <typename IO>
+__device__ __forceinline__ IO f32_to_io(float x);
+template <>
+__device__ __forceinline__ float f32_to_io<float>(float x) {
+    return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 f32_to_io<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+}  // namespace vla

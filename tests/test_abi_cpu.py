@@ -1,0 +1,100 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/vla.h declares, and rejects bad arguments on the host
+before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import rls_associative_memory_gb300 as vla
+from rls_associative_memory_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vla.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(vla_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("vla_forward", "vla_workspace_bytes", "vla_status_str", "vla_device_status"):
+        assert must in names
+    assert set(names) == set(_lib._SIGS), "binding signatures must cover exactly the header"
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    L = vla.lib()
+    raw = ctypes.CDLL(vla.lib_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+    assert L.vla_version() >= 100
+
+
+def test_status_strings():
+    for st in (vla.VLA_OK, vla.VLA_ERR_ARG, vla.VLA_ERR_UNSUPPORTED_DIM, vla.VLA_ERR_ALIGN,
+               vla.VLA_ERR_WORKSPACE, vla.VLA_ERR_CUDA, vla.VLA_ERR_TIMEOUT):
+        assert vla.vla_status_str(st) and vla.vla_status_str(st) != "unknown status"
+    assert vla.vla_status_str(12345) == "unknown status"
+
+
+def _call(**kw):
+    """vla_forward through the raw C ABI with fake (never dereferenced) pointers."""
+    base = 1 << 20
+    args = dict(q=base, k=base, v=base, u=base, io=vla.VLA_BF16, lam=1.0, B=1, H=1, T=4, d=64, S0=None,
+                A0=None, n0=None, o=base, S_T=base, A_T=base, n_T=None, kernel=0, chunk=0, ws=None,
+                ws_bytes=0, stream=None)
+    args.update(kw)
+    return vla.lib().vla_forward(args["q"], args["k"], args["v"], args["u"], args["io"], args["lam"],
+                                 args["B"], args["H"], args["T"], args["d"], args["S0"], args["A0"],
+                                 args["n0"], args["o"], args["S_T"], args["A_T"], args["n_T"],
+                                 args["kernel"], args["chunk"], args["ws"], args["ws_bytes"],
+                                 args["stream"])
+
+
+@pytest.mark.parametrize("kw,rc", [
+    (dict(d=48), vla.VLA_ERR_UNSUPPORTED_DIM),
+    (dict(d=256), vla.VLA_ERR_UNSUPPORTED_DIM),
+    (dict(lam=0.0), vla.VLA_ERR_ARG),
+    (dict(lam=-1.0), vla.VLA_ERR_ARG),
+    (dict(lam=float("nan")), vla.VLA_ERR_ARG),
+    (dict(lam=float("inf")), vla.VLA_ERR_ARG),
+    (dict(io=7), vla.VLA_ERR_ARG),
+    (dict(kernel=9), vla.VLA_ERR_ARG),
+    (dict(B=-1), vla.VLA_ERR_ARG),
+    (dict(T=-3), vla.VLA_ERR_ARG),
+    (dict(chunk=-1), vla.VLA_ERR_ARG),
+    (dict(q=None), vla.VLA_ERR_ARG),
+    (dict(o=None), vla.VLA_ERR_ARG),
+    (dict(S_T=None), vla.VLA_ERR_ARG),
+    (dict(A_T=None), vla.VLA_ERR_ARG),
+    (dict(k=(1 << 20) + 8), vla.VLA_ERR_ALIGN),
+    (dict(S0=(1 << 20) + 4), vla.VLA_ERR_ALIGN),
+    (dict(n_T=(1 << 20) + 2), vla.VLA_ERR_ALIGN),
+])
+def test_bad_arguments_rejected_on_host(kw, rc):
+    assert _call(**kw) == rc
+
+
+def test_empty_problem_is_a_no_op():
+    assert _call(B=0) == vla.VLA_OK
+    assert _call(H=0, q=None, k=None, v=None, u=None, o=None, S_T=None, A_T=None) == vla.VLA_OK
+
+
+def test_workspace_query_and_kernel_selection():
+    assert vla.vla_workspace_bytes(1, 16, 4096, 64, vla.VLA_BF16, vla.VLA_KERNEL_SEQ) == 0
+    assert vla.vla_workspace_bytes(1, 16, 4096, 48, vla.VLA_BF16, vla.VLA_KERNEL_SEQ) == 0
+    assert vla.vla_select_kernel(1, 16, 4096, 64) in (vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK)
+    assert vla.vla_select_kernel(1, 16, 4096, 40) == vla.VLA_ERR_UNSUPPORTED_DIM
+
+
+def test_debug_hook_is_host_state_only():
+    assert vla.vla_debug_inject(2) == vla.VLA_ERR_ARG
+    assert vla.vla_debug_inject(1, 1000) == vla.VLA_OK
+    assert vla.vla_debug_inject(0) == vla.VLA_OK
