@@ -45,7 +45,10 @@ FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
 # summarised under profiles/ (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by (kernel, workload).  Reported only while the kernel source still
 # hashes to the value it was captured from; otherwise null.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/seq_kernel_long.md: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
+    ("seq", "long"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
+}
 
 
 def kernel_src_hash(kernel_name: str) -> str:
