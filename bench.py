@@ -47,18 +47,29 @@ FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
 # hashes to the value it was captured from; otherwise null.
 TRAFFIC = {
     # profiles/seq_kernel_long.md: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
-    ("seq", "long"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
+    ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
 }
 
 
 def kernel_src_hash(kernel_name: str) -> str:
     fn = {"seq": "vla_seq.cu", "chunk": "vla_chunk.cu"}[kernel_name]
     path = os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", fn)
-    h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", "vla_internal.cuh")):
-        if os.path.exists(p):
-            h.update(open(p, "rb").read())
-    return h.hexdigest()[:16]
+    if not os.path.exists(path):
+        return ""
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+# Kernels of one step, in launch order, and the share of the algorithmic
+# flops per token-head each one performs (each step of the recurrence is
+# assigned to exactly one kernel; the chunked form's extra work - Grams,
+# prefix sums, chunk transitions, the chain - counts zero).
+def kernel_plan(kname, d):
+    if kname == "seq":
+        return [("seq_kernel", 12 * d * d + 16 * d)]
+    # gates: key norm, z = A u, rank-1 update, A k_hat, gate norm (a0-a2);
+    # output: S k_hat, state write, S phi(q), readout (a3-a4)
+    return [("gram_kernel", 0), ("prefix_kernel", 0), ("gates_kernel", 6 * d * d + 8 * d),
+            ("rows_kernel<summary>", 0), ("chain_kernel", 0), ("rows_kernel<output>", 6 * d * d + 8 * d)]
 
 
 def log(*a):
@@ -293,6 +304,12 @@ def main():
         vla.vla_forward(q, k, v, u, x.lambda0, o=o, S_T=S_T, A_T=A_T, n_T=n_T, kernel=resolved,
                         workspace=ws if need else None, stream=stream)
 
+    plan = kernel_plan(kname, d)
+    nb = len(plan) + 1  # launch boundaries per step
+    bounds = [[torch.cuda.Event(enable_timing=True) for _ in range(nb)] for _ in range(args.steps)]
+    for evs in bounds:
+        for ev in evs:
+            ev.record(stream)  # creates the underlying cudaEvent_t
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -309,16 +326,24 @@ def main():
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
+    launches = 0
     for i in range(args.steps):
         if flush:
             scratch.fill_(float(i))
+        vla.vla_set_launch_events(bounds[i])
         starts[i].record(stream)
         step()
         ends[i].record(stream)
+        launches += vla.vla_last_launch_count()
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
     wall = time.perf_counter() - wall0
+    vla.vla_set_launch_events(None)
+    if launches != args.steps * len(plan):
+        raise RuntimeError("expected %d launches per step, saw %d in total" % (len(plan), launches))
+    per_kernel_ms = [float(np.mean([bounds[i][j].elapsed_time(bounds[i][j + 1]) for i in range(args.steps)]))
+                     for j in range(len(plan))]
     clocks = sampler.stop() if sampler else None
     st = vla.vla_device_status(stream)
     if st != vla.VLA_OK:
@@ -369,18 +394,24 @@ def main():
         e2e = {"value": world * units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    # ---- roofline of the dominant kernel ----
+    # ---- roofline of the dominant kernel (and of the whole step) ----
     flops, byts = algorithmic_work(B, H, T, d, io_bytes)
-    kernel_ms = ms  # one kernel launch per step for the sequential path
-    achieved_tf = flops / (kernel_ms / 1e3) / 1e12
-    tr = TRAFFIC.get((kname, args.config))
+    dom = int(np.argmax(per_kernel_ms))
+    kernel_ms = per_kernel_ms[dom]
+    k_flops = units * plan[dom][1]
+    achieved_tf = k_flops / (kernel_ms / 1e3) / 1e12
+    tr = TRAFFIC.get((kname, args.config, plan[dom][0]))
     traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash(kname) else None
     roofline = {"bound": "alu", "achieved": achieved_tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                 "frac": achieved_tf / FP32_PEAK_TFLOPS, "traffic": traffic,
-                "kernel": "vla::seq_kernel<%d,%s>" % (d, "bf16" if x.dtype == "bf16" else "f32"),
-                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop/FMA x 2.070 GHz",
-                "algorithmic_flops": flops, "algorithmic_bytes": byts,
-                "hbm_frac_of_measured": (byts / (kernel_ms / 1e3) / 1e9) / measured_hbm_gbs()}
+                "kernel": "%s<%d,%s>" % (plan[dom][0], d, x.dtype), "kernel_ms": kernel_ms,
+                "algorithmic_flops_per_launch": k_flops,
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop/FMA x 2.070 GHz (no tensor cores)",
+                "step": {"algorithmic_flops": flops, "algorithmic_bytes": byts,
+                         "alu_frac": flops / (ms / 1e3) / 1e12 / FP32_PEAK_TFLOPS,
+                         "hbm_frac_of_measured": (byts / (ms / 1e3) / 1e9) / measured_hbm_gbs()},
+                "kernels": [{"name": nm, "ms": t, "share": t / sum(per_kernel_ms)}
+                            for (nm, _), t in zip(plan, per_kernel_ms)]}
 
     cpu = None
     parity = None
@@ -400,16 +431,12 @@ def main():
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": config_block(args.config, x, kname), "roofline": roofline, "e2e": e2e,
-                "gpu_launches": args.steps * launches_per_step(kname), "clocks": clocks,
+                "gpu_launches": launches, "clocks": clocks,
                 "cpu_baseline": cpu, "parity_rel_fro": parity, "wall_s_timed": wall}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
     return 0
-
-
-def launches_per_step(kname):
-    return {"seq": 1}.get(kname, 1)
 
 
 def measured_hbm_gbs():

@@ -109,6 +109,19 @@ int vla_device_status(void *stream);
  * VLA_ERR_ARG. */
 int vla_debug_inject(int mode, long long wait_limit_ns);
 
+/* Measurement hook.  With n > 0, every later vla_forward call records
+ * events[0] on its stream before its first kernel and events[i] right after
+ * its i-th kernel, for i < n, so that a caller can time each launch with
+ * cudaEventElapsedTime on the launching stream.  events are cudaEvent_t
+ * handles (as void*) created and owned by the caller.  n = 0 or
+ * events = NULL turns recording off.  Process-wide host state; returns
+ * VLA_OK, or VLA_ERR_ARG when n is negative or above 16. */
+int vla_set_launch_events(void *const *events, int n);
+
+/* Number of kernels the last successful vla_forward call on this host
+ * thread launched (1 for the sequential path, 6 or 7 for the chunked one). */
+int vla_last_launch_count(void);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int vla_version(void);
 

@@ -23,7 +23,9 @@ from ._lib import (  # noqa: F401
     vla_debug_inject,
     vla_device_status,
     vla_forward,
+    vla_last_launch_count,
     vla_select_kernel,
+    vla_set_launch_events,
     vla_status_str,
     vla_workspace_bytes,
 )

@@ -44,6 +44,8 @@ _SIGS = {
     "vla_last_cuda_error": (_i, []),
     "vla_device_status": (_i, [_vp]),
     "vla_debug_inject": (_i, [_i, ctypes.c_longlong]),
+    "vla_set_launch_events": (_i, [ctypes.POINTER(_vp), _i]),
+    "vla_last_launch_count": (_i, []),
     "vla_version": (_i, []),
 }
 
@@ -101,6 +103,27 @@ def vla_device_status(stream=None) -> int:
 
 def vla_debug_inject(mode: int, wait_limit_ns: int = 0) -> int:
     return int(lib().vla_debug_inject(int(mode), int(wait_limit_ns)))
+
+
+def vla_set_launch_events(events) -> int:
+    """Register torch.cuda.Event objects (or raw cudaEvent_t ints) that
+    vla_forward records around each of its launches; None turns it off."""
+    if not events:
+        return int(lib().vla_set_launch_events(None, 0))
+    handles = []
+    for e in events:
+        if hasattr(e, "cuda_event"):
+            if not e.cuda_event:
+                raise ValueError("record each torch.cuda.Event once before registering it")
+            handles.append(e.cuda_event)
+        else:
+            handles.append(int(e))
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    return int(lib().vla_set_launch_events(arr, len(handles)))
+
+
+def vla_last_launch_count() -> int:
+    return int(lib().vla_last_launch_count())
 
 
 def _ptr(t) -> Optional[int]:

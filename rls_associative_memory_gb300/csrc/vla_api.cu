@@ -17,6 +17,9 @@ thread_local int t_last_cuda_error = 0;
 
 long long g_wait_limit_ns = 1000000000LL;  // 1 s bound on every device-side wait
 int g_inject = 0;
+void *g_events[16];
+int g_n_events = 0;
+thread_local int t_last_launches = 0;
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = (int)e;
@@ -45,10 +48,19 @@ int check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int 
     return VLA_OK;
 }
 
+// AUTO: the chunk-parallel path when there are too few (b, h) units to fill
+// the GPU with one CTA each and the stream is long enough to cut.
 int resolve_kernel(int B, int H, int T, int d_h, int kernel) {
-    (void)B; (void)H; (void)T; (void)d_h;
-    if (kernel == VLA_KERNEL_AUTO) return VLA_KERNEL_SEQ;
-    return kernel;
+    (void)d_h;
+    if (kernel != VLA_KERNEL_AUTO) return kernel;
+    const long long BH = (long long)B * H;
+    if (BH < 2 * 152 && T >= 1024) return VLA_KERNEL_CHUNK;
+    return VLA_KERNEL_SEQ;
+}
+
+int chunk_len(int B, int H, int T, int d_h, int chunk) {
+    if (chunk > 0) return chunk;
+    return vla::chunk_default(B * H, T, d_h);
 }
 
 }  // namespace
@@ -72,6 +84,16 @@ const char *vla_status_str(int status) {
 
 int vla_last_cuda_error(void) { return t_last_cuda_error; }
 
+int vla_set_launch_events(void *const *events, int n) {
+    if (n < 0 || n > 16) return VLA_ERR_ARG;
+    if (!events) n = 0;
+    for (int i = 0; i < n; ++i) g_events[i] = events[i];
+    g_n_events = n;
+    return VLA_OK;
+}
+
+int vla_last_launch_count(void) { return t_last_launches; }
+
 int vla_select_kernel(int B, int H, int T, int d_h) {
     const int rc = check_common(VLA_F32, 1.f, B, H, T, d_h, VLA_KERNEL_AUTO);
     if (rc != VLA_OK) return rc;
@@ -80,10 +102,10 @@ int vla_select_kernel(int B, int H, int T, int d_h) {
 
 size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk) {
     if (check_common(io_dtype, 1.f, B, H, T, d_h, kernel) != VLA_OK) return 0;
-    (void)chunk;
+    if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return 0;
     const int kk = resolve_kernel(B, H, T, d_h, kernel);
-    if (kk == VLA_KERNEL_SEQ) return 0;
-    return 0;
+    if (kk == VLA_KERNEL_SEQ || T == 0 || (long long)B * H == 0) return 0;
+    return vla::chunk_layout(B * H, T, d_h, chunk_len(B, H, T, d_h, chunk)).total;
 }
 
 int vla_debug_inject(int mode, long long wait_limit_ns) {
@@ -122,7 +144,7 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
                 size_t ws_bytes, void *stream) {
     int rc = check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
     if (rc != VLA_OK) return rc;
-    if (chunk < 0) return VLA_ERR_ARG;
+    if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
     const long long BH = (long long)B * H;
     if (BH > 0) {
         if (!S_T || !A_T) return VLA_ERR_ARG;
@@ -150,14 +172,22 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
     p.wait_limit_ns = g_wait_limit_ns;
     p.inject = g_inject;
     p.ws = workspace; p.ws_bytes = ws_bytes; p.chunk = chunk;
+    p.events = g_n_events > 0 ? g_events : nullptr;
+    p.n_events = g_n_events;
+    int launches = 0;
+    p.launches = &launches;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    switch (kk) {
-        case VLA_KERNEL_SEQ: e = vla::launch_seq(p, st); break;
-        default: return VLA_ERR_ARG;
+    if (kk == VLA_KERNEL_CHUNK && T > 0) {
+        const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk_len(B, H, T, d_h, chunk));
+        e = vla::launch_chunk(p, L, st);
+    } else {
+        // the sequential kernel also serves T == 0 (state copy) for either choice
+        e = vla::launch_seq(p, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
+    t_last_launches = launches;
     return VLA_OK;
 }
 

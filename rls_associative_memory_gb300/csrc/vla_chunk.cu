@@ -1,0 +1,930 @@
+// vla_chunk.cu -- chunk-parallel VLA forward path (few (b, h) units, long T).
+//
+// The token axis is cut into chunks of C tokens.  Everything that does not
+// need the state at the chunk start runs for all chunks at once; only two
+// cheap chains run along the chunks.
+//
+//  gram     per chunk: G_c = sum_t u_t u_t^T and m_c = sum_t phi(k_hat_t)
+//  prefix   per (b, h): exclusive prefix M^(c) = M_0 + sum_{c'<c} G_c',
+//           n^(c) = n_0 + sum_{c'<c} m_c'  (M_0 = lambda0 I, or A0^{-1})
+//  gates    per chunk: A^(c) = (M^(c))^{-1} (Gauss-Jordan), then the exact
+//           Sherman-Morrison recursion over the chunk's tokens from A^(c):
+//           this is section 2.2's A_t = M_t^{-1} with M_t = M_{t-1} + u u^T,
+//           restarted at every chunk boundary from its definition.  Emits
+//           the unit gates alpha_t (and A_T from the last chunk).
+//  summary  per chunk: the chunk's affine map S_end = S_start P_c + H_c.
+//           Rows of [H; P] follow the state write of section 2.3 step 3
+//           (row x <- x + (value - x.k_hat) alpha^T) with values [v; 0] and
+//           initial rows [0; I].
+//  chain    per (b, h, block of rows): S^(c+1) = S^(c) P_c + H_c, storing
+//           every chunk-start state; writes S_T.
+//  output   per chunk: the state write and ELU+1 readout of every token,
+//           from S^(c), with the gates of the gates pass.
+//
+// Rows of S (and of [H; P]) evolve independently once the gates are known,
+// so the summary and output passes need no block-wide reduction per token.
+#include "vla_internal.cuh"
+
+namespace vla {
+namespace {
+
+constexpr int kTT = 16;  // tokens per staged tile
+
+struct ChunkArgs {
+    FwdParams p;
+    ChunkLayout L;
+};
+
+__device__ __forceinline__ float *ws_f(const ChunkArgs &a, size_t off) {
+    return reinterpret_cast<float *>(static_cast<unsigned char *>(a.p.ws) + off);
+}
+
+// Kahan-compensated accumulation.
+__device__ __forceinline__ void kahan_add(float &sum, float &comp, float x) {
+    const float y = x - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+}
+
+// ---------------------------------------------------------------------------
+// gram: chunk Gram matrices of u and chunk sums of phi(k_hat)
+// ---------------------------------------------------------------------------
+template <int D, typename IO>
+__global__ void __launch_bounds__(256) gram_kernel(ChunkArgs a) {
+    constexpr int MT = D / 16;  // microtile edge on a 16 x 16 thread grid
+    __shared__ __align__(16) float su[kTT][D];
+    __shared__ __align__(16) float sf[kTT][D];
+    const int c = (int)(blockIdx.x % (unsigned)a.L.NC), bh = (int)(blockIdx.x / (unsigned)a.L.NC);
+    const int T = a.p.T, C = a.L.C;
+    const int t0 = c * C, t1 = min(T, t0 + C);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ty = tid >> 4, tx = tid & 15;
+    const IO *gu = static_cast<const IO *>(a.p.u) + (size_t)bh * T * D;
+    const IO *gk = static_cast<const IO *>(a.p.k) + (size_t)bh * T * D;
+    float acc[MT][MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < MT; ++n) acc[m][n] = 0.f;
+    float nacc = 0.f;
+    for (int tb = t0; tb < t1; tb += kTT) {
+        const int ntok = min(kTT, t1 - tb);
+        for (int e = tid; e < ntok * D; e += 256) {
+            su[e / D][e % D] = io_to_f32(gu[(size_t)tb * D + e]);
+            sf[e / D][e % D] = io_to_f32(gk[(size_t)tb * D + e]);
+        }
+        __syncthreads();
+        for (int tt = warp; tt < ntok; tt += 8) {
+            float kk[D / 32], ss = 0.f;
+#pragma unroll
+            for (int m = 0; m < D / 32; ++m) {
+                kk[m] = sf[tt][lane + 32 * m];
+                ss = fmaf(kk[m], kk[m], ss);
+            }
+            ss = warp_sum(ss);
+            const float ks = 1.f / fmaxf(sqrtf(ss), kEps);
+#pragma unroll
+            for (int m = 0; m < D / 32; ++m) sf[tt][lane + 32 * m] = phi_elu1(kk[m] * ks);
+        }
+        __syncthreads();
+        if (tid < D)
+            for (int tt = 0; tt < ntok; ++tt) nacc += sf[tt][tid];
+        for (int tt = 0; tt < ntok; ++tt) {
+            float ui[MT], uj[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                ui[m] = su[tt][ty * MT + m];
+                uj[m] = su[tt][tx * MT + m];
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int n = 0; n < MT; ++n) acc[m][n] = fmaf(ui[m], uj[n], acc[m][n]);
+        }
+        __syncthreads();
+    }
+    float *G = ws_f(a, a.L.off_M) + ((size_t)bh * a.L.NC + c) * D * D;
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < MT; ++n) G[(ty * MT + m) * D + tx * MT + n] = acc[m][n];
+    if (tid < D) ws_f(a, a.L.off_n)[((size_t)bh * (a.L.NC + 1) + c) * D + tid] = nacc;
+}
+
+// ---------------------------------------------------------------------------
+// prefix: exclusive prefix sums of G and m along the chunks (Kahan, fp32)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) prefix_kernel(ChunkArgs a) {
+    constexpr int NB = (D * D + D + 255) / 256;  // blocks per (b, h)
+    const int bh = (int)(blockIdx.x / NB);
+    const int e = (int)(blockIdx.x % NB) * 256 + threadIdx.x;
+    const int NC = a.L.NC;
+    if (e < D * D) {
+        const int i = e / D, j = e % D;
+        float run = a.p.A0 ? ws_f(a, a.L.off_M0)[(size_t)bh * D * D + e] : (i == j ? a.p.lambda0 : 0.f);
+        float comp = 0.f;
+        float *M = ws_f(a, a.L.off_M) + (size_t)bh * NC * D * D + e;
+        for (int c = 0; c < NC; ++c) {
+            const float g = M[(size_t)c * D * D];
+            M[(size_t)c * D * D] = run;
+            kahan_add(run, comp, g);
+        }
+    } else if (e < D * D + D) {
+        const int j = e - D * D;
+        float run = a.p.n0 ? a.p.n0[(size_t)bh * D + j] : 0.f;
+        float comp = 0.f;
+        float *n = ws_f(a, a.L.off_n) + (size_t)bh * (NC + 1) * D + j;
+        for (int c = 0; c < NC; ++c) {
+            const float g = n[(size_t)c * D];
+            n[(size_t)c * D] = run;
+            kahan_add(run, comp, g);
+        }
+        n[(size_t)NC * D] = run;
+        if (a.p.n_T) a.p.n_T[(size_t)bh * D + j] = run;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Register-resident inverse of an SPD matrix by Gauss-Jordan elimination
+// (no pivoting: the pivots of an SPD matrix are positive).  Thread (row i,
+// part) holds x[32] = row i, columns [32 part, 32 part + 32).  piv: two
+// skewed shared vectors for the pivot row (double-buffered).  All threads of
+// the block must call it.
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void gj_inverse(float (&x)[32], float *piv, int row, int part) {
+    constexpr int TPR = D / 32;
+    constexpr int VLEN = TPR * kPart;
+    const int vo = part * kPart;
+    const int lane = threadIdx.x & 31;
+    // pivot row 0
+    if (row == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) piv[vo + j] = x[j];
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int k = 0; k < D; ++k) {
+        const float *pr = piv + (k & 1) * VLEN;
+        const float p = pr[vidx(k)];
+        const float rp = 1.f / p;
+        // m = x[i][k]: held by part k/32 of this row, register k%32
+        float mk = 0.f;
+        const int kp = k >> 5, kr = k & 31;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j == kr) mk = x[j];
+        mk = __shfl_sync(0xffffffffu, mk, (lane & ~(TPR - 1)) | kp);
+        if (row == k) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = (part * 32 + j == k) ? rp : x[j] * rp;
+        } else {
+            const float f = mk * rp;
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 pv = *reinterpret_cast<const float4 *>(pr + vo + 4 * c4);
+                const float pj[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = 4 * c4 + q;
+                    x[j] = (part * 32 + j == k) ? -f : fmaf(-f, pj[q], x[j]);
+                }
+            }
+        }
+        if (k + 1 < D && row == k + 1) {
+            float *nx = piv + ((k + 1) & 1) * VLEN + vo;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) nx[j] = x[j];
+        }
+        __syncthreads();
+    }
+}
+
+template <int D>
+struct RowCfg {
+    static constexpr int TPR = D / 32;
+    static constexpr int NT = D * TPR;
+    static constexpr int NW = NT / 32;
+    static constexpr int VLEN = TPR * kPart;
+};
+
+// Issue the bulk copies of one tile: ntens tensors of ntok tokens each.
+__device__ __forceinline__ void issue_tile(uint64_t *bar, void *const *dst, const void *const *src,
+                                           const uint32_t *bytes_per_tok, int ntens, int ntok) {
+    uint32_t total = 0;
+    for (int x = 0; x < ntens; ++x) total += bytes_per_tok[x] * ntok;
+    mbar_arrive_expect_tx(bar, total);
+    for (int x = 0; x < ntens; ++x) bulk_g2s(dst[x], src[x], bytes_per_tok[x] * ntok, bar);
+}
+
+// ---------------------------------------------------------------------------
+// gates: A^(c) by Gauss-Jordan, then Sherman-Morrison over the chunk
+// ---------------------------------------------------------------------------
+template <int D, typename IO>
+struct GatesSmem {
+    using R = RowCfg<D>;
+    static constexpr size_t bars = 0;
+    static constexpr size_t raw = 128;                                        // [2][2][TT*D] IO (u, k)
+    static constexpr size_t raw_t = (size_t)kTT * D * sizeof(IO);
+    static constexpr size_t khat = raw + 4 * raw_t;                           // [2][TT][VLEN]
+    static constexpr size_t uu = khat + 2 * kTT * R::VLEN * 4;                // [2][TT][VLEN]
+    static constexpr size_t zbuf = uu + 2 * kTT * R::VLEN * 4;                // [2][VLEN]
+    static constexpr size_t piv = zbuf + 2 * R::VLEN * 4;                     // [2][VLEN]
+    static constexpr size_t red = piv + 2 * R::VLEN * 4;                      // [2][NW] float4
+    static constexpr size_t total = red + 2 * R::NW * 16;
+};
+
+template <int D, typename IO>
+__global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
+    using R = RowCfg<D>;
+    using Lo = GatesSmem<D, IO>;
+    constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 16);
+    IO *raw = reinterpret_cast<IO *>(smem + Lo::raw);
+    float *s_khat = reinterpret_cast<float *>(smem + Lo::khat);
+    float *s_u = reinterpret_cast<float *>(smem + Lo::uu);
+    float *s_z = reinterpret_cast<float *>(smem + Lo::zbuf);
+    float *s_piv = reinterpret_cast<float *>(smem + Lo::piv);
+    float4 *s_red = reinterpret_cast<float4 *>(smem + Lo::red);
+
+    const int c = (int)(blockIdx.x % (unsigned)a.L.NC), bh = (int)(blockIdx.x / (unsigned)a.L.NC);
+    const int T = a.p.T, C = a.L.C, NC = a.L.NC;
+    const int t0 = c * C, ntok = min(C, T - t0);
+    const int ntiles = (ntok + kTT - 1) / kTT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = tid / TPR, part = tid % TPR;
+    const int c0 = part * 32, vo = part * kPart;
+    const size_t tok0 = ((size_t)bh * T + t0) * D;
+    const IO *gu = static_cast<const IO *>(a.p.u) + tok0;
+    const IO *gk = static_cast<const IO *>(a.p.k) + tok0;
+    float *galpha = ws_f(a, a.L.off_alpha) + tok0;
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    for (int i = tid; i < 2 * VLEN; i += R::NT) s_z[i] = 0.f;
+    __syncthreads();
+    const uint32_t bpt[2] = {(uint32_t)(D * sizeof(IO)), (uint32_t)(D * sizeof(IO))};
+    auto issue = [&](int m) {
+        const int buf = m & 1;
+        const int nt = min(kTT, ntok - m * kTT);
+        void *dst[2] = {raw + ((size_t)buf * 2 + 0) * kTT * D, raw + ((size_t)buf * 2 + 1) * kTT * D};
+        const void *src[2] = {gu + (size_t)m * kTT * D, gk + (size_t)m * kTT * D};
+        issue_tile(&bars[buf], dst, src, bpt, 2, nt);
+    };
+    int issued = 0;
+    if (tid == 0) {
+        if (ntiles > 0) issue(0);
+        if (ntiles > 1) issue(1);
+        issued = min(ntiles, 2);
+    }
+
+    // ---- A at the chunk start ----
+    float x[32];
+    if (c == 0) {
+        if (a.p.A0) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.p.A0 + (size_t)bh * D * D + row * D + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = src[q];
+                x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+            }
+        } else {
+            const float il = 1.f / a.p.lambda0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = (c0 + j == row) ? il : 0.f;
+        }
+    } else {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            ws_f(a, a.L.off_M) + ((size_t)bh * NC + c) * D * D + row * D + c0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = src[q];
+            x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+        }
+        gj_inverse<D>(x, s_piv, row, part);
+    }
+
+    float beta_prev = 0.f, s2_prev = 0.f, z_prev = 0.f, y_prev = 0.f;
+    int failed = -1;
+    for (int t = 0; t <= ntok; ++t) {
+        const int tt = t % kTT, m = t / kTT;
+        if (tt == 0 && t < ntok) {
+            const int buf = m & 1;
+            if (!mbar_wait_bounded(&bars[buf], (m >> 1) & 1, a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+            __syncthreads();
+            if (*abort_flag) {
+                failed = m;
+                break;
+            }
+            const IO *ru = raw + ((size_t)buf * 2 + 0) * kTT * D;
+            const IO *rk = raw + ((size_t)buf * 2 + 1) * kTT * D;
+            const int nt = min(kTT, ntok - t);
+            for (int q = warp; q < nt; q += NW) {
+                float kk[D / 32], ss = 0.f;
+#pragma unroll
+                for (int mm = 0; mm < D / 32; ++mm) {
+                    kk[mm] = io_to_f32(rk[q * D + lane + 32 * mm]);
+                    ss = fmaf(kk[mm], kk[mm], ss);
+                }
+                ss = warp_sum(ss);
+                const float ks = 1.f / fmaxf(sqrtf(ss), kEps);
+#pragma unroll
+                for (int mm = 0; mm < D / 32; ++mm) {
+                    const int j = lane + 32 * mm;
+                    s_khat[(buf * kTT + q) * VLEN + vidx(j)] = kk[mm] * ks;
+                    s_u[(buf * kTT + q) * VLEN + vidx(j)] = io_to_f32(ru[q * D + j]);
+                }
+            }
+            __syncthreads();
+            if (tid == 0 && m + 2 < ntiles) {
+                issue(m + 2);
+                issued = m + 3;
+            }
+        }
+        const bool hasA = t < ntok, hasG = t > 0;
+        const int buf = m & 1;
+        const float *uA = s_u + (buf * kTT + tt) * VLEN;
+        const float *kA = s_khat + (buf * kTT + tt) * VLEN;
+        const float4 *zp = reinterpret_cast<const float4 *>(s_z + ((t - 1) & 1) * VLEN + vo);
+        float z0 = 0.f, z1 = 0.f, y0 = 0.f, y1 = 0.f;
+        if (hasA) {
+            const float4 *up = reinterpret_cast<const float4 *>(uA + vo);
+            const float4 *kp = reinterpret_cast<const float4 *>(kA + vo);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 zz = zp[q], u4 = up[q], k4 = kp[q];
+                x[4 * q + 0] = fmaf(-beta_prev, z_prev * zz.x, x[4 * q + 0]);
+                x[4 * q + 1] = fmaf(-beta_prev, z_prev * zz.y, x[4 * q + 1]);
+                x[4 * q + 2] = fmaf(-beta_prev, z_prev * zz.z, x[4 * q + 2]);
+                x[4 * q + 3] = fmaf(-beta_prev, z_prev * zz.w, x[4 * q + 3]);
+                z0 = fmaf(x[4 * q + 0], u4.x, z0);
+                z1 = fmaf(x[4 * q + 1], u4.y, z1);
+                z0 = fmaf(x[4 * q + 2], u4.z, z0);
+                z1 = fmaf(x[4 * q + 3], u4.w, z1);
+                y0 = fmaf(x[4 * q + 0], k4.x, y0);
+                y1 = fmaf(x[4 * q + 1], k4.y, y1);
+                y0 = fmaf(x[4 * q + 2], k4.z, y0);
+                y1 = fmaf(x[4 * q + 3], k4.w, y1);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 zz = zp[q];
+                x[4 * q + 0] = fmaf(-beta_prev, z_prev * zz.x, x[4 * q + 0]);
+                x[4 * q + 1] = fmaf(-beta_prev, z_prev * zz.y, x[4 * q + 1]);
+                x[4 * q + 2] = fmaf(-beta_prev, z_prev * zz.z, x[4 * q + 2]);
+                x[4 * q + 3] = fmaf(-beta_prev, z_prev * zz.w, x[4 * q + 3]);
+            }
+        }
+        float z = z0 + z1, y = y0 + y1;
+#pragma unroll
+        for (int o = 1; o < TPR; o <<= 1) {
+            z += __shfl_xor_sync(0xffffffffu, z, o);
+            y += __shfl_xor_sync(0xffffffffu, y, o);
+        }
+        const float g = y_prev - beta_prev * s2_prev * z_prev;  // gate row of token t-1
+        float p1 = 0.f, p2 = 0.f, p3 = 0.f;
+        if (part == 0) {
+            if (hasA) {
+                p1 = uA[vidx(row)] * z;
+                p2 = kA[vidx(row)] * z;
+                s_z[(t & 1) * VLEN + vidx(row)] = z;
+            }
+            if (hasG) p3 = g * g;
+        }
+        p1 = warp_sum(p1);
+        p2 = warp_sum(p2);
+        p3 = warp_sum(p3);
+        if constexpr (NW > 1) {
+            if (lane == 0) s_red[(t & 1) * NW + warp] = make_float4(p1, p2, p3, 0.f);
+            __syncthreads();
+            float4 acc = s_red[(t & 1) * NW];
+#pragma unroll
+            for (int w = 1; w < NW; ++w) {
+                const float4 v = s_red[(t & 1) * NW + w];
+                acc.x += v.x; acc.y += v.y; acc.z += v.z;
+            }
+            p1 = acc.x; p2 = acc.y; p3 = acc.z;
+        } else {
+            __syncwarp();
+        }
+        if (hasG && part == 0) galpha[(size_t)(t - 1) * D + row] = g * (1.f / fmaxf(sqrtf(p3), kEps));
+        beta_prev = 1.f / (1.f + p1);
+        s2_prev = p2;
+        z_prev = z;
+        y_prev = y;
+    }
+    if (failed >= 0) {
+        if (tid == 0)
+            for (int m = failed; m < issued; ++m)
+                (void)mbar_wait_bounded(&bars[m & 1], (m >> 1) & 1, a.p.wait_limit_ns, a.p.err);
+        return;
+    }
+    if (c == NC - 1) {
+        float4 *dA = reinterpret_cast<float4 *>(a.p.A_T + (size_t)bh * D * D + row * D + c0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dA[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Row recurrences given the gates (summary and output passes)
+// ---------------------------------------------------------------------------
+// Shared tile for both passes: raw IO tiles of up to three tensors plus the
+// fp32 gate tile, and processed skewed vectors.
+template <int D, typename IO>
+struct RowsSmem {
+    using R = RowCfg<D>;
+    static constexpr size_t bars = 0;
+    static constexpr size_t raw = 128;                                   // [2][3][TT*D] IO (q, k, v)
+    static constexpr size_t raw_t = (size_t)kTT * D * sizeof(IO);
+    static constexpr size_t ral = raw + 6 * raw_t;                       // [2][TT*D] fp32 gates
+    static constexpr size_t khat = ral + 2 * (size_t)kTT * D * 4;        // [2][TT][VLEN]
+    static constexpr size_t alp = khat + 2 * kTT * R::VLEN * 4;          // [2][TT][VLEN]
+    static constexpr size_t phiq = alp + 2 * kTT * R::VLEN * 4;          // [2][TT][VLEN]
+    static constexpr size_t vv = phiq + 2 * kTT * R::VLEN * 4;           // [2][TT][D]
+    static constexpr size_t den = vv + 2 * (size_t)kTT * D * 4;          // [2][TT]
+    static constexpr size_t ga = den + 2 * kTT * 4;                      // [2][TT]
+    static constexpr size_t work = ga + 2 * kTT * 4;                     // [TT][D]
+    static constexpr size_t total = work + (size_t)kTT * D * 4;
+};
+
+// MODE 0 (summary): rows h (values v, start 0) and p (values 0, start I);
+//                   writes P_c, H_c.
+// MODE 1 (output):  rows s (values v, start S^(c)); writes o.
+template <int D, typename IO, int MODE>
+__global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
+    using R = RowCfg<D>;
+    using Lo = RowsSmem<D, IO>;
+    constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW;
+    constexpr int NIO = (MODE == 0) ? 2 : 3;  // k, v (+ q)
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 16);
+    IO *raw = reinterpret_cast<IO *>(smem + Lo::raw);
+    float *s_ral = reinterpret_cast<float *>(smem + Lo::ral);
+    float *s_khat = reinterpret_cast<float *>(smem + Lo::khat);
+    float *s_alp = reinterpret_cast<float *>(smem + Lo::alp);
+    float *s_phiq = reinterpret_cast<float *>(smem + Lo::phiq);
+    float *s_v = reinterpret_cast<float *>(smem + Lo::vv);
+    float *s_den = reinterpret_cast<float *>(smem + Lo::den);
+    float *s_ga = reinterpret_cast<float *>(smem + Lo::ga);
+    float *s_work = reinterpret_cast<float *>(smem + Lo::work);
+
+    const int c = (int)(blockIdx.x % (unsigned)a.L.NC), bh = (int)(blockIdx.x / (unsigned)a.L.NC);
+    const int T = a.p.T, C = a.L.C, NC = a.L.NC;
+    const int t0 = c * C, ntok = min(C, T - t0);
+    const int ntiles = (ntok + kTT - 1) / kTT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = tid / TPR, part = tid % TPR;
+    const int c0 = part * 32, vo = part * kPart;
+    const size_t tok0 = ((size_t)bh * T + t0) * D;
+    const IO *gk = static_cast<const IO *>(a.p.k) + tok0;
+    const IO *gv = static_cast<const IO *>(a.p.v) + tok0;
+    const IO *gq = static_cast<const IO *>(a.p.q) + tok0;
+    const float *galpha = ws_f(a, a.L.off_alpha) + tok0;
+    IO *gout = static_cast<IO *>(a.p.o) + tok0;
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    const uint32_t bio = (uint32_t)(D * sizeof(IO));
+    const uint32_t bpt[4] = {bio, bio, bio, (uint32_t)(D * 4)};
+    auto issue = [&](int m) {
+        const int buf = m & 1;
+        const int nt = min(kTT, ntok - m * kTT);
+        const size_t off = (size_t)m * kTT * D;
+        void *dst[4];
+        const void *src[4];
+        dst[0] = raw + ((size_t)buf * 3 + 0) * kTT * D; src[0] = gk + off;
+        dst[1] = raw + ((size_t)buf * 3 + 1) * kTT * D; src[1] = gv + off;
+        if (MODE == 1) {
+            dst[2] = raw + ((size_t)buf * 3 + 2) * kTT * D;
+            src[2] = gq + off;
+        }
+        dst[NIO] = s_ral + (size_t)buf * kTT * D;
+        src[NIO] = galpha + off;
+        uint32_t b[4] = {bpt[0], bpt[1], MODE == 1 ? bpt[2] : bpt[3], bpt[3]};
+        issue_tile(&bars[buf], dst, src, b, NIO + 1, nt);
+    };
+    int issued = 0;
+    if (tid == 0) {
+        if (ntiles > 0) issue(0);
+        if (ntiles > 1) issue(1);
+        issued = min(ntiles, 2);
+    }
+
+    // row state
+    float h[32], p[32];
+    const size_t moff = (size_t)row * D + c0;
+    if (MODE == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            h[j] = 0.f;
+            p[j] = (c0 + j == row) ? 1.f : 0.f;
+        }
+    } else {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            ws_f(a, a.L.off_S) + ((size_t)bh * NC + c) * D * D + moff);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = src[q];
+            h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+        }
+    }
+    float nbase = 0.f;
+    if (MODE == 1 && tid < D) nbase = ws_f(a, a.L.off_n)[((size_t)bh * (NC + 1) + c) * D + tid];
+
+    int failed = -1;
+    for (int m = 0; m < ntiles; ++m) {
+        const int buf = m & 1;
+        const int nt = min(kTT, ntok - m * kTT);
+        if (!mbar_wait_bounded(&bars[buf], (m >> 1) & 1, a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+        __syncthreads();
+        if (*abort_flag) {
+            failed = m;
+            break;
+        }
+        // ---- preprocess the tile ----
+        const IO *rk = raw + ((size_t)buf * 3 + 0) * kTT * D;
+        const IO *rv = raw + ((size_t)buf * 3 + 1) * kTT * D;
+        const IO *rq = raw + ((size_t)buf * 3 + 2) * kTT * D;
+        const float *ra = s_ral + (size_t)buf * kTT * D;
+        float *khat = s_khat + buf * kTT * VLEN;
+        float *alp = s_alp + buf * kTT * VLEN;
+        float *phiq = s_phiq + buf * kTT * VLEN;
+        float *vv = s_v + buf * kTT * D;
+        for (int q = warp; q < nt; q += NW) {
+            float kk[D / 32], ss = 0.f;
+#pragma unroll
+            for (int mm = 0; mm < D / 32; ++mm) {
+                kk[mm] = io_to_f32(rk[q * D + lane + 32 * mm]);
+                ss = fmaf(kk[mm], kk[mm], ss);
+            }
+            ss = warp_sum(ss);
+            const float ks = 1.f / fmaxf(sqrtf(ss), kEps);
+            float gdot = 0.f;
+#pragma unroll
+            for (int mm = 0; mm < D / 32; ++mm) {
+                const int j = lane + 32 * mm;
+                const float kh = kk[mm] * ks;
+                const float al = ra[q * D + j];
+                khat[q * VLEN + vidx(j)] = kh;
+                alp[q * VLEN + vidx(j)] = al;
+                vv[q * D + j] = io_to_f32(rv[q * D + j]);
+                if (MODE == 1) {
+                    const float fq = phi_elu1(io_to_f32(rq[q * D + j]));
+                    phiq[q * VLEN + vidx(j)] = fq;
+                    s_work[q * D + j] = phi_elu1(kh);
+                    gdot = fmaf(al, fq, gdot);
+                }
+            }
+            if (MODE == 1) {
+                gdot = warp_sum(gdot);
+                if (lane == 0) s_ga[buf * kTT + q] = gdot;
+            }
+        }
+        __syncthreads();
+        if (MODE == 1) {
+            if (tid < D) {
+                float run = 0.f;
+                for (int q = 0; q < nt; ++q) {
+                    run += s_work[q * D + tid];
+                    s_work[q * D + tid] = phiq[q * VLEN + vidx(tid)] * (nbase + run);
+                }
+                nbase += run;
+            }
+            __syncthreads();
+            for (int q = warp; q < nt; q += NW) {
+                float sacc = 0.f;
+#pragma unroll
+                for (int mm = 0; mm < D / 32; ++mm) sacc += s_work[q * D + lane + 32 * mm];
+                sacc = warp_sum(sacc);
+                if (lane == 0) s_den[buf * kTT + q] = sacc + kEps;
+            }
+            __syncthreads();
+        }
+        if (tid == 0 && m + 2 < ntiles) {
+            issue(m + 2);
+            issued = m + 3;
+        }
+        // ---- token recurrences (row-local, no barrier) ----
+        for (int q = 0; q < nt; ++q) {
+            const float4 *kp = reinterpret_cast<const float4 *>(khat + q * VLEN + vo);
+            const float4 *ap = reinterpret_cast<const float4 *>(alp + q * VLEN + vo);
+            const float vi = vv[q * D + row];
+            if (MODE == 0) {
+                float h0 = 0.f, h1 = 0.f, p0 = 0.f, p1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const float4 k4 = kp[w];
+                    h0 = fmaf(h[4 * w + 0], k4.x, h0);
+                    h1 = fmaf(h[4 * w + 1], k4.y, h1);
+                    h0 = fmaf(h[4 * w + 2], k4.z, h0);
+                    h1 = fmaf(h[4 * w + 3], k4.w, h1);
+                    p0 = fmaf(p[4 * w + 0], k4.x, p0);
+                    p1 = fmaf(p[4 * w + 1], k4.y, p1);
+                    p0 = fmaf(p[4 * w + 2], k4.z, p0);
+                    p1 = fmaf(p[4 * w + 3], k4.w, p1);
+                }
+                float hk = h0 + h1, pk = p0 + p1;
+#pragma unroll
+                for (int o = 1; o < TPR; o <<= 1) {
+                    hk += __shfl_xor_sync(0xffffffffu, hk, o);
+                    pk += __shfl_xor_sync(0xffffffffu, pk, o);
+                }
+                const float rh = vi - hk, rp = -pk;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const float4 a4 = ap[w];
+                    h[4 * w + 0] = fmaf(rh, a4.x, h[4 * w + 0]);
+                    h[4 * w + 1] = fmaf(rh, a4.y, h[4 * w + 1]);
+                    h[4 * w + 2] = fmaf(rh, a4.z, h[4 * w + 2]);
+                    h[4 * w + 3] = fmaf(rh, a4.w, h[4 * w + 3]);
+                    p[4 * w + 0] = fmaf(rp, a4.x, p[4 * w + 0]);
+                    p[4 * w + 1] = fmaf(rp, a4.y, p[4 * w + 1]);
+                    p[4 * w + 2] = fmaf(rp, a4.z, p[4 * w + 2]);
+                    p[4 * w + 3] = fmaf(rp, a4.w, p[4 * w + 3]);
+                }
+            } else {
+                const float4 *fp = reinterpret_cast<const float4 *>(phiq + q * VLEN + vo);
+                float k0 = 0.f, k1 = 0.f, f0 = 0.f, f1 = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const float4 k4 = kp[w], f4 = fp[w];
+                    k0 = fmaf(h[4 * w + 0], k4.x, k0);
+                    k1 = fmaf(h[4 * w + 1], k4.y, k1);
+                    k0 = fmaf(h[4 * w + 2], k4.z, k0);
+                    k1 = fmaf(h[4 * w + 3], k4.w, k1);
+                    f0 = fmaf(h[4 * w + 0], f4.x, f0);
+                    f1 = fmaf(h[4 * w + 1], f4.y, f1);
+                    f0 = fmaf(h[4 * w + 2], f4.z, f0);
+                    f1 = fmaf(h[4 * w + 3], f4.w, f1);
+                }
+                float sk = k0 + k1, sq = f0 + f1;
+#pragma unroll
+                for (int o = 1; o < TPR; o <<= 1) {
+                    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                }
+                const float r = vi - sk;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    const float4 a4 = ap[w];
+                    h[4 * w + 0] = fmaf(r, a4.x, h[4 * w + 0]);
+                    h[4 * w + 1] = fmaf(r, a4.y, h[4 * w + 1]);
+                    h[4 * w + 2] = fmaf(r, a4.z, h[4 * w + 2]);
+                    h[4 * w + 3] = fmaf(r, a4.w, h[4 * w + 3]);
+                }
+                if (part == 0) {
+                    const float num = fmaf(r, s_ga[buf * kTT + q], sq);
+                    gout[(size_t)(m * kTT + q) * D + row] = f32_to_io<IO>(num / s_den[buf * kTT + q]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (failed >= 0) {
+        if (tid == 0)
+            for (int m = failed; m < issued; ++m)
+                (void)mbar_wait_bounded(&bars[m & 1], (m >> 1) & 1, a.p.wait_limit_ns, a.p.err);
+        return;
+    }
+    if (MODE == 0) {
+        float4 *dP = reinterpret_cast<float4 *>(ws_f(a, a.L.off_P) + ((size_t)bh * NC + c) * D * D + moff);
+        float4 *dH = reinterpret_cast<float4 *>(ws_f(a, a.L.off_H) + ((size_t)bh * NC + c) * D * D + moff);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            dP[q] = make_float4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+            dH[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// chain: S^(c+1) = S^(c) P_c + H_c for a block of RB rows of S
+// ---------------------------------------------------------------------------
+constexpr int kRB = 16;
+
+template <int D>
+struct ChainSmem {
+    static constexpr size_t bars = 0;
+    static constexpr size_t P = 128;                                 // [2][D][D]
+    static constexpr size_t H = P + 2 * (size_t)D * D * 4;           // [2][RB][D]
+    static constexpr size_t S = H + 2 * (size_t)kRB * D * 4;         // [RB][D]
+    static constexpr size_t total = S + (size_t)kRB * D * 4;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
+    using Lo = ChainSmem<D>;
+    constexpr int OPT = kRB * D / 256;  // outputs per thread: one row, OPT consecutive columns
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 16);
+    float *sP = reinterpret_cast<float *>(smem + Lo::P);
+    float *sH = reinterpret_cast<float *>(smem + Lo::H);
+    float *sS = reinterpret_cast<float *>(smem + Lo::S);
+    const int rb = (int)(blockIdx.x % (D / kRB)), bh = (int)(blockIdx.x / (D / kRB));
+    const int NC = a.L.NC;
+    const int tid = threadIdx.x;
+    const int r = tid / (D / OPT), j0 = (tid % (D / OPT)) * OPT;
+    const int grow = rb * kRB + r;  // row of S
+    const float *gP = ws_f(a, a.L.off_P) + (size_t)bh * NC * D * D;
+    const float *gH = ws_f(a, a.L.off_H) + (size_t)bh * NC * D * D + (size_t)rb * kRB * D;
+    float *gS = ws_f(a, a.L.off_S) + (size_t)bh * NC * D * D + (size_t)rb * kRB * D;
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    float s[OPT];
+#pragma unroll
+    for (int q = 0; q < OPT; ++q)
+        s[q] = a.p.S0 ? a.p.S0[((size_t)bh * D + grow) * D + j0 + q] : 0.f;
+#pragma unroll
+    for (int q = 0; q < OPT; ++q) sS[r * D + j0 + q] = s[q];
+    __syncthreads();
+    auto issue = [&](int cc) {
+        const int buf = cc & 1;
+        mbar_arrive_expect_tx(&bars[buf], (uint32_t)((D * D + kRB * D) * 4));
+        bulk_g2s(sP + (size_t)buf * D * D, gP + (size_t)cc * D * D, (uint32_t)(D * D * 4), &bars[buf]);
+        bulk_g2s(sH + (size_t)buf * kRB * D, gH + (size_t)cc * D * D, (uint32_t)(kRB * D * 4), &bars[buf]);
+    };
+    int issued = 0;
+    if (tid == 0) {
+        if (NC > 0) issue(0);
+        if (NC > 1) issue(1);
+        issued = min(NC, 2);
+    }
+    int failed = -1;
+    for (int cc = 0; cc < NC; ++cc) {
+        // chunk-start state S^(cc)
+#pragma unroll
+        for (int q = 0; q < OPT; ++q) gS[(size_t)cc * D * D + r * D + j0 + q] = s[q];
+        const int buf = cc & 1;
+        if (!mbar_wait_bounded(&bars[buf], (cc >> 1) & 1, a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+        __syncthreads();
+        if (*abort_flag) {
+            failed = cc;
+            break;
+        }
+        const float *P = sP + (size_t)buf * D * D;
+        const float *Hh = sH + (size_t)buf * kRB * D;
+        float acc[OPT];
+#pragma unroll
+        for (int q = 0; q < OPT; ++q) acc[q] = Hh[r * D + j0 + q];
+        const float *srow = sS + r * D;
+#pragma unroll 8
+        for (int k = 0; k < D; ++k) {
+            const float sk = srow[k];
+#pragma unroll
+            for (int q = 0; q < OPT; ++q) acc[q] = fmaf(sk, P[k * D + j0 + q], acc[q]);
+        }
+        __syncthreads();  // everyone done reading sS and this buffer
+#pragma unroll
+        for (int q = 0; q < OPT; ++q) {
+            s[q] = acc[q];
+            sS[r * D + j0 + q] = acc[q];
+        }
+        if (tid == 0 && cc + 2 < NC) {
+            issue(cc + 2);
+            issued = cc + 3;
+        }
+        __syncthreads();
+    }
+    if (failed >= 0) {
+        if (tid == 0)
+            for (int m = failed; m < issued; ++m)
+                (void)mbar_wait_bounded(&bars[m & 1], (m >> 1) & 1, a.p.wait_limit_ns, a.p.err);
+        return;
+    }
+#pragma unroll
+    for (int q = 0; q < OPT; ++q) a.p.S_T[((size_t)bh * D + grow) * D + j0 + q] = s[q];
+}
+
+// ---------------------------------------------------------------------------
+// M_0 = A0^{-1} (only when A0 is given)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(RowCfg<D>::NT) invert_a0_kernel(ChunkArgs a) {
+    using R = RowCfg<D>;
+    __shared__ __align__(16) float piv[2 * R::VLEN];
+    const int bh = blockIdx.x;
+    const int tid = threadIdx.x, row = tid / R::TPR, part = tid % R::TPR, c0 = part * 32;
+    float x[32];
+    const float *src = a.p.A0 + (size_t)bh * D * D + row * D + c0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = src[j];
+    gj_inverse<D>(x, piv, row, part);
+    float *dst = ws_f(a, a.L.off_M0) + (size_t)bh * D * D + row * D + c0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dst[j] = x[j];
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int D, typename IO>
+cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
+    using R = RowCfg<D>;
+    const long long BH = a.p.BH, NC = a.L.NC;
+    if (NC * BH > 0x7fffffffLL || BH * ((D * D + D + 255) / 256) > 0x7fffffffLL)
+        return cudaErrorInvalidConfiguration;
+    cudaError_t e;
+    if ((e = set_smem(gates_kernel<D, IO>, GatesSmem<D, IO>::total)) != cudaSuccess) return e;
+    if ((e = set_smem(rows_kernel<D, IO, 0>, RowsSmem<D, IO>::total)) != cudaSuccess) return e;
+    if ((e = set_smem(chain_kernel<D>, ChainSmem<D>::total)) != cudaSuccess) return e;
+    if ((e = set_smem(rows_kernel<D, IO, 1>, RowsSmem<D, IO>::total)) != cudaSuccess) return e;
+    int n = 0;
+    mark_launch(a.p, n, st);
+    if (a.p.A0) {
+        invert_a0_kernel<D><<<(unsigned)BH, R::NT, 0, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        mark_launch(a.p, ++n, st);
+    }
+    gram_kernel<D, IO><<<(unsigned)(NC * BH), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    prefix_kernel<D><<<(unsigned)(((D * D + D + 255) / 256) * BH), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    gates_kernel<D, IO><<<(unsigned)(NC * BH), R::NT, GatesSmem<D, IO>::total, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), R::NT, RowsSmem<D, IO>::total, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    chain_kernel<D><<<(unsigned)((D / kRB) * BH), 256, ChainSmem<D>::total, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    rows_kernel<D, IO, 1><<<(unsigned)(NC * BH), R::NT, RowsSmem<D, IO>::total, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    return cudaSuccess;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+int chunk_default(int BH, int T, int d) {
+    (void)d;
+    int C = T >= 4096 ? 256 : (T >= 1024 ? 128 : 64);
+    while (C > 64 && (long long)BH * ((T + C - 1) / C) < 2 * 152) C /= 2;
+    return C;
+}
+
+ChunkLayout chunk_layout(int BH, int T, int d, int C) {
+    ChunkLayout L{};
+    L.C = C;
+    L.NC = (T + C - 1) / C;
+    const size_t bh = (size_t)BH, nc = (size_t)L.NC, dd = (size_t)d * d;
+    size_t off = 0;
+    L.off_M = off; off = align256(off + bh * nc * dd * 4);
+    L.off_n = off; off = align256(off + bh * (nc + 1) * d * 4);
+    L.off_M0 = off; off = align256(off + bh * dd * 4);
+    L.off_alpha = off; off = align256(off + bh * (size_t)T * d * 4);
+    L.off_P = off; off = align256(off + bh * nc * dd * 4);
+    L.off_H = off; off = align256(off + bh * nc * dd * 4);
+    L.off_S = off; off = align256(off + bh * nc * dd * 4);
+    L.total = off;
+    return L;
+}
+
+cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream) {
+    if (p.BH == 0) return cudaSuccess;
+    ChunkArgs a{p, L};
+    if (p.io_bf16) {
+        switch (p.d) {
+            case 32: return launch_chunk_t<32, __nv_bfloat16>(a, stream);
+            case 64: return launch_chunk_t<64, __nv_bfloat16>(a, stream);
+            case 128: return launch_chunk_t<128, __nv_bfloat16>(a, stream);
+        }
+    } else {
+        switch (p.d) {
+            case 32: return launch_chunk_t<32, float>(a, stream);
+            case 64: return launch_chunk_t<64, float>(a, stream);
+            case 128: return launch_chunk_t<128, float>(a, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace vla

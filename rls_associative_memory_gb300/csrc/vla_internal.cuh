@@ -11,6 +11,12 @@ namespace vla {
 
 constexpr float kEps = 1e-6f;  // key norm, gate norm and readout denominator guard
 
+// Shared-memory vectors are stored in 32-float parts with a stride of 36
+// floats, so that the d/32 threads of a row, which read different parts in
+// the same instruction, hit different banks.
+constexpr int kPart = 36;
+__host__ __device__ __forceinline__ int vidx(int j) { return (j >> 5) * kPart + (j & 31); }
+
 // Device error word values (written with atomicExch, read by vla_device_status).
 constexpr int kDevErrTimeout = 1;
 
@@ -28,10 +34,42 @@ struct FwdParams {
     void *ws;                   // workspace (chunked kernel)
     size_t ws_bytes;
     int chunk;                  // chunk length (chunked kernel)
+    void *const *events;        // measurement hook: cudaEvent_t handles, or null
+    int n_events;
+    int *launches;              // out: number of kernels launched
 };
+
+// Records the measurement event for launch boundary i (0 = before the first
+// kernel) and counts launches.
+inline void mark_launch(const FwdParams &p, int i, cudaStream_t st) {
+    if (p.events && i < p.n_events && p.events[i])
+        cudaEventRecord(static_cast<cudaEvent_t>(p.events[i]), st);
+    if (p.launches && i > *p.launches) *p.launches = i;
+}
 
 // Sequential kernel: one CTA per (b, h).  Returns a cudaError_t.
 cudaError_t launch_seq(const FwdParams &p, cudaStream_t stream);
+
+// Workspace of the chunk-parallel path (byte offsets, 256-byte aligned).
+struct ChunkLayout {
+    int C;               // chunk length (multiple of 16)
+    int NC;              // chunks per (b, h) = ceil(T / C)
+    size_t off_M;        // [BH][NC][d][d]  chunk Grams, then exclusive prefix M^(c)
+    size_t off_n;        // [BH][NC+1][d]   chunk sums of phi(k_hat), then exclusive prefix n^(c)
+    size_t off_M0;       // [BH][d][d]      inverse of A0 (only when A0 is given)
+    size_t off_alpha;    // [BH][T][d]      unit gates alpha_t
+    size_t off_P;        // [BH][NC][d][d]  chunk transition P_c
+    size_t off_H;        // [BH][NC][d][d]  chunk offset H_c
+    size_t off_S;        // [BH][NC][d][d]  chunk-start states S^(c)
+    size_t total;
+};
+
+// Default chunk length for a shape (chunk == 0 in the API).
+int chunk_default(int BH, int T, int d);
+// Layout for the given shape; C must be a positive multiple of 16.
+ChunkLayout chunk_layout(int BH, int T, int d, int C);
+// Chunk-parallel path (six launches).  Returns a cudaError_t.
+cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // PTX helpers

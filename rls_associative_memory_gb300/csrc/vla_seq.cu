@@ -32,10 +32,6 @@
 namespace vla {
 namespace {
 
-constexpr int kPart = 36;  // shared-memory stride of one 32-column part (4-float skew: no bank conflicts)
-
-__device__ __forceinline__ int vidx(int j) { return (j >> 5) * kPart + (j & 31); }
-
 template <int D>
 struct SeqCfg {
     static constexpr int TPR = D / 32;             // threads per row
@@ -388,8 +384,11 @@ cudaError_t launch_seq_t(const FwdParams &p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(seq_kernel<D, IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
+    mark_launch(p, 0, stream);
     seq_kernel<D, IO><<<p.BH, C::NT, smem, stream>>>(p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    mark_launch(p, 1, stream);
+    return e;
 }
 
 }  // namespace

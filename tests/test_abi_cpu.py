@@ -70,6 +70,7 @@ def _call(**kw):
     (dict(B=-1), vla.VLA_ERR_ARG),
     (dict(T=-3), vla.VLA_ERR_ARG),
     (dict(chunk=-1), vla.VLA_ERR_ARG),
+    (dict(chunk=24), vla.VLA_ERR_ARG),
     (dict(q=None), vla.VLA_ERR_ARG),
     (dict(o=None), vla.VLA_ERR_ARG),
     (dict(S_T=None), vla.VLA_ERR_ARG),
@@ -82,6 +83,13 @@ def test_bad_arguments_rejected_on_host(kw, rc):
     assert _call(**kw) == rc
 
 
+def test_chunked_path_needs_workspace():
+    assert _call(kernel=vla.VLA_KERNEL_CHUNK, T=4096) == vla.VLA_ERR_WORKSPACE
+    need = vla.vla_workspace_bytes(1, 1, 4096, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK)
+    assert _call(kernel=vla.VLA_KERNEL_CHUNK, T=4096, ws=1 << 20, ws_bytes=need - 1) == vla.VLA_ERR_WORKSPACE
+    assert _call(kernel=vla.VLA_KERNEL_CHUNK, T=4096, ws=(1 << 20) + 8, ws_bytes=need) == vla.VLA_ERR_ALIGN
+
+
 def test_empty_problem_is_a_no_op():
     assert _call(B=0) == vla.VLA_OK
     assert _call(H=0, q=None, k=None, v=None, u=None, o=None, S_T=None, A_T=None) == vla.VLA_OK
@@ -89,6 +97,13 @@ def test_empty_problem_is_a_no_op():
 
 def test_workspace_query_and_kernel_selection():
     assert vla.vla_workspace_bytes(1, 16, 4096, 64, vla.VLA_BF16, vla.VLA_KERNEL_SEQ) == 0
+    ws = vla.vla_workspace_bytes(1, 16, 4096, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK, 256)
+    # gates (T d fp32 per head) plus four d x d fp32 matrices per chunk per head, and more
+    assert ws >= 16 * (4096 * 64 * 4 + 16 * 4 * 64 * 64 * 4)
+    assert vla.vla_workspace_bytes(1, 16, 4096, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK, 24) == 0
+    assert vla.vla_workspace_bytes(1, 16, 0, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK) == 0
+    assert vla.vla_select_kernel(1, 16, 65536, 64) == vla.VLA_KERNEL_CHUNK
+    assert vla.vla_select_kernel(256, 4, 512, 32) == vla.VLA_KERNEL_SEQ
     assert vla.vla_workspace_bytes(1, 16, 4096, 48, vla.VLA_BF16, vla.VLA_KERNEL_SEQ) == 0
     assert vla.vla_select_kernel(1, 16, 4096, 64) in (vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK)
     assert vla.vla_select_kernel(1, 16, 4096, 40) == vla.VLA_ERR_UNSUPPORTED_DIM

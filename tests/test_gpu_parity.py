@@ -13,34 +13,50 @@ from vla_testutil import TOL, compare, oracle_ref, rel_fro, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [vla.VLA_KERNEL_SEQ]
+KERNELS = [vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK]
+# (kernel, chunk length): the chunked path with a short explicit chunk spans
+# many chunks and a ragged last chunk even on small streams.
+VARIANTS = [(vla.VLA_KERNEL_SEQ, 0), (vla.VLA_KERNEL_CHUNK, 32), (vla.VLA_KERNEL_CHUNK, 0)]
 
 
 def _kid(k):
     return {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk", vla.VLA_KERNEL_AUTO: "auto"}[k]
 
 
+def _vid(v):
+    return "%s%s" % (_kid(v[0]), ("-c%d" % v[1]) if v[1] else "")
+
+
 # --- small shapes: several tiles, ragged tails, every d and dtype ---
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=_kid)
+@pytest.mark.parametrize("variant", VARIANTS, ids=_vid)
 @pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("T", [1, 17, 100, 333])
-def test_small_parity(kernel, d, dtype, T):
+def test_small_parity(variant, d, dtype, T):
+    kernel, chunk = variant
     x = make_inputs(2, 3, T, d, dtype, seed=1000 + d + T, lambda0=0.8)
-    compare(run_gpu(x, kernel), oracle_ref(x), dtype)
+    compare(run_gpu(x, kernel, chunk=chunk), oracle_ref(x), dtype)
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=_kid)
+@pytest.mark.parametrize("variant", VARIANTS, ids=_vid)
 @pytest.mark.parametrize("d", [32, 64, 128])
-def test_given_initial_state(kernel, d):
+def test_given_initial_state(variant, d):
     """S0, A0, n0 supplied (streaming continuation)."""
+    kernel, chunk = variant
     pre = make_inputs(1, 2, 40, d, "f32", seed=7, lambda0=1.3)
     st = oracle_ref(pre)
     x = make_inputs(1, 2, 77, d, "f32", seed=8, lambda0=1.3)
     ref = oracle_ref(x, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"])
-    got = run_gpu(x, kernel, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"])
+    got = run_gpu(x, kernel, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"], chunk=chunk)
     compare(got, ref, "f32")
+
+
+@pytest.mark.parametrize("chunk", [16, 48, 64, 128, 256])
+def test_chunk_lengths(chunk):
+    """Every chunk length gives the same result (one ragged last chunk)."""
+    x = make_inputs(1, 4, 1000, 64, "bf16", seed=31, u_scale=0.5)
+    compare(run_gpu(x, vla.VLA_KERNEL_CHUNK, chunk=chunk), oracle_ref(x), "bf16")
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=_kid)
@@ -117,16 +133,27 @@ def test_bounded_wait_expiry_reports_timeout_and_context_survives():
 FULL = ["tiny", "heads32", "long", "batched", "recall8", "recall24", "recall48"]
 
 
+_CACHE = {}
+
+
+def _full_inputs(name):
+    # one generated batch per workload, shared by both kernels
+    if name not in _CACHE:
+        _CACHE.clear()
+        _CACHE[name] = make_config(name)
+    return _CACHE[name]
+
+
 def _sample_heads(x, limit=64):
     B, H = x.q.shape[:2]
     idx = np.linspace(0, B * H - 1, min(limit, B * H)).round().astype(int)
     return np.unique(idx)
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=_kid)
 @pytest.mark.parametrize("name", FULL)
-def test_full_config_parity(name, kernel):
-    x = make_config(name)
+@pytest.mark.parametrize("kernel", KERNELS, ids=_kid)
+def test_full_config_parity(kernel, name):
+    x = _full_inputs(name)
     got = run_gpu(x, kernel)
     B, H, T, d = x.q.shape
     heads = _sample_heads(x)
