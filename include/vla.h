@@ -44,6 +44,7 @@ extern "C" {
 #define VLA_ERR_WORKSPACE (-4)       /* workspace missing or smaller than vla_workspace_bytes() */
 #define VLA_ERR_CUDA (-5)            /* a CUDA runtime call failed; see vla_last_cuda_error() */
 #define VLA_ERR_TIMEOUT (-6)         /* a bounded device-side wait gave up (vla_device_status) */
+#define VLA_ERR_SCRATCH_LIMIT (-7)   /* vla_forward_noalloc: problem exceeds its built-in scratch */
 
 /* I/O element types of q, k, v, u and o */
 #define VLA_F32 0
@@ -121,6 +122,49 @@ int vla_set_launch_events(void *const *events, int n);
 /* Number of kernels the last successful vla_forward call on this host
  * thread launched (1 for the sequential path, 6 or 7 for the chunked one). */
 int vla_last_launch_count(void);
+
+/* Size of the device scratch array built into the library for
+ * vla_forward_noalloc (64 MiB on every GPU that loads the library). */
+#define VLA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+
+/*
+ * vla_forward_noalloc -- the chunk-parallel path of vla_forward, with its
+ * workspace taken from a scratch array compiled into the library instead of
+ * from the caller.  The pages have no counterpart: this is an integration
+ * entry point, not part of the method.
+ *
+ * Who it is for: hosts that own all device memory themselves and never let
+ * a component call cudaMalloc, for example a serving runtime that reserves
+ * its whole memory budget at start-up so that a long stream can never fail
+ * mid-sequence on an allocation and the request path never stalls in the
+ * allocator, or a plugin loaded into such a runtime that is handed only its
+ * input and output buffers.  Such callers cannot allocate a workspace to
+ * pass to vla_forward.
+ *
+ * Arguments and results are those of vla_forward with kernel =
+ * VLA_KERNEL_CHUNK (chunk: chunk length, 0 = library default); inputs and
+ * outputs are still the caller's device buffers.  The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Limits and sharing:
+ *   - Problems whose chunked workspace (vla_workspace_bytes with
+ *     VLA_KERNEL_CHUNK and the same chunk) exceeds VLA_NOALLOC_SCRATCH_BYTES
+ *     are rejected with VLA_ERR_SCRATCH_LIMIT before anything is launched.
+ *   - The array is a single static device allocation per GPU that every
+ *     call on that GPU shares, and it keeps the previous call's contents.
+ *     Nothing in it needs to start at zero: every word a call reads from it
+ *     is written earlier in the same call.  Calls that overlap on the GPU
+ *     (different streams, or different host threads without ordering)
+ *     race on the array and produce garbage; serialise them.
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address once; make that first call before any stream
+ *     capture begins.
+ * Returns VLA_OK or a VLA_ERR_* code.
+ */
+int vla_forward_noalloc(const void *q, const void *k, const void *v, const void *u, int io_dtype,
+                        float lambda0, int B, int H, int T, int d_h, const float *S0,
+                        const float *A0, const float *n0, void *o, float *S_T, float *A_T,
+                        float *n_T, int chunk, void *stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int vla_version(void);

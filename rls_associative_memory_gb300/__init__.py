@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     VLA_ERR_ALIGN,
     VLA_ERR_ARG,
     VLA_ERR_CUDA,
+    VLA_ERR_SCRATCH_LIMIT,
     VLA_ERR_TIMEOUT,
     VLA_ERR_UNSUPPORTED_DIM,
     VLA_ERR_WORKSPACE,
@@ -16,6 +17,7 @@ from ._lib import (  # noqa: F401
     VLA_KERNEL_AUTO,
     VLA_KERNEL_CHUNK,
     VLA_KERNEL_SEQ,
+    VLA_NOALLOC_SCRATCH_BYTES,
     VLA_OK,
     VLAError,
     lib,

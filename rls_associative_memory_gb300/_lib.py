@@ -24,6 +24,8 @@ VLA_ERR_ALIGN = -3
 VLA_ERR_WORKSPACE = -4
 VLA_ERR_CUDA = -5
 VLA_ERR_TIMEOUT = -6
+VLA_ERR_SCRATCH_LIMIT = -7
+VLA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 VLA_F32 = 0
 VLA_BF16 = 1
@@ -45,6 +47,8 @@ _SIGS = {
     "vla_device_status": (_i, [_vp]),
     "vla_debug_inject": (_i, [_i, ctypes.c_longlong]),
     "vla_set_launch_events": (_i, [ctypes.POINTER(_vp), _i]),
+    "vla_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, ctypes.c_float, _i, _i, _i, _i, _vp, _vp, _vp,
+                                 _vp, _vp, _vp, _vp, _i, _vp]),
     "vla_last_launch_count": (_i, []),
     "vla_version": (_i, []),
 }

@@ -65,6 +65,17 @@ int chunk_len(int B, int H, int T, int d_h, int chunk) {
 
 }  // namespace
 
+namespace vla {
+// Shared with the library's other C-ABI translation units.
+int api_check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int kernel) {
+    return check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
+}
+int api_chunk_len(int B, int H, int T, int d_h, int chunk) { return chunk_len(B, H, T, d_h, chunk); }
+int *api_device_err_word() { return device_err_word(); }
+long long api_wait_limit_ns() { return g_wait_limit_ns; }
+int api_cuda_fail(cudaError_t e) { return cuda_fail(e); }
+}  // namespace vla
+
 extern "C" {
 
 int vla_version(void) { return 100; }
@@ -78,6 +89,9 @@ const char *vla_status_str(int status) {
         case VLA_ERR_WORKSPACE: return "workspace missing or too small";
         case VLA_ERR_CUDA: return "CUDA runtime error (see vla_last_cuda_error)";
         case VLA_ERR_TIMEOUT: return "a bounded device-side wait expired";
+        case VLA_ERR_SCRATCH_LIMIT:
+            return "problem needs more scratch than vla_forward_noalloc's built-in array holds "
+                   "(VLA_NOALLOC_SCRATCH_BYTES)";
         default: return "unknown status";
     }
 }

@@ -64,6 +64,13 @@ struct ChunkLayout {
     size_t total;
 };
 
+// C-ABI helpers defined in vla_api.cu, shared by the other entry points.
+int api_check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int kernel);
+int api_chunk_len(int B, int H, int T, int d_h, int chunk);
+int *api_device_err_word();
+long long api_wait_limit_ns();
+int api_cuda_fail(cudaError_t e);
+
 // Default chunk length for a shape (chunk == 0 in the API).
 int chunk_default(int BH, int T, int d);
 // Layout for the given shape; C must be a positive multiple of 16.
