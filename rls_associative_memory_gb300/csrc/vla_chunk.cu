@@ -228,9 +228,9 @@ struct GatesSmem {
     static constexpr size_t bars = 0;
     static constexpr size_t raw = 128;                                        // [2][2][TT*D] IO (u, k)
     static constexpr size_t raw_t = (size_t)kTT * D * sizeof(IO);
-    static constexpr size_t khat = raw + 4 * raw_t;                           // [2][TT][VLEN]
-    static constexpr size_t uu = khat + 2 * kTT * R::VLEN * 4;                // [2][TT][VLEN]
-    static constexpr size_t zbuf = uu + 2 * kTT * R::VLEN * 4;                // [2][VLEN]
+    static constexpr size_t khat = raw + 4 * raw_t;                           // [TT][VLEN]
+    static constexpr size_t uu = khat + kTT * R::VLEN * 4;                    // [TT][VLEN]
+    static constexpr size_t zbuf = uu + kTT * R::VLEN * 4;                    // [2][VLEN]
     static constexpr size_t piv = zbuf + 2 * R::VLEN * 4;                     // [2][VLEN]
     static constexpr size_t red = piv + 2 * R::VLEN * 4;                      // [2][NW] float4
     static constexpr size_t total = red + 2 * R::NW * 16;
@@ -311,6 +311,9 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
         }
         gj_inverse<D>(x, s_piv, row, part);
     }
+    float2 am[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) am[j] = make_float2(x[2 * j], x[2 * j + 1]);
 
     float beta_prev = 0.f, s2_prev = 0.f, z_prev = 0.f, y_prev = 0.f;
     int failed = -1;
@@ -339,8 +342,8 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
 #pragma unroll
                 for (int mm = 0; mm < D / 32; ++mm) {
                     const int j = lane + 32 * mm;
-                    s_khat[(buf * kTT + q) * VLEN + vidx(j)] = kk[mm] * ks;
-                    s_u[(buf * kTT + q) * VLEN + vidx(j)] = io_to_f32(ru[q * D + j]);
+                    s_khat[q * VLEN + vidx(j)] = kk[mm] * ks;
+                    s_u[q * VLEN + vidx(j)] = io_to_f32(ru[q * D + j]);
                 }
             }
             __syncthreads();
@@ -350,41 +353,33 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
             }
         }
         const bool hasA = t < ntok, hasG = t > 0;
-        const int buf = m & 1;
-        const float *uA = s_u + (buf * kTT + tt) * VLEN;
-        const float *kA = s_khat + (buf * kTT + tt) * VLEN;
+        const float *uA = s_u + tt * VLEN;
+        const float *kA = s_khat + tt * VLEN;
         const float4 *zp = reinterpret_cast<const float4 *>(s_z + ((t - 1) & 1) * VLEN + vo);
-        float z0 = 0.f, z1 = 0.f, y0 = 0.f, y1 = 0.f;
+        const float2 mb = f2(-beta_prev), zi = f2(z_prev);
+        float2 za = f2(0.f), zb = f2(0.f), ya = f2(0.f), yb = f2(0.f);
         if (hasA) {
             const float4 *up = reinterpret_cast<const float4 *>(uA + vo);
             const float4 *kp = reinterpret_cast<const float4 *>(kA + vo);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 zz = zp[q], u4 = up[q], k4 = kp[q];
-                x[4 * q + 0] = fmaf(-beta_prev, z_prev * zz.x, x[4 * q + 0]);
-                x[4 * q + 1] = fmaf(-beta_prev, z_prev * zz.y, x[4 * q + 1]);
-                x[4 * q + 2] = fmaf(-beta_prev, z_prev * zz.z, x[4 * q + 2]);
-                x[4 * q + 3] = fmaf(-beta_prev, z_prev * zz.w, x[4 * q + 3]);
-                z0 = fmaf(x[4 * q + 0], u4.x, z0);
-                z1 = fmaf(x[4 * q + 1], u4.y, z1);
-                z0 = fmaf(x[4 * q + 2], u4.z, z0);
-                z1 = fmaf(x[4 * q + 3], u4.w, z1);
-                y0 = fmaf(x[4 * q + 0], k4.x, y0);
-                y1 = fmaf(x[4 * q + 1], k4.y, y1);
-                y0 = fmaf(x[4 * q + 2], k4.z, y0);
-                y1 = fmaf(x[4 * q + 3], k4.w, y1);
+                am[2 * q] = fma2(mb, mul2(zi, lo2(zz)), am[2 * q]);
+                am[2 * q + 1] = fma2(mb, mul2(zi, hi2(zz)), am[2 * q + 1]);
+                za = fma2(am[2 * q], lo2(u4), za);
+                zb = fma2(am[2 * q + 1], hi2(u4), zb);
+                ya = fma2(am[2 * q], lo2(k4), ya);
+                yb = fma2(am[2 * q + 1], hi2(k4), yb);
             }
         } else {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const float4 zz = zp[q];
-                x[4 * q + 0] = fmaf(-beta_prev, z_prev * zz.x, x[4 * q + 0]);
-                x[4 * q + 1] = fmaf(-beta_prev, z_prev * zz.y, x[4 * q + 1]);
-                x[4 * q + 2] = fmaf(-beta_prev, z_prev * zz.z, x[4 * q + 2]);
-                x[4 * q + 3] = fmaf(-beta_prev, z_prev * zz.w, x[4 * q + 3]);
+                am[2 * q] = fma2(mb, mul2(zi, lo2(zz)), am[2 * q]);
+                am[2 * q + 1] = fma2(mb, mul2(zi, hi2(zz)), am[2 * q + 1]);
             }
         }
-        float z = z0 + z1, y = y0 + y1;
+        float z = hsum2(add2(za, zb)), y = hsum2(add2(ya, yb));
 #pragma unroll
         for (int o = 1; o < TPR; o <<= 1) {
             z += __shfl_xor_sync(0xffffffffu, z, o);
@@ -400,11 +395,9 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
             }
             if (hasG) p3 = g * g;
         }
-        p1 = warp_sum(p1);
-        p2 = warp_sum(p2);
-        p3 = warp_sum(p3);
+        const float red = warp_reduce4(p1, p2, p3, 0.f);
         if constexpr (NW > 1) {
-            if (lane == 0) s_red[(t & 1) * NW + warp] = make_float4(p1, p2, p3, 0.f);
+            if ((lane & 7) == 0) reinterpret_cast<float *>(s_red)[((t & 1) * NW + warp) * 4 + (lane >> 3)] = red;
             __syncthreads();
             float4 acc = s_red[(t & 1) * NW];
 #pragma unroll
@@ -414,9 +407,12 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
             }
             p1 = acc.x; p2 = acc.y; p3 = acc.z;
         } else {
+            p1 = __shfl_sync(0xffffffffu, red, 0);
+            p2 = __shfl_sync(0xffffffffu, red, 8);
+            p3 = __shfl_sync(0xffffffffu, red, 16);
             __syncwarp();
         }
-        if (hasG && part == 0) galpha[(size_t)(t - 1) * D + row] = g * (1.f / fmaxf(sqrtf(p3), kEps));
+        if (hasG && part == 0) galpha[(size_t)(t - 1) * D + row] = g * fminf(rsqrtf(p3), 1.f / kEps);
         beta_prev = 1.f / (1.f + p1);
         s2_prev = p2;
         z_prev = z;
@@ -431,7 +427,7 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
     if (c == NC - 1) {
         float4 *dA = reinterpret_cast<float4 *>(a.p.A_T + (size_t)bh * D * D + row * D + c0);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) dA[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        for (int q = 0; q < 8; ++q) dA[q] = make_float4(am[2 * q].x, am[2 * q].y, am[2 * q + 1].x, am[2 * q + 1].y);
     }
 }
 
@@ -447,13 +443,13 @@ struct RowsSmem {
     static constexpr size_t raw = 128;                                   // [2][3][TT*D] IO (q, k, v)
     static constexpr size_t raw_t = (size_t)kTT * D * sizeof(IO);
     static constexpr size_t ral = raw + 6 * raw_t;                       // [2][TT*D] fp32 gates
-    static constexpr size_t khat = ral + 2 * (size_t)kTT * D * 4;        // [2][TT][VLEN]
-    static constexpr size_t alp = khat + 2 * kTT * R::VLEN * 4;          // [2][TT][VLEN]
-    static constexpr size_t phiq = alp + 2 * kTT * R::VLEN * 4;          // [2][TT][VLEN]
-    static constexpr size_t vv = phiq + 2 * kTT * R::VLEN * 4;           // [2][TT][D]
-    static constexpr size_t den = vv + 2 * (size_t)kTT * D * 4;          // [2][TT]
-    static constexpr size_t ga = den + 2 * kTT * 4;                      // [2][TT]
-    static constexpr size_t work = ga + 2 * kTT * 4;                     // [TT][D]
+    static constexpr size_t khat = ral + 2 * (size_t)kTT * D * 4;        // [TT][VLEN]
+    static constexpr size_t alp = khat + kTT * R::VLEN * 4;              // [TT][VLEN]
+    static constexpr size_t phiq = alp + kTT * R::VLEN * 4;              // [TT][VLEN]
+    static constexpr size_t vv = phiq + kTT * R::VLEN * 4;               // [TT][D]
+    static constexpr size_t den = vv + (size_t)kTT * D * 4;              // [TT] reciprocal denominators
+    static constexpr size_t ga = den + kTT * 4;                          // [TT]
+    static constexpr size_t work = ga + kTT * 4;                         // [TT][D]
     static constexpr size_t total = work + (size_t)kTT * D * 4;
 };
 
@@ -527,13 +523,13 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
     }
 
     // row state
-    float h[32], p[32];
+    float2 h[16], p[16];  // columns 2j, 2j+1 of this thread's 32
     const size_t moff = (size_t)row * D + c0;
     if (MODE == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            h[j] = 0.f;
-            p[j] = (c0 + j == row) ? 1.f : 0.f;
+        for (int j = 0; j < 16; ++j) {
+            h[j] = f2(0.f);
+            p[j] = make_float2((c0 + 2 * j == row) ? 1.f : 0.f, (c0 + 2 * j + 1 == row) ? 1.f : 0.f);
         }
     } else {
         const float4 *src = reinterpret_cast<const float4 *>(
@@ -541,7 +537,8 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const float4 v = src[q];
-            h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+            h[2 * q] = lo2(v);
+            h[2 * q + 1] = hi2(v);
         }
     }
     float nbase = 0.f;
@@ -562,10 +559,10 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
         const IO *rv = raw + ((size_t)buf * 3 + 1) * kTT * D;
         const IO *rq = raw + ((size_t)buf * 3 + 2) * kTT * D;
         const float *ra = s_ral + (size_t)buf * kTT * D;
-        float *khat = s_khat + buf * kTT * VLEN;
-        float *alp = s_alp + buf * kTT * VLEN;
-        float *phiq = s_phiq + buf * kTT * VLEN;
-        float *vv = s_v + buf * kTT * D;
+        float *khat = s_khat;
+        float *alp = s_alp;
+        float *phiq = s_phiq;
+        float *vv = s_v;
         for (int q = warp; q < nt; q += NW) {
             float kk[D / 32], ss = 0.f;
 #pragma unroll
@@ -593,7 +590,7 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
             }
             if (MODE == 1) {
                 gdot = warp_sum(gdot);
-                if (lane == 0) s_ga[buf * kTT + q] = gdot;
+                if (lane == 0) s_ga[q] = gdot;
             }
         }
         __syncthreads();
@@ -612,7 +609,7 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
 #pragma unroll
                 for (int mm = 0; mm < D / 32; ++mm) sacc += s_work[q * D + lane + 32 * mm];
                 sacc = warp_sum(sacc);
-                if (lane == 0) s_den[buf * kTT + q] = sacc + kEps;
+                if (lane == 0) s_den[q] = 1.f / (sacc + kEps);
             }
             __syncthreads();
         }
@@ -626,75 +623,62 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
             const float4 *ap = reinterpret_cast<const float4 *>(alp + q * VLEN + vo);
             const float vi = vv[q * D + row];
             if (MODE == 0) {
-                float h0 = 0.f, h1 = 0.f, p0 = 0.f, p1 = 0.f;
+                float2 ha = f2(0.f), hb = f2(0.f), pa = f2(0.f), pb = f2(0.f);
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
                     const float4 k4 = kp[w];
-                    h0 = fmaf(h[4 * w + 0], k4.x, h0);
-                    h1 = fmaf(h[4 * w + 1], k4.y, h1);
-                    h0 = fmaf(h[4 * w + 2], k4.z, h0);
-                    h1 = fmaf(h[4 * w + 3], k4.w, h1);
-                    p0 = fmaf(p[4 * w + 0], k4.x, p0);
-                    p1 = fmaf(p[4 * w + 1], k4.y, p1);
-                    p0 = fmaf(p[4 * w + 2], k4.z, p0);
-                    p1 = fmaf(p[4 * w + 3], k4.w, p1);
+                    ha = fma2(h[2 * w], lo2(k4), ha);
+                    hb = fma2(h[2 * w + 1], hi2(k4), hb);
+                    pa = fma2(p[2 * w], lo2(k4), pa);
+                    pb = fma2(p[2 * w + 1], hi2(k4), pb);
                 }
-                float hk = h0 + h1, pk = p0 + p1;
+                float hk = hsum2(add2(ha, hb)), pk = hsum2(add2(pa, pb));
 #pragma unroll
                 for (int o = 1; o < TPR; o <<= 1) {
                     hk += __shfl_xor_sync(0xffffffffu, hk, o);
                     pk += __shfl_xor_sync(0xffffffffu, pk, o);
                 }
-                const float rh = vi - hk, rp = -pk;
+                const float2 rh = f2(vi - hk), rp = f2(-pk);
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
                     const float4 a4 = ap[w];
-                    h[4 * w + 0] = fmaf(rh, a4.x, h[4 * w + 0]);
-                    h[4 * w + 1] = fmaf(rh, a4.y, h[4 * w + 1]);
-                    h[4 * w + 2] = fmaf(rh, a4.z, h[4 * w + 2]);
-                    h[4 * w + 3] = fmaf(rh, a4.w, h[4 * w + 3]);
-                    p[4 * w + 0] = fmaf(rp, a4.x, p[4 * w + 0]);
-                    p[4 * w + 1] = fmaf(rp, a4.y, p[4 * w + 1]);
-                    p[4 * w + 2] = fmaf(rp, a4.z, p[4 * w + 2]);
-                    p[4 * w + 3] = fmaf(rp, a4.w, p[4 * w + 3]);
+                    h[2 * w] = fma2(rh, lo2(a4), h[2 * w]);
+                    h[2 * w + 1] = fma2(rh, hi2(a4), h[2 * w + 1]);
+                    p[2 * w] = fma2(rp, lo2(a4), p[2 * w]);
+                    p[2 * w + 1] = fma2(rp, hi2(a4), p[2 * w + 1]);
                 }
             } else {
                 const float4 *fp = reinterpret_cast<const float4 *>(phiq + q * VLEN + vo);
-                float k0 = 0.f, k1 = 0.f, f0 = 0.f, f1 = 0.f;
+                float2 ka = f2(0.f), kb = f2(0.f), fa = f2(0.f), fb = f2(0.f);
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
                     const float4 k4 = kp[w], f4 = fp[w];
-                    k0 = fmaf(h[4 * w + 0], k4.x, k0);
-                    k1 = fmaf(h[4 * w + 1], k4.y, k1);
-                    k0 = fmaf(h[4 * w + 2], k4.z, k0);
-                    k1 = fmaf(h[4 * w + 3], k4.w, k1);
-                    f0 = fmaf(h[4 * w + 0], f4.x, f0);
-                    f1 = fmaf(h[4 * w + 1], f4.y, f1);
-                    f0 = fmaf(h[4 * w + 2], f4.z, f0);
-                    f1 = fmaf(h[4 * w + 3], f4.w, f1);
+                    ka = fma2(h[2 * w], lo2(k4), ka);
+                    kb = fma2(h[2 * w + 1], hi2(k4), kb);
+                    fa = fma2(h[2 * w], lo2(f4), fa);
+                    fb = fma2(h[2 * w + 1], hi2(f4), fb);
                 }
-                float sk = k0 + k1, sq = f0 + f1;
+                float sk = hsum2(add2(ka, kb)), sq = hsum2(add2(fa, fb));
 #pragma unroll
                 for (int o = 1; o < TPR; o <<= 1) {
                     sk += __shfl_xor_sync(0xffffffffu, sk, o);
                     sq += __shfl_xor_sync(0xffffffffu, sq, o);
                 }
                 const float r = vi - sk;
+                const float2 r2 = f2(r);
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
                     const float4 a4 = ap[w];
-                    h[4 * w + 0] = fmaf(r, a4.x, h[4 * w + 0]);
-                    h[4 * w + 1] = fmaf(r, a4.y, h[4 * w + 1]);
-                    h[4 * w + 2] = fmaf(r, a4.z, h[4 * w + 2]);
-                    h[4 * w + 3] = fmaf(r, a4.w, h[4 * w + 3]);
+                    h[2 * w] = fma2(r2, lo2(a4), h[2 * w]);
+                    h[2 * w + 1] = fma2(r2, hi2(a4), h[2 * w + 1]);
                 }
                 if (part == 0) {
-                    const float num = fmaf(r, s_ga[buf * kTT + q], sq);
-                    gout[(size_t)(m * kTT + q) * D + row] = f32_to_io<IO>(num / s_den[buf * kTT + q]);
+                    const float num = fmaf(r, s_ga[q], sq);
+                    gout[(size_t)(m * kTT + q) * D + row] = f32_to_io<IO>(num * s_den[q]);
                 }
             }
         }
-        __syncthreads();
+        __syncthreads();  // the next tile's preprocessing overwrites the processed arrays
     }
     if (failed >= 0) {
         if (tid == 0)
@@ -707,8 +691,8 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
         float4 *dH = reinterpret_cast<float4 *>(ws_f(a, a.L.off_H) + ((size_t)bh * NC + c) * D * D + moff);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            dP[q] = make_float4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
-            dH[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+            dP[q] = make_float4(p[2 * q].x, p[2 * q].y, p[2 * q + 1].x, p[2 * q + 1].y);
+            dH[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
         }
     }
 }
@@ -886,7 +870,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int chunk_default(int BH, int T, int d) {
     (void)d;
-    int C = T >= 4096 ? 256 : (T >= 1024 ? 128 : 64);
+    int C = T >= 16384 ? 512 : (T >= 4096 ? 256 : (T >= 1024 ? 128 : 64));
     while (C > 64 && (long long)BH * ((T + C - 1) / C) < 2 * 152) C /= 2;
     return C;
 }

@@ -149,6 +149,36 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Packed fp32 pairs (sm_100 family FFMA2/FMUL2: one instruction, two IEEE
+// single-precision results).
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float hsum2(float2 a) { return a.x + a.y; }
+
+// Warp reduction of four values at once with six shuffles (transpose
+// reduction): afterwards lane L holds the warp-wide sum of value number
+// 2 * bit4(L) + bit3(L); lanes 0, 8, 16 and 24 hold the sums of v0..v3.
+__device__ __forceinline__ float warp_reduce4(float v0, float v1, float v2, float v3) {
+    const int lane = threadIdx.x & 31;
+    const bool hi16 = lane & 16;
+    float a0 = hi16 ? v2 : v0, a1 = hi16 ? v3 : v1;
+    const float s0 = hi16 ? v0 : v2, s1 = hi16 ? v1 : v3;
+    a0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    a1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    const bool hi8 = lane & 8;
+    float b = hi8 ? a1 : a0;
+    const float sb = hi8 ? a0 : a1;
+    b += __shfl_xor_sync(0xffffffffu, sb, 8);
+    b += __shfl_xor_sync(0xffffffffu, b, 4);
+    b += __shfl_xor_sync(0xffffffffu, b, 2);
+    b += __shfl_xor_sync(0xffffffffu, b, 1);
+    return b;
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

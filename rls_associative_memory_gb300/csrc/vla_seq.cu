@@ -64,8 +64,8 @@ struct SeqSmem {
 };
 
 // Per-tile preprocessing (all threads).  raw: the four tensor tiles of ntok
-// tokens; writes k_hat, phi(q), u (skewed fp32 vectors), v, and the readout
-// denominators.  nbase/ncomp (threads tid < D): Kahan-compensated running
+// tokens; writes k_hat, phi(q), u (skewed fp32 vectors), v, and the
+// reciprocals of the readout denominators.  nbase/ncomp (threads tid < D): Kahan-compensated running
 // sum of phi(k_hat) over previous tiles, column tid.
 template <int D, typename IO>
 __device__ __forceinline__ void preprocess_tile(const IO *raw, size_t raw_stride, int ntok, float *khat,
@@ -115,7 +115,7 @@ __device__ __forceinline__ void preprocess_tile(const IO *raw, size_t raw_stride
 #pragma unroll
         for (int m = 0; m < M; ++m) sacc += work[tt * D + lane + 32 * m];
         sacc = warp_sum(sacc);
-        if (lane == 0) den[tt] = sacc + kEps;
+        if (lane == 0) den[tt] = 1.f / (sacc + kEps);  // stored as the reciprocal
     }
 }
 
@@ -150,30 +150,33 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT, (D == 128) ? 1 : 2) seq_kernel(
     IO *gout = static_cast<IO *>(p.o) + tok0;
 
     // ---- initial state (thread-owned slices) ----
-    float a[32], s[32];
+    float2 a[16], s[16];  // columns 2j, 2j+1 of this thread's 32
     const size_t moff = (size_t)bh * D * D + (size_t)row * D + c0;
     if (p.A0) {
         const float4 *src = reinterpret_cast<const float4 *>(p.A0 + moff);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const float4 x = src[c];
-            a[4 * c] = x.x; a[4 * c + 1] = x.y; a[4 * c + 2] = x.z; a[4 * c + 3] = x.w;
+            a[2 * c] = lo2(x);
+            a[2 * c + 1] = hi2(x);
         }
     } else {
         const float inv_l = 1.f / p.lambda0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) a[j] = (c0 + j == row) ? inv_l : 0.f;
+        for (int j = 0; j < 16; ++j)
+            a[j] = make_float2((c0 + 2 * j == row) ? inv_l : 0.f, (c0 + 2 * j + 1 == row) ? inv_l : 0.f);
     }
     if (p.S0) {
         const float4 *src = reinterpret_cast<const float4 *>(p.S0 + moff);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const float4 x = src[c];
-            s[4 * c] = x.x; s[4 * c + 1] = x.y; s[4 * c + 2] = x.z; s[4 * c + 3] = x.w;
+            s[2 * c] = lo2(x);
+            s[2 * c + 1] = hi2(x);
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) s[j] = 0.f;
+        for (int j = 0; j < 16; ++j) s[j] = f2(0.f);
     }
     float nbase = 0.f, ncomp = 0.f;
     if (tid < D && p.n0) nbase = p.n0[(size_t)bh * D + tid];
@@ -241,55 +244,45 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT, (D == 128) ? 1 : 2) seq_kernel(
 
         // ---- A chain: rank-1 update of token t-1, then z_t = A u_t, y_t = A k_hat_t ----
         const float4 *zp = reinterpret_cast<const float4 *>(s_z + ((t - 1) & 1) * VLEN + vo);
-        float z0 = 0.f, z1 = 0.f, y0 = 0.f, y1 = 0.f;
+        const float2 mb = f2(-beta_prev), zi = f2(z_prev);
+        float2 za = f2(0.f), zb = f2(0.f), ya = f2(0.f), yb = f2(0.f);
         if (hasA) {
             const float4 *up = reinterpret_cast<const float4 *>(uA + vo);
             const float4 *kp = reinterpret_cast<const float4 *>(kA + vo);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 zz = zp[c], uu4 = up[c], kk = kp[c];
-                a[4 * c + 0] = fmaf(-beta_prev, z_prev * zz.x, a[4 * c + 0]);
-                a[4 * c + 1] = fmaf(-beta_prev, z_prev * zz.y, a[4 * c + 1]);
-                a[4 * c + 2] = fmaf(-beta_prev, z_prev * zz.z, a[4 * c + 2]);
-                a[4 * c + 3] = fmaf(-beta_prev, z_prev * zz.w, a[4 * c + 3]);
-                z0 = fmaf(a[4 * c + 0], uu4.x, z0);
-                z1 = fmaf(a[4 * c + 1], uu4.y, z1);
-                z0 = fmaf(a[4 * c + 2], uu4.z, z0);
-                z1 = fmaf(a[4 * c + 3], uu4.w, z1);
-                y0 = fmaf(a[4 * c + 0], kk.x, y0);
-                y1 = fmaf(a[4 * c + 1], kk.y, y1);
-                y0 = fmaf(a[4 * c + 2], kk.z, y0);
-                y1 = fmaf(a[4 * c + 3], kk.w, y1);
+                a[2 * c] = fma2(mb, mul2(zi, lo2(zz)), a[2 * c]);
+                a[2 * c + 1] = fma2(mb, mul2(zi, hi2(zz)), a[2 * c + 1]);
+                za = fma2(a[2 * c], lo2(uu4), za);
+                zb = fma2(a[2 * c + 1], hi2(uu4), zb);
+                ya = fma2(a[2 * c], lo2(kk), ya);
+                yb = fma2(a[2 * c + 1], hi2(kk), yb);
             }
         } else {
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 zz = zp[c];
-                a[4 * c + 0] = fmaf(-beta_prev, z_prev * zz.x, a[4 * c + 0]);
-                a[4 * c + 1] = fmaf(-beta_prev, z_prev * zz.y, a[4 * c + 1]);
-                a[4 * c + 2] = fmaf(-beta_prev, z_prev * zz.z, a[4 * c + 2]);
-                a[4 * c + 3] = fmaf(-beta_prev, z_prev * zz.w, a[4 * c + 3]);
+                a[2 * c] = fma2(mb, mul2(zi, lo2(zz)), a[2 * c]);
+                a[2 * c + 1] = fma2(mb, mul2(zi, hi2(zz)), a[2 * c + 1]);
             }
         }
         // ---- S chain reads: S_{t-2} k_hat_{t-1}, S_{t-2} phi(q_{t-1}) ----
-        float k0 = 0.f, k1 = 0.f, q0 = 0.f, q1 = 0.f;
+        float2 ka = f2(0.f), kb = f2(0.f), qa = f2(0.f), qb = f2(0.f);
         if (hasS) {
             const float4 *kp = reinterpret_cast<const float4 *>(kS + vo);
             const float4 *fp = reinterpret_cast<const float4 *>(fS + vo);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 kk = kp[c], ff = fp[c];
-                k0 = fmaf(s[4 * c + 0], kk.x, k0);
-                k1 = fmaf(s[4 * c + 1], kk.y, k1);
-                k0 = fmaf(s[4 * c + 2], kk.z, k0);
-                k1 = fmaf(s[4 * c + 3], kk.w, k1);
-                q0 = fmaf(s[4 * c + 0], ff.x, q0);
-                q1 = fmaf(s[4 * c + 1], ff.y, q1);
-                q0 = fmaf(s[4 * c + 2], ff.z, q0);
-                q1 = fmaf(s[4 * c + 3], ff.w, q1);
+                ka = fma2(s[2 * c], lo2(kk), ka);
+                kb = fma2(s[2 * c + 1], hi2(kk), kb);
+                qa = fma2(s[2 * c], lo2(ff), qa);
+                qb = fma2(s[2 * c + 1], hi2(ff), qb);
             }
         }
-        float z = z0 + z1, y = y0 + y1, skv = k0 + k1, sqv = q0 + q1;
+        float z = hsum2(add2(za, zb)), y = hsum2(add2(ya, yb));
+        float skv = hsum2(add2(ka, kb)), sqv = hsum2(add2(qa, qb));
 #pragma unroll
         for (int o = 1; o < TPR; o <<= 1) {
             z += __shfl_xor_sync(0xffffffffu, z, o);
@@ -312,12 +305,9 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT, (D == 128) ? 1 : 2) seq_kernel(
                 s_g[((t - 1) & 1) * VLEN + vidx(row)] = g;
             }
         }
-        p1 = warp_sum(p1);
-        p2 = warp_sum(p2);
-        p3 = warp_sum(p3);
-        p4 = warp_sum(p4);
+        const float red = warp_reduce4(p1, p2, p3, p4);  // lanes 0/8/16/24: sums of p1..p4
         if constexpr (NW > 1) {
-            if (lane == 0) s_red[(t & 1) * NW + warp] = make_float4(p1, p2, p3, p4);
+            if ((lane & 7) == 0) reinterpret_cast<float *>(s_red)[((t & 1) * NW + warp) * 4 + (lane >> 3)] = red;
             __syncthreads();
             float4 acc = s_red[(t & 1) * NW];
 #pragma unroll
@@ -327,26 +317,29 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT, (D == 128) ? 1 : 2) seq_kernel(
             }
             p1 = acc.x; p2 = acc.y; p3 = acc.z; p4 = acc.w;
         } else {
+            p1 = __shfl_sync(0xffffffffu, red, 0);
+            p2 = __shfl_sync(0xffffffffu, red, 8);
+            p3 = __shfl_sync(0xffffffffu, red, 16);
+            p4 = __shfl_sync(0xffffffffu, red, 24);
             __syncwarp();
         }
         const float beta = 1.f / (1.f + p1);
         if (hasS) {
             // ---- state write and readout of token t-1 ----
-            const float inv = 1.f / fmaxf(sqrtf(p3), kEps);
+            const float inv = fminf(rsqrtf(p3), 1.f / kEps);  // 1 / max(|g|, eps)
             const float r = s_v[(bufS * TT + ttS) * D + row] - skv;
             const float ri = r * inv;
+            const float2 ri2 = f2(ri);
             const float4 *gp = reinterpret_cast<const float4 *>(s_g + ((t - 1) & 1) * VLEN + vo);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 gg = gp[c];
-                s[4 * c + 0] = fmaf(ri, gg.x, s[4 * c + 0]);
-                s[4 * c + 1] = fmaf(ri, gg.y, s[4 * c + 1]);
-                s[4 * c + 2] = fmaf(ri, gg.z, s[4 * c + 2]);
-                s[4 * c + 3] = fmaf(ri, gg.w, s[4 * c + 3]);
+                s[2 * c] = fma2(ri2, lo2(gg), s[2 * c]);
+                s[2 * c + 1] = fma2(ri2, hi2(gg), s[2 * c + 1]);
             }
             if (part == 0) {
                 const float num = fmaf(ri, p4, sqv);
-                gout[(size_t)tS * D + row] = f32_to_io<IO>(num / s_den[bufS * TT + ttS]);
+                gout[(size_t)tS * D + row] = f32_to_io<IO>(num * s_den[bufS * TT + ttS]);
             }
         }
         beta_prev = beta;
@@ -370,8 +363,8 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT, (D == 128) ? 1 : 2) seq_kernel(
         float4 *dS = reinterpret_cast<float4 *>(p.S_T + moff);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            dA[c] = make_float4(a[4 * c], a[4 * c + 1], a[4 * c + 2], a[4 * c + 3]);
-            dS[c] = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+            dA[c] = make_float4(a[2 * c].x, a[2 * c].y, a[2 * c + 1].x, a[2 * c + 1].y);
+            dS[c] = make_float4(s[2 * c].x, s[2 * c].y, s[2 * c + 1].x, s[2 * c + 1].y);
         }
         if (tid < D && p.n_T) p.n_T[(size_t)bh * D + tid] = nbase;
     }
