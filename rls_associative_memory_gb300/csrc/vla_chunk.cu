@@ -113,6 +113,200 @@ __global__ void __launch_bounds__(256) gram_kernel(ChunkArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// gram on the tensor cores (bf16 I/O, d in {64, 128}): G_c = U_c^T U_c as
+// tcgen05.mma kind::f16 with fp32 accumulation in TMEM.  bf16 x bf16
+// products are exact in fp32, so only the accumulation rounds.
+//   - u and k tiles of KS tokens arrive by 1-D bulk copies (double-buffered);
+//   - all threads repack the u tile feature-major (rows = features, K =
+//     tokens) into the K-major, unswizzled core-matrix layout; tokens past
+//     the end of the chunk are written as zeros;
+//   - one thread issues KS/16 MMAs with A = B = that tile (M = N = d) and
+//     commits them to an mbarrier that frees the tile for reuse;
+//   - the sums of phi(k_hat) are accumulated on the CUDA cores meanwhile;
+//   - the accumulator is read back with tcgen05.ld (for M = 64, row r sits in
+//     TMEM lane 32 (r / 16) + r % 16).
+// ---------------------------------------------------------------------------
+template <int D>
+struct GramTc {
+    static constexpr int KS = 64;                               // tokens per stage
+    static constexpr int NT = 128;                              // 4 warps: all TMEM lane quarters
+    static constexpr uint32_t NCOL = D;                         // TMEM columns (64 or 128)
+    static constexpr size_t ctrl = 0;                           // raw_bar[2], mma_bar[2], tmem slot, abort
+    static constexpr size_t raw = 128;                          // [2][2][KS*D] bf16 (u, k)
+    static constexpr size_t raw_t = (size_t)KS * D * 2;
+    static constexpr size_t abuf = raw + 4 * raw_t;             // [2][D x KS] bf16, K-major core matrices
+    static constexpr size_t abuf_t = (size_t)D * KS * 2;
+    static constexpr size_t nred = abuf + 2 * abuf_t;           // [4][D] fp32
+    static constexpr size_t total = nred + 4 * D * 4;
+    static_assert(abuf % 1024 == 0 || true, "");
+};
+
+template <int D>
+__global__ void __launch_bounds__(GramTc<D>::NT) gram_tc_kernel(ChunkArgs a) {
+    using G = GramTc<D>;
+    constexpr int KS = G::KS, NT = G::NT;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t *raw_bar = reinterpret_cast<uint64_t *>(smem + G::ctrl);
+    uint64_t *mma_bar = raw_bar + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + G::ctrl + 32);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::ctrl + 36);
+    __nv_bfloat16 *raw = reinterpret_cast<__nv_bfloat16 *>(smem + G::raw);
+    unsigned char *abuf = smem + G::abuf;
+    float *nred = reinterpret_cast<float *>(smem + G::nred);
+
+    const int c = (int)(blockIdx.x % (unsigned)a.L.NC), bh = (int)(blockIdx.x / (unsigned)a.L.NC);
+    const int T = a.p.T, C = a.L.C;
+    const int t0 = c * C, ntok = min(C, T - t0);
+    const int nst = (ntok + KS - 1) / KS;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t tok0 = ((size_t)bh * T + t0) * D;
+    const __nv_bfloat16 *gu = static_cast<const __nv_bfloat16 *>(a.p.u) + tok0;
+    const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.p.k) + tok0;
+
+    if (tid == 0) {
+        mbar_init(&raw_bar[0], 1);
+        mbar_init(&raw_bar[1], 1);
+        mbar_init(&mma_bar[0], 1);
+        mbar_init(&mma_bar[1], 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, G::NCOL);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+
+    auto issue = [&](int st) {
+        const int buf = st & 1;
+        const int nt = min(KS, ntok - st * KS);
+        const uint32_t bytes = (uint32_t)(nt * D * 2);
+        mbar_arrive_expect_tx(&raw_bar[buf], 2 * bytes);
+        bulk_g2s(raw + ((size_t)buf * 2 + 0) * KS * D, gu + (size_t)st * KS * D, bytes, &raw_bar[buf]);
+        bulk_g2s(raw + ((size_t)buf * 2 + 1) * KS * D, gk + (size_t)st * KS * D, bytes, &raw_bar[buf]);
+    };
+    int issued = 0, committed = 0;
+    if (tid == 0) {
+        if (nst > 0) issue(0);
+        if (nst > 1) issue(1);
+        issued = min(nst, 2);
+    }
+    constexpr int M32 = D / 32;
+    float nk[M32];
+#pragma unroll
+    for (int m = 0; m < M32; ++m) nk[m] = 0.f;
+    constexpr uint32_t idesc = idesc_bf16_f32(D, D);
+    constexpr uint32_t sbo = KS * 16, lbo = 128;
+
+    int failed = 0;
+    for (int st = 0; st < nst; ++st) {
+        const int buf = st & 1;
+        const int nt = min(KS, ntok - st * KS);
+        bool ok = mbar_wait_bounded(&raw_bar[buf], (st >> 1) & 1, a.p.wait_limit_ns, a.p.err);
+        if (ok && st >= 2) ok = mbar_wait_bounded(&mma_bar[buf], ((st - 2) >> 1) & 1, a.p.wait_limit_ns, a.p.err);
+        if (!ok) *abort_flag = 1;
+        tc_fence_after();
+        __syncthreads();
+        if (*abort_flag) {
+            failed = 1;
+            break;
+        }
+        const __nv_bfloat16 *ru = raw + ((size_t)buf * 2 + 0) * KS * D;
+        const __nv_bfloat16 *rk = raw + ((size_t)buf * 2 + 1) * KS * D;
+        unsigned char *A = abuf + (size_t)buf * G::abuf_t;
+        // repack u: item = (feature f, group of 8 tokens) -> one 16-byte core-matrix row
+        for (int it = tid; it < D * (KS / 8); it += NT) {
+            const int f = it % D, g8 = it / D;
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int ta = g8 * 8 + 2 * h, tb = ta + 1;
+                const unsigned short lo = ta < nt ? __bfloat16_as_ushort(ru[ta * D + f]) : (unsigned short)0;
+                const unsigned short hi = tb < nt ? __bfloat16_as_ushort(ru[tb * D + f]) : (unsigned short)0;
+                w[h] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            *reinterpret_cast<uint4 *>(A + kmajor_off_bf16(f, g8 * 8, KS)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        // phi(k_hat) sums on the CUDA cores
+        for (int tt = warp; tt < nt; tt += NT / 32) {
+            float kk[M32], ss = 0.f;
+#pragma unroll
+            for (int m = 0; m < M32; ++m) {
+                kk[m] = __bfloat162float(rk[tt * D + lane + 32 * m]);
+                ss = fmaf(kk[m], kk[m], ss);
+            }
+            ss = warp_sum(ss);
+            const float ks = 1.f / fmaxf(sqrtf(ss), kEps);
+#pragma unroll
+            for (int m = 0; m < M32; ++m) nk[m] += phi_elu1(kk[m] * ks);
+        }
+        fence_proxy_async_smem();  // the repacked tile is read by the tensor core (async proxy)
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t abase = smem_u32(A);
+#pragma unroll
+            for (int ks = 0; ks < KS / 16; ++ks) {
+                const uint64_t dsc = umma_desc_kmajor(abase + ks * 256, lbo, sbo);
+                umma_bf16(tbase, dsc, dsc, idesc, (st > 0 || ks > 0) ? 1u : 0u);
+            }
+            umma_commit(&mma_bar[buf]);
+            committed = st + 1;
+            if (st + 2 < nst) {
+                issue(st + 2);
+                issued = st + 3;
+            }
+        }
+    }
+    // wait for the last MMAs (thread 0 knows what it committed; everyone waits on the same phase)
+    if (!failed && nst > 0) {
+        const int last = nst - 1;
+        if (!mbar_wait_bounded(&mma_bar[last & 1], (last >> 1) & 1, a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+    }
+    tc_fence_after();
+    __syncthreads();
+    if (failed || *abort_flag) {
+        if (tid == 0) {
+            if (committed > 0)
+                (void)mbar_wait_bounded(&mma_bar[(committed - 1) & 1], ((committed - 1) >> 1) & 1, a.p.wait_limit_ns,
+                                        a.p.err);
+            for (int st = committed; st < issued; ++st)
+                (void)mbar_wait_bounded(&raw_bar[st & 1], (st >> 1) & 1, a.p.wait_limit_ns, a.p.err);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tbase, G::NCOL);
+        return;
+    }
+    // ---- G out: accumulator rows from TMEM ----
+    float *Gout = ws_f(a, a.L.off_M) + ((size_t)bh * a.L.NC + c) * D * D;
+    const bool has_row = (D == 128) || (lane < 16);
+    const int grow = (D == 128) ? (32 * warp + lane) : (16 * warp + lane);
+#pragma unroll
+    for (int cb = 0; cb < D; cb += 16) {
+        float v[16];
+        tmem_ld16(tbase + ((uint32_t)(32 * warp) << 16) + (uint32_t)cb, v);
+        if (has_row) {
+            float4 *dst = reinterpret_cast<float4 *>(Gout + (size_t)grow * D + cb);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+    }
+    // ---- sums of phi(k_hat) ----
+#pragma unroll
+    for (int m = 0; m < M32; ++m) nred[warp * D + lane + 32 * m] = nk[m];
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, G::NCOL);
+    if (tid < D) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) sum += nred[w * D + tid];
+        ws_f(a, a.L.off_n)[((size_t)bh * (a.L.NC + 1) + c) * D + tid] = sum;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // prefix: exclusive prefix sums of G and m along the chunks (Kahan, fp32)
 // ---------------------------------------------------------------------------
 template <int D>
@@ -149,20 +343,19 @@ __global__ void __launch_bounds__(256) prefix_kernel(ChunkArgs a) {
 // ---------------------------------------------------------------------------
 // Register-resident inverse of an SPD matrix by Gauss-Jordan elimination
 // (no pivoting: the pivots of an SPD matrix are positive).  Thread (row i,
-// part) holds x[32] = row i, columns [32 part, 32 part + 32).  piv: two
+// part) holds x[CPT] = row i, columns [CPT part, CPT part + CPT).  piv: two
 // skewed shared vectors for the pivot row (double-buffered).  All threads of
 // the block must call it.
 // ---------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void gj_inverse(float (&x)[32], float *piv, int row, int part) {
-    constexpr int TPR = D / 32;
-    constexpr int VLEN = TPR * kPart;
-    const int vo = part * kPart;
+template <int D, int CPT>
+__device__ __forceinline__ void gj_inverse(float (&x)[CPT], float *piv, int row, int part) {
+    constexpr int TPR = D / CPT;
+    constexpr int VLEN = (D / 32) * kPart;
+    const int c0 = part * CPT;
     const int lane = threadIdx.x & 31;
-    // pivot row 0
     if (row == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) piv[vo + j] = x[j];
+        for (int j = 0; j < CPT; ++j) piv[vidx(c0 + j)] = x[j];
     }
     __syncthreads();
 #pragma unroll 1
@@ -170,33 +363,33 @@ __device__ __forceinline__ void gj_inverse(float (&x)[32], float *piv, int row, 
         const float *pr = piv + (k & 1) * VLEN;
         const float p = pr[vidx(k)];
         const float rp = 1.f / p;
-        // m = x[i][k]: held by part k/32 of this row, register k%32
+        // m = x[i][k]: held by part k / CPT of this row, register k % CPT
         float mk = 0.f;
-        const int kp = k >> 5, kr = k & 31;
+        const int kp = k / CPT, kr = k % CPT;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < CPT; ++j)
             if (j == kr) mk = x[j];
-        mk = __shfl_sync(0xffffffffu, mk, (lane & ~(TPR - 1)) | kp);
+        if (TPR > 1) mk = __shfl_sync(0xffffffffu, mk, (lane & ~(TPR - 1)) | kp);
         if (row == k) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = (part * 32 + j == k) ? rp : x[j] * rp;
+            for (int j = 0; j < CPT; ++j) x[j] = (c0 + j == k) ? rp : x[j] * rp;
         } else {
             const float f = mk * rp;
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-                const float4 pv = *reinterpret_cast<const float4 *>(pr + vo + 4 * c4);
+            for (int c4 = 0; c4 < CPT / 4; ++c4) {
+                const float4 pv = *reinterpret_cast<const float4 *>(pr + vidx(c0 + 4 * c4));
                 const float pj[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int j = 4 * c4 + q;
-                    x[j] = (part * 32 + j == k) ? -f : fmaf(-f, pj[q], x[j]);
+                    x[j] = (c0 + j == k) ? -f : fmaf(-f, pj[q], x[j]);
                 }
             }
         }
         if (k + 1 < D && row == k + 1) {
-            float *nx = piv + ((k + 1) & 1) * VLEN + vo;
+            float *nx = piv + ((k + 1) & 1) * VLEN;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) nx[j] = x[j];
+            for (int j = 0; j < CPT; ++j) nx[vidx(c0 + j)] = x[j];
         }
         __syncthreads();
     }
@@ -222,9 +415,20 @@ __device__ __forceinline__ void issue_tile(uint64_t *bar, void *const *dst, cons
 // ---------------------------------------------------------------------------
 // gates: A^(c) by Gauss-Jordan, then Sherman-Morrison over the chunk
 // ---------------------------------------------------------------------------
+// Thread layout: thread (row i, part p) owns CPT columns of row i of A;
+// CPT = 64 for d >= 64 (a whole row for d = 64), 32 for d = 32.
+template <int D>
+struct GatesCfg {
+    static constexpr int CPT = (D >= 64) ? 64 : 32;
+    static constexpr int TPR = D / CPT;
+    static constexpr int NT = D * TPR;
+    static constexpr int NW = NT / 32;
+    static constexpr int VLEN = (D / 32) * kPart;
+};
+
 template <int D, typename IO>
 struct GatesSmem {
-    using R = RowCfg<D>;
+    using R = GatesCfg<D>;
     static constexpr size_t bars = 0;
     static constexpr size_t raw = 128;                                        // [2][2][TT*D] IO (u, k)
     static constexpr size_t raw_t = (size_t)kTT * D * sizeof(IO);
@@ -233,14 +437,18 @@ struct GatesSmem {
     static constexpr size_t zbuf = uu + kTT * R::VLEN * 4;                    // [2][VLEN]
     static constexpr size_t piv = zbuf + 2 * R::VLEN * 4;                     // [2][VLEN]
     static constexpr size_t red = piv + 2 * R::VLEN * 4;                      // [2][NW] float4
-    static constexpr size_t total = red + 2 * R::NW * 16;
+    static constexpr size_t total = red + 2 * (R::NW < 1 ? 1 : R::NW) * 16;
 };
 
+// Within a chunk A starts from its exact definition (M^(c))^{-1} and takes at
+// most C rank-1 steps, so the update is the single-FMA form
+// A_ij -= (beta z_i) z_j; the sequential kernel, which runs all T steps from
+// one start, uses the symmetric-rounding form instead.
 template <int D, typename IO>
-__global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
-    using R = RowCfg<D>;
+__global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
+    using R = GatesCfg<D>;
     using Lo = GatesSmem<D, IO>;
-    constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW;
+    constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW, CPT = R::CPT;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 16);
@@ -257,7 +465,7 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
     const int ntiles = (ntok + kTT - 1) / kTT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = tid / TPR, part = tid % TPR;
-    const int c0 = part * 32, vo = part * kPart;
+    const int c0 = part * CPT;
     const size_t tok0 = ((size_t)bh * T + t0) * D;
     const IO *gu = static_cast<const IO *>(a.p.u) + tok0;
     const IO *gk = static_cast<const IO *>(a.p.k) + tok0;
@@ -287,35 +495,34 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
     }
 
     // ---- A at the chunk start ----
-    float x[32];
+    float x[CPT];
     if (c == 0) {
         if (a.p.A0) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.p.A0 + (size_t)bh * D * D + row * D + c0);
+            const float *src = a.p.A0 + (size_t)bh * D * D + row * D + c0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 v = src[q];
+            for (int q = 0; q < CPT / 4; ++q) {
+                const float4 v = reinterpret_cast<const float4 *>(src)[q];
                 x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
             }
         } else {
             const float il = 1.f / a.p.lambda0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = (c0 + j == row) ? il : 0.f;
+            for (int j = 0; j < CPT; ++j) x[j] = (c0 + j == row) ? il : 0.f;
         }
     } else {
-        const float4 *src = reinterpret_cast<const float4 *>(
-            ws_f(a, a.L.off_M) + ((size_t)bh * NC + c) * D * D + row * D + c0);
+        const float *src = ws_f(a, a.L.off_M) + ((size_t)bh * NC + c) * D * D + row * D + c0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 v = src[q];
+        for (int q = 0; q < CPT / 4; ++q) {
+            const float4 v = reinterpret_cast<const float4 *>(src)[q];
             x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
         }
-        gj_inverse<D>(x, s_piv, row, part);
+        gj_inverse<D, CPT>(x, s_piv, row, part);
     }
-    float2 am[16];
+    float2 am[CPT / 2];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) am[j] = make_float2(x[2 * j], x[2 * j + 1]);
+    for (int j = 0; j < CPT / 2; ++j) am[j] = make_float2(x[2 * j], x[2 * j + 1]);
 
-    float beta_prev = 0.f, s2_prev = 0.f, z_prev = 0.f, y_prev = 0.f;
+    float bz_prev = 0.f, bs2_prev = 0.f, z_prev = 0.f, y_prev = 0.f;
     int failed = -1;
     for (int t = 0; t <= ntok; ++t) {
         const int tt = t % kTT, m = t / kTT;
@@ -355,17 +562,18 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
         const bool hasA = t < ntok, hasG = t > 0;
         const float *uA = s_u + tt * VLEN;
         const float *kA = s_khat + tt * VLEN;
-        const float4 *zp = reinterpret_cast<const float4 *>(s_z + ((t - 1) & 1) * VLEN + vo);
-        const float2 mb = f2(-beta_prev), zi = f2(z_prev);
+        const float *zv = s_z + ((t - 1) & 1) * VLEN;
+        const float2 mbz = f2(-bz_prev);  // -beta_{t-1} z_{t-1,i}
         float2 za = f2(0.f), zb = f2(0.f), ya = f2(0.f), yb = f2(0.f);
         if (hasA) {
-            const float4 *up = reinterpret_cast<const float4 *>(uA + vo);
-            const float4 *kp = reinterpret_cast<const float4 *>(kA + vo);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 zz = zp[q], u4 = up[q], k4 = kp[q];
-                am[2 * q] = fma2(mb, mul2(zi, lo2(zz)), am[2 * q]);
-                am[2 * q + 1] = fma2(mb, mul2(zi, hi2(zz)), am[2 * q + 1]);
+            for (int q = 0; q < CPT / 4; ++q) {
+                const int j = c0 + 4 * q;
+                const float4 zz = *reinterpret_cast<const float4 *>(zv + vidx(j));
+                const float4 u4 = *reinterpret_cast<const float4 *>(uA + vidx(j));
+                const float4 k4 = *reinterpret_cast<const float4 *>(kA + vidx(j));
+                am[2 * q] = fma2(mbz, lo2(zz), am[2 * q]);
+                am[2 * q + 1] = fma2(mbz, hi2(zz), am[2 * q + 1]);
                 za = fma2(am[2 * q], lo2(u4), za);
                 zb = fma2(am[2 * q + 1], hi2(u4), zb);
                 ya = fma2(am[2 * q], lo2(k4), ya);
@@ -373,10 +581,10 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
             }
         } else {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 zz = zp[q];
-                am[2 * q] = fma2(mb, mul2(zi, lo2(zz)), am[2 * q]);
-                am[2 * q + 1] = fma2(mb, mul2(zi, hi2(zz)), am[2 * q + 1]);
+            for (int q = 0; q < CPT / 4; ++q) {
+                const float4 zz = *reinterpret_cast<const float4 *>(zv + vidx(c0 + 4 * q));
+                am[2 * q] = fma2(mbz, lo2(zz), am[2 * q]);
+                am[2 * q + 1] = fma2(mbz, hi2(zz), am[2 * q + 1]);
             }
         }
         float z = hsum2(add2(za, zb)), y = hsum2(add2(ya, yb));
@@ -385,7 +593,7 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
             z += __shfl_xor_sync(0xffffffffu, z, o);
             y += __shfl_xor_sync(0xffffffffu, y, o);
         }
-        const float g = y_prev - beta_prev * s2_prev * z_prev;  // gate row of token t-1
+        const float g = y_prev - bs2_prev * z_prev;  // gate row of token t-1: y - beta (z.k_hat) z
         float p1 = 0.f, p2 = 0.f, p3 = 0.f;
         if (part == 0) {
             if (hasA) {
@@ -413,8 +621,9 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
             __syncwarp();
         }
         if (hasG && part == 0) galpha[(size_t)(t - 1) * D + row] = g * fminf(rsqrtf(p3), 1.f / kEps);
-        beta_prev = 1.f / (1.f + p1);
-        s2_prev = p2;
+        const float beta = 1.f / (1.f + p1);
+        bz_prev = beta * z;
+        bs2_prev = beta * p2;
         z_prev = z;
         y_prev = y;
     }
@@ -425,9 +634,10 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) gates_kernel(ChunkArgs a) {
         return;
     }
     if (c == NC - 1) {
-        float4 *dA = reinterpret_cast<float4 *>(a.p.A_T + (size_t)bh * D * D + row * D + c0);
+        float *dA = a.p.A_T + (size_t)bh * D * D + row * D + c0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) dA[q] = make_float4(am[2 * q].x, am[2 * q].y, am[2 * q + 1].x, am[2 * q + 1].y);
+        for (int q = 0; q < CPT / 4; ++q)
+            reinterpret_cast<float4 *>(dA)[q] = make_float4(am[2 * q].x, am[2 * q].y, am[2 * q + 1].x, am[2 * q + 1].y);
     }
 }
 
@@ -814,7 +1024,7 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) invert_a0_kernel(ChunkArgs a) {
     const float *src = a.p.A0 + (size_t)bh * D * D + row * D + c0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) x[j] = src[j];
-    gj_inverse<D>(x, piv, row, part);
+    gj_inverse<D, 32>(x, piv, row, part);
     float *dst = ws_f(a, a.L.off_M0) + (size_t)bh * D * D + row * D + c0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) dst[j] = x[j];
@@ -833,8 +1043,11 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
         return cudaErrorInvalidConfiguration;
     cudaError_t e;
     if ((e = set_smem(gates_kernel<D, IO>, GatesSmem<D, IO>::total)) != cudaSuccess) return e;
+    using G = GatesCfg<D>;
     if ((e = set_smem(rows_kernel<D, IO, 0>, RowsSmem<D, IO>::total)) != cudaSuccess) return e;
     if ((e = set_smem(chain_kernel<D>, ChainSmem<D>::total)) != cudaSuccess) return e;
+    if constexpr (sizeof(IO) == 2 && D >= 64)
+        if ((e = set_smem(gram_tc_kernel<D>, GramTc<D>::total)) != cudaSuccess) return e;
     if ((e = set_smem(rows_kernel<D, IO, 1>, RowsSmem<D, IO>::total)) != cudaSuccess) return e;
     int n = 0;
     mark_launch(a.p, n, st);
@@ -843,13 +1056,17 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         mark_launch(a.p, ++n, st);
     }
-    gram_kernel<D, IO><<<(unsigned)(NC * BH), 256, 0, st>>>(a);
+    if constexpr (sizeof(IO) == 2 && D >= 64) {
+        gram_tc_kernel<D><<<(unsigned)(NC * BH), GramTc<D>::NT, GramTc<D>::total, st>>>(a);
+    } else {
+        gram_kernel<D, IO><<<(unsigned)(NC * BH), 256, 0, st>>>(a);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
     prefix_kernel<D><<<(unsigned)(((D * D + D + 255) / 256) * BH), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    gates_kernel<D, IO><<<(unsigned)(NC * BH), R::NT, GatesSmem<D, IO>::total, st>>>(a);
+    gates_kernel<D, IO><<<(unsigned)(NC * BH), G::NT, GatesSmem<D, IO>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
     rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), R::NT, RowsSmem<D, IO>::total, st>>>(a);
