@@ -52,7 +52,7 @@ TRAFFIC = {
 
 
 def kernel_src_hash(kernel_name: str) -> str:
-    fn = {"seq": "vla_seq.cu", "chunk": "vla_chunk.cu"}[kernel_name]
+    fn = {"seq": "vla_seq.cu", "chunk": "vla_chunk.cu", "decode": "vla_decode.cu"}[kernel_name]
     path = os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", fn)
     if not os.path.exists(path):
         return ""
@@ -63,13 +63,24 @@ def kernel_src_hash(kernel_name: str) -> str:
 # flops per token-head each one performs (each step of the recurrence is
 # assigned to exactly one kernel; the chunked form's extra work - Grams,
 # prefix sums, chunk transitions, the chain - counts zero).
-def kernel_plan(kname, d):
+def kernel_plan(kname, d, io_dtype="bf16"):
+    """[(kernel, algorithmic flops per token-head, bound)] in launch order."""
     if kname == "seq":
-        return [("seq_kernel", 12 * d * d + 16 * d)]
+        return [("seq_kernel", 12 * d * d + 16 * d, "alu")]
+    if kname == "decode":
+        # one token per call: the state read and written back dominates
+        return [("decode_kernel", 12 * d * d + 16 * d, "hbm")]
     # gates: key norm, z = A u, rank-1 update, A k_hat, gate norm (a0-a2);
     # output: S k_hat, state write, S phi(q), readout (a3-a4)
-    return [("gram_kernel", 0), ("prefix_kernel", 0), ("gates_kernel", 6 * d * d + 8 * d),
-            ("rows_kernel<summary>", 0), ("chain_kernel", 0), ("rows_kernel<output>", 6 * d * d + 8 * d)]
+    gram = "gram_tc_kernel" if (io_dtype == "bf16" and d >= 64) else "gram_kernel"
+    return [(gram, 0, "alu"), ("prefix_kernel", 0, "alu"), ("gates_kernel", 6 * d * d + 8 * d, "alu"),
+            ("rows_kernel<summary>", 0, "alu"), ("chain_kernel", 0, "alu"),
+            ("rows_kernel<output>", 6 * d * d + 8 * d, "alu")]
+
+
+def state_bytes(B, H, d):
+    """fp32 state words read and written per call: S, A (d x d) and n (d)."""
+    return B * H * 2 * (2 * d * d + d) * 4
 
 
 def log(*a):
@@ -253,7 +264,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="long")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "seq", "chunk"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "seq", "chunk", "decode"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--set", action="append", help="workload override, e.g. T=4096")
     ap.add_argument("--no-e2e", action="store_true")
@@ -278,7 +289,8 @@ def main():
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    kernel = {"auto": vla.VLA_KERNEL_AUTO, "seq": vla.VLA_KERNEL_SEQ, "chunk": vla.VLA_KERNEL_CHUNK}[args.kernel]
+    kernel = {"auto": vla.VLA_KERNEL_AUTO, "seq": vla.VLA_KERNEL_SEQ, "chunk": vla.VLA_KERNEL_CHUNK,
+              "decode": vla.VLA_KERNEL_DECODE}[args.kernel]
 
     t_gen = time.perf_counter()
     x = make_host_inputs(args.config, rank, parse_overrides(args))
@@ -288,11 +300,17 @@ def main():
     hq, hk, hv, hu = to_torch_host(x)
     q, k, v, u = (t.to(dev) for t in (hq, hk, hv, hu))
     resolved = kernel if kernel != vla.VLA_KERNEL_AUTO else vla.vla_select_kernel(B, H, T, d)
-    kname = {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk"}[resolved]
+    kname = {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk", vla.VLA_KERNEL_DECODE: "decode"}[resolved]
     o = torch.empty_like(q)
     S_T = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
     A_T = torch.empty_like(S_T)
     n_T = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    # decode steps carry the state in place from call to call
+    in_place = kname == "decode"
+    if in_place:
+        S_T.zero_()
+        n_T.zero_()
+        A_T.copy_((torch.eye(d, device=dev) / x.lambda0).expand(B, H, d, d))
     need = vla.vla_workspace_bytes(B, H, T, d, vla.VLA_BF16 if x.dtype == "bf16" else vla.VLA_F32, resolved)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     in_bytes = 4 * B * H * T * d * io_bytes
@@ -301,10 +319,11 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        vla.vla_forward(q, k, v, u, x.lambda0, o=o, S_T=S_T, A_T=A_T, n_T=n_T, kernel=resolved,
-                        workspace=ws if need else None, stream=stream)
+        st = (S_T, A_T, n_T) if in_place else (None, None, None)
+        vla.vla_forward(q, k, v, u, x.lambda0, S0=st[0], A0=st[1], n0=st[2], o=o, S_T=S_T, A_T=A_T, n_T=n_T,
+                        kernel=resolved, workspace=ws if need else None, stream=stream)
 
-    plan = kernel_plan(kname, d)
+    plan = kernel_plan(kname, d, x.dtype)
     nb = len(plan) + 1  # launch boundaries per step
     bounds = [[torch.cuda.Event(enable_timing=True) for _ in range(nb)] for _ in range(args.steps)]
     for evs in bounds:
@@ -365,11 +384,14 @@ def main():
         hA = torch.empty(A_T.shape, dtype=torch.float32).pin_memory()
         hn = torch.empty(n_T.shape, dtype=torch.float32).pin_memory()
 
+        # a decode step returns o; its state stays resident on the device
+        results = ((ho, o),) if in_place else ((ho, o), (hS, S_T), (hA, A_T), (hn, n_T))
+
         def e2e_step():
             for dst, src in ((q, hq), (k, hk), (v, hv), (u, hu)):
                 dst.copy_(src, non_blocking=True)
             step()
-            for dst, src in ((ho, o), (hS, S_T), (hA, A_T), (hn, n_T)):
+            for dst, src in results:
                 dst.copy_(src, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
@@ -390,28 +412,36 @@ def main():
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
         h2d = 4 * units * d * io_bytes
-        d2h = units * d * io_bytes + B * H * (2 * d * d + d) * 4
+        d2h = units * d * io_bytes + (0 if in_place else B * H * (2 * d * d + d) * 4)
         e2e = {"value": world * units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # ---- roofline of the dominant kernel (and of the whole step) ----
     flops, byts = algorithmic_work(B, H, T, d, io_bytes)
+    if in_place:
+        byts += state_bytes(B, H, d) - B * H * 8 * d * d  # the state is read and written each call
     dom = int(np.argmax(per_kernel_ms))
     kernel_ms = per_kernel_ms[dom]
-    k_flops = units * plan[dom][1]
-    achieved_tf = k_flops / (kernel_ms / 1e3) / 1e12
-    tr = TRAFFIC.get((kname, args.config, plan[dom][0]))
+    k_name, k_fpt, k_bound = plan[dom]
+    tr = TRAFFIC.get((kname, args.config, k_name))
     traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash(kname) else None
-    roofline = {"bound": "alu", "achieved": achieved_tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                "frac": achieved_tf / FP32_PEAK_TFLOPS, "traffic": traffic,
-                "kernel": "%s<%d,%s>" % (plan[dom][0], d, x.dtype), "kernel_ms": kernel_ms,
-                "algorithmic_flops_per_launch": k_flops,
-                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop/FMA x 2.070 GHz (no tensor cores)",
+    if k_bound == "hbm":
+        achieved = byts / (kernel_ms / 1e3) / 1e9
+        peak, unit = measured_hbm_gbs(), "GB/s"
+        peak_src = "MEASURED_PEAKS.json hbm_gbs (of measured)"
+    else:
+        achieved = units * k_fpt / (kernel_ms / 1e3) / 1e12
+        peak, unit = FP32_PEAK_TFLOPS, "TFLOP/s"
+        peak_src = "derived: 152 SMs x 128 FP32 lanes x 2 flop/FMA x 2.070 GHz (of derived)"
+    roofline = {"bound": k_bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": traffic, "kernel": "%s<%d,%s>" % (k_name, d, x.dtype), "kernel_ms": kernel_ms,
+                "algorithmic_per_launch": byts if k_bound == "hbm" else units * k_fpt,
+                "peak_source": peak_src,
                 "step": {"algorithmic_flops": flops, "algorithmic_bytes": byts,
                          "alu_frac": flops / (ms / 1e3) / 1e12 / FP32_PEAK_TFLOPS,
                          "hbm_frac_of_measured": (byts / (ms / 1e3) / 1e9) / measured_hbm_gbs()},
                 "kernels": [{"name": nm, "ms": t, "share": t / sum(per_kernel_ms)}
-                            for (nm, _), t in zip(plan, per_kernel_ms)]}
+                            for (nm, _, _), t in zip(plan, per_kernel_ms)]}
 
     cpu = None
     parity = None
@@ -421,8 +451,14 @@ def main():
                "sample": "first %d of %d (b,h) units, all %d tokens (%.1f s)" % (nh, B * H, T, dt),
                "host_cores": os.cpu_count()}
         flat = lambda a: a.reshape((B * H,) + tuple(a.shape[2:]))[:nh]  # noqa: E731
-        got = {"o": flat(o.float().cpu().numpy()), "S_T": flat(S_T.cpu().numpy()),
-               "A_T": flat(A_T.cpu().numpy()), "n_T": flat(n_T.cpu().numpy())}
+        if in_place:
+            # the timed calls advanced the state; redo one call from the initial state
+            o2, S2, A2, n2 = vla.vla_forward(q, k, v, u, x.lambda0, kernel=resolved)
+            torch.cuda.synchronize(dev)
+        else:
+            o2, S2, A2, n2 = o, S_T, A_T, n_T
+        got = {"o": flat(o2.float().cpu().numpy()), "S_T": flat(S2.cpu().numpy()),
+               "A_T": flat(A2.cpu().numpy()), "n_T": flat(n2.cpu().numpy())}
         parity = {key: float(np.linalg.norm((got[key] - ref[key]).ravel()) / np.linalg.norm(ref[key].ravel()))
                   for key in got}
 

@@ -54,6 +54,7 @@ extern "C" {
 #define VLA_KERNEL_AUTO 0  /* pick by shape */
 #define VLA_KERNEL_SEQ 1   /* one CTA per (b, h), token-sequential, no workspace */
 #define VLA_KERNEL_CHUNK 2 /* chunk-parallel over T, needs workspace */
+#define VLA_KERNEL_DECODE 3 /* a few tokens per call (decode step), state streamed from HBM */
 
 /*
  * vla_forward -- run the recurrence over T tokens for all B*H units.
@@ -70,7 +71,8 @@ extern "C" {
  * o            [B,H,T,d] io_dtype, written.
  * S_T, A_T     [B,H,d,d] fp32, written (required).
  * n_T          [B,H,d] fp32, written when non-NULL.
- * kernel       VLA_KERNEL_AUTO / _SEQ / _CHUNK.
+ * kernel       VLA_KERNEL_AUTO / _SEQ / _CHUNK / _DECODE.  AUTO takes DECODE for
+ *              T <= 4, CHUNK when B*H < 304 and T >= 1024, SEQ otherwise.
  * chunk        chunk length for VLA_KERNEL_CHUNK (0 = library default).
  * workspace    device scratch of at least vla_workspace_bytes(...) bytes
  *              (may be NULL when that is 0).  Contents on entry are ignored.
@@ -86,8 +88,9 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * sequential kernel).  Returns 0 for invalid arguments as well. */
 size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk);
 
-/* Which kernel VLA_KERNEL_AUTO resolves to for this shape (VLA_KERNEL_SEQ or
- * VLA_KERNEL_CHUNK), or a VLA_ERR_* code for invalid arguments. */
+/* Which kernel VLA_KERNEL_AUTO resolves to for this shape (VLA_KERNEL_SEQ,
+ * VLA_KERNEL_CHUNK or VLA_KERNEL_DECODE), or a VLA_ERR_* code for invalid
+ * arguments. */
 int vla_select_kernel(int B, int H, int T, int d_h);
 
 /* Static, human-readable text for a status code. */
@@ -120,7 +123,8 @@ int vla_debug_inject(int mode, long long wait_limit_ns);
 int vla_set_launch_events(void *const *events, int n);
 
 /* Number of kernels the last successful vla_forward call on this host
- * thread launched (1 for the sequential path, 6 or 7 for the chunked one). */
+ * thread launched (1 for the sequential and decode paths, 6 or 7 for the
+ * chunked one). */
 int vla_last_launch_count(void);
 
 /* Size of the device scratch array built into the library for

@@ -33,6 +33,7 @@ VLA_BF16 = 1
 VLA_KERNEL_AUTO = 0
 VLA_KERNEL_SEQ = 1
 VLA_KERNEL_CHUNK = 2
+VLA_KERNEL_DECODE = 3
 
 # every symbol include/vla.h declares, with (restype, argtypes)
 _vp = ctypes.c_void_p

@@ -39,7 +39,8 @@ int check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int 
     if (B < 0 || H < 0 || T < 0) return VLA_ERR_ARG;
     if (io_dtype != VLA_F32 && io_dtype != VLA_BF16) return VLA_ERR_ARG;
     if (!(lambda0 > 0.f) || !isfinite(lambda0)) return VLA_ERR_ARG;
-    if (kernel != VLA_KERNEL_AUTO && kernel != VLA_KERNEL_SEQ && kernel != VLA_KERNEL_CHUNK)
+    if (kernel != VLA_KERNEL_AUTO && kernel != VLA_KERNEL_SEQ && kernel != VLA_KERNEL_CHUNK &&
+        kernel != VLA_KERNEL_DECODE)
         return VLA_ERR_ARG;
     if (d_h != 32 && d_h != 64 && d_h != 128) return VLA_ERR_UNSUPPORTED_DIM;
     // element offsets are computed in size_t; counts themselves must fit the kernels' int math
@@ -48,12 +49,14 @@ int check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int 
     return VLA_OK;
 }
 
-// AUTO: the chunk-parallel path when there are too few (b, h) units to fill
-// the GPU with one CTA each and the stream is long enough to cut.
+// AUTO: the decode step for a handful of tokens; the chunk-parallel path
+// when there are too few (b, h) units to fill the GPU with one CTA each and
+// the stream is long enough to cut; otherwise the sequential kernel.
 int resolve_kernel(int B, int H, int T, int d_h, int kernel) {
     (void)d_h;
     if (kernel != VLA_KERNEL_AUTO) return kernel;
     const long long BH = (long long)B * H;
+    if (T >= 1 && T <= 4) return VLA_KERNEL_DECODE;
     if (BH < 2 * 152 && T >= 1024) return VLA_KERNEL_CHUNK;
     return VLA_KERNEL_SEQ;
 }
@@ -118,7 +121,7 @@ size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kerne
     if (check_common(io_dtype, 1.f, B, H, T, d_h, kernel) != VLA_OK) return 0;
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return 0;
     const int kk = resolve_kernel(B, H, T, d_h, kernel);
-    if (kk == VLA_KERNEL_SEQ || T == 0 || (long long)B * H == 0) return 0;
+    if (kk != VLA_KERNEL_CHUNK || T == 0 || (long long)B * H == 0) return 0;
     return vla::chunk_layout(B * H, T, d_h, chunk_len(B, H, T, d_h, chunk)).total;
 }
 
@@ -196,6 +199,8 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
     if (kk == VLA_KERNEL_CHUNK && T > 0) {
         const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk_len(B, H, T, d_h, chunk));
         e = vla::launch_chunk(p, L, st);
+    } else if (kk == VLA_KERNEL_DECODE) {
+        e = vla::launch_decode(p, st);
     } else {
         // the sequential kernel also serves T == 0 (state copy) for either choice
         e = vla::launch_seq(p, st);

@@ -50,6 +50,9 @@ inline void mark_launch(const FwdParams &p, int i, cudaStream_t st) {
 // Sequential kernel: one CTA per (b, h).  Returns a cudaError_t.
 cudaError_t launch_seq(const FwdParams &p, cudaStream_t stream);
 
+// Decode step: one CTA per (b, h), state streamed from HBM.  Returns a cudaError_t.
+cudaError_t launch_decode(const FwdParams &p, cudaStream_t stream);
+
 // Workspace of the chunk-parallel path (byte offsets, 256-byte aligned).
 struct ChunkLayout {
     int C;               // chunk length (multiple of 16)

@@ -245,7 +245,8 @@ def make_recall_stream(B: int, H: int, T: int, d: int, n_pairs: int, seed: int =
 # well under a second; "heads32" is B=4 H=8 T=4096 d=64 bf16; "long" is the
 # long stream B=1 H=16 T=65536 d=64 bf16 with u scaled by 0.5; "batched" is
 # B=32 H=16 T=2048 d=128 bf16 with lambda0=0.5; "recall" is the key-value
-# recall streams B=256 H=4 T=512 d=32 fp32 with n in {8, 24, 48}.
+# recall streams B=256 H=4 T=512 d=32 fp32 with n in {8, 24, 48}; "decode" is
+# one token per call for B=32 H=64 d=64 bf16 with the state kept in HBM.
 CONFIGS = {
     "tiny": dict(kind="iid", B=1, H=1, T=256, d=32, dtype="f32", seed=0, lambda0=1.0,
                  unit_keys=True),
@@ -257,6 +258,8 @@ CONFIGS = {
     "recall8": dict(kind="recall", B=256, H=4, T=512, d=32, n_pairs=8, dtype="f32", seed=5),
     "recall24": dict(kind="recall", B=256, H=4, T=512, d=32, n_pairs=24, dtype="f32", seed=5),
     "recall48": dict(kind="recall", B=256, H=4, T=512, d=32, n_pairs=48, dtype="f32", seed=5),
+    # streaming decode step: one token per call for 2048 (b, h) units
+    "decode": dict(kind="iid", B=32, H=64, T=1, d=64, dtype="bf16", seed=6, lambda0=1.0),
 }
 
 

@@ -67,6 +67,7 @@ def _call(**kw):
     (dict(lam=float("inf")), vla.VLA_ERR_ARG),
     (dict(io=7), vla.VLA_ERR_ARG),
     (dict(kernel=9), vla.VLA_ERR_ARG),
+    (dict(kernel=4), vla.VLA_ERR_ARG),
     (dict(B=-1), vla.VLA_ERR_ARG),
     (dict(T=-3), vla.VLA_ERR_ARG),
     (dict(chunk=-1), vla.VLA_ERR_ARG),
@@ -104,6 +105,10 @@ def test_workspace_query_and_kernel_selection():
     assert vla.vla_workspace_bytes(1, 16, 0, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK) == 0
     assert vla.vla_select_kernel(1, 16, 65536, 64) == vla.VLA_KERNEL_CHUNK
     assert vla.vla_select_kernel(256, 4, 512, 32) == vla.VLA_KERNEL_SEQ
+    assert vla.vla_select_kernel(32, 64, 1, 64) == vla.VLA_KERNEL_DECODE
+    assert vla.vla_select_kernel(32, 64, 4, 64) == vla.VLA_KERNEL_DECODE
+    assert vla.vla_select_kernel(32, 64, 5, 64) == vla.VLA_KERNEL_SEQ
+    assert vla.vla_workspace_bytes(32, 64, 1, 64, vla.VLA_BF16, vla.VLA_KERNEL_DECODE) == 0
     assert vla.vla_workspace_bytes(1, 16, 4096, 48, vla.VLA_BF16, vla.VLA_KERNEL_SEQ) == 0
     assert vla.vla_select_kernel(1, 16, 4096, 64) in (vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK)
     assert vla.vla_select_kernel(1, 16, 4096, 40) == vla.VLA_ERR_UNSUPPORTED_DIM
