@@ -83,6 +83,21 @@ def state_bytes(B, H, d):
     return B * H * 2 * (2 * d * d + d) * 4
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """Slowest rank's value (the job finishes when the last rank does)."""
+    if dist is None or not dist.is_initialized():
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, units_per_rank: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank processes its own batch (weak scaling)."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
@@ -368,13 +383,9 @@ def main():
     if st != vla.VLA_OK:
         raise RuntimeError("device status after timed steps: " + vla.vla_status_str(st))
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = float(np.mean(step_ms))
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.mean(step_ms)), dist, dev)
     units = B * H * T
-    value = world * units / (ms / 1e3)
+    value = job_value(world, units, ms)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -406,14 +417,10 @@ def main():
             e2e_step()
             ee[i].record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(es, ee)]))
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(es, ee)])), dist, dev)
         h2d = 4 * units * d * io_bytes
         d2h = units * d * io_bytes + (0 if in_place else B * H * (2 * d * d + d) * 4)
-        e2e = {"value": world * units / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_value(world, units, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # ---- roofline of the dominant kernel (and of the whole step) ----

@@ -395,6 +395,60 @@ __device__ __forceinline__ void gj_inverse(float (&x)[CPT], float *piv, int row,
     }
 }
 
+// Same elimination with RPT rows per thread: rows row0 + r * rstride.
+template <int D, int CPT, int RPT>
+__device__ __forceinline__ void gj_inverse_rows(float (&x)[RPT][CPT], float *piv, int row0, int rstride, int part) {
+    constexpr int TPR = D / CPT;
+    constexpr int VLEN = (D / 32) * kPart;
+    const int c0 = part * CPT;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r)
+        if (row0 + r * rstride == 0) {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) piv[vidx(c0 + j)] = x[r][j];
+        }
+    __syncthreads();
+#pragma unroll 1
+    for (int k = 0; k < D; ++k) {
+        const float *pr = piv + (k & 1) * VLEN;
+        const float rp = 1.f / pr[vidx(k)];
+        const int kp = k / CPT, kr = k % CPT;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            float mk = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j)
+                if (j == kr) mk = x[r][j];
+            if (TPR > 1) mk = __shfl_sync(0xffffffffu, mk, (lane & ~(TPR - 1)) | kp);
+            if (row0 + r * rstride == k) {
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) x[r][j] = (c0 + j == k) ? rp : x[r][j] * rp;
+            } else {
+                const float f = mk * rp;
+#pragma unroll
+                for (int c4 = 0; c4 < CPT / 4; ++c4) {
+                    const float4 pv = *reinterpret_cast<const float4 *>(pr + vidx(c0 + 4 * c4));
+                    const float pj[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int j = 4 * c4 + q;
+                        x[r][j] = (c0 + j == k) ? -f : fmaf(-f, pj[q], x[r][j]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPT; ++r)
+            if (k + 1 < D && row0 + r * rstride == k + 1) {
+                float *nx = piv + ((k + 1) & 1) * VLEN;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) nx[vidx(c0 + j)] = x[r][j];
+            }
+        __syncthreads();
+    }
+}
+
 template <int D>
 struct RowCfg {
     static constexpr int TPR = D / 32;
@@ -415,14 +469,19 @@ __device__ __forceinline__ void issue_tile(uint64_t *bar, void *const *dst, cons
 // ---------------------------------------------------------------------------
 // gates: A^(c) by Gauss-Jordan, then Sherman-Morrison over the chunk
 // ---------------------------------------------------------------------------
-// Thread layout: thread (row i, part p) owns CPT columns of row i of A;
-// CPT = 64 for d >= 64 (a whole row for d = 64), 32 for d = 32.
+// Thread layout: thread (rows row0 + r * RSTRIDE, part p) owns CPT columns of
+// RPT rows of A.  d = 64: two warps per chunk, a whole row per thread;
+// d = 128: 256 threads, half a row each; d = 32: one warp, a row each.  (Two
+// rows per lane with one warp per chunk was measured 24% slower at d = 64:
+// the per-token dependency chain doubles while few more chunks fit per SM.)
 template <int D>
 struct GatesCfg {
     static constexpr int CPT = (D >= 64) ? 64 : 32;
     static constexpr int TPR = D / CPT;
-    static constexpr int NT = D * TPR;
+    static constexpr int RPT = 1;
+    static constexpr int NT = D * TPR / RPT;
     static constexpr int NW = NT / 32;
+    static constexpr int RSTRIDE = NT / TPR;  // distance between a thread's rows
     static constexpr int VLEN = (D / 32) * kPart;
 };
 
@@ -437,7 +496,7 @@ struct GatesSmem {
     static constexpr size_t zbuf = uu + kTT * R::VLEN * 4;                    // [2][VLEN]
     static constexpr size_t piv = zbuf + 2 * R::VLEN * 4;                     // [2][VLEN]
     static constexpr size_t red = piv + 2 * R::VLEN * 4;                      // [2][NW] float4
-    static constexpr size_t total = red + 2 * (R::NW < 1 ? 1 : R::NW) * 16;
+    static constexpr size_t total = red + 2 * R::NW * 16;
 };
 
 // Within a chunk A starts from its exact definition (M^(c))^{-1} and takes at
@@ -448,7 +507,7 @@ template <int D, typename IO>
 __global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
     using R = GatesCfg<D>;
     using Lo = GatesSmem<D, IO>;
-    constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW, CPT = R::CPT;
+    constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW, CPT = R::CPT, RPT = R::RPT, RS = R::RSTRIDE;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 16);
@@ -464,7 +523,7 @@ __global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
     const int t0 = c * C, ntok = min(C, T - t0);
     const int ntiles = (ntok + kTT - 1) / kTT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = tid / TPR, part = tid % TPR;
+    const int row0 = tid / TPR, part = tid % TPR;
     const int c0 = part * CPT;
     const size_t tok0 = ((size_t)bh * T + t0) * D;
     const IO *gu = static_cast<const IO *>(a.p.u) + tok0;
@@ -495,34 +554,38 @@ __global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
     }
 
     // ---- A at the chunk start ----
-    float x[CPT];
-    if (c == 0) {
-        if (a.p.A0) {
-            const float *src = a.p.A0 + (size_t)bh * D * D + row * D + c0;
+    float2 am[RPT][CPT / 2];
+    {
+        float x[RPT][CPT];
 #pragma unroll
-            for (int q = 0; q < CPT / 4; ++q) {
-                const float4 v = reinterpret_cast<const float4 *>(src)[q];
-                x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+        for (int r = 0; r < RPT; ++r) {
+            const int row = row0 + r * RS;
+            const float *src = nullptr;
+            if (c > 0) src = ws_f(a, a.L.off_M) + ((size_t)bh * NC + c) * D * D + row * D + c0;
+            else if (a.p.A0) src = a.p.A0 + (size_t)bh * D * D + row * D + c0;
+            if (src) {
+#pragma unroll
+                for (int q = 0; q < CPT / 4; ++q) {
+                    const float4 v = reinterpret_cast<const float4 *>(src)[q];
+                    x[r][4 * q] = v.x; x[r][4 * q + 1] = v.y; x[r][4 * q + 2] = v.z; x[r][4 * q + 3] = v.w;
+                }
+            } else {
+                const float il = 1.f / a.p.lambda0;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) x[r][j] = (c0 + j == row) ? il : 0.f;
             }
-        } else {
-            const float il = 1.f / a.p.lambda0;
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) x[j] = (c0 + j == row) ? il : 0.f;
         }
-    } else {
-        const float *src = ws_f(a, a.L.off_M) + ((size_t)bh * NC + c) * D * D + row * D + c0;
+        if (c > 0) gj_inverse_rows<D, CPT, RPT>(x, s_piv, row0, RS, part);
 #pragma unroll
-        for (int q = 0; q < CPT / 4; ++q) {
-            const float4 v = reinterpret_cast<const float4 *>(src)[q];
-            x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
-        }
-        gj_inverse<D, CPT>(x, s_piv, row, part);
+        for (int r = 0; r < RPT; ++r)
+#pragma unroll
+            for (int j = 0; j < CPT / 2; ++j) am[r][j] = make_float2(x[r][2 * j], x[r][2 * j + 1]);
     }
-    float2 am[CPT / 2];
-#pragma unroll
-    for (int j = 0; j < CPT / 2; ++j) am[j] = make_float2(x[2 * j], x[2 * j + 1]);
 
-    float bz_prev = 0.f, bs2_prev = 0.f, z_prev = 0.f, y_prev = 0.f;
+    float bz_prev[RPT], z_prev[RPT], y_prev[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) bz_prev[r] = z_prev[r] = y_prev[r] = 0.f;
+    float bs2_prev = 0.f;
     int failed = -1;
     for (int t = 0; t <= ntok; ++t) {
         const int tt = t % kTT, m = t / kTT;
@@ -563,45 +626,52 @@ __global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
         const float *uA = s_u + tt * VLEN;
         const float *kA = s_khat + tt * VLEN;
         const float *zv = s_z + ((t - 1) & 1) * VLEN;
-        const float2 mbz = f2(-bz_prev);  // -beta_{t-1} z_{t-1,i}
-        float2 za = f2(0.f), zb = f2(0.f), ya = f2(0.f), yb = f2(0.f);
-        if (hasA) {
+        float2 za[RPT], zb[RPT], ya[RPT], yb[RPT];
 #pragma unroll
-            for (int q = 0; q < CPT / 4; ++q) {
-                const int j = c0 + 4 * q;
-                const float4 zz = *reinterpret_cast<const float4 *>(zv + vidx(j));
+        for (int r = 0; r < RPT; ++r) za[r] = zb[r] = ya[r] = yb[r] = f2(0.f);
+#pragma unroll
+        for (int q = 0; q < CPT / 4; ++q) {
+            const int j = c0 + 4 * q;
+            const float4 zz = *reinterpret_cast<const float4 *>(zv + vidx(j));
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const float2 mbz = f2(-bz_prev[r]);  // -beta_{t-1} z_{t-1,i}
+                am[r][2 * q] = fma2(mbz, lo2(zz), am[r][2 * q]);
+                am[r][2 * q + 1] = fma2(mbz, hi2(zz), am[r][2 * q + 1]);
+            }
+            if (hasA) {
                 const float4 u4 = *reinterpret_cast<const float4 *>(uA + vidx(j));
                 const float4 k4 = *reinterpret_cast<const float4 *>(kA + vidx(j));
-                am[2 * q] = fma2(mbz, lo2(zz), am[2 * q]);
-                am[2 * q + 1] = fma2(mbz, hi2(zz), am[2 * q + 1]);
-                za = fma2(am[2 * q], lo2(u4), za);
-                zb = fma2(am[2 * q + 1], hi2(u4), zb);
-                ya = fma2(am[2 * q], lo2(k4), ya);
-                yb = fma2(am[2 * q + 1], hi2(k4), yb);
-            }
-        } else {
 #pragma unroll
-            for (int q = 0; q < CPT / 4; ++q) {
-                const float4 zz = *reinterpret_cast<const float4 *>(zv + vidx(c0 + 4 * q));
-                am[2 * q] = fma2(mbz, lo2(zz), am[2 * q]);
-                am[2 * q + 1] = fma2(mbz, hi2(zz), am[2 * q + 1]);
+                for (int r = 0; r < RPT; ++r) {
+                    za[r] = fma2(am[r][2 * q], lo2(u4), za[r]);
+                    zb[r] = fma2(am[r][2 * q + 1], hi2(u4), zb[r]);
+                    ya[r] = fma2(am[r][2 * q], lo2(k4), ya[r]);
+                    yb[r] = fma2(am[r][2 * q + 1], hi2(k4), yb[r]);
+                }
             }
         }
-        float z = hsum2(add2(za, zb)), y = hsum2(add2(ya, yb));
-#pragma unroll
-        for (int o = 1; o < TPR; o <<= 1) {
-            z += __shfl_xor_sync(0xffffffffu, z, o);
-            y += __shfl_xor_sync(0xffffffffu, y, o);
-        }
-        const float g = y_prev - bs2_prev * z_prev;  // gate row of token t-1: y - beta (z.k_hat) z
+        float z[RPT], y[RPT], g[RPT];
         float p1 = 0.f, p2 = 0.f, p3 = 0.f;
-        if (part == 0) {
-            if (hasA) {
-                p1 = uA[vidx(row)] * z;
-                p2 = kA[vidx(row)] * z;
-                s_z[(t & 1) * VLEN + vidx(row)] = z;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            z[r] = hsum2(add2(za[r], zb[r]));
+            y[r] = hsum2(add2(ya[r], yb[r]));
+#pragma unroll
+            for (int o = 1; o < TPR; o <<= 1) {
+                z[r] += __shfl_xor_sync(0xffffffffu, z[r], o);
+                y[r] += __shfl_xor_sync(0xffffffffu, y[r], o);
             }
-            if (hasG) p3 = g * g;
+            g[r] = y_prev[r] - bs2_prev * z_prev[r];  // gate of token t-1: y - beta (z.k_hat) z
+            const int row = row0 + r * RS;
+            if (part == 0) {
+                if (hasA) {
+                    p1 += uA[vidx(row)] * z[r];
+                    p2 += kA[vidx(row)] * z[r];
+                    s_z[(t & 1) * VLEN + vidx(row)] = z[r];
+                }
+                if (hasG) p3 += g[r] * g[r];
+            }
         }
         const float red = warp_reduce4(p1, p2, p3, 0.f);
         if constexpr (NW > 1) {
@@ -620,12 +690,16 @@ __global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
             p3 = __shfl_sync(0xffffffffu, red, 16);
             __syncwarp();
         }
-        if (hasG && part == 0) galpha[(size_t)(t - 1) * D + row] = g * fminf(rsqrtf(p3), 1.f / kEps);
+        const float inv = fminf(rsqrtf(p3), 1.f / kEps);
         const float beta = 1.f / (1.f + p1);
-        bz_prev = beta * z;
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            if (hasG && part == 0) galpha[(size_t)(t - 1) * D + row0 + r * RS] = g[r] * inv;
+            bz_prev[r] = beta * z[r];
+            z_prev[r] = z[r];
+            y_prev[r] = y[r];
+        }
         bs2_prev = beta * p2;
-        z_prev = z;
-        y_prev = y;
     }
     if (failed >= 0) {
         if (tid == 0)
@@ -634,10 +708,14 @@ __global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
         return;
     }
     if (c == NC - 1) {
-        float *dA = a.p.A_T + (size_t)bh * D * D + row * D + c0;
 #pragma unroll
-        for (int q = 0; q < CPT / 4; ++q)
-            reinterpret_cast<float4 *>(dA)[q] = make_float4(am[2 * q].x, am[2 * q].y, am[2 * q + 1].x, am[2 * q + 1].y);
+        for (int r = 0; r < RPT; ++r) {
+            float *dA = a.p.A_T + (size_t)bh * D * D + (row0 + r * RS) * D + c0;
+#pragma unroll
+            for (int q = 0; q < CPT / 4; ++q)
+                reinterpret_cast<float4 *>(dA)[q] =
+                    make_float4(am[r][2 * q].x, am[r][2 * q].y, am[r][2 * q + 1].x, am[r][2 * q + 1].y);
+        }
     }
 }
 
@@ -663,14 +741,29 @@ struct RowsSmem {
     static constexpr size_t total = work + (size_t)kTT * D * 4;
 };
 
-// MODE 0 (summary): rows h (values v, start 0) and p (values 0, start I);
-//                   writes P_c, H_c.
-// MODE 1 (output):  rows s (values v, start S^(c)); writes o.
+// MODE 0 (summary): per thread, rows h_i (values v, start 0) and p_i (values
+//                   0, start I) of one row index i; writes P_c, H_c.
+// MODE 1 (output):  rows s (values v, start S^(c)); writes o.  For d = 128
+//                   each thread owns two rows, i and i + d/2, so that every
+//                   vector loaded from shared memory feeds two independent
+//                   dot products (measured 1.6x faster at d = 128; at d = 64
+//                   the halved thread count costs more latency hiding than
+//                   it saves, 1.09 -> 1.24 ms, so d = 64 keeps one row).
+template <int D, int MODE>
+struct RowsCfg {
+    static constexpr int TPR = D / 32;
+    static constexpr int RPT = (MODE == 1 && D >= 128) ? 2 : 1;
+    static constexpr int NT = D * TPR / RPT;
+    static constexpr int NW = NT / 32;
+    static constexpr int VLEN = TPR * kPart;
+};
+
 template <int D, typename IO, int MODE>
-__global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
-    using R = RowCfg<D>;
+__global__ void __launch_bounds__(RowsCfg<D, MODE>::NT) rows_kernel(ChunkArgs a) {
+    using R = RowsCfg<D, MODE>;
     using Lo = RowsSmem<D, IO>;
-    constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW;
+    constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW, RPT = R::RPT;
+    constexpr int ROW2 = D / 2;  // second row of a thread in MODE 1 with RPT = 2
     constexpr int NIO = (MODE == 0) ? 2 : 3;  // k, v (+ q)
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
@@ -742,13 +835,19 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
             p[j] = make_float2((c0 + 2 * j == row) ? 1.f : 0.f, (c0 + 2 * j + 1 == row) ? 1.f : 0.f);
         }
     } else {
-        const float4 *src = reinterpret_cast<const float4 *>(
-            ws_f(a, a.L.off_S) + ((size_t)bh * NC + c) * D * D + moff);
+        const float *sbase = ws_f(a, a.L.off_S) + ((size_t)bh * NC + c) * D * D;
+        const float4 *src = reinterpret_cast<const float4 *>(sbase + moff);
+        const float4 *src2 = reinterpret_cast<const float4 *>(sbase + moff + (size_t)ROW2 * D);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const float4 v = src[q];
             h[2 * q] = lo2(v);
             h[2 * q + 1] = hi2(v);
+            if (RPT == 2) {
+                const float4 w = src2[q];
+                p[2 * q] = lo2(w);
+                p[2 * q + 1] = hi2(w);
+            }
         }
     }
     float nbase = 0.f;
@@ -860,6 +959,7 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
             } else {
                 const float4 *fp = reinterpret_cast<const float4 *>(phiq + q * VLEN + vo);
                 float2 ka = f2(0.f), kb = f2(0.f), fa = f2(0.f), fb = f2(0.f);
+                float2 kc = f2(0.f), kd = f2(0.f), fc = f2(0.f), fd = f2(0.f);
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
                     const float4 k4 = kp[w], f4 = fp[w];
@@ -867,24 +967,42 @@ __global__ void __launch_bounds__(RowCfg<D>::NT) rows_kernel(ChunkArgs a) {
                     kb = fma2(h[2 * w + 1], hi2(k4), kb);
                     fa = fma2(h[2 * w], lo2(f4), fa);
                     fb = fma2(h[2 * w + 1], hi2(f4), fb);
+                    if (RPT == 2) {
+                        kc = fma2(p[2 * w], lo2(k4), kc);
+                        kd = fma2(p[2 * w + 1], hi2(k4), kd);
+                        fc = fma2(p[2 * w], lo2(f4), fc);
+                        fd = fma2(p[2 * w + 1], hi2(f4), fd);
+                    }
                 }
                 float sk = hsum2(add2(ka, kb)), sq = hsum2(add2(fa, fb));
+                float sk2 = hsum2(add2(kc, kd)), sq2 = hsum2(add2(fc, fd));
 #pragma unroll
                 for (int o = 1; o < TPR; o <<= 1) {
                     sk += __shfl_xor_sync(0xffffffffu, sk, o);
                     sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                    if (RPT == 2) {
+                        sk2 += __shfl_xor_sync(0xffffffffu, sk2, o);
+                        sq2 += __shfl_xor_sync(0xffffffffu, sq2, o);
+                    }
                 }
                 const float r = vi - sk;
-                const float2 r2 = f2(r);
+                const float r2s = (RPT == 2) ? vv[q * D + row + ROW2] - sk2 : 0.f;
+                const float2 r2 = f2(r), rr2 = f2(r2s);
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
                     const float4 a4 = ap[w];
                     h[2 * w] = fma2(r2, lo2(a4), h[2 * w]);
                     h[2 * w + 1] = fma2(r2, hi2(a4), h[2 * w + 1]);
+                    if (RPT == 2) {
+                        p[2 * w] = fma2(rr2, lo2(a4), p[2 * w]);
+                        p[2 * w + 1] = fma2(rr2, hi2(a4), p[2 * w + 1]);
+                    }
                 }
                 if (part == 0) {
-                    const float num = fmaf(r, s_ga[q], sq);
-                    gout[(size_t)(m * kTT + q) * D + row] = f32_to_io<IO>(num * s_den[q]);
+                    const float ga = s_ga[q], rd = s_den[q];
+                    gout[(size_t)(m * kTT + q) * D + row] = f32_to_io<IO>(fmaf(r, ga, sq) * rd);
+                    if (RPT == 2)
+                        gout[(size_t)(m * kTT + q) * D + row + ROW2] = f32_to_io<IO>(fmaf(r2s, ga, sq2) * rd);
                 }
             }
         }
@@ -914,20 +1032,22 @@ constexpr int kRB = 16;
 
 template <int D>
 struct ChainSmem {
-    static constexpr size_t bars = 0;
-    static constexpr size_t P = 128;                                 // [2][D][D]
-    static constexpr size_t H = P + 2 * (size_t)D * D * 4;           // [2][RB][D]
-    static constexpr size_t S = H + 2 * (size_t)kRB * D * 4;         // [RB][D]
+    static constexpr int NS = (D == 128) ? 2 : 4;                    // prefetch depth (chunk maps in flight)
+    static constexpr size_t bars = 0;                                // NS mbarriers + abort flag
+    static constexpr size_t P = 128;                                 // [NS][D][D]
+    static constexpr size_t H = P + NS * (size_t)D * D * 4;          // [NS][RB][D]
+    static constexpr size_t S = H + NS * (size_t)kRB * D * 4;        // [RB][D]
     static constexpr size_t total = S + (size_t)kRB * D * 4;
 };
 
 template <int D>
 __global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
     using Lo = ChainSmem<D>;
+    constexpr int NS = Lo::NS;
     constexpr int OPT = kRB * D / 256;  // outputs per thread: one row, OPT consecutive columns
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 8 * NS);
     float *sP = reinterpret_cast<float *>(smem + Lo::P);
     float *sH = reinterpret_cast<float *>(smem + Lo::H);
     float *sS = reinterpret_cast<float *>(smem + Lo::S);
@@ -941,8 +1061,7 @@ __global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
     float *gS = ws_f(a, a.L.off_S) + (size_t)bh * NC * D * D + (size_t)rb * kRB * D;
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -954,24 +1073,23 @@ __global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
     for (int q = 0; q < OPT; ++q) sS[r * D + j0 + q] = s[q];
     __syncthreads();
     auto issue = [&](int cc) {
-        const int buf = cc & 1;
+        const int buf = cc % NS;
         mbar_arrive_expect_tx(&bars[buf], (uint32_t)((D * D + kRB * D) * 4));
         bulk_g2s(sP + (size_t)buf * D * D, gP + (size_t)cc * D * D, (uint32_t)(D * D * 4), &bars[buf]);
         bulk_g2s(sH + (size_t)buf * kRB * D, gH + (size_t)cc * D * D, (uint32_t)(kRB * D * 4), &bars[buf]);
     };
     int issued = 0;
     if (tid == 0) {
-        if (NC > 0) issue(0);
-        if (NC > 1) issue(1);
-        issued = min(NC, 2);
+        for (int cc = 0; cc < NS && cc < NC; ++cc) issue(cc);
+        issued = min(NC, NS);
     }
     int failed = -1;
     for (int cc = 0; cc < NC; ++cc) {
         // chunk-start state S^(cc)
 #pragma unroll
         for (int q = 0; q < OPT; ++q) gS[(size_t)cc * D * D + r * D + j0 + q] = s[q];
-        const int buf = cc & 1;
-        if (!mbar_wait_bounded(&bars[buf], (cc >> 1) & 1, a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+        const int buf = cc % NS;
+        if (!mbar_wait_bounded(&bars[buf], (cc / NS) & 1, a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
         __syncthreads();
         if (*abort_flag) {
             failed = cc;
@@ -995,16 +1113,16 @@ __global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
             s[q] = acc[q];
             sS[r * D + j0 + q] = acc[q];
         }
-        if (tid == 0 && cc + 2 < NC) {
-            issue(cc + 2);
-            issued = cc + 3;
+        if (tid == 0 && cc + NS < NC) {
+            issue(cc + NS);
+            issued = cc + NS + 1;
         }
         __syncthreads();
     }
     if (failed >= 0) {
         if (tid == 0)
             for (int m = failed; m < issued; ++m)
-                (void)mbar_wait_bounded(&bars[m & 1], (m >> 1) & 1, a.p.wait_limit_ns, a.p.err);
+                (void)mbar_wait_bounded(&bars[m % NS], (m / NS) & 1, a.p.wait_limit_ns, a.p.err);
         return;
     }
 #pragma unroll
@@ -1069,13 +1187,13 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     gates_kernel<D, IO><<<(unsigned)(NC * BH), G::NT, GatesSmem<D, IO>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), R::NT, RowsSmem<D, IO>::total, st>>>(a);
+    rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), RowsCfg<D, 0>::NT, RowsSmem<D, IO>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
     chain_kernel<D><<<(unsigned)((D / kRB) * BH), 256, ChainSmem<D>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    rows_kernel<D, IO, 1><<<(unsigned)(NC * BH), R::NT, RowsSmem<D, IO>::total, st>>>(a);
+    rows_kernel<D, IO, 1><<<(unsigned)(NC * BH), RowsCfg<D, 1>::NT, RowsSmem<D, IO>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
     return cudaSuccess;
