@@ -61,10 +61,6 @@ int resolve_kernel(int B, int H, int T, int d_h, int kernel) {
     return VLA_KERNEL_SEQ;
 }
 
-int chunk_len(int B, int H, int T, int d_h, int chunk) {
-    if (chunk > 0) return chunk;
-    return vla::chunk_default(B * H, T, d_h);
-}
 
 }  // namespace
 
@@ -73,7 +69,6 @@ namespace vla {
 int api_check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int kernel) {
     return check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
 }
-int api_chunk_len(int B, int H, int T, int d_h, int chunk) { return chunk_len(B, H, T, d_h, chunk); }
 int *api_device_err_word() { return device_err_word(); }
 long long api_wait_limit_ns() { return g_wait_limit_ns; }
 int api_cuda_fail(cudaError_t e) { return cuda_fail(e); }
@@ -122,7 +117,7 @@ size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kerne
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return 0;
     const int kk = resolve_kernel(B, H, T, d_h, kernel);
     if (kk != VLA_KERNEL_CHUNK || T == 0 || (long long)B * H == 0) return 0;
-    return vla::chunk_layout(B * H, T, d_h, chunk_len(B, H, T, d_h, chunk)).total;
+    return vla::chunk_layout(B * H, T, d_h, chunk).total;
 }
 
 int vla_debug_inject(int mode, long long wait_limit_ns) {
@@ -197,7 +192,7 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (kk == VLA_KERNEL_CHUNK && T > 0) {
-        const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk_len(B, H, T, d_h, chunk));
+        const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk);
         e = vla::launch_chunk(p, L, st);
     } else if (kk == VLA_KERNEL_DECODE) {
         e = vla::launch_decode(p, st);

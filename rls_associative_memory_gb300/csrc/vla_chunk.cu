@@ -55,8 +55,8 @@ __global__ void __launch_bounds__(256) gram_kernel(ChunkArgs a) {
     constexpr int MT = D / 16;  // microtile edge on a 16 x 16 thread grid
     __shared__ __align__(16) float su[kTT][D];
     __shared__ __align__(16) float sf[kTT][D];
-    const int c = (int)(blockIdx.x % (unsigned)a.L.NC), bh = (int)(blockIdx.x / (unsigned)a.L.NC);
-    const int T = a.p.T, C = a.L.C;
+    const int c = (int)(blockIdx.x % (unsigned)a.L.NCA), bh = (int)(blockIdx.x / (unsigned)a.L.NCA);
+    const int T = a.p.T, C = a.L.CA;
     const int t0 = c * C, t1 = min(T, t0 + C);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ty = tid >> 4, tx = tid & 15;
@@ -104,12 +104,12 @@ __global__ void __launch_bounds__(256) gram_kernel(ChunkArgs a) {
         }
         __syncthreads();
     }
-    float *G = ws_f(a, a.L.off_M) + ((size_t)bh * a.L.NC + c) * D * D;
+    float *G = ws_f(a, a.L.off_M) + ((size_t)bh * a.L.NCA + c) * D * D;
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int n = 0; n < MT; ++n) G[(ty * MT + m) * D + tx * MT + n] = acc[m][n];
-    if (tid < D) ws_f(a, a.L.off_n)[((size_t)bh * (a.L.NC + 1) + c) * D + tid] = nacc;
+    if (tid < D) ws_f(a, a.L.off_n)[((size_t)bh * (a.L.NCA + 1) + c) * D + tid] = nacc;
 }
 
 // ---------------------------------------------------------------------------
@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(GramTc<D>::NT) gram_tc_kernel(ChunkArgs a) {
     unsigned char *abuf = smem + G::abuf;
     float *nred = reinterpret_cast<float *>(smem + G::nred);
 
-    const int c = (int)(blockIdx.x % (unsigned)a.L.NC), bh = (int)(blockIdx.x / (unsigned)a.L.NC);
-    const int T = a.p.T, C = a.L.C;
+    const int c = (int)(blockIdx.x % (unsigned)a.L.NCA), bh = (int)(blockIdx.x / (unsigned)a.L.NCA);
+    const int T = a.p.T, C = a.L.CA;
     const int t0 = c * C, ntok = min(C, T - t0);
     const int nst = (ntok + KS - 1) / KS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(GramTc<D>::NT) gram_tc_kernel(ChunkArgs a) {
         return;
     }
     // ---- G out: accumulator rows from TMEM ----
-    float *Gout = ws_f(a, a.L.off_M) + ((size_t)bh * a.L.NC + c) * D * D;
+    float *Gout = ws_f(a, a.L.off_M) + ((size_t)bh * a.L.NCA + c) * D * D;
     const bool has_row = (D == 128) || (lane < 16);
     const int grow = (D == 128) ? (32 * warp + lane) : (16 * warp + lane);
 #pragma unroll
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(GramTc<D>::NT) gram_tc_kernel(ChunkArgs a) {
         float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < NT / 32; ++w) sum += nred[w * D + tid];
-        ws_f(a, a.L.off_n)[((size_t)bh * (a.L.NC + 1) + c) * D + tid] = sum;
+        ws_f(a, a.L.off_n)[((size_t)bh * (a.L.NCA + 1) + c) * D + tid] = sum;
     }
 }
 
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(256) prefix_kernel(ChunkArgs a) {
     constexpr int NB = (D * D + D + 255) / 256;  // blocks per (b, h)
     const int bh = (int)(blockIdx.x / NB);
     const int e = (int)(blockIdx.x % NB) * 256 + threadIdx.x;
-    const int NC = a.L.NC;
+    const int NC = a.L.NCA;  // A-chunks
     if (e < D * D) {
         const int i = e / D, j = e % D;
         float run = a.p.A0 ? ws_f(a, a.L.off_M0)[(size_t)bh * D * D + e] : (i == j ? a.p.lambda0 : 0.f);
@@ -518,8 +518,8 @@ __global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
     float *s_piv = reinterpret_cast<float *>(smem + Lo::piv);
     float4 *s_red = reinterpret_cast<float4 *>(smem + Lo::red);
 
-    const int c = (int)(blockIdx.x % (unsigned)a.L.NC), bh = (int)(blockIdx.x / (unsigned)a.L.NC);
-    const int T = a.p.T, C = a.L.C, NC = a.L.NC;
+    const int c = (int)(blockIdx.x % (unsigned)a.L.NCA), bh = (int)(blockIdx.x / (unsigned)a.L.NCA);
+    const int T = a.p.T, C = a.L.CA, NC = a.L.NCA;  // A-chunks
     const int t0 = c * C, ntok = min(C, T - t0);
     const int ntiles = (ntok + kTT - 1) / kTT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -851,7 +851,8 @@ __global__ void __launch_bounds__(RowsCfg<D, MODE>::NT) rows_kernel(ChunkArgs a)
         }
     }
     float nbase = 0.f;
-    if (MODE == 1 && tid < D) nbase = ws_f(a, a.L.off_n)[((size_t)bh * (NC + 1) + c) * D + tid];
+    if (MODE == 1 && tid < D)  // n^(c) at this S-chunk's start = at A-chunk c * C / CA
+        nbase = ws_f(a, a.L.off_n)[((size_t)bh * (a.L.NCA + 1) + (size_t)c * (C / a.L.CA)) * D + tid];
 
     int failed = -1;
     for (int m = 0; m < ntiles; ++m) {
@@ -1028,30 +1029,36 @@ __global__ void __launch_bounds__(RowsCfg<D, MODE>::NT) rows_kernel(ChunkArgs a)
 // ---------------------------------------------------------------------------
 // chain: S^(c+1) = S^(c) P_c + H_c for a block of RB rows of S
 // ---------------------------------------------------------------------------
-constexpr int kRB = 16;
+// Rows of S per chain CTA: few rows per CTA keep each step a single short dot
+// product per thread (one or two outputs), with many CTAs walking the chain
+// side by side; every CTA of a (b, h) reads the same chunk maps (L2 hits).
+template <int D>
+constexpr int chain_rows() { return D == 32 ? 8 : 4; }
 
 template <int D>
 struct ChainSmem {
+    static constexpr int RB = chain_rows<D>();
     static constexpr int NS = (D == 128) ? 2 : 4;                    // prefetch depth (chunk maps in flight)
     static constexpr size_t bars = 0;                                // NS mbarriers + abort flag
     static constexpr size_t P = 128;                                 // [NS][D][D]
     static constexpr size_t H = P + NS * (size_t)D * D * 4;          // [NS][RB][D]
-    static constexpr size_t S = H + NS * (size_t)kRB * D * 4;        // [RB][D]
-    static constexpr size_t total = S + (size_t)kRB * D * 4;
+    static constexpr size_t S = H + NS * (size_t)RB * D * 4;         // [RB][D]
+    static constexpr size_t total = S + (size_t)RB * D * 4;
 };
 
 template <int D>
 __global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
     using Lo = ChainSmem<D>;
-    constexpr int NS = Lo::NS;
+    constexpr int NS = Lo::NS, kRB = Lo::RB;
     constexpr int OPT = kRB * D / 256;  // outputs per thread: one row, OPT consecutive columns
+    static_assert(OPT >= 1, "at least one output per thread");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 8 * NS);
     float *sP = reinterpret_cast<float *>(smem + Lo::P);
     float *sH = reinterpret_cast<float *>(smem + Lo::H);
     float *sS = reinterpret_cast<float *>(smem + Lo::S);
-    const int rb = (int)(blockIdx.x % (D / kRB)), bh = (int)(blockIdx.x / (D / kRB));
+    const int rb = (int)(blockIdx.x % (D / kRB)), bh = (int)(blockIdx.x / (D / kRB));  // row block, unit
     const int NC = a.L.NC;
     const int tid = threadIdx.x;
     const int r = tid / (D / OPT), j0 = (tid % (D / OPT)) * OPT;
@@ -1156,8 +1163,8 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 template <int D, typename IO>
 cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     using R = RowCfg<D>;
-    const long long BH = a.p.BH, NC = a.L.NC;
-    if (NC * BH > 0x7fffffffLL || BH * ((D * D + D + 255) / 256) > 0x7fffffffLL)
+    const long long BH = a.p.BH, NC = a.L.NC, NCA = a.L.NCA;
+    if (NCA * BH > 0x7fffffffLL || BH * ((D * D + D + 255) / 256) > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     cudaError_t e;
     if ((e = set_smem(gates_kernel<D, IO>, GatesSmem<D, IO>::total)) != cudaSuccess) return e;
@@ -1175,22 +1182,22 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
         mark_launch(a.p, ++n, st);
     }
     if constexpr (sizeof(IO) == 2 && D >= 64) {
-        gram_tc_kernel<D><<<(unsigned)(NC * BH), GramTc<D>::NT, GramTc<D>::total, st>>>(a);
+        gram_tc_kernel<D><<<(unsigned)(NCA * BH), GramTc<D>::NT, GramTc<D>::total, st>>>(a);
     } else {
-        gram_kernel<D, IO><<<(unsigned)(NC * BH), 256, 0, st>>>(a);
+        gram_kernel<D, IO><<<(unsigned)(NCA * BH), 256, 0, st>>>(a);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
     prefix_kernel<D><<<(unsigned)(((D * D + D + 255) / 256) * BH), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    gates_kernel<D, IO><<<(unsigned)(NC * BH), G::NT, GatesSmem<D, IO>::total, st>>>(a);
+    gates_kernel<D, IO><<<(unsigned)(NCA * BH), G::NT, GatesSmem<D, IO>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
     rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), RowsCfg<D, 0>::NT, RowsSmem<D, IO>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    chain_kernel<D><<<(unsigned)((D / kRB) * BH), 256, ChainSmem<D>::total, st>>>(a);
+    chain_kernel<D><<<(unsigned)((D / chain_rows<D>()) * BH), 256, ChainSmem<D>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
     rows_kernel<D, IO, 1><<<(unsigned)(NC * BH), RowsCfg<D, 1>::NT, RowsSmem<D, IO>::total, st>>>(a);
@@ -1203,21 +1210,45 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
-int chunk_default(int BH, int T, int d) {
-    (void)d;
+// S-chunk length: long chunks keep the chain along the chunks short.
+int chunk_default(int BH, int T) {
     int C = T >= 16384 ? 512 : (T >= 4096 ? 256 : (T >= 1024 ? 128 : 64));
     while (C > 64 && (long long)BH * ((T + C - 1) / C) < 2 * 152) C /= 2;
     return C;
 }
 
-ChunkLayout chunk_layout(int BH, int T, int d, int C) {
+// A-chunk length (divides C): the gates pass is a latency-bound recurrence,
+// one CTA per A-chunk, so pick the length that minimises
+// waves x (chunk length + Gauss-Jordan restart), with the resident CTAs per
+// SM of each d on the 152 SMs of a GB300.
+int chunk_default_a(int BH, int T, int d, int C) {
+    const long long resident = 152LL * (d == 32 ? 32 : (d == 64 ? 10 : 1));
+    const int restart = 20;  // Gauss-Jordan inverse, in token-steps
+    int best = C;
+    long long best_cost = -1;
+    for (int CA = C; CA >= 64; CA /= 2) {
+        if (C % CA) continue;
+        const long long chunks = (long long)BH * ((T + CA - 1) / CA);
+        const long long waves = (chunks + resident - 1) / resident;
+        const long long cost = waves * (CA + restart);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = CA;
+        }
+    }
+    return best;
+}
+
+ChunkLayout chunk_layout(int BH, int T, int d, int chunk) {
     ChunkLayout L{};
-    L.C = C;
-    L.NC = (T + C - 1) / C;
-    const size_t bh = (size_t)BH, nc = (size_t)L.NC, dd = (size_t)d * d;
+    L.C = chunk > 0 ? chunk : chunk_default(BH, T);
+    L.CA = chunk > 0 ? chunk : chunk_default_a(BH, T, d, L.C);
+    L.NC = (T + L.C - 1) / L.C;
+    L.NCA = (T + L.CA - 1) / L.CA;
+    const size_t bh = (size_t)BH, nc = (size_t)L.NC, nca = (size_t)L.NCA, dd = (size_t)d * d;
     size_t off = 0;
-    L.off_M = off; off = align256(off + bh * nc * dd * 4);
-    L.off_n = off; off = align256(off + bh * (nc + 1) * d * 4);
+    L.off_M = off; off = align256(off + bh * nca * dd * 4);
+    L.off_n = off; off = align256(off + bh * (nca + 1) * d * 4);
     L.off_M0 = off; off = align256(off + bh * dd * 4);
     L.off_alpha = off; off = align256(off + bh * (size_t)T * d * 4);
     L.off_P = off; off = align256(off + bh * nc * dd * 4);

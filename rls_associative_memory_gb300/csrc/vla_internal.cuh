@@ -54,11 +54,15 @@ cudaError_t launch_seq(const FwdParams &p, cudaStream_t stream);
 cudaError_t launch_decode(const FwdParams &p, cudaStream_t stream);
 
 // Workspace of the chunk-parallel path (byte offsets, 256-byte aligned).
+// Two chunkings of the token axis: A-chunks of CA tokens (Grams, prefix,
+// gates) and S-chunks of C tokens (transitions, chain, readout); CA divides C.
 struct ChunkLayout {
-    int C;               // chunk length (multiple of 16)
-    int NC;              // chunks per (b, h) = ceil(T / C)
-    size_t off_M;        // [BH][NC][d][d]  chunk Grams, then exclusive prefix M^(c)
-    size_t off_n;        // [BH][NC+1][d]   chunk sums of phi(k_hat), then exclusive prefix n^(c)
+    int C;               // S-chunk length (multiple of 16)
+    int NC;              // S-chunks per (b, h) = ceil(T / C)
+    int CA;              // A-chunk length (multiple of 16, divides C)
+    int NCA;             // A-chunks per (b, h) = ceil(T / CA)
+    size_t off_M;        // [BH][NCA][d][d]  A-chunk Grams, then exclusive prefix M^(c)
+    size_t off_n;        // [BH][NCA+1][d]   A-chunk sums of phi(k_hat), then exclusive prefix n^(c)
     size_t off_M0;       // [BH][d][d]      inverse of A0 (only when A0 is given)
     size_t off_alpha;    // [BH][T][d]      unit gates alpha_t
     size_t off_P;        // [BH][NC][d][d]  chunk transition P_c
@@ -69,15 +73,13 @@ struct ChunkLayout {
 
 // C-ABI helpers defined in vla_api.cu, shared by the other entry points.
 int api_check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int kernel);
-int api_chunk_len(int B, int H, int T, int d_h, int chunk);
 int *api_device_err_word();
 long long api_wait_limit_ns();
 int api_cuda_fail(cudaError_t e);
 
-// Default chunk length for a shape (chunk == 0 in the API).
-int chunk_default(int BH, int T, int d);
-// Layout for the given shape; C must be a positive multiple of 16.
-ChunkLayout chunk_layout(int BH, int T, int d, int C);
+// Layout for a shape; chunk > 0 (a multiple of 16) sets both chunk lengths,
+// chunk == 0 picks the defaults.
+ChunkLayout chunk_layout(int BH, int T, int d, int chunk);
 // Chunk-parallel path (six launches).  Returns a cudaError_t.
 cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream);
 

@@ -61,7 +61,7 @@ extern "C" int vla_forward_noalloc(const void *q, const void *k, const void *v, 
 
     vla::ChunkLayout L{};
     if (T > 0) {
-        L = vla::chunk_layout((int)BH, T, d_h, vla::api_chunk_len(B, H, T, d_h, chunk));
+        L = vla::chunk_layout((int)BH, T, d_h, chunk);
         if (L.total > (size_t)VLA_NOALLOC_SCRATCH_BYTES) return VLA_ERR_SCRATCH_LIMIT;
     }
     void *scratch = nullptr;
