@@ -273,6 +273,46 @@ def type_of(v):
     return v
 
 
+def run_backward(args):
+    """--pass backward: gradients of sum <dO, o> for one batch of the workload
+    (vla_backward: forward recompute + reverse sweep in one launch)."""
+    import torch
+    import rls_associative_memory_gb300 as vla
+    dev = torch.device("cuda", 0)
+    x = make_host_inputs(args.config, 0, parse_overrides(args))
+    B, H, T, d = x.q.shape
+    hq, hk, hv, hu = to_torch_host(x, pin=False)
+    q, k, v, u = (t.to(dev) for t in (hq, hk, hv, hu))
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    dO = torch.randn(q.shape, generator=gen).to(q.dtype).to(dev)
+    ws = torch.empty(vla.vla_backward_workspace_bytes(B, H, T, d), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        vla.vla_backward(q, k, v, u, dO, x.lambda0, workspace=ws)
+    torch.cuda.synchronize(dev)
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        st[i].record()
+        vla.vla_backward(q, k, v, u, dO, x.lambda0, workspace=ws)
+        en[i].record()
+    torch.cuda.synchronize(dev)
+    ms = float(np.mean([a.elapsed_time(b) for a, b in zip(st, en)]))
+    units = B * H * T
+    # forward recompute (12 d^2) + reverse sweep (28 d^2: four matrix-vector
+    # products, three column sums, six rank-1 updates, two state undos)
+    flops = units * (40 * d * d + 64 * d)
+    tf = flops / (ms / 1e3) / 1e12
+    line = {"metric": "VLA backward tokens*heads/sec", "value": units / (ms / 1e3), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "f32", "data": "synthetic", "config": config_block(args.config, x, "backward"),
+            "roofline": {"bound": "alu", "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                         "frac": tf / FP32_PEAK_TFLOPS, "traffic": None, "kernel": "backward_kernel<%d,%s>" % (d, x.dtype),
+                         "algorithmic_flops": flops},
+            "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -285,11 +325,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=64)
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         log("note: fewer than 3 warm-up steps")
     if args.impl == "reference":
         return run_reference(args)
+    if args.which == "backward":
+        return run_backward(args)
 
     import torch
     import rls_associative_memory_gb300 as vla

@@ -127,6 +127,37 @@ int vla_set_launch_events(void *const *events, int n);
  * chunked one). */
 int vla_last_launch_count(void);
 
+/*
+ * vla_backward -- gradients of the recurrence (reverse mode).
+ *
+ * Loss L = sum_t <dO_t, o_t> + <dS_T, S_T> + <dA_T, A_T> + <dn_T, n_T>, with
+ * o, S_T, A_T, n_T the outputs of vla_forward on the same inputs and initial
+ * state.  The transition of S, J_t = I - alpha_t k_hat_t^T, is the one of
+ * section 3.1 (Proposition 2); at |k| <= eps or |A_t k_hat| <= eps the
+ * max(., eps) guards pass the gradient of their constant branch.
+ *
+ * q, k, v, u, dO  [B,H,T,d] io_dtype (dO: upstream gradient of o).
+ * S0, A0, n0      initial state as in vla_forward (NULL = defaults).
+ * dS_T, dA_T, dn_T upstream gradients of the final state, or NULL (= 0).
+ * dq, dk, dv, du  [B,H,T,d] fp32, written when non-NULL.
+ * dS0, dA0, dn0   gradients of the initial state ([B,H,d,d], [B,H,d,d],
+ *                 [B,H,d] fp32), written when non-NULL.  dA0 is the full,
+ *                 unsymmetrised adjoint of A_0.
+ * d_h             32 or 64 (VLA_ERR_UNSUPPORTED_DIM otherwise).
+ * workspace       at least vla_backward_workspace_bytes(B, H, T, d_h) bytes.
+ * One CTA per (b, h) reruns the forward, storing per-token records and a
+ * state checkpoint every 64 tokens, then sweeps the tokens in reverse.
+ * Asynchronous on stream; returns VLA_OK or a VLA_ERR_* code.
+ */
+int vla_backward(const void *q, const void *k, const void *v, const void *u, const void *dO,
+                 int io_dtype, float lambda0, int B, int H, int T, int d_h, const float *S0,
+                 const float *A0, const float *n0, const float *dS_T, const float *dA_T,
+                 const float *dn_T, float *dq, float *dk, float *dv, float *du, float *dS0,
+                 float *dA0, float *dn0, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes of vla_backward (0 for invalid arguments). */
+size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h);
+
 /* Size of the device scratch array built into the library for
  * vla_forward_noalloc (64 MiB on every GPU that loads the library). */
 #define VLA_NOALLOC_SCRATCH_BYTES (64ull << 20)

@@ -23,6 +23,8 @@ from ._lib import (  # noqa: F401
     VLAError,
     lib,
     lib_path,
+    vla_backward,
+    vla_backward_workspace_bytes,
     vla_debug_inject,
     vla_device_status,
     vla_forward,

@@ -51,6 +51,8 @@ _SIGS = {
     "vla_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, ctypes.c_float, _i, _i, _i, _i, _vp, _vp, _vp,
                                  _vp, _vp, _vp, _vp, _i, _vp]),
     "vla_last_launch_count": (_i, []),
+    "vla_backward": (_i, [_vp] * 5 + [_i, ctypes.c_float, _i, _i, _i, _i] + [_vp] * 14 + [ctypes.c_size_t, _vp]),
+    "vla_backward_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
     "vla_version": (_i, []),
 }
 
@@ -129,6 +131,43 @@ def vla_set_launch_events(events) -> int:
 
 def vla_last_launch_count() -> int:
     return int(lib().vla_last_launch_count())
+
+
+def vla_backward_workspace_bytes(B, H, T, d_h) -> int:
+    return int(lib().vla_backward_workspace_bytes(B, H, T, d_h))
+
+
+def vla_backward(q, k, v, u, dO, lambda0: float, S0=None, A0=None, n0=None, dS_T=None, dA_T=None, dn_T=None,
+                 workspace=None, stream=None):
+    """Gradients of sum <dO, o> + <dS_T, S_T> + <dA_T, A_T> + <dn_T, n_T>.
+
+    Inputs as for vla_forward plus dO (same shape and dtype as q).  Returns
+    a dict of fp32 CUDA tensors dq, dk, dv, du, dS0, dA0, dn0.
+    """
+    import torch
+    B, H, T, d = q.shape
+    for t in (k, v, u, dO):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("q, k, v, u, dO must share shape and dtype and be contiguous")
+    io = VLA_BF16 if q.dtype == torch.bfloat16 else VLA_F32
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {n: torch.empty((B, H, T, d), **f32) for n in ("dq", "dk", "dv", "du")}
+    g["dS0"] = torch.empty((B, H, d, d), **f32)
+    g["dA0"] = torch.empty((B, H, d, d), **f32)
+    g["dn0"] = torch.empty((B, H, d), **f32)
+    need = vla_backward_workspace_bytes(B, H, T, d)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    rc = lib().vla_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(u), _ptr(dO), io, float(lambda0), B, H, T, d,
+                            _ptr(S0), _ptr(A0), _ptr(n0), _ptr(dS_T), _ptr(dA_T), _ptr(dn_T),
+                            _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["du"]), _ptr(g["dS0"]),
+                            _ptr(g["dA0"]), _ptr(g["dn0"]), _ptr(workspace), ws_bytes, ctypes.c_void_p(s.cuda_stream))
+    if rc != VLA_OK:
+        raise VLAError(rc, "vla_backward")
+    return g
 
 
 def _ptr(t) -> Optional[int]:

@@ -120,6 +120,39 @@ size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kerne
     return vla::chunk_layout(B * H, T, d_h, chunk).total;
 }
 
+size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h) {
+    if (check_common(VLA_F32, 1.f, B, H, T, d_h, VLA_KERNEL_AUTO) != VLA_OK) return 0;
+    if (d_h != 32 && d_h != 64) return 0;
+    return vla::backward_workspace_floats(B * H, T, d_h) * sizeof(float);
+}
+
+int vla_backward(const void *q, const void *k, const void *v, const void *u, const void *dO, int io_dtype,
+                 float lambda0, int B, int H, int T, int d_h, const float *S0, const float *A0, const float *n0,
+                 const float *dS_T, const float *dA_T, const float *dn_T, float *dq, float *dk, float *dv,
+                 float *du, float *dS0, float *dA0, float *dn0, void *workspace, size_t ws_bytes, void *stream) {
+    int rc = check_common(io_dtype, lambda0, B, H, T, d_h, VLA_KERNEL_AUTO);
+    if (rc != VLA_OK) return rc;
+    if (d_h != 32 && d_h != 64) return VLA_ERR_UNSUPPORTED_DIM;
+    const long long BH = (long long)B * H;
+    if (BH > 0 && T > 0 && (!q || !k || !v || !u || !dO)) return VLA_ERR_ARG;
+    const void *ptrs[] = {q, k, v, u, dO, S0, A0, n0, dS_T, dA_T, dn_T, dq, dk, dv, du, dS0, dA0, dn0, workspace};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return VLA_ERR_ALIGN;
+    const size_t need = vla_backward_workspace_bytes(B, H, T, d_h);
+    if (need > 0 && (!workspace || ws_bytes < need)) return VLA_ERR_WORKSPACE;
+    if (BH == 0) return VLA_OK;
+    vla::BwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.u = u; p.dO = dO;
+    p.S0 = S0; p.A0 = A0; p.n0 = n0; p.dS_T = dS_T; p.dA_T = dA_T; p.dn_T = dn_T;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.du = du; p.dS0 = dS0; p.dA0 = dA0; p.dn0 = dn0;
+    p.BH = (int)BH; p.T = T; p.d = d_h; p.io_bf16 = (io_dtype == VLA_BF16); p.lambda0 = lambda0;
+    p.ws = static_cast<float *>(workspace);
+    const cudaError_t e = vla::launch_backward(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    t_last_launches = 1;
+    return VLA_OK;
+}
+
 int vla_debug_inject(int mode, long long wait_limit_ns) {
     if (mode != 0 && mode != 1) return VLA_ERR_ARG;
     g_inject = mode;

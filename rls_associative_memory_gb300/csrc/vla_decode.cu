@@ -26,22 +26,6 @@ struct DecCfg {
     static constexpr int VLEN = TPR * kPart;
 };
 
-// Block-wide sum of four values; every thread gets the four totals.
-template <int NW>
-__device__ __forceinline__ float4 block_sum4(float v0, float v1, float v2, float v3, float4 *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float r = warp_reduce4(v0, v1, v2, v3);
-    if ((lane & 7) == 0) reinterpret_cast<float *>(red)[warp * 4 + (lane >> 3)] = r;
-    __syncthreads();
-    float4 acc = red[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) {
-        const float4 x = red[w];
-        acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
-    }
-    return acc;
-}
-
 template <int D, typename IO>
 __global__ void __launch_bounds__(DecCfg<D>::NT) decode_kernel(FwdParams p) {
     using C = DecCfg<D>;

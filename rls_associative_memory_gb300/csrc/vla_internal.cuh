@@ -50,6 +50,19 @@ inline void mark_launch(const FwdParams &p, int i, cudaStream_t st) {
 // Sequential kernel: one CTA per (b, h).  Returns a cudaError_t.
 cudaError_t launch_seq(const FwdParams &p, cudaStream_t stream);
 
+// Backward pass (gradients of the recurrence); one CTA per (b, h).
+struct BwdParams {
+    const void *q, *k, *v, *u, *dO;                  // [BH, T, d] io dtype
+    const float *S0, *A0, *n0, *dS_T, *dA_T, *dn_T;  // optional
+    float *dq, *dk, *dv, *du;                        // [BH, T, d] fp32 (each optional)
+    float *dS0, *dA0, *dn0;                          // optional
+    int BH, T, d, io_bf16;
+    float lambda0;
+    float *ws;                                       // backward_workspace_floats(BH, T, d) floats
+};
+size_t backward_workspace_floats(int BH, int T, int d);
+cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
+
 // Decode step: one CTA per (b, h), state streamed from HBM.  Returns a cudaError_t.
 cudaError_t launch_decode(const FwdParams &p, cudaStream_t stream);
 
@@ -242,6 +255,24 @@ __device__ __forceinline__ float warp_reduce4(float v0, float v1, float v2, floa
     b += __shfl_xor_sync(0xffffffffu, b, 2);
     b += __shfl_xor_sync(0xffffffffu, b, 1);
     return b;
+}
+
+// Block-wide sum of four values over NW warps; every thread gets the four
+// totals.  red: NW float4 of shared memory, not reused before the next
+// block barrier.
+template <int NW>
+__device__ __forceinline__ float4 block_sum4(float v0, float v1, float v2, float v3, float4 *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float r = warp_reduce4(v0, v1, v2, v3);
+    if ((lane & 7) == 0) reinterpret_cast<float *>(red)[warp * 4 + (lane >> 3)] = r;
+    __syncthreads();
+    float4 acc = red[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+        const float4 x = red[w];
+        acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+    }
+    return acc;
 }
 
 __device__ __forceinline__ float warp_sum(float x) {

@@ -114,6 +114,20 @@ def test_workspace_query_and_kernel_selection():
     assert vla.vla_select_kernel(1, 16, 4096, 40) == vla.VLA_ERR_UNSUPPORTED_DIM
 
 
+def test_backward_argument_checks():
+    f = 1 << 20
+    L = vla.lib()
+    args = lambda **kw: [kw.get(n, f) for n in ("q", "k", "v", "u", "dO")] + [  # noqa: E731
+        kw.get("io", vla.VLA_BF16), 1.0, 1, 2, 16, kw.get("d", 64)] + [None] * 6 + [f] * 7 + [
+        kw.get("ws", None), kw.get("wsb", 0), None]
+    assert L.vla_backward(*args(d=128)) == vla.VLA_ERR_UNSUPPORTED_DIM
+    assert L.vla_backward(*args()) == vla.VLA_ERR_WORKSPACE
+    assert L.vla_backward(*args(dO=None)) == vla.VLA_ERR_ARG
+    assert L.vla_backward(*args(k=f + 4)) == vla.VLA_ERR_ALIGN
+    assert vla.vla_backward_workspace_bytes(1, 2, 16, 128) == 0
+    assert vla.vla_backward_workspace_bytes(1, 2, 16, 64) == 2 * (16 * 260 + 1 * (2 * 64 * 64 + 64)) * 4
+
+
 def test_debug_hook_is_host_state_only():
     assert vla.vla_debug_inject(2) == vla.VLA_ERR_ARG
     assert vla.vla_debug_inject(1, 1000) == vla.VLA_OK
