@@ -472,8 +472,9 @@ __device__ __forceinline__ void issue_tile(uint64_t *bar, void *const *dst, cons
 // Thread layout: thread (rows row0 + r * RSTRIDE, part p) owns CPT columns of
 // RPT rows of A.  d = 64: two warps per chunk, a whole row per thread;
 // d = 128: 256 threads, half a row each; d = 32: one warp, a row each.  (Two
-// rows per lane with one warp per chunk was measured 24% slower at d = 64:
-// the per-token dependency chain doubles while few more chunks fit per SM.)
+// rows per lane was measured slower at d = 64, both with one warp per chunk
+// (1.20 -> 1.49 ms) and with 32 columns x two rows per thread (-> 1.55 ms):
+// fewer A-chains fit per SM and the pass is bound by chains in flight.)
 template <int D>
 struct GatesCfg {
     static constexpr int CPT = (D >= 64) ? 64 : 32;
