@@ -52,11 +52,15 @@ TRAFFIC = {
 
 
 def kernel_src_hash(kernel_name: str) -> str:
-    fn = {"seq": "vla_seq.cu", "chunk": "vla_chunk.cu", "decode": "vla_decode.cu"}[kernel_name]
-    path = os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", fn)
-    if not os.path.exists(path):
-        return ""
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    fns = {"seq": ["vla_seq.cu"], "chunk": ["vla_chunk.cu"], "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu"],
+           "decode": ["vla_decode.cu"]}[kernel_name]
+    h = hashlib.sha256()
+    for fn in fns:
+        path = os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", fn)
+        if not os.path.exists(path):
+            return ""
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
 
 
 # Kernels of one step, in launch order, and the share of the algorithmic
@@ -73,9 +77,11 @@ def kernel_plan(kname, d, io_dtype="bf16"):
     # gates: key norm, z = A u, rank-1 update, A k_hat, gate norm (a0-a2);
     # output: S k_hat, state write, S phi(q), readout (a3-a4)
     gram = "gram_tc_kernel" if (io_dtype == "bf16" and d >= 64) else "gram_kernel"
+    # chunk_tc at d = 64 with bf16 I/O: the state passes run on the tensor cores
+    rows = "rows_tc_kernel" if (kname == "chunk_tc" and io_dtype == "bf16" and d == 64) else "rows_kernel"
     return [(gram, 0, "alu"), ("prefix_kernel", 0, "alu"), ("gates_kernel", 6 * d * d + 8 * d, "alu"),
-            ("rows_kernel<summary>", 0, "alu"), ("chain_kernel", 0, "alu"),
-            ("rows_kernel<output>", 6 * d * d + 8 * d, "alu")]
+            (rows + "<summary>", 0, "alu"), ("chain_kernel", 0, "alu"),
+            (rows + "<output>", 6 * d * d + 8 * d, "alu")]
 
 
 def state_bytes(B, H, d):
@@ -319,7 +325,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="long")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "seq", "chunk", "decode"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "seq", "chunk", "chunk_tc", "decode"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--set", action="append", help="workload override, e.g. T=4096")
     ap.add_argument("--no-e2e", action="store_true")
@@ -348,7 +354,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     kernel = {"auto": vla.VLA_KERNEL_AUTO, "seq": vla.VLA_KERNEL_SEQ, "chunk": vla.VLA_KERNEL_CHUNK,
-              "decode": vla.VLA_KERNEL_DECODE}[args.kernel]
+              "chunk_tc": vla.VLA_KERNEL_CHUNK_TC, "decode": vla.VLA_KERNEL_DECODE}[args.kernel]
 
     t_gen = time.perf_counter()
     x = make_host_inputs(args.config, rank, parse_overrides(args))
@@ -358,7 +364,8 @@ def main():
     hq, hk, hv, hu = to_torch_host(x)
     q, k, v, u = (t.to(dev) for t in (hq, hk, hv, hu))
     resolved = kernel if kernel != vla.VLA_KERNEL_AUTO else vla.vla_select_kernel(B, H, T, d)
-    kname = {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk", vla.VLA_KERNEL_DECODE: "decode"}[resolved]
+    kname = {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk", vla.VLA_KERNEL_CHUNK_TC: "chunk_tc",
+             vla.VLA_KERNEL_DECODE: "decode"}[resolved]
     o = torch.empty_like(q)
     S_T = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
     A_T = torch.empty_like(S_T)

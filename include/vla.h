@@ -55,6 +55,9 @@ extern "C" {
 #define VLA_KERNEL_SEQ 1   /* one CTA per (b, h), token-sequential, no workspace */
 #define VLA_KERNEL_CHUNK 2 /* chunk-parallel over T, needs workspace */
 #define VLA_KERNEL_DECODE 3 /* a few tokens per call (decode step), state streamed from HBM */
+#define VLA_KERNEL_CHUNK_TC 4 /* VLA_KERNEL_CHUNK with the state passes as tcgen05 UT-transform
+                               * products (d_h = 64, bf16 I/O, chunk a multiple of 64; other
+                               * shapes run exactly as VLA_KERNEL_CHUNK); same workspace */
 
 /*
  * vla_forward -- run the recurrence over T tokens for all B*H units.
@@ -71,9 +74,9 @@ extern "C" {
  * o            [B,H,T,d] io_dtype, written.
  * S_T, A_T     [B,H,d,d] fp32, written (required).
  * n_T          [B,H,d] fp32, written when non-NULL.
- * kernel       VLA_KERNEL_AUTO / _SEQ / _CHUNK / _DECODE.  AUTO takes DECODE for
+ * kernel       VLA_KERNEL_AUTO / _SEQ / _CHUNK / _CHUNK_TC / _DECODE.  AUTO takes DECODE for
  *              T <= 4, CHUNK when B*H < 304 and T >= 1024, SEQ otherwise.
- * chunk        chunk length for VLA_KERNEL_CHUNK (0 = library default).
+ * chunk        chunk length for VLA_KERNEL_CHUNK and _CHUNK_TC (0 = library default).
  * workspace    device scratch of at least vla_workspace_bytes(...) bytes
  *              (may be NULL when that is 0).  Contents on entry are ignored.
  * stream       cudaStream_t as void*.

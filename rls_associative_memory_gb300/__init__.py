@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     VLA_F32,
     VLA_KERNEL_AUTO,
     VLA_KERNEL_CHUNK,
+    VLA_KERNEL_CHUNK_TC,
     VLA_KERNEL_DECODE,
     VLA_KERNEL_SEQ,
     VLA_NOALLOC_SCRATCH_BYTES,

@@ -34,6 +34,7 @@ VLA_KERNEL_AUTO = 0
 VLA_KERNEL_SEQ = 1
 VLA_KERNEL_CHUNK = 2
 VLA_KERNEL_DECODE = 3
+VLA_KERNEL_CHUNK_TC = 4
 
 # every symbol include/vla.h declares, with (restype, argtypes)
 _vp = ctypes.c_void_p

@@ -40,7 +40,7 @@ int check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int 
     if (io_dtype != VLA_F32 && io_dtype != VLA_BF16) return VLA_ERR_ARG;
     if (!(lambda0 > 0.f) || !isfinite(lambda0)) return VLA_ERR_ARG;
     if (kernel != VLA_KERNEL_AUTO && kernel != VLA_KERNEL_SEQ && kernel != VLA_KERNEL_CHUNK &&
-        kernel != VLA_KERNEL_DECODE)
+        kernel != VLA_KERNEL_DECODE && kernel != VLA_KERNEL_CHUNK_TC)
         return VLA_ERR_ARG;
     if (d_h != 32 && d_h != 64 && d_h != 128) return VLA_ERR_UNSUPPORTED_DIM;
     // element offsets are computed in size_t; counts themselves must fit the kernels' int math
@@ -116,7 +116,7 @@ size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kerne
     if (check_common(io_dtype, 1.f, B, H, T, d_h, kernel) != VLA_OK) return 0;
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return 0;
     const int kk = resolve_kernel(B, H, T, d_h, kernel);
-    if (kk != VLA_KERNEL_CHUNK || T == 0 || (long long)B * H == 0) return 0;
+    if ((kk != VLA_KERNEL_CHUNK && kk != VLA_KERNEL_CHUNK_TC) || T == 0 || (long long)B * H == 0) return 0;
     return vla::chunk_layout(B * H, T, d_h, chunk).total;
 }
 
@@ -224,8 +224,9 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if (kk == VLA_KERNEL_CHUNK && T > 0) {
+    if ((kk == VLA_KERNEL_CHUNK || kk == VLA_KERNEL_CHUNK_TC) && T > 0) {
         const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk);
+        p.rows_tc = (kk == VLA_KERNEL_CHUNK_TC);
         e = vla::launch_chunk(p, L, st);
     } else if (kk == VLA_KERNEL_DECODE) {
         e = vla::launch_decode(p, st);

@@ -30,15 +30,6 @@ namespace {
 
 constexpr int kTT = 16;  // tokens per staged tile
 
-struct ChunkArgs {
-    FwdParams p;
-    ChunkLayout L;
-};
-
-__device__ __forceinline__ float *ws_f(const ChunkArgs &a, size_t off) {
-    return reinterpret_cast<float *>(static_cast<unsigned char *>(a.p.ws) + off);
-}
-
 // Kahan-compensated accumulation.
 __device__ __forceinline__ void kahan_add(float &sum, float &comp, float x) {
     const float y = x - comp;
@@ -1195,14 +1186,23 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     gates_kernel<D, IO><<<(unsigned)(NCA * BH), G::NT, GatesSmem<D, IO>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), RowsCfg<D, 0>::NT, RowsSmem<D, IO>::total, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const bool tc = a.p.rows_tc && rows_tc_supported(a.p, a.L);
+    if (tc) {
+        if ((e = launch_rows_tc(a, 0, st)) != cudaSuccess) return e;
+    } else {
+        rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), RowsCfg<D, 0>::NT, RowsSmem<D, IO>::total, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     mark_launch(a.p, ++n, st);
     chain_kernel<D><<<(unsigned)((D / chain_rows<D>()) * BH), 256, ChainSmem<D>::total, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    rows_kernel<D, IO, 1><<<(unsigned)(NC * BH), RowsCfg<D, 1>::NT, RowsSmem<D, IO>::total, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (tc) {
+        if ((e = launch_rows_tc(a, 1, st)) != cudaSuccess) return e;
+    } else {
+        rows_kernel<D, IO, 1><<<(unsigned)(NC * BH), RowsCfg<D, 1>::NT, RowsSmem<D, IO>::total, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     mark_launch(a.p, ++n, st);
     return cudaSuccess;
 }

@@ -1,0 +1,528 @@
+// vla_chunk_tc.cu -- tensor-core state passes of the chunk-parallel path for
+// d = 64 with bf16 I/O: the chunk transitions (mode 0) and the readout
+// (mode 1) of the state write and ELU+1 readout of "Variational Linear
+// Attention: Stable Associative Memory for Long-Context Transformers",
+// section 2.3 (step 3 and the readout), taken 64 tokens at a time in the UT
+// (WY) form of a product of rank-1 updates.
+//
+// Within a sub-block of c = 64 tokens whose state at the start is X, the
+// state write x <- x + (value - x.k_hat) alpha^T, applied token by token,
+// is equivalent to
+//   R (I + N) = Vals - X K_hat,        N = strictly-upper(Al^T K_hat)  (c x c)
+//   X_end     = X + R Al^T
+//   X_t phi(q_t) = X phi(q_t) + sum_{s <= t} r_s (alpha_s . phi(q_t))
+// where R = [r_1 .. r_c] holds the per-token residuals value_t - X_{t-1} k_hat_t
+// (the residual of token t is its value minus what the earlier tokens of
+// the sub-block left in the state, hence the triangular system).  A
+// sub-block is three rounds of tcgen05.mma plus one triangular inverse on
+// the CUDA cores:
+//   1. D1 = X [K | Phi]^T   and   D2 = [K ; Phi] Al^T  (= N^T, Qm^T)
+//   2. R  = E T_inv,   E = Vals - (X K) diag(1/|k|),  T_inv = (I + N)^{-1}
+//   3. X += R Al^T    and (mode 1)  X Phi += R Qm,  Qm = upper-incl(Al^T Phi)
+//
+// Mode 0 runs the rows [H; P] of the chunk map S_end = S_start P_c + H_c
+// (values [v; 0], start [0; I]: M = 128); mode 1 runs S itself from the
+// chunk-start state of the chain pass and writes o (M = 64).
+//
+// Precision: fp32 operands enter the tensor cores as bf16 pairs
+// x = hi + lo (hi = bf16(x), lo = bf16(x - hi)), and a product takes
+// hi*hi + hi*lo + lo*hi with fp32 accumulation (relative error about
+// 2^-16).  k and v are bf16 inputs and exact: the raw key enters once and
+// the key norm is applied as a column scale in fp32.
+#include "vla_internal.cuh"
+
+namespace vla {
+namespace {
+
+constexpr int kD = 64;        // head dimension of this path
+constexpr int kSB = 64;       // tokens per sub-block
+constexpr int kTile = 8192;   // bytes of a 64-row, 64-column bf16 operand tile
+constexpr int kThreads = 256;
+
+// Operand tiles: K-major, unswizzled, K = 64 (core matrices of 8 rows x 16
+// bytes, adjacent along K 128 bytes apart, row groups 1024 bytes apart).
+__device__ __forceinline__ uint32_t toff(int r, int k) { return kmajor_off_bf16(r, k, 64); }
+
+template <int MODE>
+struct TcLayout {
+    static constexpr int XR = MODE == 0 ? 128 : 64;            // state rows
+    static constexpr uint32_t ncols = MODE == 0 ? 128 : 256;    // TMEM columns
+    static constexpr size_t ctrl = 0;                            // mbarrier, TMEM slot, abort flag
+    static constexpr size_t xs = 1024;                           // X / E / R tiles: hi, lo
+    static constexpr size_t xs_t = (size_t)XR * 128;
+    static constexpr size_t kb = xs + 2 * xs_t;                  // [K; Phi_hi] (mode 1) or K; then Qm^T hi, lo
+    static constexpr size_t kblo = kb + (MODE == 0 ? kTile : 2 * kTile);  // [0; Phi_lo] (mode 1)
+    static constexpr size_t al = kblo + (MODE == 0 ? 0 : 2 * kTile);     // Al hi, lo; N (fp32); T_inv^T hi, lo
+    static constexpr size_t alf = al + 2 * kTile;                // Al^T (feature rows) hi, lo
+    static constexpr size_t vt = alf + 2 * kTile;                // v [t][i] bf16; then the o stage
+    static constexpr size_t ks = vt + kTile;                     // [64] 1 / max(|k|, eps)
+    static constexpr size_t rden = ks + 256;                     // [64] 1 / (phi(q).n + eps)
+    static constexpr size_t tot = rden + 256;                    // [8][64] warp totals of phi(k_hat)
+    static constexpr size_t total = tot + 8 * 64 * 4;
+};
+
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// bf16 pairs (hi, lo) of 8 consecutive fp32 values, in element order.
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(hb);
+        h[e] = bf2_bits(hb);
+        l[e] = bf2_bits(__floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y));
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void unpack8(uint4 w, float *x) {
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(a[e] << 16);
+        x[2 * e + 1] = __uint_as_float(a[e] & 0xffff0000u);
+    }
+}
+
+// 32 consecutive fp32 values as (hi, lo) into row `row`, columns k0 .. k0+31.
+__device__ __forceinline__ void put_row32(unsigned char *hi, unsigned char *lo, int row, int k0, const float *v) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint4 h, l;
+        split8(v + 8 * g, h, l);
+        *reinterpret_cast<uint4 *>(hi + toff(row, k0 + 8 * g)) = h;
+        *reinterpret_cast<uint4 *>(lo + toff(row, k0 + 8 * g)) = l;
+    }
+}
+
+// 32 consecutive TMEM columns of this warp's lane quarter (shape 32x32b).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// D (+)= A B^T over K = 64 (four K-steps of 16); A, B are 64- or 128-row tiles.
+__device__ __forceinline__ void mma64(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(d, umma_desc_kmajor(a + ks * 256, 128, 1024), umma_desc_kmajor(b + ks * 256, 128, 1024), idesc,
+                  (acc || ks > 0) ? 1u : 0u);
+}
+
+// Split product D (+)= (Ah + Al)(Bh + Bl)^T without the lo*lo term.
+__device__ __forceinline__ void mma64x3(uint32_t d, uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl,
+                                        uint32_t idesc, bool acc) {
+    mma64(d, ah, bh, idesc, acc);
+    mma64(d, ah, bl, idesc, true);
+    mma64(d, al, bh, idesc, true);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
+    using L = TcLayout<MODE>;
+    constexpr int XR = L::XR;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
+    unsigned char *xs_hi = smem + L::xs, *xs_lo = smem + L::xs + L::xs_t;
+    unsigned char *kb = smem + L::kb, *kblo = smem + L::kblo;
+    unsigned char *al_hi = smem + L::al, *al_lo = smem + L::al + kTile;
+    float *nbuf = reinterpret_cast<float *>(smem + L::al);
+    unsigned char *alf_hi = smem + L::alf, *alf_lo = smem + L::alf + kTile;
+    __nv_bfloat16 *vt = reinterpret_cast<__nv_bfloat16 *>(smem + L::vt);
+    float *s_ks = reinterpret_cast<float *>(smem + L::ks);
+    float *s_rden = reinterpret_cast<float *>(smem + L::rden);
+    float *s_tot = reinterpret_cast<float *>(smem + L::tot);
+
+    const int NC = a.L.NC, C = a.L.C, T = a.p.T;
+    const int c = (int)(blockIdx.x % (unsigned)NC), bh = (int)(blockIdx.x / (unsigned)NC);
+    const int t0 = c * C, ntok = min(C, T - t0), nsb = (ntok + kSB - 1) / kSB;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int qw = warp & 3, hw = warp >> 2;  // TMEM lane quarter, column half
+    const int pt = tid >> 2, pq = tid & 3;    // operand staging: token, feature quarter
+    const size_t tok0 = ((size_t)bh * T + t0) * kD;
+    const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.p.k) + tok0;
+    const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.p.v) + tok0;
+    const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.p.q) + tok0;
+    const float *gal = ws_f(a, a.L.off_alpha) + tok0;
+    __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.p.o) + tok0;
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, L::ncols);
+    if (MODE == 1)  // rows 0..63 of [0; Phi_lo] stay zero
+        for (int x = tid; x < kTile / 16; x += kThreads) reinterpret_cast<uint4 *>(kblo)[x] = make_uint4(0, 0, 0, 0);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    const uint32_t tq = tbase + ((uint32_t)(32 * qw) << 16);  // this warp's lane quarter
+
+    // State rows held in registers: the row and 32 columns this thread reads
+    // back from TMEM (M = 128: row 32 qw + lane; M = 64: row 16 qw + lane,
+    // lanes 0..15 of each quarter).
+    const int xrow = MODE == 0 ? 32 * qw + lane : 16 * qw + lane;
+    const bool xact = MODE == 0 || lane < 16;
+    float x[32];
+    if (MODE == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = (xrow - 64 == 32 * hw + j) ? 1.f : 0.f;
+    } else {
+        const float4 *src = reinterpret_cast<const float4 *>(ws_f(a, a.L.off_S) + ((size_t)bh * NC + c) * kD * kD +
+                                                             (size_t)(xrow & 63) * kD + 32 * hw);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = xact ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+        }
+    }
+    if (xact) put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
+
+    // Inputs of the next sub-block, prefetched into registers (token pt,
+    // features 16 pq .. 16 pq + 15).
+    uint4 rk[2], rv[2], rq[2];
+    float4 ra[4];
+    auto load_in = [&](int sb) {
+        const int t = sb * kSB + pt;
+        const bool in = sb < nsb && t < ntok;
+        const size_t off = (size_t)t * kD + 16 * pq;
+        const uint4 z4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            rk[h] = in ? reinterpret_cast<const uint4 *>(gk + off)[h] : z4;
+            rv[h] = in ? reinterpret_cast<const uint4 *>(gv + off)[h] : z4;
+            if (MODE == 1) rq[h] = in ? reinterpret_cast<const uint4 *>(gq + off)[h] : z4;
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            ra[h] = in ? reinterpret_cast<const float4 *>(gal + off)[h] : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float nb[16];  // n at the sub-block start, features 16 pq .. (mode 1)
+    if (MODE == 1) {
+        const float *n0 = ws_f(a, a.L.off_n) + ((size_t)bh * (a.L.NCA + 1) + (size_t)c * (C / a.L.CA)) * kD + 16 * pq;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) nb[m] = n0[m];
+    }
+
+    uint32_t phase = 0;
+    auto round_wait = [&]() -> bool {
+        const bool w = mbar_wait_bounded(bar, phase, a.p.wait_limit_ns, a.p.err);
+        phase ^= 1u;
+        if (!w) *abort_flag = 1;
+        __syncthreads();
+        tc_fence_after();
+        return *abort_flag == 0;
+    };
+    constexpr uint32_t id_x_kb = MODE == 1 ? idesc_bf16_f32(64, 128) : idesc_bf16_f32(128, 64);
+    constexpr uint32_t id_kb_al = MODE == 1 ? idesc_bf16_f32(128, 64) : idesc_bf16_f32(64, 64);
+    constexpr uint32_t id_x64 = idesc_bf16_f32(XR, 64);
+    constexpr uint32_t col_d2 = MODE == 1 ? 128 : 64;   // D2, then D3 = R
+    constexpr uint32_t col_d4 = MODE == 1 ? 192 : 0;    // D4 = R Al^T
+
+    bool ok = true;
+    load_in(0);
+    for (int sb = 0; sb < nsb; ++sb) {
+        const int nt = min(kSB, ntok - sb * kSB);
+        float fq[16], fk[16];
+        // ---- stage the sub-block's operands ----
+        {
+            float kf[16];
+            unpack8(rk[0], kf);
+            unpack8(rk[1], kf + 8);
+            float ss = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) ss = fmaf(kf[m], kf[m], ss);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            const float ksc = 1.f / fmaxf(sqrtf(ss), kEps);
+            if (pq == 0) s_ks[pt] = ksc;
+            *reinterpret_cast<uint4 *>(kb + toff(pt, 16 * pq)) = rk[0];
+            *reinterpret_cast<uint4 *>(kb + toff(pt, 16 * pq + 8)) = rk[1];
+            *reinterpret_cast<uint4 *>(vt + pt * kD + 16 * pq) = rv[0];
+            *reinterpret_cast<uint4 *>(vt + pt * kD + 16 * pq + 8) = rv[1];
+            float af[16];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                af[4 * h] = ra[h].x; af[4 * h + 1] = ra[h].y; af[4 * h + 2] = ra[h].z; af[4 * h + 3] = ra[h].w;
+            }
+            uint4 h4, l4;
+            split8(af, h4, l4);
+            *reinterpret_cast<uint4 *>(al_hi + toff(pt, 16 * pq)) = h4;
+            *reinterpret_cast<uint4 *>(al_lo + toff(pt, 16 * pq)) = l4;
+            split8(af + 8, h4, l4);
+            *reinterpret_cast<uint4 *>(al_hi + toff(pt, 16 * pq + 8)) = h4;
+            *reinterpret_cast<uint4 *>(al_lo + toff(pt, 16 * pq + 8)) = l4;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const __nv_bfloat16 hb = __float2bfloat16_rn(af[m]);
+                const __nv_bfloat16 lb = __float2bfloat16_rn(af[m] - __bfloat162float(hb));
+                *reinterpret_cast<__nv_bfloat16 *>(alf_hi + toff(16 * pq + m, pt)) = hb;
+                *reinterpret_cast<__nv_bfloat16 *>(alf_lo + toff(16 * pq + m, pt)) = lb;
+            }
+            if (MODE == 1) {
+                float qf[16];
+                unpack8(rq[0], qf);
+                unpack8(rq[1], qf + 8);
+#pragma unroll
+                for (int m = 0; m < 16; ++m) fq[m] = phi_elu1(qf[m]);
+                split8(fq, h4, l4);
+                *reinterpret_cast<uint4 *>(kb + toff(64 + pt, 16 * pq)) = h4;
+                *reinterpret_cast<uint4 *>(kblo + toff(64 + pt, 16 * pq)) = l4;
+                split8(fq + 8, h4, l4);
+                *reinterpret_cast<uint4 *>(kb + toff(64 + pt, 16 * pq + 8)) = h4;
+                *reinterpret_cast<uint4 *>(kblo + toff(64 + pt, 16 * pq + 8)) = l4;
+                // phi(k_hat): inclusive scan over this warp's 8 tokens (lanes 4 apart)
+#pragma unroll
+                for (int m = 0; m < 16; ++m) fk[m] = pt < nt ? phi_elu1(kf[m] * ksc) : 0.f;
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const float y = __shfl_up_sync(0xffffffffu, fk[m], off);
+                        if (lane >= off) fk[m] += y;
+                    }
+                }
+                if (lane >= 28) {
+                    float4 *dst = reinterpret_cast<float4 *>(s_tot + warp * 64 + 16 * pq);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) dst[h] = make_float4(fk[4 * h], fk[4 * h + 1], fk[4 * h + 2], fk[4 * h + 3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // ---- round 1: D1 = X [K | Phi]^T, D2 = [K; Phi] Al^T ----
+        if (tid == 0) {
+            tc_fence_after();
+            if (MODE == 1) {
+                mma64x3(tbase, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(kb), smem_u32(kblo), id_x_kb, false);
+                mma64x3(tbase + col_d2, smem_u32(kb), smem_u32(kblo), smem_u32(al_hi), smem_u32(al_lo), id_kb_al, false);
+            } else {
+                mma64(tbase, smem_u32(xs_hi), smem_u32(kb), id_x_kb, false);
+                mma64(tbase, smem_u32(xs_lo), smem_u32(kb), id_x_kb, true);
+                mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_kb_al, false);
+                mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_kb_al, true);
+            }
+            umma_commit(bar);
+        }
+        if (MODE == 1) {  // readout denominators 1 / (phi(q_t) . n_t + eps)
+            float pre[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) pre[m] = nb[m];
+            for (int w = 0; w < 8; ++w) {
+                const float4 *tw = reinterpret_cast<const float4 *>(s_tot + w * 64 + 16 * pq);
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float4 t4 = tw[h];
+                    const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (w < warp) pre[4 * h + e] += tv[e];
+                        nb[4 * h + e] += tv[e];
+                    }
+                }
+            }
+            float dp = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) dp = fmaf(fq[m], pre[m] + fk[m], dp);
+            dp += __shfl_xor_sync(0xffffffffu, dp, 1);
+            dp += __shfl_xor_sync(0xffffffffu, dp, 2);
+            if (pq == 0) s_rden[pt] = 1.f / (dp + kEps);
+        }
+        load_in(sb + 1);
+        if (!round_wait()) {
+            ok = false;
+            break;
+        }
+        // ---- N (fp32, for the inverse), Qm^T tiles (mode 1), E tiles ----
+        {
+            float v[32];
+            tmem_ld32(tq + col_d2 + 32 * hw, v);
+            if (MODE == 1) {
+                const int t = 32 * (qw & 1) + lane;
+                if (qw < 2) {  // rows 0..63: (Al^T K)^T
+                    const float kt = s_ks[t];
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) {
+                        const int s = 32 * hw + m;
+                        nbuf[s * 64 + t] = s < t ? v[m] * kt : 0.f;
+                    }
+                } else {       // rows 64..127: Qm^T
+#pragma unroll
+                    for (int m = 0; m < 32; ++m)
+                        if (32 * hw + m > t) v[m] = 0.f;
+                    put_row32(kb, kb + kTile, t, 32 * hw, v);
+                }
+            } else if (lane < 16) {
+                const int t = 16 * qw + lane;
+                const float kt = s_ks[t];
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int s = 32 * hw + m;
+                    nbuf[s * 64 + t] = s < t ? v[m] * kt : 0.f;
+                }
+            }
+            tmem_ld32(tq + 32 * hw, v);  // X K, columns 32 hw ..
+            if (xact) {
+#pragma unroll
+                for (int m = 0; m < 32; ++m) {
+                    const int t = 32 * hw + m;
+                    const float val = (MODE == 1 || xrow < 64) ? __bfloat162float(vt[t * kD + (xrow & 63)]) : 0.f;
+                    v[m] = val - v[m] * s_ks[t];
+                }
+                put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- T_inv = (I + N)^{-1}: column t by back substitution, 4 threads a column ----
+        // (a warp holds columns 8 warp .. 8 warp + 7 and skips the steps s
+        // that none of them needs, s >= 8 warp + 7)
+        {
+            const int t = tid >> 2, p = tid & 3;
+            float xr[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) xr[m] = (16 * p + m == t) ? 1.f : 0.f;
+#pragma unroll
+            for (int s = kSB - 2; s >= 0; --s) {
+                if (8 * warp + 7 <= s) continue;
+                const float4 *nr = reinterpret_cast<const float4 *>(nbuf + s * 64 + 16 * p);
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 n4 = nr[q];
+                    acc0 = fmaf(n4.x, xr[4 * q], acc0);
+                    acc1 = fmaf(n4.y, xr[4 * q + 1], acc1);
+                    acc0 = fmaf(n4.z, xr[4 * q + 2], acc0);
+                    acc1 = fmaf(n4.w, xr[4 * q + 3], acc1);
+                }
+                float acc = acc0 + acc1;
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                if (p == (s >> 4) && s < t) xr[s & 15] = -acc;
+            }
+            __syncthreads();  // every read of N is done before T_inv^T overwrites it
+            uint4 h4, l4;
+            split8(xr, h4, l4);
+            *reinterpret_cast<uint4 *>(al_hi + toff(t, 16 * p)) = h4;
+            *reinterpret_cast<uint4 *>(al_lo + toff(t, 16 * p)) = l4;
+            split8(xr + 8, h4, l4);
+            *reinterpret_cast<uint4 *>(al_hi + toff(t, 16 * p + 8)) = h4;
+            *reinterpret_cast<uint4 *>(al_lo + toff(t, 16 * p + 8)) = l4;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // ---- round 2: R = E T_inv ----
+        if (tid == 0) {
+            tc_fence_after();
+            mma64x3(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi), smem_u32(al_lo), id_x64, false);
+            umma_commit(bar);
+        }
+        if (!round_wait()) {
+            ok = false;
+            break;
+        }
+        {
+            float v[32];
+            tmem_ld32(tq + col_d2 + 32 * hw, v);
+            if (xact) put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
+        // ---- round 3: X += R Al^T; (mode 1) X Phi += R Qm ----
+        if (tid == 0) {
+            tc_fence_after();
+            mma64x3(tbase + col_d4, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(alf_hi), smem_u32(alf_lo), id_x64, false);
+            if (MODE == 1)
+                mma64x3(tbase + 64, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(kb), smem_u32(kb + kTile), id_x64, true);
+            umma_commit(bar);
+        }
+        if (!round_wait()) {
+            ok = false;
+            break;
+        }
+        {
+            float v[32];
+            tmem_ld32(tq + col_d4 + 32 * hw, v);
+            if (xact) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] += v[j];
+                put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
+            }
+            if (MODE == 1) {
+                tmem_ld32(tq + 64 + 32 * hw, v);  // numerators S_t phi(q_t), token columns
+                if (xact) {
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) {
+                        const int t = 32 * hw + m;
+                        vt[t * kD + xrow] = __float2bfloat16_rn(v[m] * s_rden[t]);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (MODE == 1) {  // o of the sub-block: 64 tokens x 128 bytes
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int id = tid + kThreads * e, t = id >> 3, part = id & 7;
+                if (t < nt)
+                    *reinterpret_cast<uint4 *>(gout + (size_t)(sb * kSB + t) * kD + 8 * part) =
+                        *reinterpret_cast<const uint4 *>(vt + t * kD + 8 * part);
+            }
+            __syncthreads();  // the stage becomes the next v tile
+        }
+    }
+    if (!ok) {
+        if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
+    } else if (MODE == 0) {  // rows 0..63 are H_c, rows 64..127 P_c
+        float4 *dst = reinterpret_cast<float4 *>(ws_f(a, xrow < 64 ? a.L.off_H : a.L.off_P) +
+                                                 ((size_t)bh * NC + c) * kD * kD + (size_t)(xrow & 63) * kD + 32 * hw);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, L::ncols);
+}
+
+template <int MODE>
+cudaError_t launch_mode(const ChunkArgs &a, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(rows_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)TcLayout<MODE>::total);
+    if (e != cudaSuccess) return e;
+    const long long grid = (long long)a.L.NC * a.p.BH;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    rows_tc_kernel<MODE><<<(unsigned)grid, kThreads, TcLayout<MODE>::total, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool rows_tc_supported(const FwdParams &p, const ChunkLayout &L) {
+    return p.d == kD && p.io_bf16 && L.C % kSB == 0;
+}
+
+cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream) {
+    return mode == 0 ? launch_mode<0>(a, stream) : launch_mode<1>(a, stream);
+}
+
+}  // namespace vla

@@ -34,6 +34,7 @@ struct FwdParams {
     void *ws;                   // workspace (chunked kernel)
     size_t ws_bytes;
     int chunk;                  // chunk length (chunked kernel)
+    int rows_tc;                // chunked kernel: state passes on the tensor cores where supported
     void *const *events;        // measurement hook: cudaEvent_t handles, or null
     int n_events;
     int *launches;              // out: number of kernels launched
@@ -95,6 +96,21 @@ int api_cuda_fail(cudaError_t e);
 ChunkLayout chunk_layout(int BH, int T, int d, int chunk);
 // Chunk-parallel path (six launches).  Returns a cudaError_t.
 cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream);
+
+// Kernel argument of the chunk-parallel kernels.
+struct ChunkArgs {
+    FwdParams p;
+    ChunkLayout L;
+};
+__device__ __forceinline__ float *ws_f(const ChunkArgs &a, size_t off) {
+    return reinterpret_cast<float *>(static_cast<unsigned char *>(a.p.ws) + off);
+}
+
+// Tensor-core state passes (UT transform over 64-token sub-blocks) for d = 64
+// with bf16 I/O and S-chunks a multiple of 64 tokens; mode 0 = chunk
+// transitions (P_c, H_c), mode 1 = readout.  Defined in vla_chunk_tc.cu.
+bool rows_tc_supported(const FwdParams &p, const ChunkLayout &L);
+cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // PTX helpers

@@ -67,7 +67,8 @@ def _call(**kw):
     (dict(lam=float("inf")), vla.VLA_ERR_ARG),
     (dict(io=7), vla.VLA_ERR_ARG),
     (dict(kernel=9), vla.VLA_ERR_ARG),
-    (dict(kernel=4), vla.VLA_ERR_ARG),
+    (dict(kernel=5), vla.VLA_ERR_ARG),
+    (dict(kernel=-1), vla.VLA_ERR_ARG),
     (dict(B=-1), vla.VLA_ERR_ARG),
     (dict(T=-3), vla.VLA_ERR_ARG),
     (dict(chunk=-1), vla.VLA_ERR_ARG),

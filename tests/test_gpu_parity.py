@@ -13,14 +13,18 @@ from vla_testutil import TOL, compare, oracle_ref, rel_fro, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK]
+KERNELS = [vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK, vla.VLA_KERNEL_CHUNK_TC]
 # (kernel, chunk length): the chunked path with a short explicit chunk spans
-# many chunks and a ragged last chunk even on small streams.
-VARIANTS = [(vla.VLA_KERNEL_SEQ, 0), (vla.VLA_KERNEL_CHUNK, 32), (vla.VLA_KERNEL_CHUNK, 0)]
+# many chunks and a ragged last chunk even on small streams.  CHUNK_TC runs
+# its tensor-core state passes at d = 64 with bf16 I/O (chunks of 64 and 128
+# tokens: one and two sub-blocks) and the plain chunked path elsewhere.
+VARIANTS = [(vla.VLA_KERNEL_SEQ, 0), (vla.VLA_KERNEL_CHUNK, 32), (vla.VLA_KERNEL_CHUNK, 0),
+            (vla.VLA_KERNEL_CHUNK_TC, 0), (vla.VLA_KERNEL_CHUNK_TC, 128)]
 
 
 def _kid(k):
-    return {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk", vla.VLA_KERNEL_AUTO: "auto"}[k]
+    return {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk", vla.VLA_KERNEL_CHUNK_TC: "chunk_tc",
+            vla.VLA_KERNEL_AUTO: "auto"}[k]
 
 
 def _vid(v):
@@ -57,6 +61,15 @@ def test_chunk_lengths(chunk):
     """Every chunk length gives the same result (one ragged last chunk)."""
     x = make_inputs(1, 4, 1000, 64, "bf16", seed=31, u_scale=0.5)
     compare(run_gpu(x, vla.VLA_KERNEL_CHUNK, chunk=chunk), oracle_ref(x), "bf16")
+
+
+@pytest.mark.parametrize("chunk", [64, 192, 512])
+@pytest.mark.parametrize("T", [64, 1000, 1536])
+def test_tensor_core_state_passes(chunk, T):
+    """The UT-transform state passes (d = 64, bf16): whole and ragged
+    sub-blocks, one to eight sub-blocks per chunk, one or several chunks."""
+    x = make_inputs(1, 4, T, 64, "bf16", seed=41 + T, u_scale=0.5)
+    compare(run_gpu(x, vla.VLA_KERNEL_CHUNK_TC, chunk=chunk), oracle_ref(x), "bf16")
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=_kid)
