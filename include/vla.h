@@ -75,7 +75,7 @@ extern "C" {
  * S_T, A_T     [B,H,d,d] fp32, written (required).
  * n_T          [B,H,d] fp32, written when non-NULL.
  * kernel       VLA_KERNEL_AUTO / _SEQ / _CHUNK / _CHUNK_TC / _DECODE.  AUTO takes DECODE for
- *              T <= 4, CHUNK when B*H < 304 and T >= 1024, SEQ otherwise.
+ *              T <= 4, CHUNK_TC when B*H < 304 and T >= 1024, SEQ otherwise.
  * chunk        chunk length for VLA_KERNEL_CHUNK and _CHUNK_TC (0 = library default).
  * workspace    device scratch of at least vla_workspace_bytes(...) bytes
  *              (may be NULL when that is 0).  Contents on entry are ignored.
@@ -92,7 +92,7 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
 size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk);
 
 /* Which kernel VLA_KERNEL_AUTO resolves to for this shape (VLA_KERNEL_SEQ,
- * VLA_KERNEL_CHUNK or VLA_KERNEL_DECODE), or a VLA_ERR_* code for invalid
+ * VLA_KERNEL_CHUNK_TC or VLA_KERNEL_DECODE), or a VLA_ERR_* code for invalid
  * arguments. */
 int vla_select_kernel(int B, int H, int T, int d_h);
 

@@ -50,14 +50,15 @@ int check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int 
 }
 
 // AUTO: the decode step for a handful of tokens; the chunk-parallel path
-// when there are too few (b, h) units to fill the GPU with one CTA each and
-// the stream is long enough to cut; otherwise the sequential kernel.
+// (with the tensor-core state passes where they apply) when there are too
+// few (b, h) units to fill the GPU with one CTA each and the stream is long
+// enough to cut; otherwise the sequential kernel.
 int resolve_kernel(int B, int H, int T, int d_h, int kernel) {
     (void)d_h;
     if (kernel != VLA_KERNEL_AUTO) return kernel;
     const long long BH = (long long)B * H;
     if (T >= 1 && T <= 4) return VLA_KERNEL_DECODE;
-    if (BH < 2 * 152 && T >= 1024) return VLA_KERNEL_CHUNK;
+    if (BH < 2 * 152 && T >= 1024) return VLA_KERNEL_CHUNK_TC;
     return VLA_KERNEL_SEQ;
 }
 

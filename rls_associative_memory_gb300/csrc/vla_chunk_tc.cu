@@ -16,9 +16,11 @@
 // the sub-block left in the state, hence the triangular system).  A
 // sub-block is three rounds of tcgen05.mma plus one triangular inverse on
 // the CUDA cores:
-//   1. D1 = X [K | Phi]^T   and   D2 = [K ; Phi] Al^T  (= N^T, Qm^T)
+//   1. D1 = X K^T,  D2 = [K ; Phi] Al^T  (= N^T, Qm^T),  (mode 1) DO = Phi X^T
 //   2. R  = E T_inv,   E = Vals - (X K) diag(1/|k|),  T_inv = (I + N)^{-1}
-//   3. X += R Al^T    and (mode 1)  X Phi += R Qm,  Qm = upper-incl(Al^T Phi)
+//   3. X += R Al^T    and (mode 1)  DO += Qm^T R^T,  Qm = upper-incl(Al^T Phi)
+// DO holds the readout numerators token-major (rows = tokens), so o leaves
+// as whole 16-byte vectors.
 //
 // Mode 0 runs the rows [H; P] of the chunk map S_end = S_start P_c + H_c
 // (values [v; 0], start [0; I]: M = 128); mode 1 runs S itself from the
@@ -43,6 +45,10 @@ constexpr int kThreads = 256;
 // bytes, adjacent along K 128 bytes apart, row groups 1024 bytes apart).
 __device__ __forceinline__ uint32_t toff(int r, int k) { return kmajor_off_bf16(r, k, 64); }
 
+// phi(x) = ELU(x) + 1 with the fast exponential (bf16 I/O only: its relative
+// error, about 2^-21, is far below the output rounding).
+__device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+
 template <int MODE>
 struct TcLayout {
     static constexpr int XR = MODE == 0 ? 128 : 64;            // state rows
@@ -52,13 +58,15 @@ struct TcLayout {
     static constexpr size_t xs_t = (size_t)XR * 128;
     static constexpr size_t kb = xs + 2 * xs_t;                  // [K; Phi_hi] (mode 1) or K; then Qm^T hi, lo
     static constexpr size_t kblo = kb + (MODE == 0 ? kTile : 2 * kTile);  // [0; Phi_lo] (mode 1)
-    static constexpr size_t al = kblo + (MODE == 0 ? 0 : 2 * kTile);     // Al hi, lo; N (fp32); T_inv^T hi, lo
-    static constexpr size_t alf = al + 2 * kTile;                // Al^T (feature rows) hi, lo
-    static constexpr size_t vt = alf + 2 * kTile;                // v [t][i] bf16; then the o stage
-    static constexpr size_t ks = vt + kTile;                     // [64] 1 / max(|k|, eps)
+    static constexpr size_t al = kblo + (MODE == 0 ? 0 : 2 * kTile);     // Al (token rows) hi, lo
+    static constexpr int kNT = 68;                               // row stride (floats) of N^T: conflict-free rows
+    static constexpr size_t ti = al + 2 * kTile;                 // N^T (fp32), then T_inv^T hi, lo
+    static constexpr int kVS = 72;                               // row stride (bf16) of the v tile
+    static constexpr size_t vt = ti + (size_t)64 * kNT * 4;      // v [t][i] bf16
+    static constexpr size_t ks = vt + (size_t)64 * kVS * 2;      // [64] 1 / max(|k|, eps)
     static constexpr size_t rden = ks + 256;                     // [64] 1 / (phi(q).n + eps)
-    static constexpr size_t tot = rden + 256;                    // [8][64] warp totals of phi(k_hat)
-    static constexpr size_t total = tot + 8 * 64 * 4;
+    static constexpr size_t tot = rden + 256;                    // [9][64] warp totals of phi(k_hat), then prefixes
+    static constexpr size_t total = tot + 9 * 64 * 4;
 };
 
 __device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -114,19 +122,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // D (+)= A B^T over K = 64 (four K-steps of 16); A, B are 64- or 128-row tiles.
+// With B_MN, B is read MN-major from a K-major tile of the transposed
+// matrix: a tile whose rows are K and whose 16-byte core-matrix rows run
+// along N.  In the MN-major descriptor the stride between core matrices
+// along N is SBO (128 bytes here) and along K is LBO (1024 bytes), so one
+// K-step of 16 advances two row groups.
+template <bool B_MN = false>
 __device__ __forceinline__ void mma64(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool acc) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(d, umma_desc_kmajor(a + ks * 256, 128, 1024), umma_desc_kmajor(b + ks * 256, 128, 1024), idesc,
+        umma_bf16(d, umma_desc_kmajor(a + ks * 256, 128, 1024),
+                  B_MN ? umma_desc_kmajor(b + ks * 2048, 1024, 128) : umma_desc_kmajor(b + ks * 256, 128, 1024),
+                  idesc | (B_MN ? (1u << 16) : 0u),
                   (acc || ks > 0) ? 1u : 0u);
 }
 
 // Split product D (+)= (Ah + Al)(Bh + Bl)^T without the lo*lo term.
+template <bool B_MN = false>
 __device__ __forceinline__ void mma64x3(uint32_t d, uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl,
                                         uint32_t idesc, bool acc) {
-    mma64(d, ah, bh, idesc, acc);
-    mma64(d, ah, bl, idesc, true);
-    mma64(d, al, bh, idesc, true);
+    mma64<B_MN>(d, ah, bh, idesc, acc);
+    mma64<B_MN>(d, ah, bl, idesc, true);
+    mma64<B_MN>(d, al, bh, idesc, true);
 }
 
 template <int MODE>
@@ -140,8 +157,8 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     unsigned char *xs_hi = smem + L::xs, *xs_lo = smem + L::xs + L::xs_t;
     unsigned char *kb = smem + L::kb, *kblo = smem + L::kblo;
     unsigned char *al_hi = smem + L::al, *al_lo = smem + L::al + kTile;
-    float *nbuf = reinterpret_cast<float *>(smem + L::al);
-    unsigned char *alf_hi = smem + L::alf, *alf_lo = smem + L::alf + kTile;
+    float *ntb = reinterpret_cast<float *>(smem + L::ti);  // N^T[t][s] = N[s][t], row stride kNT
+    unsigned char *ti_hi = smem + L::ti, *ti_lo = smem + L::ti + kTile;  // T_inv^T
     __nv_bfloat16 *vt = reinterpret_cast<__nv_bfloat16 *>(smem + L::vt);
     float *s_ks = reinterpret_cast<float *>(smem + L::ks);
     float *s_rden = reinterpret_cast<float *>(smem + L::rden);
@@ -152,7 +169,9 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     const int t0 = c * C, ntok = min(C, T - t0), nsb = (ntok + kSB - 1) / kSB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int qw = warp & 3, hw = warp >> 2;  // TMEM lane quarter, column half
-    const int pt = tid >> 2, pq = tid & 3;    // operand staging: token, feature quarter
+    // operand staging: token pt (8 consecutive tokens in the 8 lanes of a
+    // quarter-warp), features 16 pq .. 16 pq + 15
+    const int pt = 8 * warp + (lane & 7), pq = lane >> 3;
     const size_t tok0 = ((size_t)bh * T + t0) * kD;
     const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.p.k) + tok0;
     const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.p.v) + tok0;
@@ -229,11 +248,13 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         tc_fence_after();
         return *abort_flag == 0;
     };
-    constexpr uint32_t id_x_kb = MODE == 1 ? idesc_bf16_f32(64, 128) : idesc_bf16_f32(128, 64);
+    constexpr uint32_t id_x64 = idesc_bf16_f32(XR, 64);                       // X-row products
     constexpr uint32_t id_kb_al = MODE == 1 ? idesc_bf16_f32(128, 64) : idesc_bf16_f32(64, 64);
-    constexpr uint32_t id_x64 = idesc_bf16_f32(XR, 64);
+    constexpr uint32_t id_64 = idesc_bf16_f32(64, 64);
+    constexpr int kNT = L::kNT, kVS = L::kVS;
     constexpr uint32_t col_d2 = MODE == 1 ? 128 : 64;   // D2, then D3 = R
-    constexpr uint32_t col_d4 = MODE == 1 ? 192 : 0;    // D4 = R Al^T
+    constexpr uint32_t col_d4 = 0;                      // D1 = X K^T, then D4 = R Al^T
+    constexpr uint32_t col_do = 64;                     // (mode 1) readout numerators, token rows
 
     bool ok = true;
     load_in(0);
@@ -248,14 +269,14 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             float ss = 0.f;
 #pragma unroll
             for (int m = 0; m < 16; ++m) ss = fmaf(kf[m], kf[m], ss);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 16);
             const float ksc = 1.f / fmaxf(sqrtf(ss), kEps);
             if (pq == 0) s_ks[pt] = ksc;
             *reinterpret_cast<uint4 *>(kb + toff(pt, 16 * pq)) = rk[0];
             *reinterpret_cast<uint4 *>(kb + toff(pt, 16 * pq + 8)) = rk[1];
-            *reinterpret_cast<uint4 *>(vt + pt * kD + 16 * pq) = rv[0];
-            *reinterpret_cast<uint4 *>(vt + pt * kD + 16 * pq + 8) = rv[1];
+            *reinterpret_cast<uint4 *>(vt + pt * kVS + 16 * pq) = rv[0];
+            *reinterpret_cast<uint4 *>(vt + pt * kVS + 16 * pq + 8) = rv[1];
             float af[16];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -268,37 +289,30 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             split8(af + 8, h4, l4);
             *reinterpret_cast<uint4 *>(al_hi + toff(pt, 16 * pq + 8)) = h4;
             *reinterpret_cast<uint4 *>(al_lo + toff(pt, 16 * pq + 8)) = l4;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const __nv_bfloat16 hb = __float2bfloat16_rn(af[m]);
-                const __nv_bfloat16 lb = __float2bfloat16_rn(af[m] - __bfloat162float(hb));
-                *reinterpret_cast<__nv_bfloat16 *>(alf_hi + toff(16 * pq + m, pt)) = hb;
-                *reinterpret_cast<__nv_bfloat16 *>(alf_lo + toff(16 * pq + m, pt)) = lb;
-            }
             if (MODE == 1) {
                 float qf[16];
                 unpack8(rq[0], qf);
                 unpack8(rq[1], qf + 8);
 #pragma unroll
-                for (int m = 0; m < 16; ++m) fq[m] = phi_elu1(qf[m]);
+                for (int m = 0; m < 16; ++m) fq[m] = phi_fast(qf[m]);
                 split8(fq, h4, l4);
                 *reinterpret_cast<uint4 *>(kb + toff(64 + pt, 16 * pq)) = h4;
                 *reinterpret_cast<uint4 *>(kblo + toff(64 + pt, 16 * pq)) = l4;
                 split8(fq + 8, h4, l4);
                 *reinterpret_cast<uint4 *>(kb + toff(64 + pt, 16 * pq + 8)) = h4;
                 *reinterpret_cast<uint4 *>(kblo + toff(64 + pt, 16 * pq + 8)) = l4;
-                // phi(k_hat): inclusive scan over this warp's 8 tokens (lanes 4 apart)
+                // phi(k_hat): inclusive scan over this warp's 8 tokens (adjacent lanes)
 #pragma unroll
-                for (int m = 0; m < 16; ++m) fk[m] = pt < nt ? phi_elu1(kf[m] * ksc) : 0.f;
+                for (int m = 0; m < 16; ++m) fk[m] = pt < nt ? phi_fast(kf[m] * ksc) : 0.f;
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
+                for (int off = 1; off < 8; off <<= 1) {
 #pragma unroll
                     for (int m = 0; m < 16; ++m) {
                         const float y = __shfl_up_sync(0xffffffffu, fk[m], off);
-                        if (lane >= off) fk[m] += y;
+                        if ((lane & 7) >= off) fk[m] += y;
                     }
                 }
-                if (lane >= 28) {
+                if ((lane & 7) == 7) {
                     float4 *dst = reinterpret_cast<float4 *>(s_tot + warp * 64 + 16 * pq);
 #pragma unroll
                     for (int h = 0; h < 4; ++h) dst[h] = make_float4(fk[4 * h], fk[4 * h + 1], fk[4 * h + 2], fk[4 * h + 3]);
@@ -307,42 +321,49 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         }
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 1: D1 = X [K | Phi]^T, D2 = [K; Phi] Al^T ----
+        // ---- round 1: D1 = X K^T, D2 = [K; Phi] Al^T, (mode 1) DO = Phi X^T ----
         if (tid == 0) {
             tc_fence_after();
+            mma64(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x64, false);
+            mma64(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x64, true);
             if (MODE == 1) {
-                mma64x3(tbase, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(kb), smem_u32(kblo), id_x_kb, false);
                 mma64x3(tbase + col_d2, smem_u32(kb), smem_u32(kblo), smem_u32(al_hi), smem_u32(al_lo), id_kb_al, false);
+                mma64x3(tbase + col_do, smem_u32(kb + kTile), smem_u32(kblo + kTile), smem_u32(xs_hi), smem_u32(xs_lo),
+                        id_64, false);
             } else {
-                mma64(tbase, smem_u32(xs_hi), smem_u32(kb), id_x_kb, false);
-                mma64(tbase, smem_u32(xs_lo), smem_u32(kb), id_x_kb, true);
                 mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_kb_al, false);
                 mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_kb_al, true);
             }
             umma_commit(bar);
         }
         if (MODE == 1) {  // readout denominators 1 / (phi(q_t) . n_t + eps)
-            float pre[16];
+            if (tid < 64) {  // per feature: exclusive prefix of the warp totals, and the total
+                float run = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) pre[m] = nb[m];
-            for (int w = 0; w < 8; ++w) {
-                const float4 *tw = reinterpret_cast<const float4 *>(s_tot + w * 64 + 16 * pq);
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float4 t4 = tw[h];
-                    const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (w < warp) pre[4 * h + e] += tv[e];
-                        nb[4 * h + e] += tv[e];
-                    }
+                for (int w = 0; w < 8; ++w) {
+                    const float x = s_tot[w * 64 + tid];
+                    s_tot[w * 64 + tid] = run;
+                    run += x;
                 }
+                s_tot[8 * 64 + tid] = run;
             }
+            __syncthreads();
+            const float4 *pw = reinterpret_cast<const float4 *>(s_tot + warp * 64 + 16 * pq);
+            const float4 *pa = reinterpret_cast<const float4 *>(s_tot + 8 * 64 + 16 * pq);
             float dp = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) dp = fmaf(fq[m], pre[m] + fk[m], dp);
-            dp += __shfl_xor_sync(0xffffffffu, dp, 1);
-            dp += __shfl_xor_sync(0xffffffffu, dp, 2);
+            for (int h = 0; h < 4; ++h) {
+                const float4 p4 = pw[h], a4 = pa[h];
+                const float pv[4] = {p4.x, p4.y, p4.z, p4.w}, av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int m = 4 * h + e;
+                    dp = fmaf(fq[m], nb[m] + pv[e] + fk[m], dp);
+                    nb[m] += av[e];
+                }
+            }
+            dp += __shfl_xor_sync(0xffffffffu, dp, 8);
+            dp += __shfl_xor_sync(0xffffffffu, dp, 16);
             if (pq == 0) s_rden[pt] = 1.f / (dp + kEps);
         }
         load_in(sb + 1);
@@ -359,10 +380,10 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                 if (qw < 2) {  // rows 0..63: (Al^T K)^T
                     const float kt = s_ks[t];
 #pragma unroll
-                    for (int m = 0; m < 32; ++m) {
-                        const int s = 32 * hw + m;
-                        nbuf[s * 64 + t] = s < t ? v[m] * kt : 0.f;
-                    }
+                    for (int m = 0; m < 32; ++m) v[m] = (32 * hw + m < t) ? v[m] * kt : 0.f;
+                    float4 *dst = reinterpret_cast<float4 *>(ntb + t * kNT + 32 * hw);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 } else {       // rows 64..127: Qm^T
 #pragma unroll
                     for (int m = 0; m < 32; ++m)
@@ -373,65 +394,87 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                 const int t = 16 * qw + lane;
                 const float kt = s_ks[t];
 #pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int s = 32 * hw + m;
-                    nbuf[s * 64 + t] = s < t ? v[m] * kt : 0.f;
-                }
-            }
-            tmem_ld32(tq + 32 * hw, v);  // X K, columns 32 hw ..
-            if (xact) {
+                for (int m = 0; m < 32; ++m) v[m] = (32 * hw + m < t) ? v[m] * kt : 0.f;
+                float4 *dst = reinterpret_cast<float4 *>(ntb + t * kNT + 32 * hw);
 #pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int t = 32 * hw + m;
-                    const float val = (MODE == 1 || xrow < 64) ? __bfloat162float(vt[t * kD + (xrow & 63)]) : 0.f;
-                    v[m] = val - v[m] * s_ks[t];
+                for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            tmem_ld32(tq + col_d4 + 32 * hw, v);  // X K, columns 32 hw ..
+            if (xact) {
+                const float4 *ks4 = reinterpret_cast<const float4 *>(s_ks + 32 * hw);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 k4 = ks4[q];
+                    const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = 4 * q + e, t = 32 * hw + m;
+                        const float val = (MODE == 1 || xrow < 64) ? __bfloat162float(vt[t * kVS + (xrow & 63)]) : 0.f;
+                        v[m] = fmaf(-v[m], kv[e], val);
+                    }
                 }
                 put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
             }
         }
         tc_fence_before();
         __syncthreads();
-        // ---- T_inv = (I + N)^{-1}: column t by back substitution, 4 threads a column ----
-        // (a warp holds columns 8 warp .. 8 warp + 7 and skips the steps s
-        // that none of them needs, s >= 8 warp + 7)
+        // ---- T_inv = (I + N)^{-1}, right-looking ----
+        // Accumulator A[s][t] = sum_{r > s} N[s][r] T[r][t] - [s == t], so
+        // that T = -A everywhere (A[s][t] stays 0 for s > t because T[r][t]
+        // = 0 for r > t).  Row r of T is final once the steps r' > r are
+        // done; step r adds N[:, r] T[r, :].  Thread tile: rows 4 rb ..
+        // 4 rb + 3, columns 4 cb .. 4 cb + 3 with lane = 16 h + rb and
+        // cb = 2 warp + h; the owner of row r (row block r / 4 of the same
+        // half-warp) broadcasts it by shuffle.  A warp holds columns 8 warp ..
+        // 8 warp + 7 and skips the steps r > 8 warp + 7 (T[r][t] = 0 there).
         {
-            const int t = tid >> 2, p = tid & 3;
-            float xr[16];
+            const int rb = lane & 15, cb = 2 * warp + (lane >> 4), src = lane & 16;
+            float2 acc[4][2];  // acc[i][jp] = columns 4 cb + 2 jp, + 1 of row 4 rb + i
 #pragma unroll
-            for (int m = 0; m < 16; ++m) xr[m] = (16 * p + m == t) ? 1.f : 0.f;
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int s = kSB - 2; s >= 0; --s) {
-                if (8 * warp + 7 <= s) continue;
-                const float4 *nr = reinterpret_cast<const float4 *>(nbuf + s * 64 + 16 * p);
-                float acc0 = 0.f, acc1 = 0.f;
+                for (int jp = 0; jp < 2; ++jp)
+                    acc[i][jp] = make_float2(4 * rb + i == 4 * cb + 2 * jp ? -1.f : 0.f,
+                                             4 * rb + i == 4 * cb + 2 * jp + 1 ? -1.f : 0.f);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 n4 = nr[q];
-                    acc0 = fmaf(n4.x, xr[4 * q], acc0);
-                    acc1 = fmaf(n4.y, xr[4 * q + 1], acc1);
-                    acc0 = fmaf(n4.z, xr[4 * q + 2], acc0);
-                    acc1 = fmaf(n4.w, xr[4 * q + 3], acc1);
+            for (int r = kSB - 1; r >= 1; --r) {
+                if (8 * warp + 7 < r) continue;
+                const float4 n4 = *reinterpret_cast<const float4 *>(ntb + r * kNT + 4 * rb);  // N[4 rb + i][r]
+                float2 mt[2];  // -T[r][t] = A[r][t] for this thread's columns
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    mt[jp].x = __shfl_sync(0xffffffffu, acc[r & 3][jp].x, src + (r >> 2));
+                    mt[jp].y = __shfl_sync(0xffffffffu, acc[r & 3][jp].y, src + (r >> 2));
                 }
-                float acc = acc0 + acc1;
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                if (p == (s >> 4) && s < t) xr[s & 15] = -acc;
+                const float nv[4] = {-n4.x, -n4.y, -n4.z, -n4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int jp = 0; jp < 2; ++jp) acc[i][jp] = fma2(f2(nv[i]), mt[jp], acc[i][jp]);
             }
-            __syncthreads();  // every read of N is done before T_inv^T overwrites it
-            uint4 h4, l4;
-            split8(xr, h4, l4);
-            *reinterpret_cast<uint4 *>(al_hi + toff(t, 16 * p)) = h4;
-            *reinterpret_cast<uint4 *>(al_lo + toff(t, 16 * p)) = l4;
-            split8(xr + 8, h4, l4);
-            *reinterpret_cast<uint4 *>(al_hi + toff(t, 16 * p + 8)) = h4;
-            *reinterpret_cast<uint4 *>(al_lo + toff(t, 16 * p + 8)) = l4;
+            __syncthreads();  // every read of N^T is done before T_inv^T overwrites it
+            // T_inv^T rows t = 4 cb + j, K = s = 4 rb .. 4 rb + 3 (8 bytes each of hi, lo)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = 4 * cb + j;
+                float tv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tv[i] = -((j & 1) ? acc[i][j >> 1].y : acc[i][j >> 1].x);
+                const __nv_bfloat162 h0 = __floats2bfloat162_rn(tv[0], tv[1]);
+                const __nv_bfloat162 h1 = __floats2bfloat162_rn(tv[2], tv[3]);
+                const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+                const __nv_bfloat162 l0 = __floats2bfloat162_rn(tv[0] - f0.x, tv[1] - f0.y);
+                const __nv_bfloat162 l1 = __floats2bfloat162_rn(tv[2] - f1.x, tv[3] - f1.y);
+                *reinterpret_cast<uint2 *>(ti_hi + toff(t, 4 * rb)) = make_uint2(bf2_bits(h0), bf2_bits(h1));
+                *reinterpret_cast<uint2 *>(ti_lo + toff(t, 4 * rb)) = make_uint2(bf2_bits(l0), bf2_bits(l1));
+            }
         }
         fence_proxy_async_smem();
         __syncthreads();
         // ---- round 2: R = E T_inv ----
         if (tid == 0) {
             tc_fence_after();
-            mma64x3(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi), smem_u32(al_lo), id_x64, false);
+            mma64x3(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi), smem_u32(ti_lo), id_x64, false);
             umma_commit(bar);
         }
         if (!round_wait()) {
@@ -446,12 +489,13 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 3: X += R Al^T; (mode 1) X Phi += R Qm ----
+        // ---- round 3: X += R Al^T; (mode 1) DO += Qm^T R^T ----
         if (tid == 0) {
             tc_fence_after();
-            mma64x3(tbase + col_d4, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(alf_hi), smem_u32(alf_lo), id_x64, false);
+            mma64x3<true>(tbase + col_d4, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi), smem_u32(al_lo), id_x64,
+                          false);
             if (MODE == 1)
-                mma64x3(tbase + 64, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(kb), smem_u32(kb + kTile), id_x64, true);
+                mma64x3(tbase + col_do, smem_u32(kb), smem_u32(kb + kTile), smem_u32(xs_hi), smem_u32(xs_lo), id_64, true);
             umma_commit(bar);
         }
         if (!round_wait()) {
@@ -467,12 +511,18 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                 put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
             }
             if (MODE == 1) {
-                tmem_ld32(tq + 64 + 32 * hw, v);  // numerators S_t phi(q_t), token columns
-                if (xact) {
+                tmem_ld32(tq + col_do + 32 * hw, v);  // numerators of token 16 qw + lane, columns 32 hw ..
+                const int t = 16 * qw + lane;
+                if (lane < 16 && t < nt) {
+                    const float rd = s_rden[t];
+                    uint4 *dst = reinterpret_cast<uint4 *>(gout + (size_t)(sb * kSB + t) * kD + 32 * hw);
 #pragma unroll
-                    for (int m = 0; m < 32; ++m) {
-                        const int t = 32 * hw + m;
-                        vt[t * kD + xrow] = __float2bfloat16_rn(v[m] * s_rden[t]);
+                    for (int g = 0; g < 4; ++g) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = bf2_bits(__floats2bfloat162_rn(v[8 * g + 2 * e] * rd, v[8 * g + 2 * e + 1] * rd));
+                        dst[g] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
@@ -480,16 +530,6 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
-        if (MODE == 1) {  // o of the sub-block: 64 tokens x 128 bytes
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int id = tid + kThreads * e, t = id >> 3, part = id & 7;
-                if (t < nt)
-                    *reinterpret_cast<uint4 *>(gout + (size_t)(sb * kSB + t) * kD + 8 * part) =
-                        *reinterpret_cast<const uint4 *>(vt + t * kD + 8 * part);
-            }
-            __syncthreads();  // the stage becomes the next v tile
-        }
     }
     if (!ok) {
         if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);

@@ -104,14 +104,14 @@ def test_workspace_query_and_kernel_selection():
     assert ws >= 16 * (4096 * 64 * 4 + 16 * 4 * 64 * 64 * 4)
     assert vla.vla_workspace_bytes(1, 16, 4096, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK, 24) == 0
     assert vla.vla_workspace_bytes(1, 16, 0, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK) == 0
-    assert vla.vla_select_kernel(1, 16, 65536, 64) == vla.VLA_KERNEL_CHUNK
+    assert vla.vla_select_kernel(1, 16, 65536, 64) == vla.VLA_KERNEL_CHUNK_TC
     assert vla.vla_select_kernel(256, 4, 512, 32) == vla.VLA_KERNEL_SEQ
     assert vla.vla_select_kernel(32, 64, 1, 64) == vla.VLA_KERNEL_DECODE
     assert vla.vla_select_kernel(32, 64, 4, 64) == vla.VLA_KERNEL_DECODE
     assert vla.vla_select_kernel(32, 64, 5, 64) == vla.VLA_KERNEL_SEQ
     assert vla.vla_workspace_bytes(32, 64, 1, 64, vla.VLA_BF16, vla.VLA_KERNEL_DECODE) == 0
     assert vla.vla_workspace_bytes(1, 16, 4096, 48, vla.VLA_BF16, vla.VLA_KERNEL_SEQ) == 0
-    assert vla.vla_select_kernel(1, 16, 4096, 64) in (vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK)
+    assert vla.vla_select_kernel(1, 16, 4096, 64) in (vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK_TC)
     assert vla.vla_select_kernel(1, 16, 4096, 40) == vla.VLA_ERR_UNSUPPORTED_DIM
 
 
