@@ -118,7 +118,7 @@ size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kerne
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return 0;
     const int kk = resolve_kernel(B, H, T, d_h, kernel);
     if ((kk != VLA_KERNEL_CHUNK && kk != VLA_KERNEL_CHUNK_TC) || T == 0 || (long long)B * H == 0) return 0;
-    return vla::chunk_layout(B * H, T, d_h, chunk).total;
+    return vla::chunk_layout(B * H, T, d_h, chunk, kk == VLA_KERNEL_CHUNK_TC && io_dtype == VLA_BF16).total;
 }
 
 size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h) {
@@ -226,8 +226,9 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if ((kk == VLA_KERNEL_CHUNK || kk == VLA_KERNEL_CHUNK_TC) && T > 0) {
-        const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk);
-        p.rows_tc = (kk == VLA_KERNEL_CHUNK_TC);
+        const bool tc = (kk == VLA_KERNEL_CHUNK_TC);
+        const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk, tc && io_dtype == VLA_BF16);
+        p.rows_tc = tc;
         e = vla::launch_chunk(p, L, st);
     } else if (kk == VLA_KERNEL_DECODE) {
         e = vla::launch_decode(p, st);

@@ -1240,7 +1240,7 @@ int chunk_default_a(int BH, int T, int d, int C) {
     return best;
 }
 
-ChunkLayout chunk_layout(int BH, int T, int d, int chunk) {
+ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tinv) {
     ChunkLayout L{};
     L.C = chunk > 0 ? chunk : chunk_default(BH, T);
     L.CA = chunk > 0 ? chunk : chunk_default_a(BH, T, d, L.C);
@@ -1255,6 +1255,9 @@ ChunkLayout chunk_layout(int BH, int T, int d, int chunk) {
     L.off_P = off; off = align256(off + bh * nc * dd * 4);
     L.off_H = off; off = align256(off + bh * nc * dd * 4);
     L.off_S = off; off = align256(off + bh * nc * dd * 4);
+    L.off_tinv = off;
+    L.tinv = (tinv && d == 64 && L.C % 64 == 0) ? 1 : 0;
+    if (L.tinv) off = align256(off + bh * nc * (size_t)(L.C / 64) * 16384);
     L.total = off;
     return L;
 }

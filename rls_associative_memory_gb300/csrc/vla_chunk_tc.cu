@@ -16,11 +16,14 @@
 // the sub-block left in the state, hence the triangular system).  A
 // sub-block is three rounds of tcgen05.mma plus one triangular inverse on
 // the CUDA cores:
-//   1. D1 = X K^T,  D2 = [K ; Phi] Al^T  (= N^T, Qm^T),  (mode 1) DO = Phi X^T
+//   1. D1 = X K^T;  mode 0: D2 = K Al^T (= N^T);  mode 1: D2 = Phi Al^T
+//      (= Qm^T, Qm = upper-incl(Al^T Phi)) and DO = Phi X^T
 //   2. R  = E T_inv,   E = Vals - (X K) diag(1/|k|),  T_inv = (I + N)^{-1}
-//   3. X += R Al^T    and (mode 1)  DO += Qm^T R^T,  Qm = upper-incl(Al^T Phi)
-// DO holds the readout numerators token-major (rows = tokens), so o leaves
-// as whole 16-byte vectors.
+//   3. X += R Al^T    and (mode 1)  DO += Qm^T R^T
+// T_inv depends on the keys and gates only: mode 0 computes it and stores
+// it (bf16 hi/lo operand tiles) in the workspace, and mode 1 loads it with a
+// bulk copy.  DO holds the readout numerators token-major (rows = tokens),
+// so o leaves as whole 16-byte vectors.
 //
 // Mode 0 runs the rows [H; P] of the chunk map S_end = S_start P_c + H_c
 // (values [v; 0], start [0; I]: M = 128); mode 1 runs S itself from the
@@ -53,16 +56,16 @@ template <int MODE>
 struct TcLayout {
     static constexpr int XR = MODE == 0 ? 128 : 64;            // state rows
     static constexpr uint32_t ncols = MODE == 0 ? 128 : 256;    // TMEM columns
-    static constexpr size_t ctrl = 0;                            // mbarrier, TMEM slot, abort flag
+    static constexpr size_t ctrl = 0;                            // mbarriers (MMA, T_inv load), TMEM slot, abort flag
     static constexpr size_t xs = 1024;                           // X / E / R tiles: hi, lo
     static constexpr size_t xs_t = (size_t)XR * 128;
     static constexpr size_t kb = xs + 2 * xs_t;                  // [K; Phi_hi] (mode 1) or K; then Qm^T hi, lo
-    static constexpr size_t kblo = kb + (MODE == 0 ? kTile : 2 * kTile);  // [0; Phi_lo] (mode 1)
-    static constexpr size_t al = kblo + (MODE == 0 ? 0 : 2 * kTile);     // Al (token rows) hi, lo
+    static constexpr size_t kblo = kb + (MODE == 0 ? kTile : 2 * kTile);  // Phi_lo (mode 1)
+    static constexpr size_t al = kblo + (MODE == 0 ? 0 : kTile);          // Al (token rows) hi, lo
     static constexpr int kNT = 68;                               // row stride (floats) of N^T: conflict-free rows
-    static constexpr size_t ti = al + 2 * kTile;                 // N^T (fp32), then T_inv^T hi, lo
+    static constexpr size_t ti = al + 2 * kTile;                 // (mode 0) N^T fp32; T_inv^T hi, lo
     static constexpr int kVS = 72;                               // row stride (bf16) of the v tile
-    static constexpr size_t vt = ti + (size_t)64 * kNT * 4;      // v [t][i] bf16
+    static constexpr size_t vt = ti + (MODE == 0 ? (size_t)64 * kNT * 4 : 2 * (size_t)kTile);  // v [t][i] bf16
     static constexpr size_t ks = vt + (size_t)64 * kVS * 2;      // [64] 1 / max(|k|, eps)
     static constexpr size_t rden = ks + 256;                     // [64] 1 / (phi(q).n + eps)
     static constexpr size_t tot = rden + 256;                    // [9][64] warp totals of phi(k_hat), then prefixes
@@ -129,12 +132,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // K-step of 16 advances two row groups.
 template <bool B_MN = false>
 __device__ __forceinline__ void mma64(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool acc) {
+    // descriptor address fields count 16-byte units: a K-step adds 256 bytes
+    // (K-major) or 2048 bytes (MN-major) to the start address
+    const uint64_t ad = umma_desc_kmajor(a, 128, 1024);
+    const uint64_t bd = B_MN ? umma_desc_kmajor(b, 1024, 128) : umma_desc_kmajor(b, 128, 1024);
+    const uint32_t id = idesc | (B_MN ? (1u << 16) : 0u);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(d, umma_desc_kmajor(a + ks * 256, 128, 1024),
-                  B_MN ? umma_desc_kmajor(b + ks * 2048, 1024, 128) : umma_desc_kmajor(b + ks * 256, 128, 1024),
-                  idesc | (B_MN ? (1u << 16) : 0u),
-                  (acc || ks > 0) ? 1u : 0u);
+        umma_bf16(d, ad + (uint64_t)(16 * ks), bd + (uint64_t)((B_MN ? 128 : 16) * ks), id, (acc || ks > 0) ? 1u : 0u);
 }
 
 // Split product D (+)= (Ah + Al)(Bh + Bl)^T without the lo*lo term.
@@ -154,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
+    uint64_t *bar_t = reinterpret_cast<uint64_t *>(smem + L::ctrl + 16);  // T_inv^T load (mode 1)
     unsigned char *xs_hi = smem + L::xs, *xs_lo = smem + L::xs + L::xs_t;
     unsigned char *kb = smem + L::kb, *kblo = smem + L::kblo;
     unsigned char *al_hi = smem + L::al, *al_lo = smem + L::al + kTile;
@@ -179,14 +185,15 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     const float *gal = ws_f(a, a.L.off_alpha) + tok0;
     __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.p.o) + tok0;
 
+    unsigned char *gtinv = static_cast<unsigned char *>(a.p.ws) + a.L.off_tinv +
+                           (size_t)(bh * NC + c) * (C / kSB) * (2 * kTile);  // this chunk's T_inv^T tiles
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar_t, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
     if (warp == 0) tmem_alloc(tslot, L::ncols);
-    if (MODE == 1)  // rows 0..63 of [0; Phi_lo] stay zero
-        for (int x = tid; x < kTile / 16; x += kThreads) reinterpret_cast<uint4 *>(kblo)[x] = make_uint4(0, 0, 0, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -249,7 +256,6 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         return *abort_flag == 0;
     };
     constexpr uint32_t id_x64 = idesc_bf16_f32(XR, 64);                       // X-row products
-    constexpr uint32_t id_kb_al = MODE == 1 ? idesc_bf16_f32(128, 64) : idesc_bf16_f32(64, 64);
     constexpr uint32_t id_64 = idesc_bf16_f32(64, 64);
     constexpr int kNT = L::kNT, kVS = L::kVS;
     constexpr uint32_t col_d2 = MODE == 1 ? 128 : 64;   // D2, then D3 = R
@@ -257,10 +263,16 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     constexpr uint32_t col_do = 64;                     // (mode 1) readout numerators, token rows
 
     bool ok = true;
+    int tinv_issued = 0, tinv_done = 0;  // T_inv^T loads (mode 1)
     load_in(0);
     for (int sb = 0; sb < nsb; ++sb) {
         const int nt = min(kSB, ntok - sb * kSB);
         float fq[16], fk[16];
+        if (MODE == 1 && tid == 0) {  // T_inv^T of this sub-block (the slot is free: round 2 is done)
+            mbar_arrive_expect_tx(bar_t, 2 * kTile);
+            bulk_g2s(ti_hi, gtinv + (size_t)sb * 2 * kTile, 2 * kTile, bar_t);
+        }
+        tinv_issued = sb + 1;
         // ---- stage the sub-block's operands ----
         {
             float kf[16];
@@ -297,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                 for (int m = 0; m < 16; ++m) fq[m] = phi_fast(qf[m]);
                 split8(fq, h4, l4);
                 *reinterpret_cast<uint4 *>(kb + toff(64 + pt, 16 * pq)) = h4;
-                *reinterpret_cast<uint4 *>(kblo + toff(64 + pt, 16 * pq)) = l4;
+                *reinterpret_cast<uint4 *>(kblo + toff(pt, 16 * pq)) = l4;
                 split8(fq + 8, h4, l4);
                 *reinterpret_cast<uint4 *>(kb + toff(64 + pt, 16 * pq + 8)) = h4;
-                *reinterpret_cast<uint4 *>(kblo + toff(64 + pt, 16 * pq + 8)) = l4;
+                *reinterpret_cast<uint4 *>(kblo + toff(pt, 16 * pq + 8)) = l4;
                 // phi(k_hat): inclusive scan over this warp's 8 tokens (adjacent lanes)
 #pragma unroll
                 for (int m = 0; m < 16; ++m) fk[m] = pt < nt ? phi_fast(kf[m] * ksc) : 0.f;
@@ -321,18 +333,19 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         }
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 1: D1 = X K^T, D2 = [K; Phi] Al^T, (mode 1) DO = Phi X^T ----
+        // ---- round 1: D1 = X K^T; D2 = K Al^T (mode 0) or Phi Al^T (mode 1); (mode 1) DO = Phi X^T ----
         if (tid == 0) {
             tc_fence_after();
             mma64(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x64, false);
             mma64(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x64, true);
             if (MODE == 1) {
-                mma64x3(tbase + col_d2, smem_u32(kb), smem_u32(kblo), smem_u32(al_hi), smem_u32(al_lo), id_kb_al, false);
-                mma64x3(tbase + col_do, smem_u32(kb + kTile), smem_u32(kblo + kTile), smem_u32(xs_hi), smem_u32(xs_lo),
-                        id_64, false);
+                mma64x3(tbase + col_d2, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(al_hi), smem_u32(al_lo), id_64,
+                        false);
+                mma64x3(tbase + col_do, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(xs_hi), smem_u32(xs_lo), id_64,
+                        false);
             } else {
-                mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_kb_al, false);
-                mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_kb_al, true);
+                mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
+                mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
             }
             umma_commit(bar);
         }
@@ -371,33 +384,25 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             ok = false;
             break;
         }
-        // ---- N (fp32, for the inverse), Qm^T tiles (mode 1), E tiles ----
+        // ---- N^T (fp32, for the inverse; mode 0), Qm^T tiles (mode 1), E tiles ----
         {
             float v[32];
-            tmem_ld32(tq + col_d2 + 32 * hw, v);
-            if (MODE == 1) {
-                const int t = 32 * (qw & 1) + lane;
-                if (qw < 2) {  // rows 0..63: (Al^T K)^T
+            tmem_ld32(tq + col_d2 + 32 * hw, v);  // D2 row t = 16 qw + lane (M = 64), columns s = 32 hw ..
+            if (lane < 16) {
+                const int t = 16 * qw + lane;
+                if (MODE == 1) {
+#pragma unroll
+                    for (int m = 0; m < 32; ++m)
+                        if (32 * hw + m > t) v[m] = 0.f;
+                    put_row32(kb, kb + kTile, t, 32 * hw, v);
+                } else {
                     const float kt = s_ks[t];
 #pragma unroll
                     for (int m = 0; m < 32; ++m) v[m] = (32 * hw + m < t) ? v[m] * kt : 0.f;
                     float4 *dst = reinterpret_cast<float4 *>(ntb + t * kNT + 32 * hw);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                } else {       // rows 64..127: Qm^T
-#pragma unroll
-                    for (int m = 0; m < 32; ++m)
-                        if (32 * hw + m > t) v[m] = 0.f;
-                    put_row32(kb, kb + kTile, t, 32 * hw, v);
                 }
-            } else if (lane < 16) {
-                const int t = 16 * qw + lane;
-                const float kt = s_ks[t];
-#pragma unroll
-                for (int m = 0; m < 32; ++m) v[m] = (32 * hw + m < t) ? v[m] * kt : 0.f;
-                float4 *dst = reinterpret_cast<float4 *>(ntb + t * kNT + 32 * hw);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
             tmem_ld32(tq + col_d4 + 32 * hw, v);  // X K, columns 32 hw ..
             if (xact) {
@@ -427,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         // cb = 2 warp + h; the owner of row r (row block r / 4 of the same
         // half-warp) broadcasts it by shuffle.  A warp holds columns 8 warp ..
         // 8 warp + 7 and skips the steps r > 8 warp + 7 (T[r][t] = 0 there).
-        {
+        if (MODE == 0) {
             const int rb = lane & 15, cb = 2 * warp + (lane >> 4), src = lane & 16;
             float2 acc[4][2];  // acc[i][jp] = columns 4 cb + 2 jp, + 1 of row 4 rb + i
 #pragma unroll
@@ -468,6 +473,9 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                 *reinterpret_cast<uint2 *>(ti_hi + toff(t, 4 * rb)) = make_uint2(bf2_bits(h0), bf2_bits(h1));
                 *reinterpret_cast<uint2 *>(ti_lo + toff(t, 4 * rb)) = make_uint2(bf2_bits(l0), bf2_bits(l1));
             }
+        } else {  // mode 1: T_inv^T of this sub-block, stored by the transition pass
+            if (!mbar_wait_bounded(bar_t, (uint32_t)(sb & 1), a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+            tinv_done = sb + 1;
         }
         fence_proxy_async_smem();
         __syncthreads();
@@ -476,6 +484,12 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             tc_fence_after();
             mma64x3(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi), smem_u32(ti_lo), id_x64, false);
             umma_commit(bar);
+        }
+        if (MODE == 0) {  // T_inv^T tiles to the workspace for the readout pass
+            const uint4 *src4 = reinterpret_cast<const uint4 *>(ti_hi);
+            uint4 *dst4 = reinterpret_cast<uint4 *>(gtinv + (size_t)sb * 2 * kTile);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst4[tid + kThreads * e] = src4[tid + kThreads * e];
         }
         if (!round_wait()) {
             ok = false;
@@ -532,7 +546,11 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         __syncthreads();
     }
     if (!ok) {
-        if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
+        if (tid == 0) {
+            (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
+            if (MODE == 1 && tinv_issued > tinv_done)  // a T_inv^T copy may still be landing
+                (void)mbar_wait_bounded(bar_t, (uint32_t)((tinv_issued - 1) & 1), a.p.wait_limit_ns, a.p.err);
+        }
     } else if (MODE == 0) {  // rows 0..63 are H_c, rows 64..127 P_c
         float4 *dst = reinterpret_cast<float4 *>(ws_f(a, xrow < 64 ? a.L.off_H : a.L.off_P) +
                                                  ((size_t)bh * NC + c) * kD * kD + (size_t)(xrow & 63) * kD + 32 * hw);
@@ -558,7 +576,7 @@ cudaError_t launch_mode(const ChunkArgs &a, cudaStream_t st) {
 }  // namespace
 
 bool rows_tc_supported(const FwdParams &p, const ChunkLayout &L) {
-    return p.d == kD && p.io_bf16 && L.C % kSB == 0;
+    return p.d == kD && p.io_bf16 && L.C % kSB == 0 && L.tinv;
 }
 
 cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream) {

@@ -82,6 +82,9 @@ struct ChunkLayout {
     size_t off_P;        // [BH][NC][d][d]  chunk transition P_c
     size_t off_H;        // [BH][NC][d][d]  chunk offset H_c
     size_t off_S;        // [BH][NC][d][d]  chunk-start states S^(c)
+    size_t off_tinv;     // [BH][NC][C/64][2][64][64] bf16: T_inv^T (hi, lo) of every 64-token
+                         // sub-block, written by the tensor-core transition pass for the readout
+    int tinv;            // 1 when the off_tinv region is reserved
     size_t total;
 };
 
@@ -92,8 +95,9 @@ long long api_wait_limit_ns();
 int api_cuda_fail(cudaError_t e);
 
 // Layout for a shape; chunk > 0 (a multiple of 16) sets both chunk lengths,
-// chunk == 0 picks the defaults.
-ChunkLayout chunk_layout(int BH, int T, int d, int chunk);
+// chunk == 0 picks the defaults.  tinv reserves the T_inv store of the
+// tensor-core state passes (d = 64, chunks a multiple of 64 tokens).
+ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tinv = false);
 // Chunk-parallel path (six launches).  Returns a cudaError_t.
 cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream);
 
