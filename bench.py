@@ -52,7 +52,8 @@ TRAFFIC = {
 
 
 def kernel_src_hash(kernel_name: str) -> str:
-    fns = {"seq": ["vla_seq.cu"], "chunk": ["vla_chunk.cu"], "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu"],
+    fns = {"seq": ["vla_seq.cu"], "chunk": ["vla_chunk.cu"],
+           "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu", "vla_gates_tc.cu", "vla_tc_common.cuh"],
            "decode": ["vla_decode.cu"]}[kernel_name]
     h = hashlib.sha256()
     for fn in fns:
@@ -78,8 +79,10 @@ def kernel_plan(kname, d, io_dtype="bf16"):
     # output: S k_hat, state write, S phi(q), readout (a3-a4)
     gram = "gram_tc_kernel" if (io_dtype == "bf16" and d >= 64) else "gram_kernel"
     # chunk_tc at d = 64 with bf16 I/O: the state passes run on the tensor cores
-    rows = "rows_tc_kernel" if (kname == "chunk_tc" and io_dtype == "bf16" and d == 64) else "rows_kernel"
-    return [(gram, 0, "alu"), ("prefix_kernel", 0, "alu"), ("gates_kernel", 6 * d * d + 8 * d, "alu"),
+    tc = kname == "chunk_tc" and io_dtype == "bf16" and d == 64
+    rows = "rows_tc_kernel" if tc else "rows_kernel"
+    gates = "gates_tc_kernel" if tc else "gates_kernel"
+    return [(gram, 0, "alu"), ("prefix_kernel", 0, "alu"), (gates, 6 * d * d + 8 * d, "alu"),
             (rows + "<summary>", 0, "alu"), ("chain_kernel", 0, "alu"),
             (rows + "<output>", 6 * d * d + 8 * d, "alu")]
 

@@ -30,6 +30,10 @@ namespace {
 
 constexpr int kTT = 16;  // tokens per staged tile
 
+// The block-Woodbury gates (vla_gates_tc.cu) are exact but not yet faster
+// than the Sherman-Morrison gates here, so VLA_KERNEL_CHUNK_TC keeps these.
+constexpr bool kGatesOnTensorCores = false;
+
 // Kahan-compensated accumulation.
 __device__ __forceinline__ void kahan_add(float &sum, float &comp, float x) {
     const float y = x - comp;
@@ -328,61 +332,6 @@ __global__ void __launch_bounds__(256) prefix_kernel(ChunkArgs a) {
         }
         n[(size_t)NC * D] = run;
         if (a.p.n_T) a.p.n_T[(size_t)bh * D + j] = run;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Register-resident inverse of an SPD matrix by Gauss-Jordan elimination
-// (no pivoting: the pivots of an SPD matrix are positive).  Thread (row i,
-// part) holds x[CPT] = row i, columns [CPT part, CPT part + CPT).  piv: two
-// skewed shared vectors for the pivot row (double-buffered).  All threads of
-// the block must call it.
-// ---------------------------------------------------------------------------
-template <int D, int CPT>
-__device__ __forceinline__ void gj_inverse(float (&x)[CPT], float *piv, int row, int part) {
-    constexpr int TPR = D / CPT;
-    constexpr int VLEN = (D / 32) * kPart;
-    const int c0 = part * CPT;
-    const int lane = threadIdx.x & 31;
-    if (row == 0) {
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) piv[vidx(c0 + j)] = x[j];
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int k = 0; k < D; ++k) {
-        const float *pr = piv + (k & 1) * VLEN;
-        const float p = pr[vidx(k)];
-        const float rp = 1.f / p;
-        // m = x[i][k]: held by part k / CPT of this row, register k % CPT
-        float mk = 0.f;
-        const int kp = k / CPT, kr = k % CPT;
-#pragma unroll
-        for (int j = 0; j < CPT; ++j)
-            if (j == kr) mk = x[j];
-        if (TPR > 1) mk = __shfl_sync(0xffffffffu, mk, (lane & ~(TPR - 1)) | kp);
-        if (row == k) {
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) x[j] = (c0 + j == k) ? rp : x[j] * rp;
-        } else {
-            const float f = mk * rp;
-#pragma unroll
-            for (int c4 = 0; c4 < CPT / 4; ++c4) {
-                const float4 pv = *reinterpret_cast<const float4 *>(pr + vidx(c0 + 4 * c4));
-                const float pj[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j = 4 * c4 + q;
-                    x[j] = (c0 + j == k) ? -f : fmaf(-f, pj[q], x[j]);
-                }
-            }
-        }
-        if (k + 1 < D && row == k + 1) {
-            float *nx = piv + ((k + 1) & 1) * VLEN;
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) nx[vidx(c0 + j)] = x[j];
-        }
-        __syncthreads();
     }
 }
 
@@ -1183,8 +1132,12 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     prefix_kernel<D><<<(unsigned)(((D * D + D + 255) / 256) * BH), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    gates_kernel<D, IO><<<(unsigned)(NCA * BH), G::NT, GatesSmem<D, IO>::total, st>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (kGatesOnTensorCores && a.p.rows_tc && gates_tc_supported(a.p, a.L)) {
+        if ((e = launch_gates_tc(a, st)) != cudaSuccess) return e;
+    } else {
+        gates_kernel<D, IO><<<(unsigned)(NCA * BH), G::NT, GatesSmem<D, IO>::total, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     mark_launch(a.p, ++n, st);
     const bool tc = a.p.rows_tc && rows_tc_supported(a.p, a.L);
     if (tc) {
@@ -1240,10 +1193,31 @@ int chunk_default_a(int BH, int T, int d, int C) {
     return best;
 }
 
+// A-chunk length for the tensor-core gates (d = 64): two CTAs per SM, each
+// sub-block of 64 tokens one unit of time and the Gauss-Jordan restart about
+// 0.4 of one.
+int chunk_default_a_tc(int BH, int T, int C) {
+    const long long resident = 152LL * 2;
+    int best = C;
+    long long best_cost = -1;
+    for (int CA = C; CA >= 64; CA /= 2) {
+        if (C % CA) continue;
+        const long long chunks = (long long)BH * ((T + CA - 1) / CA);
+        const long long waves = (chunks + resident - 1) / resident;
+        const long long cost = waves * (10 * (CA / 64) + 4);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = CA;
+        }
+    }
+    return best;
+}
+
 ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tinv) {
     ChunkLayout L{};
     L.C = chunk > 0 ? chunk : chunk_default(BH, T);
-    L.CA = chunk > 0 ? chunk : chunk_default_a(BH, T, d, L.C);
+    const bool tc = tinv && d == 64 && L.C % 64 == 0;
+    L.CA = chunk > 0 ? chunk : (tc ? chunk_default_a_tc(BH, T, L.C) : chunk_default_a(BH, T, d, L.C));
     L.NC = (T + L.C - 1) / L.C;
     L.NCA = (T + L.CA - 1) / L.CA;
     const size_t bh = (size_t)BH, nc = (size_t)L.NC, nca = (size_t)L.NCA, dd = (size_t)d * d;

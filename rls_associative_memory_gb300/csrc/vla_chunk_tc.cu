@@ -34,23 +34,14 @@
 // hi*hi + hi*lo + lo*hi with fp32 accumulation (relative error about
 // 2^-16).  k and v are bf16 inputs and exact: the raw key enters once and
 // the key norm is applied as a column scale in fp32.
-#include "vla_internal.cuh"
+#include "vla_tc_common.cuh"
 
 namespace vla {
 namespace {
 
-constexpr int kD = 64;        // head dimension of this path
-constexpr int kSB = 64;       // tokens per sub-block
-constexpr int kTile = 8192;   // bytes of a 64-row, 64-column bf16 operand tile
+using namespace tc;
+
 constexpr int kThreads = 256;
-
-// Operand tiles: K-major, unswizzled, K = 64 (core matrices of 8 rows x 16
-// bytes, adjacent along K 128 bytes apart, row groups 1024 bytes apart).
-__device__ __forceinline__ uint32_t toff(int r, int k) { return kmajor_off_bf16(r, k, 64); }
-
-// phi(x) = ELU(x) + 1 with the fast exponential (bf16 I/O only: its relative
-// error, about 2^-21, is far below the output rounding).
-__device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
 template <int MODE>
 struct TcLayout {
@@ -72,90 +63,13 @@ struct TcLayout {
     static constexpr size_t total = tot + 9 * 64 * 4;
 };
 
-__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t *>(&h); }
-
-// bf16 pairs (hi, lo) of 8 consecutive fp32 values, in element order.
-__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-        const float2 hf = __bfloat1622float2(hb);
-        h[e] = bf2_bits(hb);
-        l[e] = bf2_bits(__floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y));
-    }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
-__device__ __forceinline__ void unpack8(uint4 w, float *x) {
-    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        x[2 * e] = __uint_as_float(a[e] << 16);
-        x[2 * e + 1] = __uint_as_float(a[e] & 0xffff0000u);
-    }
-}
-
-// 32 consecutive fp32 values as (hi, lo) into row `row`, columns k0 .. k0+31.
-__device__ __forceinline__ void put_row32(unsigned char *hi, unsigned char *lo, int row, int k0, const float *v) {
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        uint4 h, l;
-        split8(v + 8 * g, h, l);
-        *reinterpret_cast<uint4 *>(hi + toff(row, k0 + 8 * g)) = h;
-        *reinterpret_cast<uint4 *>(lo + toff(row, k0 + 8 * g)) = l;
-    }
-}
-
-// 32 consecutive TMEM columns of this warp's lane quarter (shape 32x32b).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-
-// D (+)= A B^T over K = 64 (four K-steps of 16); A, B are 64- or 128-row tiles.
-// With B_MN, B is read MN-major from a K-major tile of the transposed
-// matrix: a tile whose rows are K and whose 16-byte core-matrix rows run
-// along N.  In the MN-major descriptor the stride between core matrices
-// along N is SBO (128 bytes here) and along K is LBO (1024 bytes), so one
-// K-step of 16 advances two row groups.
-template <bool B_MN = false>
-__device__ __forceinline__ void mma64(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool acc) {
-    // descriptor address fields count 16-byte units: a K-step adds 256 bytes
-    // (K-major) or 2048 bytes (MN-major) to the start address
-    const uint64_t ad = umma_desc_kmajor(a, 128, 1024);
-    const uint64_t bd = B_MN ? umma_desc_kmajor(b, 1024, 128) : umma_desc_kmajor(b, 128, 1024);
-    const uint32_t id = idesc | (B_MN ? (1u << 16) : 0u);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(d, ad + (uint64_t)(16 * ks), bd + (uint64_t)((B_MN ? 128 : 16) * ks), id, (acc || ks > 0) ? 1u : 0u);
-}
-
-// Split product D (+)= (Ah + Al)(Bh + Bl)^T without the lo*lo term.
-template <bool B_MN = false>
-__device__ __forceinline__ void mma64x3(uint32_t d, uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl,
-                                        uint32_t idesc, bool acc) {
-    mma64<B_MN>(d, ah, bh, idesc, acc);
-    mma64<B_MN>(d, ah, bl, idesc, true);
-    mma64<B_MN>(d, al, bh, idesc, true);
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     using L = TcLayout<MODE>;
     constexpr int XR = L::XR;
-    extern __shared__ __align__(1024) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // swizzled tiles need 1024-byte aligned addresses (one extra KB is allocated)
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
@@ -336,16 +250,16 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         // ---- round 1: D1 = X K^T; D2 = K Al^T (mode 0) or Phi Al^T (mode 1); (mode 1) DO = Phi X^T ----
         if (tid == 0) {
             tc_fence_after();
-            mma64(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x64, false);
-            mma64(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x64, true);
+            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x64, false);
+            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x64, true);
             if (MODE == 1) {
-                mma64x3(tbase + col_d2, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(al_hi), smem_u32(al_lo), id_64,
+                mma_k64x3<false, false>(tbase + col_d2, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(al_hi), smem_u32(al_lo), id_64,
                         false);
-                mma64x3(tbase + col_do, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(xs_hi), smem_u32(xs_lo), id_64,
+                mma_k64x3<false, false>(tbase + col_do, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(xs_hi), smem_u32(xs_lo), id_64,
                         false);
             } else {
-                mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
-                mma64(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
+                mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
+                mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
             }
             umma_commit(bar);
         }
@@ -482,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         // ---- round 2: R = E T_inv ----
         if (tid == 0) {
             tc_fence_after();
-            mma64x3(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi), smem_u32(ti_lo), id_x64, false);
+            mma_k64x3<false, false>(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi), smem_u32(ti_lo), id_x64, false);
             umma_commit(bar);
         }
         if (MODE == 0) {  // T_inv^T tiles to the workspace for the readout pass
@@ -506,10 +420,10 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         // ---- round 3: X += R Al^T; (mode 1) DO += Qm^T R^T ----
         if (tid == 0) {
             tc_fence_after();
-            mma64x3<true>(tbase + col_d4, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi), smem_u32(al_lo), id_x64,
+            mma_k64x3<false, true>(tbase + col_d4, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi), smem_u32(al_lo), id_x64,
                           false);
             if (MODE == 1)
-                mma64x3(tbase + col_do, smem_u32(kb), smem_u32(kb + kTile), smem_u32(xs_hi), smem_u32(xs_lo), id_64, true);
+                mma_k64x3<false, false>(tbase + col_do, smem_u32(kb), smem_u32(kb + kTile), smem_u32(xs_hi), smem_u32(xs_lo), id_64, true);
             umma_commit(bar);
         }
         if (!round_wait()) {
@@ -564,12 +478,13 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
 
 template <int MODE>
 cudaError_t launch_mode(const ChunkArgs &a, cudaStream_t st) {
+    constexpr size_t bytes = TcLayout<MODE>::total + 1024;  // + alignment slack
     cudaError_t e = cudaFuncSetAttribute(rows_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)TcLayout<MODE>::total);
+                                         (int)bytes);
     if (e != cudaSuccess) return e;
     const long long grid = (long long)a.L.NC * a.p.BH;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    rows_tc_kernel<MODE><<<(unsigned)grid, kThreads, TcLayout<MODE>::total, st>>>(a);
+    rows_tc_kernel<MODE><<<(unsigned)grid, kThreads, bytes, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -115,6 +115,10 @@ __device__ __forceinline__ float *ws_f(const ChunkArgs &a, size_t off) {
 // transitions (P_c, H_c), mode 1 = readout.  Defined in vla_chunk_tc.cu.
 bool rows_tc_supported(const FwdParams &p, const ChunkLayout &L);
 cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream);
+// Tensor-core gates (block Woodbury over 64-token sub-blocks), same shapes;
+// A-chunks a multiple of 64 tokens.  Defined in vla_gates_tc.cu.
+bool gates_tc_supported(const FwdParams &p, const ChunkLayout &L);
+cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // PTX helpers
@@ -324,6 +328,61 @@ __device__ __forceinline__ float f32_to_io<float>(float x) {
 template <>
 __device__ __forceinline__ __nv_bfloat16 f32_to_io<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
+}
+
+// ---------------------------------------------------------------------------
+// Register-resident inverse of an SPD matrix by Gauss-Jordan elimination
+// (no pivoting: the pivots of an SPD matrix are positive).  Thread (row i,
+// part) holds x[CPT] = row i, columns [CPT part, CPT part + CPT).  piv: two
+// skewed shared vectors for the pivot row (double-buffered).  All threads of
+// the block must call it.
+// ---------------------------------------------------------------------------
+template <int D, int CPT>
+__device__ __forceinline__ void gj_inverse(float (&x)[CPT], float *piv, int row, int part) {
+    constexpr int TPR = D / CPT;
+    constexpr int VLEN = (D / 32) * kPart;
+    const int c0 = part * CPT;
+    const int lane = threadIdx.x & 31;
+    if (row == 0) {
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) piv[vidx(c0 + j)] = x[j];
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int k = 0; k < D; ++k) {
+        const float *pr = piv + (k & 1) * VLEN;
+        const float p = pr[vidx(k)];
+        const float rp = 1.f / p;
+        // m = x[i][k]: held by part k / CPT of this row, register k % CPT
+        float mk = 0.f;
+        const int kp = k / CPT, kr = k % CPT;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j)
+            if (j == kr) mk = x[j];
+        if (TPR > 1) mk = __shfl_sync(0xffffffffu, mk, (lane & ~(TPR - 1)) | kp);
+        if (row == k) {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) x[j] = (c0 + j == k) ? rp : x[j] * rp;
+        } else {
+            const float f = mk * rp;
+#pragma unroll
+            for (int c4 = 0; c4 < CPT / 4; ++c4) {
+                const float4 pv = *reinterpret_cast<const float4 *>(pr + vidx(c0 + 4 * c4));
+                const float pj[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = 4 * c4 + q;
+                    x[j] = (c0 + j == k) ? -f : fmaf(-f, pj[q], x[j]);
+                }
+            }
+        }
+        if (k + 1 < D && row == k + 1) {
+            float *nx = piv + ((k + 1) & 1) * VLEN;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) nx[vidx(c0 + j)] = x[j];
+        }
+        __syncthreads();
+    }
 }
 
 }  // namespace vla

@@ -1,0 +1,118 @@
+// vla_tc_common.cuh -- operand tiles and tcgen05 helpers shared by the
+// tensor-core passes of the chunk-parallel path (d = 64, bf16 I/O).
+#pragma once
+
+#include "vla_internal.cuh"
+
+namespace vla {
+namespace tc {
+
+constexpr int kD = 64;        // head dimension of this path
+constexpr int kSB = 64;       // tokens per sub-block
+constexpr int kTile = 8192;   // bytes of a 64-row, 64-column bf16 operand tile
+
+// Operand tiles: 64 bf16 (128 bytes) per row, rows 128 bytes apart, in the
+// 128-byte swizzle: the 16-byte chunk j of row r sits at chunk j ^ (r mod 8)
+// (tiles start on 1024-byte boundaries).  Read K-major (row = M/N index,
+// 8-row groups SBO = 1024 bytes apart, a K-step of 16 advances 32 bytes) or
+// MN-major (row = K index, a K-step of 16 advances two row groups, 2048
+// bytes).  The swizzle keeps both the tensor core's reads and the row-wise
+// 16-byte stores here free of bank conflicts.
+__device__ __forceinline__ uint32_t toff(int r, int k) {
+    return (uint32_t)(r * 128 + ((((k >> 3) ^ (r & 7)) << 4) | ((k & 7) * 2)));
+}
+
+// Shared-memory descriptor of a tile in that layout: start address, LBO
+// (the distance between 64-element atoms of an MN-major operand; unused by
+// K-major reads), SBO 1024 bytes, descriptor version of the sm_100 family,
+// 128-byte swizzle.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo = 16) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// phi(x) = ELU(x) + 1 with the fast exponential (bf16 I/O only: its relative
+// error, about 2^-21, is far below the output rounding).
+__device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+
+
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// bf16 pairs (hi, lo) of 8 consecutive fp32 values, in element order.
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(hb);
+        h[e] = bf2_bits(hb);
+        l[e] = bf2_bits(__floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y));
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void unpack8(uint4 w, float *x) {
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(a[e] << 16);
+        x[2 * e + 1] = __uint_as_float(a[e] & 0xffff0000u);
+    }
+}
+
+// 32 consecutive fp32 values as (hi, lo) into row `row`, columns k0 .. k0+31.
+__device__ __forceinline__ void put_row32(unsigned char *hi, unsigned char *lo, int row, int k0, const float *v) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint4 h, l;
+        split8(v + 8 * g, h, l);
+        *reinterpret_cast<uint4 *>(hi + toff(row, k0 + 8 * g)) = h;
+        *reinterpret_cast<uint4 *>(lo + toff(row, k0 + 8 * g)) = l;
+    }
+}
+
+// 32 consecutive TMEM columns of this warp's lane quarter (shape 32x32b).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// D (+)= A B^T over K = 64 (four K-steps of 16).  A (M rows) and B (N
+// rows) are tiles in the layout above, read K-major, or MN-major when A_MN /
+// B_MN (tile rows are then K and each row runs along M / N).  An MN-major
+// operand wider than 64 takes its next 64-wide atom lbo bytes further on.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc, bool acc,
+                                        uint32_t lbo_a = 16, uint32_t lbo_b = 16) {
+    // descriptor address fields count 16-byte units: a K-step adds 32 bytes
+    // (K-major) or 2048 bytes (MN-major) to the start address
+    const uint64_t ad = desc_sw128(a, lbo_a), bd = desc_sw128(b, lbo_b);
+    const uint32_t id = idesc | (A_MN ? (1u << 15) : 0u) | (B_MN ? (1u << 16) : 0u);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(d, ad + (uint64_t)((A_MN ? 128 : 2) * ks), bd + (uint64_t)((B_MN ? 128 : 2) * ks), id,
+                  (acc || ks > 0) ? 1u : 0u);
+}
+
+// Split product D (+)= (Ah + Al)(Bh + Bl)^T without the lo*lo term.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void mma_k64x3(uint32_t d, uint32_t ah, uint32_t al, uint32_t bh, uint32_t bl,
+                                          uint32_t idesc, bool acc, uint32_t lbo_a = 16, uint32_t lbo_b = 16) {
+    mma_k64<A_MN, B_MN>(d, ah, bh, idesc, acc, lbo_a, lbo_b);
+    mma_k64<A_MN, B_MN>(d, ah, bl, idesc, true, lbo_a, lbo_b);
+    mma_k64<A_MN, B_MN>(d, al, bh, idesc, true, lbo_a, lbo_b);
+}
+
+}  // namespace tc
+}  // namespace vla

@@ -63,6 +63,18 @@ def test_chunk_lengths(chunk):
     compare(run_gpu(x, vla.VLA_KERNEL_CHUNK, chunk=chunk), oracle_ref(x), "bf16")
 
 
+@pytest.mark.parametrize("chunk", [0, 128])
+def test_tensor_core_path_given_initial_state(chunk):
+    """bf16 streaming continuation on the tensor-core path: the first A-chunk
+    starts from the given A0, later ones from the inverse of the prefix."""
+    pre = make_inputs(1, 3, 150, 64, "bf16", seed=51, lambda0=0.9, u_scale=0.5)
+    st = oracle_ref(pre)
+    x = make_inputs(1, 3, 1000, 64, "bf16", seed=52, lambda0=0.9, u_scale=0.5)
+    ref = oracle_ref(x, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"])
+    got = run_gpu(x, vla.VLA_KERNEL_CHUNK_TC, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"], chunk=chunk)
+    compare(got, ref, "bf16")
+
+
 @pytest.mark.parametrize("chunk", [64, 192, 512])
 @pytest.mark.parametrize("T", [64, 1000, 1536])
 def test_tensor_core_state_passes(chunk, T):
