@@ -64,27 +64,32 @@ def kernel_src_hash(kernel_name: str) -> str:
     return h.hexdigest()[:16]
 
 
-# Kernels of one step, in launch order, and the share of the algorithmic
-# flops per token-head each one performs (each step of the recurrence is
-# assigned to exactly one kernel; the chunked form's extra work - Grams,
-# prefix sums, chunk transitions, the chain - counts zero).
+# Kernels of one step, in launch order, with the share of the algorithmic
+# work each one performs: every step of the recurrence is assigned to exactly
+# one kernel (the chunked form's extra work - Grams, prefix sums, chunk
+# transitions, the chain - counts zero), and so is every input and output
+# byte.  engine is the pipe the kernel's arithmetic runs on: "alu" (FP32 CUDA
+# cores) or "tensor" (bf16 tcgen05; its roofline takes the bf16 tensor peak).
 def kernel_plan(kname, d, io_dtype="bf16"):
-    """[(kernel, algorithmic flops per token-head, bound)] in launch order."""
+    """[(kernel, algorithmic flops, algorithmic bytes per token-head, engine)] in launch order."""
+    io = 2 if io_dtype == "bf16" else 4
+    full = 12 * d * d + 16 * d
     if kname == "seq":
-        return [("seq_kernel", 12 * d * d + 16 * d, "alu")]
+        return [("seq_kernel", full, 5 * d * io, "alu")]
     if kname == "decode":
-        # one token per call: the state read and written back dominates
-        return [("decode_kernel", 12 * d * d + 16 * d, "hbm")]
-    # gates: key norm, z = A u, rank-1 update, A k_hat, gate norm (a0-a2);
-    # output: S k_hat, state write, S phi(q), readout (a3-a4)
+        # one token per call: the state read and written back dominates (added by the caller)
+        return [("decode_kernel", full, 5 * d * io, "alu")]
+    # gates: key norm, z = A u, rank-1 update, A k_hat, gate norm (a0-a2), reading u and k;
+    # output: S k_hat, state write, S phi(q), readout (a3-a4), reading q and v, writing o
+    half = 6 * d * d + 8 * d
     gram = "gram_tc_kernel" if (io_dtype == "bf16" and d >= 64) else "gram_kernel"
-    # chunk_tc at d = 64 with bf16 I/O: the state passes run on the tensor cores
+    gram_e = "tensor" if gram == "gram_tc_kernel" else "alu"
+    # chunk_tc at d = 64 with bf16 I/O: gates and state passes run on the tensor cores
     tc = kname == "chunk_tc" and io_dtype == "bf16" and d == 64
-    rows = "rows_tc_kernel" if tc else "rows_kernel"
-    gates = "gates_tc_kernel" if tc else "gates_kernel"
-    return [(gram, 0, "alu"), ("prefix_kernel", 0, "alu"), (gates, 6 * d * d + 8 * d, "alu"),
-            (rows + "<summary>", 0, "alu"), ("chain_kernel", 0, "alu"),
-            (rows + "<output>", 6 * d * d + 8 * d, "alu")]
+    rows, gates, eng = ("rows_tc_kernel", "gates_tc_kernel", "tensor") if tc else ("rows_kernel", "gates_kernel", "alu")
+    return [(gram, 0, 0, gram_e), ("prefix_kernel", 0, 0, "alu"), (gates, half, 2 * d * io, eng),
+            (rows + "<summary>", 0, 0, eng), ("chain_kernel", 0, 0, "alu"),
+            (rows + "<output>", half, 3 * d * io, eng)]
 
 
 def state_bytes(B, H, d):
@@ -482,26 +487,34 @@ def main():
         byts += state_bytes(B, H, d) - B * H * 8 * d * d  # the state is read and written each call
     dom = int(np.argmax(per_kernel_ms))
     kernel_ms = per_kernel_ms[dom]
-    k_name, k_fpt, k_bound = plan[dom]
+    k_name, k_fpt, k_bpt, k_eng = plan[dom]
     tr = TRAFFIC.get((kname, args.config, k_name))
     traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash(kname) else None
-    if k_bound == "hbm":
-        achieved = byts / (kernel_ms / 1e3) / 1e9
-        peak, unit = measured_hbm_gbs(), "GB/s"
-        peak_src = "MEASURED_PEAKS.json hbm_gbs (of measured)"
+    k_flops = units * k_fpt
+    k_bytes = byts if len(plan) == 1 else units * k_bpt  # a one-kernel path owns all bytes (state included)
+    hbm = measured_hbm_gbs()
+    fpeak, fsrc = flop_peak(k_eng)
+    t_f, t_q = k_flops / (fpeak * 1e12), k_bytes / (hbm * 1e9)
+    if t_f >= t_q:
+        bound, achieved, peak, unit, alg, peak_src = ("alu" if k_eng == "alu" else "tensor"), \
+            k_flops / (kernel_ms / 1e3) / 1e12, fpeak, "TFLOP/s", k_flops, fsrc
     else:
-        achieved = units * k_fpt / (kernel_ms / 1e3) / 1e12
-        peak, unit = FP32_PEAK_TFLOPS, "TFLOP/s"
-        peak_src = "derived: 152 SMs x 128 FP32 lanes x 2 flop/FMA x 2.070 GHz (of derived)"
-    roofline = {"bound": k_bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+        bound, achieved, peak, unit, alg, peak_src = "hbm", k_bytes / (kernel_ms / 1e3) / 1e9, hbm, "GB/s", \
+            k_bytes, "MEASURED_PEAKS.json hbm_gbs (of measured)"
+    # whole step: the slower of its algorithmic flops at the peak of the pipe they run on and its
+    # algorithmic bytes at the measured HBM bandwidth
+    s_peak, s_src = flop_peak("tensor" if any(e == "tensor" for _, f, _, e in plan if f > 0) else "alu")
+    t_roof = max(flops / (s_peak * 1e12), byts / (hbm * 1e9))
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                 "traffic": traffic, "kernel": "%s<%d,%s>" % (k_name, d, x.dtype), "kernel_ms": kernel_ms,
-                "algorithmic_per_launch": byts if k_bound == "hbm" else units * k_fpt,
-                "peak_source": peak_src,
+                "algorithmic_per_launch": alg, "peak_source": peak_src,
                 "step": {"algorithmic_flops": flops, "algorithmic_bytes": byts,
+                         "roofline_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3),
+                         "flop_peak_source": s_src,
                          "alu_frac": flops / (ms / 1e3) / 1e12 / FP32_PEAK_TFLOPS,
-                         "hbm_frac_of_measured": (byts / (ms / 1e3) / 1e9) / measured_hbm_gbs()},
+                         "hbm_frac_of_measured": (byts / (ms / 1e3) / 1e9) / hbm},
                 "kernels": [{"name": nm, "ms": t, "share": t / sum(per_kernel_ms)}
-                            for (nm, _, _), t in zip(plan, per_kernel_ms)]}
+                            for (nm, _, _, _), t in zip(plan, per_kernel_ms)]}
 
     cpu = None
     parity = None
@@ -533,6 +546,17 @@ def main():
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def flop_peak(engine):
+    """(TFLOP/s, source) for the pipe a kernel's arithmetic runs on."""
+    if engine == "tensor":
+        try:
+            return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"]), \
+                "MEASURED_PEAKS.json bf16_tflops, burst (of measured)"
+        except Exception:
+            return 1900.0, "fallback bf16 1.9 PFLOP/s (of fallback)"
+    return FP32_PEAK_TFLOPS, "derived: 152 SMs x 128 FP32 lanes x 2 flop/FMA x 2.070 GHz (of derived)"
 
 
 def measured_hbm_gbs():

@@ -35,7 +35,6 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 256;
-constexpr int kGS = 68;  // row stride (floats) of fp32 staging matrices: conflict-free rows
 
 struct GtLayout {
     static constexpr size_t ctrl = 0;                       // mbarrier, TMEM slot, abort flag
@@ -44,15 +43,14 @@ struct GtLayout {
     static constexpr size_t slots = ah + 2 * kTile;         // six 8 KB slots:
     // R1-R3: AK^T hi, W^T hi, Y_hat hi, AK^T lo, W^T lo, Y_hat lo
     // R4:    (beta Z)^T hi, E' hi, Z^T hi, (beta Z)^T lo, E' lo, Z^T lo
-    // chunk start: fp32 staging of A (64 x kGS)
+    // elimination: published pivot rows in slot 0 (sub-blocks) or slot 4
+    // chunk start: M^(c) (fp32, 64 x kGS) in slots 0-2, then (1/D) L^{-1} hi, lo in slots 0, 1
     static constexpr size_t xt = slots + 6 * kTile;         // I + G (fp32, 64 x kGS), then X^T hi, lo
-    static constexpr size_t piv = xt + (size_t)64 * kGS * 4;  // [2][128] pivot rows (M part, L^{-1} part)
-    static constexpr size_t ksc = piv + 2 * 128 * 4;        // [64] 1 / max(|k|, eps)
+    static constexpr size_t ksc = xt + (size_t)64 * kGS * 4;  // [64] 1 / max(|k|, eps)
     static constexpr size_t kn = ksc + 256;                 // [64] max(|k|, eps)
     static constexpr size_t beta = kn + 256;                // [64]
     static constexpr size_t nrm = beta + 256;               // [2][64] halves of |row|^2
-    static constexpr size_t gjp = nrm + 512;                // Gauss-Jordan pivot rows (2 x 72 floats)
-    static constexpr size_t total = gjp + 2 * 72 * 4;
+    static constexpr size_t total = nrm + 512;
 };
 
 __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
@@ -68,12 +66,10 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     unsigned char *xt_hi = smem + L::xt, *xt_lo = smem + L::xt + kTile;
     float *gs = reinterpret_cast<float *>(smem + L::xt);
     float *stage = reinterpret_cast<float *>(slot);
-    float *piv = reinterpret_cast<float *>(smem + L::piv);
     float *s_ks = reinterpret_cast<float *>(smem + L::ksc);
     float *s_kn = reinterpret_cast<float *>(smem + L::kn);
     float *s_beta = reinterpret_cast<float *>(smem + L::beta);
     float *s_nrm = reinterpret_cast<float *>(smem + L::nrm);
-    float *s_gjp = reinterpret_cast<float *>(smem + L::gjp);
     // R1-R3 operands and R4 operands in the six slots
     unsigned char *akt_hi = slot, *wt_hi = slot + kTile, *yh_hi = slot + 2 * kTile;
     unsigned char *akt_lo = slot + 3 * kTile, *wt_lo = slot + 4 * kTile, *yh_lo = slot + 5 * kTile;
@@ -107,38 +103,54 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     const uint32_t tq = tbase + ((uint32_t)(32 * qw) << 16);  // this warp's lane quarter
     constexpr uint32_t col_d1 = 0, col_d5 = 64, col_d2 = 128;  // D2, then D3
 
-    // ---- A at the chunk start: Gauss-Jordan rows (4 threads a row, 16
-    // columns each), restaged to the M = 64 accumulator layout ----
+    // ---- A at the chunk start ----
+    // c > 0: A = (M^(c))^{-1} = L^{-T} D^{-1} L^{-1}: elimination of M^(c),
+    // then one product E^T (diag(1/D) E) on the tensor cores.  c = 0: A0 or
+    // I / lambda0 as given.
     float am[32];  // A[r64][32 hw .. 32 hw + 31]
     {
         const int gr = tid >> 2, gp = tid & 3;
-        float x[16];
         const float *src = nullptr;
-        if (c > 0) src = ws_f(a, a.L.off_M) + ((size_t)bh * NCA + c) * kD * kD + gr * kD + 16 * gp;
-        else if (a.p.A0) src = a.p.A0 + (size_t)bh * kD * kD + gr * kD + 16 * gp;
-        if (src) {
+        if (c > 0) src = ws_f(a, a.L.off_M) + ((size_t)bh * NCA + c) * kD * kD;
+        else if (a.p.A0) src = a.p.A0 + (size_t)bh * kD * kD;
+        if (c > 0) {
+            const float4 *g4 = reinterpret_cast<const float4 *>(src + gr * kD + 16 * gp);
+            float4 *st = reinterpret_cast<float4 *>(stage + gr * kGS + 16 * gp);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = reinterpret_cast<const float4 *>(src)[q];
-                x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+            for (int q = 0; q < 4; ++q) st[q] = g4[q];
+            __syncthreads();
+            eliminate64(stage, reinterpret_cast<float *>(slot + 4 * kTile), s_beta, xt_hi, xt_lo, slot, slot + kTile);
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                mma_k64x3<true, true>(tbase + col_d5, smem_u32(slot), smem_u32(slot + kTile), smem_u32(xt_hi),
+                                      smem_u32(xt_lo), idesc_bf16_f32(64, 64), false);
+                umma_commit(bar);
             }
+            const bool w = mbar_wait_bounded(bar, 0, a.p.wait_limit_ns, a.p.err);
+            if (!w) *abort_flag = 1;
+            __syncthreads();
+            tc_fence_after();
+            float v[32];
+            tmem_ld32(tq + col_d5 + 32 * hw, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) am[j] = act64 ? v[j] : 0.f;
+            tc_fence_before();
         } else {
             const float il = 1.f / a.p.lambda0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) x[j] = (16 * gp + j == gr) ? il : 0.f;
-        }
-        if (c > 0) gj_inverse<kD, 16>(x, s_gjp, gr, gp);
-        float4 *st = reinterpret_cast<float4 *>(stage + gr * kGS + 16 * gp);
+            for (int q = 0; q < 8; ++q) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (act64 && src) v = reinterpret_cast<const float4 *>(src + (size_t)r64 * kD + 32 * hw)[q];
+                am[4 * q] = v.x; am[4 * q + 1] = v.y; am[4 * q + 2] = v.z; am[4 * q + 3] = v.w;
+            }
+            if (!src && act64) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) st[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                for (int j = 0; j < 32; ++j) am[j] = (32 * hw + j == r64) ? il : 0.f;
+            }
+        }
         __syncthreads();
-        const float4 *ld = reinterpret_cast<const float4 *>(stage + (r64 & 63) * kGS + 32 * hw);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 v = act64 ? ld[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-            am[4 * q] = v.x; am[4 * q + 1] = v.y; am[4 * q + 2] = v.z; am[4 * q + 3] = v.w;
-        }
-        __syncthreads();  // the staging slots are reused below
         if (act64) put_row32(a_hi, a_lo, r64, 32 * hw, am);
     }
 
@@ -154,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             rk[h] = in ? reinterpret_cast<const uint4 *>(gk + off)[h] : z4;
         }
     };
-    uint32_t phase = 0;
+    uint32_t phase = (c > 0) ? 1u : 0u;  // the chunk-start product used phase 0
     auto round_wait = [&]() -> bool {
         const bool w = mbar_wait_bounded(bar, phase, a.p.wait_limit_ns, a.p.err);
         phase ^= 1u;
@@ -248,78 +260,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         }
         tc_fence_before();
         __syncthreads();
-        // ---- elimination of [I + G | I] ----
-        // Thread tile: rows 4 rb .. 4 rb + 3, columns 4 cb .. 4 cb + 3 of the
-        // working matrix M and of E (which becomes L^{-1}); lane = 16 h + rb,
-        // cb = 2 warp + h.  Step s: pivot p = M[s][s], beta_s = 1 / p; every
-        // row t > s takes row_t -= (M[s][t] / p) row_s (the trailing block
-        // stays symmetric, so M[t][s] = M[s][t]: the multipliers come from
-        // the pivot row, which its owners publish in a double buffer).  Only
-        // columns > s of M and columns <= s of E still change, so a warp
-        // (columns 8 warp .. 8 warp + 7) skips the half that cannot.
-        {
-            const int rb = lane & 15, cb = 2 * warp + (lane >> 4);
-            float m[4][4], e[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 g4 = *reinterpret_cast<const float4 *>(gs + (4 * rb + i) * kGS + 4 * cb);
-                m[i][0] = g4.x; m[i][1] = g4.y; m[i][2] = g4.z; m[i][3] = g4.w;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) e[i][j] = (4 * rb + i == 4 * cb + j) ? 1.f : 0.f;
-            }
-            if (rb == 0) {
-                *reinterpret_cast<float4 *>(piv + 4 * cb) = make_float4(m[0][0], m[0][1], m[0][2], m[0][3]);
-                *reinterpret_cast<float4 *>(piv + 64 + 4 * cb) = make_float4(e[0][0], e[0][1], e[0][2], e[0][3]);
-            }
-            __syncthreads();
-#pragma unroll
-            for (int s = 0; s < kSB; ++s) {
-                const float *pm = piv + (s & 1) * 128;
-                const float rp = 1.f / pm[s];
-                if (tid == 0) s_beta[s] = rp;
-                const float4 fr = *reinterpret_cast<const float4 *>(pm + 4 * rb);
-                const float f[4] = {fr.x * rp, fr.y * rp, fr.z * rp, fr.w * rp};
-                if (8 * warp + 7 > s) {  // columns > s of M
-                    const float4 pc = *reinterpret_cast<const float4 *>(pm + 4 * cb);
-                    const float p4[4] = {pc.x, pc.y, pc.z, pc.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (4 * rb + i > s) {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) m[i][j] = fmaf(-f[i], p4[j], m[i][j]);
-                        }
-                }
-                if (8 * warp <= s) {  // columns <= s of E
-                    const float4 qe = *reinterpret_cast<const float4 *>(pm + 64 + 4 * cb);
-                    const float q4[4] = {qe.x, qe.y, qe.z, qe.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (4 * rb + i > s) {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) e[i][j] = fmaf(-f[i], q4[j], e[i][j]);
-                        }
-                }
-                if (s + 1 < kSB && rb == ((s + 1) >> 2)) {
-                    float *nx = piv + ((s + 1) & 1) * 128;
-                    *reinterpret_cast<float4 *>(nx + 4 * cb) =
-                        make_float4(m[(s + 1) & 3][0], m[(s + 1) & 3][1], m[(s + 1) & 3][2], m[(s + 1) & 3][3]);
-                    *reinterpret_cast<float4 *>(nx + 64 + 4 * cb) =
-                        make_float4(e[(s + 1) & 3][0], e[(s + 1) & 3][1], e[(s + 1) & 3][2], e[(s + 1) & 3][3]);
-                }
-                __syncthreads();
-            }
-            // X^T = L^{-1}: rows s = 4 rb + i, K = r = 4 cb .. 4 cb + 3 (8 bytes each of hi, lo)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 h0 = __floats2bfloat162_rn(e[i][0], e[i][1]);
-                const __nv_bfloat162 h1 = __floats2bfloat162_rn(e[i][2], e[i][3]);
-                const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-                const __nv_bfloat162 l0 = __floats2bfloat162_rn(e[i][0] - f0.x, e[i][1] - f0.y);
-                const __nv_bfloat162 l1 = __floats2bfloat162_rn(e[i][2] - f1.x, e[i][3] - f1.y);
-                *reinterpret_cast<uint2 *>(xt_hi + toff(4 * rb + i, 4 * cb)) = make_uint2(bf2_bits(h0), bf2_bits(h1));
-                *reinterpret_cast<uint2 *>(xt_lo + toff(4 * rb + i, 4 * cb)) = make_uint2(bf2_bits(l0), bf2_bits(l1));
-            }
-        }
+        // ---- elimination of I + G: X^T = L^{-1} and beta_s = 1 / D_s ----
+        eliminate64(gs, reinterpret_cast<float *>(akt_hi), s_beta, xt_hi, xt_lo, nullptr, nullptr);
         fence_proxy_async_smem();
         __syncthreads();
         // ---- R3: D3 = X^T [W | Y_hat] (B MN-major, two atoms 8 KB apart): Z^T | P ----

@@ -114,5 +114,101 @@ __device__ __forceinline__ void mma_k64x3(uint32_t d, uint32_t ah, uint32_t al, 
     mma_k64<A_MN, B_MN>(d, al, bh, idesc, true, lbo_a, lbo_b);
 }
 
+constexpr int kGS = 68;  // row stride (floats) of fp32 staging matrices: conflict-free rows
+
+// Gaussian elimination of a 64 x 64 SPD matrix M against the identity,
+// without pivoting (the pivots of an SPD matrix are positive): with
+// M = L D L^T (unit lower L), it yields E = L^{-1} and the reciprocal pivots
+// 1 / D_s.  M is symmetric and stays so in the trailing block, so the
+// multiplier of row t for pivot s, M[t][s] / D_s, is the pivot row's entry
+// M[s][t] / D_s.  Blocked by 8 pivots: warp w owns rows 8 w .. 8 w + 7 (lane l
+// columns 2 l, 2 l + 1); the owner of a block eliminates it with shuffles,
+// publishes its 8 pivot rows (double-buffered), and after one barrier every
+// later warp applies all 8.  256 threads; all must call.
+//   ms:   M (fp32, row stride kGS), read once at the start
+//   prow: scratch, 2 x 8 x 128 floats
+//   rpiv: out, 1 / D_s
+//   e_hi, e_lo: out, E as bf16 hi/lo tile pairs (row s, column r)
+//   be_hi, be_lo: optional out, diag(1 / D) E likewise (rows scaled)
+__device__ __forceinline__ void eliminate64(const float *ms, float *prow, float *rpiv, unsigned char *e_hi,
+                                            unsigned char *e_lo, unsigned char *be_hi, unsigned char *be_lo) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float2 m[8], e[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * warp + i;
+        m[i] = *reinterpret_cast<const float2 *>(ms + r * kGS + 2 * lane);
+        e[i] = make_float2(r == 2 * lane ? 1.f : 0.f, r == 2 * lane + 1 ? 1.f : 0.f);
+    }
+    __syncthreads();  // ms may be overwritten once everyone has its rows
+#pragma unroll 1
+    for (int b = 0; b < 8; ++b) {
+        float *pb = prow + (b & 1) * 8 * 128;
+        if (warp == b) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                // pivot M[s][s], s = 8 b + p: lane s / 2, component p mod 2
+                const float pv = __shfl_sync(0xffffffffu, (p & 1) ? m[p].y : m[p].x, 4 * b + (p >> 1));
+                // fast reciprocal: the pivots are >= the smallest eigenvalue (>= 1
+                // for I + G) and its relative error (about 2^-22) is far below
+                // the bf16 operand splits downstream
+                const float rp = __fdividef(1.f, pv);
+                if (lane == 0) rpiv[8 * b + p] = rp;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (i <= p) continue;  // (constant trip count: m, e stay in registers)
+                    // multiplier of row 8 b + i: pivot row at column 8 b + i
+                    const float mv = __shfl_sync(0xffffffffu, (i & 1) ? m[p].y : m[p].x, 4 * b + (i >> 1));
+                    const float2 f = make_float2(-mv * rp, -mv * rp);
+                    m[i] = __ffma2_rn(f, m[p], m[i]);
+                    e[i] = __ffma2_rn(f, e[p], e[i]);
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                *reinterpret_cast<float2 *>(pb + p * 128 + 2 * lane) = m[p];
+                *reinterpret_cast<float2 *>(pb + p * 128 + 64 + 2 * lane) = e[p];
+            }
+        }
+        __syncthreads();
+        if (warp > b) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const float rp = rpiv[8 * b + p];
+                const float4 fa = *reinterpret_cast<const float4 *>(pb + p * 128 + 8 * warp);
+                const float4 fb = *reinterpret_cast<const float4 *>(pb + p * 128 + 8 * warp + 4);
+                const float2 pm = *reinterpret_cast<const float2 *>(pb + p * 128 + 2 * lane);
+                const float2 pe = *reinterpret_cast<const float2 *>(pb + p * 128 + 64 + 2 * lane);
+                const float fr[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 f = make_float2(-fr[i] * rp, -fr[i] * rp);
+                    m[i] = __ffma2_rn(f, pm, m[i]);
+                    e[i] = __ffma2_rn(f, pe, e[i]);
+                }
+            }
+        }
+    }
+    // E (and diag(1/D) E) rows 8 warp + i, columns 2 lane, 2 lane + 1
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * warp + i;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(e[i].x, e[i].y);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(e[i].x - hf.x, e[i].y - hf.y);
+        *reinterpret_cast<uint32_t *>(e_hi + toff(r, 2 * lane)) = bf2_bits(h);
+        *reinterpret_cast<uint32_t *>(e_lo + toff(r, 2 * lane)) = bf2_bits(l);
+        if (be_hi) {
+            const float rp = rpiv[r];  // written by this warp as owner
+            const float bx = e[i].x * rp, by = e[i].y * rp;
+            const __nv_bfloat162 bh = __floats2bfloat162_rn(bx, by);
+            const float2 bhf = __bfloat1622float2(bh);
+            *reinterpret_cast<uint32_t *>(be_hi + toff(r, 2 * lane)) = bf2_bits(bh);
+            *reinterpret_cast<uint32_t *>(be_lo + toff(r, 2 * lane)) =
+                bf2_bits(__floats2bfloat162_rn(bx - bhf.x, by - bhf.y));
+        }
+    }
+}
+
 }  // namespace tc
 }  // namespace vla
