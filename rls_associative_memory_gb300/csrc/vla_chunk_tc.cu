@@ -48,15 +48,18 @@ struct TcLayout {
     static constexpr int XR = MODE == 0 ? 128 : 64;            // state rows
     static constexpr uint32_t ncols = MODE == 0 ? 128 : 256;    // TMEM columns
     static constexpr size_t ctrl = 0;                            // mbarriers (MMA, T_inv load), TMEM slot, abort flag
-    static constexpr size_t xs = 1024;                           // X / E / R tiles: hi, lo
-    static constexpr size_t xs_t = (size_t)XR * 128;
-    static constexpr size_t kb = xs + 2 * xs_t;                  // [K; Phi_hi] (mode 1) or K; then Qm^T hi, lo
+    // X / E / R tiles (hi, lo) and the gate tiles Al (token rows; hi, lo).  In
+    // mode 1 they interleave as [X hi | Al hi | X lo | Al lo], so that [X; Al]
+    // is one 128-row operand (Phi [X; Al]^T in one product).
+    static constexpr size_t xs_hi = 1024;
+    static constexpr size_t xs_lo = MODE == 0 ? xs_hi + 2 * kTile : xs_hi + 2 * kTile;
+    static constexpr size_t al_hi = MODE == 0 ? xs_hi + 4 * kTile : xs_hi + kTile;
+    static constexpr size_t al_lo = MODE == 0 ? al_hi + kTile : xs_hi + 3 * kTile;
+    static constexpr size_t kb = xs_hi + 4 * kTile + (MODE == 0 ? 2 * kTile : 0);  // [K; Phi_hi] (mode 1) or K; then Qm^T hi, lo
     static constexpr size_t kblo = kb + (MODE == 0 ? kTile : 2 * kTile);  // Phi_lo (mode 1)
-    static constexpr size_t al = kblo + (MODE == 0 ? 0 : kTile);          // Al (token rows) hi, lo
-    static constexpr int kNT = 68;                               // row stride (floats) of N^T: conflict-free rows
-    static constexpr size_t ti = al + 2 * kTile;                 // (mode 0) N^T fp32; T_inv^T hi, lo
+    static constexpr size_t ti = kblo + (MODE == 0 ? 0 : kTile); // (mode 0) N fp32 (row stride kGS); T_inv hi, lo
     static constexpr int kVS = 72;                               // row stride (bf16) of the v tile
-    static constexpr size_t vt = ti + (MODE == 0 ? (size_t)64 * kNT * 4 : 2 * (size_t)kTile);  // v [t][i] bf16
+    static constexpr size_t vt = ti + (MODE == 0 ? (size_t)64 * kGS * 4 : 2 * (size_t)kTile);  // v [t][i] bf16
     static constexpr size_t ks = vt + (size_t)64 * kVS * 2;      // [64] 1 / max(|k|, eps)
     static constexpr size_t rden = ks + 256;                     // [64] 1 / (phi(q).n + eps)
     static constexpr size_t tot = rden + 256;                    // [9][64] warp totals of phi(k_hat), then prefixes
@@ -73,12 +76,12 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
-    uint64_t *bar_t = reinterpret_cast<uint64_t *>(smem + L::ctrl + 16);  // T_inv^T load (mode 1)
-    unsigned char *xs_hi = smem + L::xs, *xs_lo = smem + L::xs + L::xs_t;
+    uint64_t *bar_t = reinterpret_cast<uint64_t *>(smem + L::ctrl + 16);  // T_inv load (mode 1)
+    unsigned char *xs_hi = smem + L::xs_hi, *xs_lo = smem + L::xs_lo;
     unsigned char *kb = smem + L::kb, *kblo = smem + L::kblo;
-    unsigned char *al_hi = smem + L::al, *al_lo = smem + L::al + kTile;
-    float *ntb = reinterpret_cast<float *>(smem + L::ti);  // N^T[t][s] = N[s][t], row stride kNT
-    unsigned char *ti_hi = smem + L::ti, *ti_lo = smem + L::ti + kTile;  // T_inv^T
+    unsigned char *al_hi = smem + L::al_hi, *al_lo = smem + L::al_lo;
+    float *ntb = reinterpret_cast<float *>(smem + L::ti);  // N (mode 0), row stride kGS
+    unsigned char *ti_hi = smem + L::ti, *ti_lo = smem + L::ti + kTile;  // T_inv, tile row s = row s
     __nv_bfloat16 *vt = reinterpret_cast<__nv_bfloat16 *>(smem + L::vt);
     float *s_ks = reinterpret_cast<float *>(smem + L::ks);
     float *s_rden = reinterpret_cast<float *>(smem + L::rden);
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.p.o) + tok0;
 
     unsigned char *gtinv = static_cast<unsigned char *>(a.p.ws) + a.L.off_tinv +
-                           (size_t)(bh * NC + c) * (C / kSB) * (2 * kTile);  // this chunk's T_inv^T tiles
+                           (size_t)(bh * NC + c) * (C / kSB) * (2 * kTile);  // this chunk's T_inv tiles
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar_t, 1);
@@ -138,20 +141,19 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     // features 16 pq .. 16 pq + 15).
     uint4 rk[2], rv[2], rq[2];
     float4 ra[4];
+    // (always a valid token row, clamped: no select waits on the loads here;
+    // tokens past the chunk are zeroed where the values are used)
     auto load_in = [&](int sb) {
-        const int t = sb * kSB + pt;
-        const bool in = sb < nsb && t < ntok;
+        const int t = min(sb * kSB + pt, ntok - 1);
         const size_t off = (size_t)t * kD + 16 * pq;
-        const uint4 z4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            rk[h] = in ? reinterpret_cast<const uint4 *>(gk + off)[h] : z4;
-            rv[h] = in ? reinterpret_cast<const uint4 *>(gv + off)[h] : z4;
-            if (MODE == 1) rq[h] = in ? reinterpret_cast<const uint4 *>(gq + off)[h] : z4;
+            rk[h] = reinterpret_cast<const uint4 *>(gk + off)[h];
+            rv[h] = reinterpret_cast<const uint4 *>(gv + off)[h];
+            if (MODE == 1) rq[h] = reinterpret_cast<const uint4 *>(gq + off)[h];
         }
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
-            ra[h] = in ? reinterpret_cast<const float4 *>(gal + off)[h] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int h = 0; h < 4; ++h) ra[h] = reinterpret_cast<const float4 *>(gal + off)[h];
     };
     float nb[16];  // n at the sub-block start, features 16 pq .. (mode 1)
     if (MODE == 1) {
@@ -171,23 +173,28 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     };
     constexpr uint32_t id_x64 = idesc_bf16_f32(XR, 64);                       // X-row products
     constexpr uint32_t id_64 = idesc_bf16_f32(64, 64);
-    constexpr int kNT = L::kNT, kVS = L::kVS;
+    constexpr int kVS = L::kVS;
     constexpr uint32_t col_d2 = MODE == 1 ? 128 : 64;   // D2, then D3 = R
     constexpr uint32_t col_d4 = 0;                      // D1 = X K^T, then D4 = R Al^T
     constexpr uint32_t col_do = 64;                     // (mode 1) readout numerators, token rows
 
     bool ok = true;
-    int tinv_issued = 0, tinv_done = 0;  // T_inv^T loads (mode 1)
+    int tinv_issued = 0, tinv_done = 0;  // T_inv loads (mode 1)
     load_in(0);
     for (int sb = 0; sb < nsb; ++sb) {
         const int nt = min(kSB, ntok - sb * kSB);
         float fq[16], fk[16];
-        if (MODE == 1 && tid == 0) {  // T_inv^T of this sub-block (the slot is free: round 2 is done)
+        if (MODE == 1 && tid == 0) {  // T_inv of this sub-block (the slot is free: round 2 is done)
             mbar_arrive_expect_tx(bar_t, 2 * kTile);
             bulk_g2s(ti_hi, gtinv + (size_t)sb * 2 * kTile, 2 * kTile, bar_t);
         }
         tinv_issued = sb + 1;
         // ---- stage the sub-block's operands ----
+        if (pt >= nt) {  // past the chunk: zero inputs
+            rk[0] = rk[1] = rv[0] = rv[1] = rq[0] = rq[1] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) ra[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         {
             float kf[16];
             unpack8(rk[0], kf);
@@ -253,10 +260,9 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             mma_k64<false, false>(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x64, false);
             mma_k64<false, false>(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x64, true);
             if (MODE == 1) {
-                mma_k64x3<false, false>(tbase + col_d2, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(al_hi), smem_u32(al_lo), id_64,
-                        false);
-                mma_k64x3<false, false>(tbase + col_do, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(xs_hi), smem_u32(xs_lo), id_64,
-                        false);
+                // [DO | D2] = Phi [X; Al]^T: DO at col_do, D2 = Qm^T at col_do + 64 = col_d2
+                mma_k64x3<false, false>(tbase + col_do, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(xs_hi),
+                                        smem_u32(xs_lo), idesc_bf16_f32(64, 128), false);
             } else {
                 mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
                 mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             ok = false;
             break;
         }
-        // ---- N^T (fp32, for the inverse; mode 0), Qm^T tiles (mode 1), E tiles ----
+        // ---- N (fp32, row-major, for the inverse; mode 0), Qm^T tiles (mode 1), E tiles ----
         {
             float v[32];
             tmem_ld32(tq + col_d2 + 32 * hw, v);  // D2 row t = 16 qw + lane (M = 64), columns s = 32 hw ..
@@ -309,13 +315,13 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                     for (int m = 0; m < 32; ++m)
                         if (32 * hw + m > t) v[m] = 0.f;
                     put_row32(kb, kb + kTile, t, 32 * hw, v);
-                } else {
+                } else {  // N[s][t] = alpha_s . k_hat_t (s < t), row-major: lanes t write one row s together
                     const float kt = s_ks[t];
 #pragma unroll
-                    for (int m = 0; m < 32; ++m) v[m] = (32 * hw + m < t) ? v[m] * kt : 0.f;
-                    float4 *dst = reinterpret_cast<float4 *>(ntb + t * kNT + 32 * hw);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    for (int m = 0; m < 32; ++m) {
+                        const int sr = 32 * hw + m;
+                        ntb[sr * kGS + t] = sr < t ? v[m] * kt : 0.f;
+                    }
                 }
             }
             tmem_ld32(tq + col_d4 + 32 * hw, v);  // X K, columns 32 hw ..
@@ -337,57 +343,10 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         }
         tc_fence_before();
         __syncthreads();
-        // ---- T_inv = (I + N)^{-1}, right-looking ----
-        // Accumulator A[s][t] = sum_{r > s} N[s][r] T[r][t] - [s == t], so
-        // that T = -A everywhere (A[s][t] stays 0 for s > t because T[r][t]
-        // = 0 for r > t).  Row r of T is final once the steps r' > r are
-        // done; step r adds N[:, r] T[r, :].  Thread tile: rows 4 rb ..
-        // 4 rb + 3, columns 4 cb .. 4 cb + 3 with lane = 16 h + rb and
-        // cb = 2 warp + h; the owner of row r (row block r / 4 of the same
-        // half-warp) broadcasts it by shuffle.  A warp holds columns 8 warp ..
-        // 8 warp + 7 and skips the steps r > 8 warp + 7 (T[r][t] = 0 there).
+        // ---- T_inv = (I + N)^{-1} (mode 0; blocked back substitution) ----
         if (MODE == 0) {
-            const int rb = lane & 15, cb = 2 * warp + (lane >> 4), src = lane & 16;
-            float2 acc[4][2];  // acc[i][jp] = columns 4 cb + 2 jp, + 1 of row 4 rb + i
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int jp = 0; jp < 2; ++jp)
-                    acc[i][jp] = make_float2(4 * rb + i == 4 * cb + 2 * jp ? -1.f : 0.f,
-                                             4 * rb + i == 4 * cb + 2 * jp + 1 ? -1.f : 0.f);
-#pragma unroll
-            for (int r = kSB - 1; r >= 1; --r) {
-                if (8 * warp + 7 < r) continue;
-                const float4 n4 = *reinterpret_cast<const float4 *>(ntb + r * kNT + 4 * rb);  // N[4 rb + i][r]
-                float2 mt[2];  // -T[r][t] = A[r][t] for this thread's columns
-#pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
-                    mt[jp].x = __shfl_sync(0xffffffffu, acc[r & 3][jp].x, src + (r >> 2));
-                    mt[jp].y = __shfl_sync(0xffffffffu, acc[r & 3][jp].y, src + (r >> 2));
-                }
-                const float nv[4] = {-n4.x, -n4.y, -n4.z, -n4.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int jp = 0; jp < 2; ++jp) acc[i][jp] = fma2(f2(nv[i]), mt[jp], acc[i][jp]);
-            }
-            __syncthreads();  // every read of N^T is done before T_inv^T overwrites it
-            // T_inv^T rows t = 4 cb + j, K = s = 4 rb .. 4 rb + 3 (8 bytes each of hi, lo)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int t = 4 * cb + j;
-                float tv[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) tv[i] = -((j & 1) ? acc[i][j >> 1].y : acc[i][j >> 1].x);
-                const __nv_bfloat162 h0 = __floats2bfloat162_rn(tv[0], tv[1]);
-                const __nv_bfloat162 h1 = __floats2bfloat162_rn(tv[2], tv[3]);
-                const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-                const __nv_bfloat162 l0 = __floats2bfloat162_rn(tv[0] - f0.x, tv[1] - f0.y);
-                const __nv_bfloat162 l1 = __floats2bfloat162_rn(tv[2] - f1.x, tv[3] - f1.y);
-                *reinterpret_cast<uint2 *>(ti_hi + toff(t, 4 * rb)) = make_uint2(bf2_bits(h0), bf2_bits(h1));
-                *reinterpret_cast<uint2 *>(ti_lo + toff(t, 4 * rb)) = make_uint2(bf2_bits(l0), bf2_bits(l1));
-            }
-        } else {  // mode 1: T_inv^T of this sub-block, stored by the transition pass
+            tri_inv64(ntb, reinterpret_cast<float *>(kb), ti_hi, ti_lo);
+        } else {  // mode 1: T_inv of this sub-block, stored by the transition pass
             if (!mbar_wait_bounded(bar_t, (uint32_t)(sb & 1), a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
             tinv_done = sb + 1;
         }
@@ -396,10 +355,11 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         // ---- round 2: R = E T_inv ----
         if (tid == 0) {
             tc_fence_after();
-            mma_k64x3<false, false>(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi), smem_u32(ti_lo), id_x64, false);
+            mma_k64x3<false, true>(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi),
+                                   smem_u32(ti_lo), id_x64, false);
             umma_commit(bar);
         }
-        if (MODE == 0) {  // T_inv^T tiles to the workspace for the readout pass
+        if (MODE == 0) {  // T_inv tiles to the workspace for the readout pass
             const uint4 *src4 = reinterpret_cast<const uint4 *>(ti_hi);
             uint4 *dst4 = reinterpret_cast<uint4 *>(gtinv + (size_t)sb * 2 * kTile);
 #pragma unroll
@@ -462,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     if (!ok) {
         if (tid == 0) {
             (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
-            if (MODE == 1 && tinv_issued > tinv_done)  // a T_inv^T copy may still be landing
+            if (MODE == 1 && tinv_issued > tinv_done)  // a T_inv copy may still be landing
                 (void)mbar_wait_bounded(bar_t, (uint32_t)((tinv_issued - 1) & 1), a.p.wait_limit_ns, a.p.err);
         }
     } else if (MODE == 0) {  // rows 0..63 are H_c, rows 64..127 P_c

@@ -155,15 +155,15 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     }
 
     uint4 ru[2], rk[2];  // inputs of the next sub-block (token pt, features 16 pq ..)
+    // (always a valid token row, clamped: no select waits on the loads here;
+    // tokens past the chunk are zeroed where the values are used)
     auto load_in = [&](int sb) {
-        const int t = sb * kSB + pt;
-        const bool in = sb < nsb && t < ntok;
+        const int t = min(sb * kSB + pt, ntok - 1);
         const size_t off = (size_t)t * kD + 16 * pq;
-        const uint4 z4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            ru[h] = in ? reinterpret_cast<const uint4 *>(gu + off)[h] : z4;
-            rk[h] = in ? reinterpret_cast<const uint4 *>(gk + off)[h] : z4;
+            ru[h] = reinterpret_cast<const uint4 *>(gu + off)[h];
+            rk[h] = reinterpret_cast<const uint4 *>(gk + off)[h];
         }
     };
     uint32_t phase = (c > 0) ? 1u : 0u;  // the chunk-start product used phase 0
@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     for (int sb = 0; sb < nsb; ++sb) {
         const int nt = min(kSB, ntok - sb * kSB);
         // ---- stage [U; K] and the key norms ----
+        if (pt >= nt) ru[0] = ru[1] = rk[0] = rk[1] = make_uint4(0, 0, 0, 0);  // past the chunk
         {
             float kf[16];
             unpack8(rk[0], kf);

@@ -210,5 +210,71 @@ __device__ __forceinline__ void eliminate64(const float *ms, float *prow, float 
     }
 }
 
+// T = (I + N)^{-1} for a strictly upper triangular 64 x 64 N, by blocked back
+// substitution: row s of T = e_s - sum_{r > s} N[s][r] T[r].  N is known up
+// front, so no multiplier depends on the result and no step needs a
+// shuffle.  Warp w owns rows 8 w .. 8 w + 7 (lane l columns 2 l, 2 l + 1);
+// blocks run from the last: the owner solves its 8 rows in registers,
+// publishes them (double-buffered), and after one barrier every earlier warp
+// subtracts their contributions.  256 threads; all must call.
+//   ns:   N (fp32, row s, stride kGS)
+//   prow: scratch, 2 x 8 x 64 floats
+//   t_hi, t_lo: out, T as bf16 hi/lo tile pairs, tile row s = row s of T
+//               (an MN-major operand for products with T on the right)
+__device__ __forceinline__ void tri_inv64(const float *ns, float *prow, unsigned char *t_hi, unsigned char *t_lo) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float2 tr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * warp + i;
+        tr[i] = make_float2(r == 2 * lane ? 1.f : 0.f, r == 2 * lane + 1 ? 1.f : 0.f);
+    }
+#pragma unroll 1
+    for (int b = 7; b >= 0; --b) {
+        float *pb = prow + (b & 1) * 8 * 64;
+        if (warp == b) {
+#pragma unroll
+            for (int p = 7; p >= 0; --p) {
+                const float *nr = ns + (8 * b + p) * kGS + 8 * b;  // N[8 b + p][8 b .. 8 b + 7]
+                const float4 n0 = *reinterpret_cast<const float4 *>(nr);
+                const float4 n1 = *reinterpret_cast<const float4 *>(nr + 4);
+                const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (i <= p) continue;
+                    tr[p] = __ffma2_rn(make_float2(-nv[i], -nv[i]), tr[i], tr[p]);
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < 8; ++p) *reinterpret_cast<float2 *>(pb + p * 64 + 2 * lane) = tr[p];
+        }
+        __syncthreads();
+        if (warp < b) {
+            float2 pr[8];
+#pragma unroll
+            for (int p = 0; p < 8; ++p) pr[p] = *reinterpret_cast<const float2 *>(pb + p * 64 + 2 * lane);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float *nr = ns + (8 * warp + i) * kGS + 8 * b;  // N[8 warp + i][8 b .. 8 b + 7]
+                const float4 n0 = *reinterpret_cast<const float4 *>(nr);
+                const float4 n1 = *reinterpret_cast<const float4 *>(nr + 4);
+                const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+#pragma unroll
+                for (int p = 0; p < 8; ++p) tr[i] = __ffma2_rn(make_float2(-nv[p], -nv[p]), pr[p], tr[i]);
+            }
+        }
+    }
+    __syncthreads();  // every read of ns is done (the output may alias it)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * warp + i;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(tr[i].x, tr[i].y);
+        const float2 hf = __bfloat1622float2(h);
+        *reinterpret_cast<uint32_t *>(t_hi + toff(r, 2 * lane)) = bf2_bits(h);
+        *reinterpret_cast<uint32_t *>(t_lo + toff(r, 2 * lane)) =
+            bf2_bits(__floats2bfloat162_rn(tr[i].x - hf.x, tr[i].y - hf.y));
+    }
+}
+
 }  // namespace tc
 }  // namespace vla
