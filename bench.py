@@ -55,7 +55,7 @@ TRAFFIC = {
 
 def kernel_src_hash(kernel_name: str) -> str:
     fns = {"seq": ["vla_seq.cu"], "chunk": ["vla_chunk.cu"],
-           "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu", "vla_gates_tc.cu", "vla_tc_common.cuh"],
+           "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu", "vla_gates_tc.cu", "vla_gram_tc.cu", "vla_tc_common.cuh"],
            "decode": ["vla_decode.cu"]}[kernel_name]
     h = hashlib.sha256()
     for fn in fns:
@@ -89,6 +89,8 @@ def kernel_plan(kname, d, io_dtype="bf16"):
     # chunk_tc at d = 64 with bf16 I/O: gates and state passes run on the tensor cores
     tc = kname == "chunk_tc" and io_dtype == "bf16" and d == 64
     rows, gates, eng = ("rows_tc_kernel", "gates_tc_kernel", "tensor") if tc else ("rows_kernel", "gates_kernel", "alu")
+    if tc:
+        gram, gram_e = "gram_tma_kernel", "tensor"
     return [(gram, 0, 0, gram_e), ("prefix_kernel", 0, 0, "alu"), (gates, half, 2 * d * io, eng),
             (rows + "<summary>", 0, 0, eng), ("chain_kernel", 0, 0, "alu"),
             (rows + "<output>", half, 3 * d * io, eng)]

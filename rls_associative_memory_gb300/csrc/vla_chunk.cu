@@ -1123,7 +1123,9 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         mark_launch(a.p, ++n, st);
     }
-    if constexpr (sizeof(IO) == 2 && D >= 64) {
+    if (a.p.rows_tc && gram_tma_supported(a.p, a.L)) {
+        if ((e = launch_gram_tma(a, st)) != cudaSuccess) return e;
+    } else if constexpr (sizeof(IO) == 2 && D >= 64) {
         gram_tc_kernel<D><<<(unsigned)(NCA * BH), GramTc<D>::NT, GramTc<D>::total, st>>>(a);
     } else {
         gram_kernel<D, IO><<<(unsigned)(NCA * BH), 256, 0, st>>>(a);

@@ -119,6 +119,9 @@ cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream);
 // A-chunks a multiple of 64 tokens.  Defined in vla_gates_tc.cu.
 bool gates_tc_supported(const FwdParams &p, const ChunkLayout &L);
 cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream);
+// Chunk Grams with TMA tensor loads (vla_gram_tc.cu), same shapes.
+bool gram_tma_supported(const FwdParams &p, const ChunkLayout &L);
+cudaError_t launch_gram_tma(const ChunkArgs &a, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // PTX helpers
