@@ -43,7 +43,8 @@ struct GtLayout {
     static constexpr size_t slots = ah + 2 * kTile;         // six 8 KB slots:
     // R1-R3: AK^T hi, W^T hi, Y_hat hi, AK^T lo, W^T lo, Y_hat lo
     // R4:    (beta Z)^T hi, E' hi, Z^T hi, (beta Z)^T lo, E' lo, Z^T lo
-    // elimination: published pivot rows in slot 0 (sub-blocks) or slot 4
+    // elimination: published pivot rows in slot 0 (sub-blocks) or slot 4, scaled
+    // pivot rows in slot 3 (sub-blocks) or slot 5
     // chunk start: M^(c) (fp32, 64 x kGS) in slots 0-2, then (1/D) L^{-1} hi, lo in slots 0, 1
     static constexpr size_t xt = slots + 6 * kTile;         // I + G (fp32, 64 x kGS), then X^T hi, lo
     static constexpr size_t ksc = xt + (size_t)64 * kGS * 4;  // [64] 1 / max(|k|, eps)
@@ -119,7 +120,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) st[q] = g4[q];
             __syncthreads();
-            eliminate64(stage, reinterpret_cast<float *>(slot + 4 * kTile), s_beta, xt_hi, xt_lo, slot, slot + kTile);
+            eliminate64(stage, reinterpret_cast<float *>(slot + 4 * kTile), reinterpret_cast<float *>(slot + 5 * kTile),
+                        s_beta, xt_hi, xt_lo, slot, slot + kTile);
             fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0) {
@@ -262,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         tc_fence_before();
         __syncthreads();
         // ---- elimination of I + G: X^T = L^{-1} and beta_s = 1 / D_s ----
-        eliminate64(gs, reinterpret_cast<float *>(akt_hi), s_beta, xt_hi, xt_lo, nullptr, nullptr);
+        eliminate64(gs, reinterpret_cast<float *>(akt_hi), reinterpret_cast<float *>(akt_lo), s_beta, xt_hi, xt_lo,
+                    nullptr, nullptr);
         fence_proxy_async_smem();
         __syncthreads();
         // ---- R3: D3 = X^T [W | Y_hat] (B MN-major, two atoms 8 KB apart): Z^T | P ----

@@ -122,16 +122,22 @@ constexpr int kGS = 68;  // row stride (floats) of fp32 staging matrices: confli
 // 1 / D_s.  M is symmetric and stays so in the trailing block, so the
 // multiplier of row t for pivot s, M[t][s] / D_s, is the pivot row's entry
 // M[s][t] / D_s.  Blocked by 8 pivots: warp w owns rows 8 w .. 8 w + 7 (lane l
-// columns 2 l, 2 l + 1); the owner of a block eliminates it with shuffles,
-// publishes its 8 pivot rows (double-buffered), and after one barrier every
-// later warp applies all 8.  256 threads; all must call.
+// columns 2 l, 2 l + 1).  The owner of a block eliminates it with shuffles and
+// publishes its 8 pivot rows of M and E, and the rows of M scaled by -1 / D_s
+// that carry the later rows' multipliers (double-buffered); after one barrier
+// every later warp applies all 8.  The next owner applies first: the other
+// warps wait for it on a named barrier, then apply while it runs its own
+// pivot chain, which leaves most issue slots free.  256 threads; all must
+// call.
 //   ms:   M (fp32, row stride kGS), read once at the start
-//   prow: scratch, 2 x 8 x 128 floats
+//   prow: scratch, 2 x 8 x 128 floats (pivot rows of M and E)
+//   srow: scratch, 2 x 8 x 64 floats (pivot rows of M scaled by -1 / D_s)
 //   rpiv: out, 1 / D_s
 //   e_hi, e_lo: out, E as bf16 hi/lo tile pairs (row s, column r)
 //   be_hi, be_lo: optional out, diag(1 / D) E likewise (rows scaled)
-__device__ __forceinline__ void eliminate64(const float *ms, float *prow, float *rpiv, unsigned char *e_hi,
-                                            unsigned char *e_lo, unsigned char *be_hi, unsigned char *be_lo) {
+__device__ __forceinline__ void eliminate64(const float *ms, float *prow, float *srow, float *rpiv,
+                                            unsigned char *e_hi, unsigned char *e_lo, unsigned char *be_hi,
+                                            unsigned char *be_lo) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float2 m[8], e[8];
 #pragma unroll
@@ -144,6 +150,7 @@ __device__ __forceinline__ void eliminate64(const float *ms, float *prow, float 
 #pragma unroll 1
     for (int b = 0; b < 8; ++b) {
         float *pb = prow + (b & 1) * 8 * 128;
+        float *sb = srow + (b & 1) * 8 * 64;
         if (warp == b) {
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
@@ -163,30 +170,33 @@ __device__ __forceinline__ void eliminate64(const float *ms, float *prow, float 
                     m[i] = __ffma2_rn(f, m[p], m[i]);
                     e[i] = __ffma2_rn(f, e[p], e[i]);
                 }
-            }
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
                 *reinterpret_cast<float2 *>(pb + p * 128 + 2 * lane) = m[p];
                 *reinterpret_cast<float2 *>(pb + p * 128 + 64 + 2 * lane) = e[p];
+                *reinterpret_cast<float2 *>(sb + p * 64 + 2 * lane) = __fmul2_rn(m[p], make_float2(-rp, -rp));
             }
         }
         __syncthreads();
         if (warp > b) {
+            // warps after the next owner start once it has applied (named barrier 1:
+            // the next owner arrives, the 6 - b warps after it wait)
+            const uint32_t nbar = 32u * (uint32_t)(7 - b);
+            if (warp > b + 1) asm volatile("bar.sync 1, %0;" ::"r"(nbar) : "memory");
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
-                const float rp = rpiv[8 * b + p];
-                const float4 fa = *reinterpret_cast<const float4 *>(pb + p * 128 + 8 * warp);
-                const float4 fb = *reinterpret_cast<const float4 *>(pb + p * 128 + 8 * warp + 4);
+                // multipliers of this warp's rows: the scaled pivot row at their columns
+                const float4 fa = *reinterpret_cast<const float4 *>(sb + p * 64 + 8 * warp);
+                const float4 fb = *reinterpret_cast<const float4 *>(sb + p * 64 + 8 * warp + 4);
                 const float2 pm = *reinterpret_cast<const float2 *>(pb + p * 128 + 2 * lane);
                 const float2 pe = *reinterpret_cast<const float2 *>(pb + p * 128 + 64 + 2 * lane);
                 const float fr[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float2 f = make_float2(-fr[i] * rp, -fr[i] * rp);
-                    m[i] = __ffma2_rn(f, pm, m[i]);
-                    e[i] = __ffma2_rn(f, pe, e[i]);
+                    const float2 fi = make_float2(fr[i], fr[i]);
+                    m[i] = __ffma2_rn(fi, pm, m[i]);
+                    e[i] = __ffma2_rn(fi, pe, e[i]);
                 }
             }
+            if (warp == b + 1) asm volatile("bar.arrive 1, %0;" ::"r"(nbar) : "memory");
         }
     }
     // E (and diag(1/D) E) rows 8 warp + i, columns 2 lane, 2 lane + 1
