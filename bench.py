@@ -86,14 +86,17 @@ def kernel_plan(kname, d, io_dtype="bf16"):
     half = 6 * d * d + 8 * d
     gram = "gram_tc_kernel" if (io_dtype == "bf16" and d >= 64) else "gram_kernel"
     gram_e = "tensor" if gram == "gram_tc_kernel" else "alu"
-    # chunk_tc at d = 64 with bf16 I/O: gates and state passes run on the tensor cores
-    tc = kname == "chunk_tc" and io_dtype == "bf16" and d == 64
-    rows, gates, eng = ("rows_tc_kernel", "gates_tc_kernel", "tensor") if tc else ("rows_kernel", "gates_kernel", "alu")
-    if tc:
-        gram, gram_e = "gram_tma_kernel", "tensor"
-    return [(gram, 0, 0, gram_e), ("prefix_kernel", 0, 0, "alu"), (gates, half, 2 * d * io, eng),
-            (rows + "<summary>", 0, 0, eng), ("chain_kernel", 0, 0, "alu"),
-            (rows + "<output>", half, 3 * d * io, eng)]
+    # chunk_tc at d = 64 with bf16 I/O: gates and state pass on the tensor cores; the
+    # state pass does the state write and readout (a3-a4, reading q and v) for the
+    # [H; P] rows of each chunk, and the output pass combines them with the chunk-start
+    # state (o = S^(c) y + h, writing o)
+    if kname == "chunk_tc" and io_dtype == "bf16" and d == 64:
+        return [("gram_tma_kernel", 0, 0, "tensor"), ("prefix_kernel", 0, 0, "alu"),
+                ("gates_tc_kernel", half, 2 * d * io, "tensor"), ("rows_tc_kernel", half, 2 * d * io, "tensor"),
+                ("chain_kernel", 0, 0, "alu"), ("out_tc_kernel", 0, d * io, "tensor")]
+    return [(gram, 0, 0, gram_e), ("prefix_kernel", 0, 0, "alu"), ("gates_kernel", half, 2 * d * io, "alu"),
+            ("rows_kernel<summary>", 0, 0, "alu"), ("chain_kernel", 0, 0, "alu"),
+            ("rows_kernel<output>", half, 3 * d * io, "alu")]
 
 
 def state_bytes(B, H, d):

@@ -23,6 +23,12 @@
 //
 // Rows of S (and of [H; P]) evolve independently once the gates are known,
 // so the summary and output passes need no block-wide reduction per token.
+//
+// With VLA_KERNEL_CHUNK_TC at d = 64 and bf16 I/O (vla_chunk_tc.cu) the
+// summary pass also writes, per token, the readout of its [H; P] rows
+// (y_t = P_t phi(q_t) / den_t, h_t = H_t phi(q_t) / den_t; the state is affine
+// in S^(c) within a chunk), and the output pass is the product
+// o_t = S^(c) y_t + h_t, with no recurrence.
 #include "vla_internal.cuh"
 
 namespace vla {
@@ -1216,10 +1222,10 @@ int chunk_default_a_tc(int BH, int T, int C) {
     return best;
 }
 
-ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tinv) {
+ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc_path) {
     ChunkLayout L{};
     L.C = chunk > 0 ? chunk : chunk_default(BH, T);
-    const bool tc = tinv && d == 64 && L.C % 64 == 0;
+    const bool tc = tc_path && d == 64 && L.C % 64 == 0;
     L.CA = chunk > 0 ? chunk : (tc ? chunk_default_a_tc(BH, T, L.C) : chunk_default_a(BH, T, d, L.C));
     L.NC = (T + L.C - 1) / L.C;
     L.NCA = (T + L.CA - 1) / L.CA;
@@ -1232,9 +1238,9 @@ ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tinv) {
     L.off_P = off; off = align256(off + bh * nc * dd * 4);
     L.off_H = off; off = align256(off + bh * nc * dd * 4);
     L.off_S = off; off = align256(off + bh * nc * dd * 4);
-    L.off_tinv = off;
-    L.tinv = (tinv && d == 64 && L.C % 64 == 0) ? 1 : 0;
-    if (L.tinv) off = align256(off + bh * nc * (size_t)(L.C / 64) * 16384);
+    L.off_yh = off;
+    L.yh = tc ? 1 : 0;
+    if (L.yh) off = align256(off + bh * nc * (size_t)(L.C / 64) * 32768);
     L.total = off;
     return L;
 }

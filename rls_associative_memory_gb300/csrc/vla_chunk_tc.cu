@@ -1,13 +1,21 @@
-// vla_chunk_tc.cu -- tensor-core state passes of the chunk-parallel path for
-// d = 64 with bf16 I/O: the chunk transitions (mode 0) and the readout
-// (mode 1) of the state write and ELU+1 readout of "Variational Linear
-// Attention: Stable Associative Memory for Long-Context Transformers",
-// section 2.3 (step 3 and the readout), taken 64 tokens at a time in the UT
-// (WY) form of a product of rank-1 updates.
+// vla_chunk_tc.cu -- tensor-core state pass and output pass of the
+// chunk-parallel path for d = 64 with bf16 I/O: the state write and ELU+1
+// readout of "Variational Linear Attention: Stable Associative Memory for
+// Long-Context Transformers", section 2.3 (step 3 and the readout), taken
+// 64 tokens at a time in the UT (WY) form of a product of rank-1 updates.
 //
-// Within a sub-block of c = 64 tokens whose state at the start is X, the
-// state write x <- x + (value - x.k_hat) alpha^T, applied token by token,
-// is equivalent to
+// Within a chunk the state write is affine in the chunk-start state S_c:
+// S_t = S_c P_t + H_t, where P_t and H_t are the states reached from the
+// starts I and 0 (with values 0 and v).  So the readout is
+//   o_t = S_c y_t + h_t,   y_t = P_t phi(q_t) / den_t,   h_t = H_t phi(q_t) / den_t
+// with den_t = phi(q_t) . n_t + eps.  The state pass runs the 128 rows
+// [H; P] of each chunk, writes the chunk map (H_c, P_c) for the chain along
+// the chunks and y_t, h_t for every token; the output pass then only forms
+// S_c y_t + h_t, with no recurrence left in it.
+//
+// Within a sub-block of c = 64 tokens whose state at the start is X (128 x
+// 64), the token-by-token state write x <- x + (value - x.k_hat) alpha^T is
+// equivalent to
 //   R (I + N) = Vals - X K_hat,        N = strictly-upper(Al^T K_hat)  (c x c)
 //   X_end     = X + R Al^T
 //   X_t phi(q_t) = X phi(q_t) + sum_{s <= t} r_s (alpha_s . phi(q_t))
@@ -16,18 +24,12 @@
 // the sub-block left in the state, hence the triangular system).  A
 // sub-block is three rounds of tcgen05.mma plus one triangular inverse on
 // the CUDA cores:
-//   1. D1 = X K^T;  mode 0: D2 = K Al^T (= N^T);  mode 1: D2 = Phi Al^T
-//      (= Qm^T, Qm = upper-incl(Al^T Phi)) and DO = Phi X^T
-//   2. R  = E T_inv,   E = Vals - (X K) diag(1/|k|),  T_inv = (I + N)^{-1}
-//   3. X += R Al^T    and (mode 1)  DO += Qm^T R^T
-// T_inv depends on the keys and gates only: mode 0 computes it and stores
-// it (bf16 hi/lo operand tiles) in the workspace, and mode 1 loads it with a
-// bulk copy.  DO holds the readout numerators token-major (rows = tokens),
-// so o leaves as whole 16-byte vectors.
-//
-// Mode 0 runs the rows [H; P] of the chunk map S_end = S_start P_c + H_c
-// (values [v; 0], start [0; I]: M = 128); mode 1 runs S itself from the
-// chunk-start state of the chain pass and writes o (M = 64).
+//   1. D1 = X K^T,  D2 = K Al^T (= N^T),  DO = Phi X^T
+//   2. R = E T_inv  (E = Vals - (X K) diag(1/|k|), T_inv = (I + N)^{-1}),
+//      and Qm^T = Phi Al^T  (Qm = upper-incl(Al^T Phi))
+//   3. X += R Al^T,  DO += Qm^T R^T
+// DO holds the readout numerators token-major (rows = tokens; columns = the
+// 128 state rows, h_t then y_t, before the division by den_t).
 //
 // Precision: fp32 operands enter the tensor cores as bf16 pairs
 // x = hi + lo (hi = bf16(x), lo = bf16(x - hi)), and a product takes
@@ -43,49 +45,45 @@ using namespace tc;
 
 constexpr int kThreads = 256;
 
-template <int MODE>
 struct TcLayout {
-    static constexpr int XR = MODE == 0 ? 128 : 64;            // state rows
-    static constexpr uint32_t ncols = MODE == 0 ? 128 : 256;    // TMEM columns
-    static constexpr size_t ctrl = 0;                            // mbarriers (MMA, T_inv load), TMEM slot, abort flag
-    // X / E / R tiles (hi, lo) and the gate tiles Al (token rows; hi, lo).  In
-    // mode 1 they interleave as [X hi | Al hi | X lo | Al lo], so that [X; Al]
-    // is one 128-row operand (Phi [X; Al]^T in one product).
+    static constexpr size_t ctrl = 0;  // mbarrier, TMEM slot, abort flag
+    // X / E / R tiles: 128 rows (0..63 the H rows, 64..127 the P rows), hi then lo
     static constexpr size_t xs_hi = 1024;
-    static constexpr size_t xs_lo = MODE == 0 ? xs_hi + 2 * kTile : xs_hi + 2 * kTile;
-    static constexpr size_t al_hi = MODE == 0 ? xs_hi + 4 * kTile : xs_hi + kTile;
-    static constexpr size_t al_lo = MODE == 0 ? al_hi + kTile : xs_hi + 3 * kTile;
-    static constexpr size_t kb = xs_hi + 4 * kTile + (MODE == 0 ? 2 * kTile : 0);  // [K; Phi_hi] (mode 1) or K; then Qm^T hi, lo
-    static constexpr size_t kblo = kb + (MODE == 0 ? kTile : 2 * kTile);  // Phi_lo (mode 1)
-    static constexpr size_t ti = kblo + (MODE == 0 ? 0 : kTile); // (mode 0) N fp32 (row stride kGS); T_inv hi, lo
-    static constexpr int kVS = 72;                               // row stride (bf16) of the v tile
-    static constexpr size_t vt = ti + (MODE == 0 ? (size_t)64 * kGS * 4 : 2 * (size_t)kTile);  // v [t][i] bf16
-    static constexpr size_t ks = vt + (size_t)64 * kVS * 2;      // [64] 1 / max(|k|, eps)
-    static constexpr size_t rden = ks + 256;                     // [64] 1 / (phi(q).n + eps)
-    static constexpr size_t tot = rden + 256;                    // [9][64] warp totals of phi(k_hat), then prefixes
-    static constexpr size_t total = tot + 9 * 64 * 4;
+    static constexpr size_t xs_lo = xs_hi + 2 * kTile;
+    static constexpr size_t al_hi = xs_hi + 4 * kTile;       // gates (token rows), hi, lo
+    static constexpr size_t al_lo = al_hi + kTile;
+    static constexpr size_t kb = al_hi + 2 * kTile;          // K (raw bf16, token rows)
+    static constexpr size_t ph_hi = kb + kTile;              // Phi = phi(Q) (token rows), then Qm^T; hi, lo
+    static constexpr size_t ph_lo = ph_hi + kTile;
+    static constexpr size_t ti = ph_hi + 2 * kTile;          // N fp32 (row stride kGS), then T_inv hi, lo
+    static constexpr int kVS = 72;                           // row stride (bf16) of the v tile
+    static constexpr size_t vt = ti + (size_t)64 * kGS * 4;  // v [t][i] bf16
+    static constexpr size_t ks = vt + (size_t)64 * kVS * 2;  // [64] 1 / max(|k|, eps)
+    static constexpr size_t rden = ks + 256;                 // [64] 1 / (phi(q).n + eps)
+    static constexpr size_t tot = rden + 256;                // [8][64] warp totals of phi(k_hat), then prefixes
+    static constexpr size_t nrun = tot + 8 * 64 * 4;         // [64] n at the sub-block start
+    static constexpr size_t total = nrun + 256;
 };
+static_assert(TcLayout::ti % 1024 == 0, "T_inv tiles must be 1024-byte aligned");
 
-template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
-    using L = TcLayout<MODE>;
-    constexpr int XR = L::XR;
+    using L = TcLayout;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // swizzled tiles need 1024-byte aligned addresses (one extra KB is allocated)
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
-    uint64_t *bar_t = reinterpret_cast<uint64_t *>(smem + L::ctrl + 16);  // T_inv load (mode 1)
     unsigned char *xs_hi = smem + L::xs_hi, *xs_lo = smem + L::xs_lo;
-    unsigned char *kb = smem + L::kb, *kblo = smem + L::kblo;
+    unsigned char *kb = smem + L::kb, *ph_hi = smem + L::ph_hi, *ph_lo = smem + L::ph_lo;
     unsigned char *al_hi = smem + L::al_hi, *al_lo = smem + L::al_lo;
-    float *ntb = reinterpret_cast<float *>(smem + L::ti);  // N (mode 0), row stride kGS
+    float *ntb = reinterpret_cast<float *>(smem + L::ti);  // N, row stride kGS
     unsigned char *ti_hi = smem + L::ti, *ti_lo = smem + L::ti + kTile;  // T_inv, tile row s = row s
     __nv_bfloat16 *vt = reinterpret_cast<__nv_bfloat16 *>(smem + L::vt);
     float *s_ks = reinterpret_cast<float *>(smem + L::ks);
     float *s_rden = reinterpret_cast<float *>(smem + L::rden);
     float *s_tot = reinterpret_cast<float *>(smem + L::tot);
+    float *s_nrun = reinterpret_cast<float *>(smem + L::nrun);
 
     const int NC = a.L.NC, C = a.L.C, T = a.p.T;
     const int c = (int)(blockIdx.x % (unsigned)NC), bh = (int)(blockIdx.x / (unsigned)NC);
@@ -100,42 +98,31 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.p.v) + tok0;
     const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.p.q) + tok0;
     const float *gal = ws_f(a, a.L.off_alpha) + tok0;
-    __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.p.o) + tok0;
+    // this chunk's readout coefficients: per sub-block [y hi | y lo | h hi | h lo] (token rows)
+    unsigned char *gyh = static_cast<unsigned char *>(a.p.ws) + a.L.off_yh +
+                         (size_t)(bh * NC + c) * (C / kSB) * (4 * kTile);
 
-    unsigned char *gtinv = static_cast<unsigned char *>(a.p.ws) + a.L.off_tinv +
-                           (size_t)(bh * NC + c) * (C / kSB) * (2 * kTile);  // this chunk's T_inv tiles
     if (tid == 0) {
         mbar_init(bar, 1);
-        mbar_init(bar_t, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
-    if (warp == 0) tmem_alloc(tslot, L::ncols);
+    if (tid < 64)  // n at the chunk start (chunks start on A-chunk boundaries)
+        s_nrun[tid] = ws_f(a, a.L.off_n)[((size_t)bh * (a.L.NCA + 1) + (size_t)c * (C / a.L.CA)) * kD + tid];
+    if (warp == 0) tmem_alloc(tslot, 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
     const uint32_t tq = tbase + ((uint32_t)(32 * qw) << 16);  // this warp's lane quarter
 
-    // State rows held in registers: the row and 32 columns this thread reads
-    // back from TMEM (M = 128: row 32 qw + lane; M = 64: row 16 qw + lane,
-    // lanes 0..15 of each quarter).
-    const int xrow = MODE == 0 ? 32 * qw + lane : 16 * qw + lane;
-    const bool xact = MODE == 0 || lane < 16;
+    // State row held in registers: row 32 qw + lane of [H; P], the 32 columns
+    // 32 hw .. this thread reads back from TMEM (M = 128).  H starts at 0, P at I.
+    const int xrow = 32 * qw + lane;
     float x[32];
-    if (MODE == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = (xrow - 64 == 32 * hw + j) ? 1.f : 0.f;
-    } else {
-        const float4 *src = reinterpret_cast<const float4 *>(ws_f(a, a.L.off_S) + ((size_t)bh * NC + c) * kD * kD +
-                                                             (size_t)(xrow & 63) * kD + 32 * hw);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 v = xact ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-            x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
-        }
-    }
-    if (xact) put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
+    for (int j = 0; j < 32; ++j) x[j] = (xrow - 64 == 32 * hw + j) ? 1.f : 0.f;
+    put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
 
     // Inputs of the next sub-block, prefetched into registers (token pt,
     // features 16 pq .. 16 pq + 15).
@@ -150,17 +137,11 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         for (int h = 0; h < 2; ++h) {
             rk[h] = reinterpret_cast<const uint4 *>(gk + off)[h];
             rv[h] = reinterpret_cast<const uint4 *>(gv + off)[h];
-            if (MODE == 1) rq[h] = reinterpret_cast<const uint4 *>(gq + off)[h];
+            rq[h] = reinterpret_cast<const uint4 *>(gq + off)[h];
         }
 #pragma unroll
         for (int h = 0; h < 4; ++h) ra[h] = reinterpret_cast<const float4 *>(gal + off)[h];
     };
-    float nb[16];  // n at the sub-block start, features 16 pq .. (mode 1)
-    if (MODE == 1) {
-        const float *n0 = ws_f(a, a.L.off_n) + ((size_t)bh * (a.L.NCA + 1) + (size_t)c * (C / a.L.CA)) * kD + 16 * pq;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) nb[m] = n0[m];
-    }
 
     uint32_t phase = 0;
     auto round_wait = [&]() -> bool {
@@ -171,24 +152,19 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         tc_fence_after();
         return *abort_flag == 0;
     };
-    constexpr uint32_t id_x64 = idesc_bf16_f32(XR, 64);                       // X-row products
+    constexpr uint32_t id_x = idesc_bf16_f32(128, 64);   // products with the 128 state rows
     constexpr uint32_t id_64 = idesc_bf16_f32(64, 64);
+    constexpr uint32_t id_do = idesc_bf16_f32(64, 128);  // token rows x the 128 state rows
     constexpr int kVS = L::kVS;
-    constexpr uint32_t col_d2 = MODE == 1 ? 128 : 64;   // D2, then D3 = R
-    constexpr uint32_t col_d4 = 0;                      // D1 = X K^T, then D4 = R Al^T
-    constexpr uint32_t col_do = 64;                     // (mode 1) readout numerators, token rows
+    constexpr uint32_t col_d4 = 0;    // D1 = X K^T, then Qm^T, then D4 = R Al^T
+    constexpr uint32_t col_d2 = 64;   // D2 = N^T, then D3 = R
+    constexpr uint32_t col_do = 128;  // readout numerators, token rows (128 columns)
 
     bool ok = true;
-    int tinv_issued = 0, tinv_done = 0;  // T_inv loads (mode 1)
     load_in(0);
     for (int sb = 0; sb < nsb; ++sb) {
         const int nt = min(kSB, ntok - sb * kSB);
         float fq[16], fk[16];
-        if (MODE == 1 && tid == 0) {  // T_inv of this sub-block (the slot is free: round 2 is done)
-            mbar_arrive_expect_tx(bar_t, 2 * kTile);
-            bulk_g2s(ti_hi, gtinv + (size_t)sb * 2 * kTile, 2 * kTile, bar_t);
-        }
-        tinv_issued = sb + 1;
         // ---- stage the sub-block's operands ----
         if (pt >= nt) {  // past the chunk: zero inputs
             rk[0] = rk[1] = rv[0] = rv[1] = rq[0] = rq[1] = make_uint4(0, 0, 0, 0);
@@ -222,78 +198,68 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             split8(af + 8, h4, l4);
             *reinterpret_cast<uint4 *>(al_hi + toff(pt, 16 * pq + 8)) = h4;
             *reinterpret_cast<uint4 *>(al_lo + toff(pt, 16 * pq + 8)) = l4;
-            if (MODE == 1) {
-                float qf[16];
-                unpack8(rq[0], qf);
-                unpack8(rq[1], qf + 8);
+            float qf[16];
+            unpack8(rq[0], qf);
+            unpack8(rq[1], qf + 8);
 #pragma unroll
-                for (int m = 0; m < 16; ++m) fq[m] = phi_fast(qf[m]);
-                split8(fq, h4, l4);
-                *reinterpret_cast<uint4 *>(kb + toff(64 + pt, 16 * pq)) = h4;
-                *reinterpret_cast<uint4 *>(kblo + toff(pt, 16 * pq)) = l4;
-                split8(fq + 8, h4, l4);
-                *reinterpret_cast<uint4 *>(kb + toff(64 + pt, 16 * pq + 8)) = h4;
-                *reinterpret_cast<uint4 *>(kblo + toff(pt, 16 * pq + 8)) = l4;
-                // phi(k_hat): inclusive scan over this warp's 8 tokens (adjacent lanes)
+            for (int m = 0; m < 16; ++m) fq[m] = phi_fast(qf[m]);
+            split8(fq, h4, l4);
+            *reinterpret_cast<uint4 *>(ph_hi + toff(pt, 16 * pq)) = h4;
+            *reinterpret_cast<uint4 *>(ph_lo + toff(pt, 16 * pq)) = l4;
+            split8(fq + 8, h4, l4);
+            *reinterpret_cast<uint4 *>(ph_hi + toff(pt, 16 * pq + 8)) = h4;
+            *reinterpret_cast<uint4 *>(ph_lo + toff(pt, 16 * pq + 8)) = l4;
+            // phi(k_hat): inclusive scan over this warp's 8 tokens (adjacent lanes)
 #pragma unroll
-                for (int m = 0; m < 16; ++m) fk[m] = pt < nt ? phi_fast(kf[m] * ksc) : 0.f;
+            for (int m = 0; m < 16; ++m) fk[m] = pt < nt ? phi_fast(kf[m] * ksc) : 0.f;
 #pragma unroll
-                for (int off = 1; off < 8; off <<= 1) {
+            for (int off = 1; off < 8; off <<= 1) {
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        const float y = __shfl_up_sync(0xffffffffu, fk[m], off);
-                        if ((lane & 7) >= off) fk[m] += y;
-                    }
+                for (int m = 0; m < 16; ++m) {
+                    const float y = __shfl_up_sync(0xffffffffu, fk[m], off);
+                    if ((lane & 7) >= off) fk[m] += y;
                 }
-                if ((lane & 7) == 7) {
-                    float4 *dst = reinterpret_cast<float4 *>(s_tot + warp * 64 + 16 * pq);
+            }
+            if ((lane & 7) == 7) {
+                float4 *dst = reinterpret_cast<float4 *>(s_tot + warp * 64 + 16 * pq);
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) dst[h] = make_float4(fk[4 * h], fk[4 * h + 1], fk[4 * h + 2], fk[4 * h + 3]);
-                }
+                for (int h = 0; h < 4; ++h) dst[h] = make_float4(fk[4 * h], fk[4 * h + 1], fk[4 * h + 2], fk[4 * h + 3]);
             }
         }
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 1: D1 = X K^T; D2 = K Al^T (mode 0) or Phi Al^T (mode 1); (mode 1) DO = Phi X^T ----
+        // ---- round 1: D1 = X K^T, D2 = K Al^T, DO = Phi X^T ----
         if (tid == 0) {
             tc_fence_after();
-            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x64, false);
-            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x64, true);
-            if (MODE == 1) {
-                // [DO | D2] = Phi [X; Al]^T: DO at col_do, D2 = Qm^T at col_do + 64 = col_d2
-                mma_k64x3<false, false>(tbase + col_do, smem_u32(kb + kTile), smem_u32(kblo), smem_u32(xs_hi),
-                                        smem_u32(xs_lo), idesc_bf16_f32(64, 128), false);
-            } else {
-                mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
-                mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
-            }
+            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x, false);
+            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x, true);
+            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
+            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
+            mma_k64x3<false, false>(tbase + col_do, smem_u32(ph_hi), smem_u32(ph_lo), smem_u32(xs_hi),
+                                    smem_u32(xs_lo), id_do, false);
             umma_commit(bar);
         }
-        if (MODE == 1) {  // readout denominators 1 / (phi(q_t) . n_t + eps)
-            if (tid < 64) {  // per feature: exclusive prefix of the warp totals, and the total
-                float run = 0.f;
+        // ---- readout denominators 1 / (phi(q_t) . n_t + eps) ----
+        if (tid < 64) {  // per feature: n before each warp's tokens, and n after the sub-block
+            float run = s_nrun[tid];
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const float x = s_tot[w * 64 + tid];
-                    s_tot[w * 64 + tid] = run;
-                    run += x;
-                }
-                s_tot[8 * 64 + tid] = run;
+            for (int w = 0; w < 8; ++w) {
+                const float y = s_tot[w * 64 + tid];
+                s_tot[w * 64 + tid] = run;
+                run += y;
             }
-            __syncthreads();
+            s_nrun[tid] = run;
+        }
+        __syncthreads();
+        {
             const float4 *pw = reinterpret_cast<const float4 *>(s_tot + warp * 64 + 16 * pq);
-            const float4 *pa = reinterpret_cast<const float4 *>(s_tot + 8 * 64 + 16 * pq);
             float dp = 0.f;
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const float4 p4 = pw[h], a4 = pa[h];
-                const float pv[4] = {p4.x, p4.y, p4.z, p4.w}, av[4] = {a4.x, a4.y, a4.z, a4.w};
+                const float4 p4 = pw[h];
+                const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = 4 * h + e;
-                    dp = fmaf(fq[m], nb[m] + pv[e] + fk[m], dp);
-                    nb[m] += av[e];
-                }
+                for (int e = 0; e < 4; ++e) dp = fmaf(fq[4 * h + e], pv[e] + fk[4 * h + e], dp);
             }
             dp += __shfl_xor_sync(0xffffffffu, dp, 8);
             dp += __shfl_xor_sync(0xffffffffu, dp, 16);
@@ -304,86 +270,77 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             ok = false;
             break;
         }
-        // ---- N (fp32, row-major, for the inverse; mode 0), Qm^T tiles (mode 1), E tiles ----
+        // ---- N (fp32, row-major, for the inverse), E tiles ----
         {
             float v[32];
             tmem_ld32(tq + col_d2 + 32 * hw, v);  // D2 row t = 16 qw + lane (M = 64), columns s = 32 hw ..
-            if (lane < 16) {
+            if (lane < 16) {  // N[s][t] = alpha_s . k_hat_t (s < t), row-major: lanes t write one row s together
                 const int t = 16 * qw + lane;
-                if (MODE == 1) {
+                const float kt = s_ks[t];
 #pragma unroll
-                    for (int m = 0; m < 32; ++m)
-                        if (32 * hw + m > t) v[m] = 0.f;
-                    put_row32(kb, kb + kTile, t, 32 * hw, v);
-                } else {  // N[s][t] = alpha_s . k_hat_t (s < t), row-major: lanes t write one row s together
-                    const float kt = s_ks[t];
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) {
-                        const int sr = 32 * hw + m;
-                        ntb[sr * kGS + t] = sr < t ? v[m] * kt : 0.f;
-                    }
+                for (int m = 0; m < 32; ++m) {
+                    const int sr = 32 * hw + m;
+                    ntb[sr * kGS + t] = sr < t ? v[m] * kt : 0.f;
                 }
             }
             tmem_ld32(tq + col_d4 + 32 * hw, v);  // X K, columns 32 hw ..
-            if (xact) {
-                const float4 *ks4 = reinterpret_cast<const float4 *>(s_ks + 32 * hw);
+            const float4 *ks4 = reinterpret_cast<const float4 *>(s_ks + 32 * hw);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 k4 = ks4[q];
-                    const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+            for (int q = 0; q < 8; ++q) {
+                const float4 k4 = ks4[q];
+                const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int m = 4 * q + e, t = 32 * hw + m;
-                        const float val = (MODE == 1 || xrow < 64) ? __bfloat162float(vt[t * kVS + (xrow & 63)]) : 0.f;
-                        v[m] = fmaf(-v[m], kv[e], val);
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    const int m = 4 * q + e, t = 32 * hw + m;
+                    const float val = xrow < 64 ? __bfloat162float(vt[t * kVS + xrow]) : 0.f;
+                    v[m] = fmaf(-v[m], kv[e], val);
                 }
-                put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
             }
+            put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
         }
         tc_fence_before();
         __syncthreads();
-        // ---- T_inv = (I + N)^{-1} (mode 0; blocked back substitution) ----
-        if (MODE == 0) {
-            tri_inv64(ntb, reinterpret_cast<float *>(kb), ti_hi, ti_lo);
-        } else {  // mode 1: T_inv of this sub-block, stored by the transition pass
-            if (!mbar_wait_bounded(bar_t, (uint32_t)(sb & 1), a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
-            tinv_done = sb + 1;
-        }
+        // ---- T_inv = (I + N)^{-1} (blocked back substitution) ----
+        tri_inv64(ntb, reinterpret_cast<float *>(kb), ti_hi, ti_lo);
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 2: R = E T_inv ----
+        // ---- round 2: R = E T_inv, Qm^T = Phi Al^T ----
         if (tid == 0) {
             tc_fence_after();
             mma_k64x3<false, true>(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi),
-                                   smem_u32(ti_lo), id_x64, false);
+                                   smem_u32(ti_lo), id_x, false);
+            mma_k64x3<false, false>(tbase + col_d4, smem_u32(ph_hi), smem_u32(ph_lo), smem_u32(al_hi),
+                                    smem_u32(al_lo), id_64, false);
             umma_commit(bar);
-        }
-        if (MODE == 0) {  // T_inv tiles to the workspace for the readout pass
-            const uint4 *src4 = reinterpret_cast<const uint4 *>(ti_hi);
-            uint4 *dst4 = reinterpret_cast<uint4 *>(gtinv + (size_t)sb * 2 * kTile);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dst4[tid + kThreads * e] = src4[tid + kThreads * e];
         }
         if (!round_wait()) {
             ok = false;
             break;
         }
+        // ---- R tiles; Qm^T tiles over Phi (round 2 has read it) ----
         {
             float v[32];
             tmem_ld32(tq + col_d2 + 32 * hw, v);
-            if (xact) put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
+            put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
+            tmem_ld32(tq + col_d4 + 32 * hw, v);  // Qm^T row t = 16 qw + lane, columns s = 32 hw ..
+            if (lane < 16) {
+                const int t = 16 * qw + lane;
+#pragma unroll
+                for (int m = 0; m < 32; ++m)
+                    if (32 * hw + m > t) v[m] = 0.f;
+                put_row32(ph_hi, ph_lo, t, 32 * hw, v);
+            }
         }
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 3: X += R Al^T; (mode 1) DO += Qm^T R^T ----
+        // ---- round 3: X += R Al^T, DO += Qm^T R^T ----
         if (tid == 0) {
             tc_fence_after();
-            mma_k64x3<false, true>(tbase + col_d4, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi), smem_u32(al_lo), id_x64,
-                          false);
-            if (MODE == 1)
-                mma_k64x3<false, false>(tbase + col_do, smem_u32(kb), smem_u32(kb + kTile), smem_u32(xs_hi), smem_u32(xs_lo), id_64, true);
+            mma_k64x3<false, true>(tbase + col_d4, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi),
+                                   smem_u32(al_lo), id_x, false);
+            mma_k64x3<false, false>(tbase + col_do, smem_u32(ph_hi), smem_u32(ph_lo), smem_u32(xs_hi),
+                                    smem_u32(xs_lo), id_do, true);
             umma_commit(bar);
         }
         if (!round_wait()) {
@@ -393,26 +350,25 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         {
             float v[32];
             tmem_ld32(tq + col_d4 + 32 * hw, v);
-            if (xact) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] += v[j];
-                put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
+            for (int j = 0; j < 32; ++j) x[j] += v[j];
+            put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
+            // readout coefficients of token t = 16 qw + lane: y_t (state rows
+            // 64..127) and h_t (rows 0..63), columns 32 hw .., divided by den_t
+            unsigned char *dst = gyh + (size_t)sb * (4 * kTile);
+            const int t = 16 * qw + lane;
+            const float rd = s_rden[t & 63];
+            tmem_ld32(tq + col_do + 64 + 32 * hw, v);
+            if (lane < 16) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= rd;
+                put_row32(dst, dst + kTile, t, 32 * hw, v);
             }
-            if (MODE == 1) {
-                tmem_ld32(tq + col_do + 32 * hw, v);  // numerators of token 16 qw + lane, columns 32 hw ..
-                const int t = 16 * qw + lane;
-                if (lane < 16 && t < nt) {
-                    const float rd = s_rden[t];
-                    uint4 *dst = reinterpret_cast<uint4 *>(gout + (size_t)(sb * kSB + t) * kD + 32 * hw);
+            tmem_ld32(tq + col_do + 32 * hw, v);
+            if (lane < 16) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = bf2_bits(__floats2bfloat162_rn(v[8 * g + 2 * e] * rd, v[8 * g + 2 * e + 1] * rd));
-                        dst[g] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                }
+                for (int j = 0; j < 32; ++j) v[j] *= rd;
+                put_row32(dst + 2 * kTile, dst + 3 * kTile, t, 32 * hw, v);
             }
         }
         tc_fence_before();
@@ -420,12 +376,8 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         __syncthreads();
     }
     if (!ok) {
-        if (tid == 0) {
-            (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
-            if (MODE == 1 && tinv_issued > tinv_done)  // a T_inv copy may still be landing
-                (void)mbar_wait_bounded(bar_t, (uint32_t)((tinv_issued - 1) & 1), a.p.wait_limit_ns, a.p.err);
-        }
-    } else if (MODE == 0) {  // rows 0..63 are H_c, rows 64..127 P_c
+        if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
+    } else {  // rows 0..63 are H_c, rows 64..127 P_c
         float4 *dst = reinterpret_cast<float4 *>(ws_f(a, xrow < 64 ? a.L.off_H : a.L.off_P) +
                                                  ((size_t)bh * NC + c) * kD * kD + (size_t)(xrow & 63) * kD + 32 * hw);
 #pragma unroll
@@ -433,29 +385,172 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, L::ncols);
+    if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
-template <int MODE>
-cudaError_t launch_mode(const ChunkArgs &a, cudaStream_t st) {
-    constexpr size_t bytes = TcLayout<MODE>::total + 1024;  // + alignment slack
-    cudaError_t e = cudaFuncSetAttribute(rows_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)bytes);
-    if (e != cudaSuccess) return e;
-    const long long grid = (long long)a.L.NC * a.p.BH;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    rows_tc_kernel<MODE><<<(unsigned)grid, kThreads, bytes, st>>>(a);
-    return cudaGetLastError();
+// ---------------------------------------------------------------------------
+// Output pass: o_t = S_c y_t + h_t for every token, one CTA per chunk.  Per
+// sub-block one product D = [Y | H] [S_c | I]^T on the tensor cores (S_c as
+// a bf16 hi/lo pair, H as hi + lo against the exact identity), with the
+// sub-block's coefficient tiles brought in by bulk copies two sub-blocks
+// ahead.
+// ---------------------------------------------------------------------------
+constexpr int kOutThreads = 128;
+
+struct OutLayout {
+    static constexpr size_t ctrl = 0;                   // mbarriers (2 stages, MMA), TMEM slot, abort flag
+    static constexpr size_t stage = 1024;               // 2 x [y hi | y lo | h hi | h lo]
+    static constexpr size_t sc_hi = stage + 8 * kTile;  // S_c (row i, column j), hi, lo
+    static constexpr size_t sc_lo = sc_hi + kTile;
+    static constexpr size_t eye = sc_hi + 2 * kTile;    // identity (bf16)
+    static constexpr size_t total = eye + kTile;
+};
+
+__global__ void __launch_bounds__(kOutThreads) out_tc_kernel(ChunkArgs a) {
+    using L = OutLayout;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::ctrl);  // [2]
+    uint64_t *mbar = full + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 24);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 28);
+    unsigned char *st = smem + L::stage, *sc_hi = smem + L::sc_hi, *sc_lo = smem + L::sc_lo, *eye = smem + L::eye;
+
+    const int NC = a.L.NC, C = a.L.C, T = a.p.T;
+    const int c = (int)(blockIdx.x % (unsigned)NC), bh = (int)(blockIdx.x / (unsigned)NC);
+    const int t0 = c * C, ntok = min(C, T - t0), nsb = (ntok + kSB - 1) / kSB;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned char *gyh = static_cast<const unsigned char *>(a.p.ws) + a.L.off_yh +
+                               (size_t)(bh * NC + c) * (C / kSB) * (4 * kTile);
+    __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.p.o) + ((size_t)bh * T + t0) * kD;
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(mbar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 0) tmem_alloc(tslot, 64);
+    {  // S_c row i, columns 32 h .. as a hi/lo pair; the identity
+        const int i = tid >> 1, h = tid & 1;
+        const float4 *src = reinterpret_cast<const float4 *>(ws_f(a, a.L.off_S) + ((size_t)bh * NC + c) * kD * kD +
+                                                             (size_t)i * kD + 32 * h);
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 s4 = src[q];
+            v[4 * q] = s4.x; v[4 * q + 1] = s4.y; v[4 * q + 2] = s4.z; v[4 * q + 3] = s4.w;
+        }
+        put_row32(sc_hi, sc_lo, i, 32 * h, v);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {  // bf16 1.0 = 0x3f80; element k in the low half
+                const int k = 32 * h + 8 * g + 2 * e;
+                w[e] = (k == i ? 0x3f80u : 0u) | (k + 1 == i ? 0x3f800000u : 0u);
+            }
+            *reinterpret_cast<uint4 *>(eye + toff(i, 32 * h + 8 * g)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+    int issued = min(2, nsb), landed = 0, mma_open = -1;  // (thread 0's bookkeeping)
+    if (tid == 0) {
+        for (int s = 0; s < issued; ++s) {
+            mbar_arrive_expect_tx(&full[s], 4 * kTile);
+            bulk_g2s(st + (size_t)s * 4 * kTile, gyh + (size_t)s * 4 * kTile, 4 * kTile, &full[s]);
+        }
+    }
+    constexpr uint32_t id_64 = idesc_bf16_f32(64, 64);
+    for (int sb = 0; sb < nsb; ++sb) {
+        const int s = sb & 1;
+        unsigned char *yh = st + (size_t)s * 4 * kTile;
+        if (tid == 0) {
+            bool w = mbar_wait_bounded(&full[s], (uint32_t)((sb >> 1) & 1), a.p.wait_limit_ns, a.p.err);
+            if (w) {
+                landed = sb + 1;
+                tc_fence_after();
+                // D = Y S_c^T (hi/lo split) + H I^T
+                mma_k64x3<false, false>(tbase, smem_u32(yh), smem_u32(yh + kTile), smem_u32(sc_hi), smem_u32(sc_lo),
+                                        id_64, false);
+                mma_k64<false, false>(tbase, smem_u32(yh + 2 * kTile), smem_u32(eye), id_64, true);
+                mma_k64<false, false>(tbase, smem_u32(yh + 3 * kTile), smem_u32(eye), id_64, true);
+                umma_commit(mbar);
+                w = mbar_wait_bounded(mbar, (uint32_t)(sb & 1), a.p.wait_limit_ns, a.p.err);
+                if (!w) mma_open = sb;
+            }
+            if (!w) {
+                *abort_flag = 1;
+            } else if (sb + 2 < nsb) {  // the stage is free again: bring in sub-block sb + 2
+                mbar_arrive_expect_tx(&full[s], 4 * kTile);
+                bulk_g2s(yh, gyh + (size_t)(sb + 2) * 4 * kTile, 4 * kTile, &full[s]);
+                issued = sb + 3;
+            }
+        }
+        __syncthreads();
+        tc_fence_after();
+        if (*abort_flag) break;
+        // o rows: token t = 16 warp + lane (lanes 0..15 hold the M = 64 rows)
+        const int t = 16 * warp + lane;
+        const bool act = lane < 16 && sb * kSB + t < ntok;
+        uint4 *dst = reinterpret_cast<uint4 *>(gout + (size_t)(sb * kSB + (t & 63)) * kD);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_ld32(tbase + ((uint32_t)(32 * warp) << 16) + 32 * h, v);
+            if (act) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = bf2_bits(__floats2bfloat162_rn(v[8 * g + 2 * e], v[8 * g + 2 * e + 1]));
+                    dst[4 * h + g] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    if (tid == 0) {  // after an abort: copies and products that may still be in flight
+        for (int sb = landed; sb < issued; ++sb)
+            (void)mbar_wait_bounded(&full[sb & 1], (uint32_t)((sb >> 1) & 1), a.p.wait_limit_ns, a.p.err);
+        if (mma_open >= 0) (void)mbar_wait_bounded(mbar, (uint32_t)(mma_open & 1), a.p.wait_limit_ns, a.p.err);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 64);
 }
 
 }  // namespace
 
 bool rows_tc_supported(const FwdParams &p, const ChunkLayout &L) {
-    return p.d == kD && p.io_bf16 && L.C % kSB == 0 && L.tinv;
+    return p.d == kD && p.io_bf16 && L.C % kSB == 0 && L.yh;
 }
 
 cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream) {
-    return mode == 0 ? launch_mode<0>(a, stream) : launch_mode<1>(a, stream);
+    const long long grid = (long long)a.L.NC * a.p.BH;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    cudaError_t e;
+    if (mode == 0) {
+        constexpr size_t bytes = TcLayout::total + 1024;  // + alignment slack
+        if ((e = cudaFuncSetAttribute(rows_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes)) !=
+            cudaSuccess)
+            return e;
+        rows_tc_kernel<<<(unsigned)grid, kThreads, bytes, stream>>>(a);
+    } else {
+        constexpr size_t bytes = OutLayout::total + 1024;
+        if ((e = cudaFuncSetAttribute(out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes)) !=
+            cudaSuccess)
+            return e;
+        out_tc_kernel<<<(unsigned)grid, kOutThreads, bytes, stream>>>(a);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace vla

@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
 }  // namespace
 
 bool gates_tc_supported(const FwdParams &p, const ChunkLayout &L) {
-    return p.d == kD && p.io_bf16 && L.CA % kSB == 0 && L.tinv;
+    return p.d == kD && p.io_bf16 && L.CA % kSB == 0 && L.yh;
 }
 
 cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream) {

@@ -214,7 +214,7 @@ bool make_map(CUtensorMap *m, const void *base, int BH, int T) {
 }  // namespace
 
 bool gram_tma_supported(const FwdParams &p, const ChunkLayout &L) {
-    return p.d == kD && p.io_bf16 && L.CA % kSB == 0 && L.tinv && encode_fn() != nullptr;
+    return p.d == kD && p.io_bf16 && L.CA % kSB == 0 && L.yh && encode_fn() != nullptr;
 }
 
 cudaError_t launch_gram_tma(const ChunkArgs &a, cudaStream_t stream) {

@@ -82,9 +82,10 @@ struct ChunkLayout {
     size_t off_P;        // [BH][NC][d][d]  chunk transition P_c
     size_t off_H;        // [BH][NC][d][d]  chunk offset H_c
     size_t off_S;        // [BH][NC][d][d]  chunk-start states S^(c)
-    size_t off_tinv;     // [BH][NC][C/64][2][64][64] bf16: T_inv^T (hi, lo) of every 64-token
-                         // sub-block, written by the tensor-core transition pass for the readout
-    int tinv;            // 1 when the off_tinv region is reserved
+    size_t off_yh;       // [BH][NC][C/64][4][64][64] bf16: readout coefficients y_t, h_t (hi, lo
+                         // operand tiles) of every 64-token sub-block, written by the
+                         // tensor-core state pass for the output pass
+    int yh;              // 1 when the off_yh region is reserved
     size_t total;
 };
 
@@ -95,9 +96,9 @@ long long api_wait_limit_ns();
 int api_cuda_fail(cudaError_t e);
 
 // Layout for a shape; chunk > 0 (a multiple of 16) sets both chunk lengths,
-// chunk == 0 picks the defaults.  tinv reserves the T_inv store of the
-// tensor-core state passes (d = 64, chunks a multiple of 64 tokens).
-ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tinv = false);
+// chunk == 0 picks the defaults.  tc reserves the readout coefficients of
+// the tensor-core state pass (d = 64, chunks a multiple of 64 tokens).
+ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc = false);
 // Chunk-parallel path (six launches).  Returns a cudaError_t.
 cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream);
 
@@ -111,8 +112,9 @@ __device__ __forceinline__ float *ws_f(const ChunkArgs &a, size_t off) {
 }
 
 // Tensor-core state passes (UT transform over 64-token sub-blocks) for d = 64
-// with bf16 I/O and S-chunks a multiple of 64 tokens; mode 0 = chunk
-// transitions (P_c, H_c), mode 1 = readout.  Defined in vla_chunk_tc.cu.
+// with bf16 I/O and S-chunks a multiple of 64 tokens; mode 0 = the state
+// pass (chunk transitions P_c, H_c and the readout coefficients y_t, h_t),
+// mode 1 = the output pass o_t = S^(c) y_t + h_t.  Defined in vla_chunk_tc.cu.
 bool rows_tc_supported(const FwdParams &p, const ChunkLayout &L);
 cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream);
 // Tensor-core gates (block Woodbury over 64-token sub-blocks), same shapes;
