@@ -23,7 +23,7 @@
 // (the residual of token t is its value minus what the earlier tokens of
 // the sub-block left in the state, hence the triangular system).  A
 // sub-block is three rounds of tcgen05.mma plus one triangular inverse on
-// the CUDA cores:
+// the CUDA cores (recursive doubling on the 8 x 8 block structure):
 //   1. D1 = X K^T,  D2 = K Al^T (= N^T),  DO = Phi X^T
 //   2. R = E T_inv  (E = Vals - (X K) diag(1/|k|), T_inv = (I + N)^{-1}),
 //      and Qm^T = Phi Al^T  (Qm = upper-incl(Al^T Phi))
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         }
         tc_fence_before();
         __syncthreads();
-        // ---- T_inv = (I + N)^{-1} (blocked back substitution) ----
+        // ---- T_inv = (I + N)^{-1} (recursive doubling, in place over N) ----
         tri_inv64(ntb, reinterpret_cast<float *>(kb), ti_hi, ti_lo);
         fence_proxy_async_smem();
         __syncthreads();

@@ -220,61 +220,177 @@ __device__ __forceinline__ void eliminate64(const float *ms, float *prow, float 
     }
 }
 
-// T = (I + N)^{-1} for a strictly upper triangular 64 x 64 N, by blocked back
-// substitution: row s of T = e_s - sum_{r > s} N[s][r] T[r].  N is known up
-// front, so no multiplier depends on the result and no step needs a
-// shuffle.  Warp w owns rows 8 w .. 8 w + 7 (lane l columns 2 l, 2 l + 1);
-// blocks run from the last: the owner solves its 8 rows in registers,
-// publishes them (double-buffered), and after one barrier every earlier warp
-// subtracts their contributions.  256 threads; all must call.
-//   ns:   N (fp32, row s, stride kGS)
-//   prow: scratch, 2 x 8 x 64 floats
-//   t_hi, t_lo: out, T as bf16 hi/lo tile pairs, tile row s = row s of T
-//               (an MN-major operand for products with T on the right)
-__device__ __forceinline__ void tri_inv64(const float *ns, float *prow, unsigned char *t_hi, unsigned char *t_lo) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float2 tr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = 8 * warp + i;
-        tr[i] = make_float2(r == 2 * lane ? 1.f : 0.f, r == 2 * lane + 1 ? 1.f : 0.f);
+// One doubling level of tri_inv64: for each pair of consecutive diagonal
+// blocks A, B of size Bk whose inverses T_A, T_B are already in place, the
+// off-diagonal block of the inverse of the pair is T_AB = -T_A N_AB T_B,
+// written over N_AB.  Step 1 forms M = N_AB T_B into scratch, step 2
+// T_AB = -T_A M.  Thread t takes pair t / (8 Bk), row (t / 8) mod Bk and the
+// E = Bk / 8 consecutive columns E (t mod 8); zero entries below the
+// diagonal make every product a full sum (no divergent trip counts).  Four
+// multipliers arrive in one 16-byte load, the rows they scale as float4 /
+// float2 / float.
+template <int E>
+__device__ __forceinline__ void fma_row(float (&acc)[E], float m, const float *row) {
+    if constexpr (E == 4) {
+        const float4 r = *reinterpret_cast<const float4 *>(row);
+        const float2 a = __ffma2_rn(make_float2(m, m), make_float2(r.x, r.y), make_float2(acc[0], acc[1]));
+        const float2 b = __ffma2_rn(make_float2(m, m), make_float2(r.z, r.w), make_float2(acc[2], acc[3]));
+        acc[0] = a.x; acc[1] = a.y; acc[2] = b.x; acc[3] = b.y;
+    } else if constexpr (E == 2) {
+        const float2 r = *reinterpret_cast<const float2 *>(row);
+        const float2 a = __ffma2_rn(make_float2(m, m), r, make_float2(acc[0], acc[1]));
+        acc[0] = a.x; acc[1] = a.y;
+    } else {
+        acc[0] = fmaf(m, row[0], acc[0]);
     }
-#pragma unroll 1
-    for (int b = 7; b >= 0; --b) {
-        float *pb = prow + (b & 1) * 8 * 64;
-        if (warp == b) {
+}
+
+template <int Bk>
+__device__ __forceinline__ void tri_level(float *ts, float *ms) {
+    constexpr int E = Bk / 8;   // columns per thread
+    constexpr int MS = Bk + 4;  // scratch row stride (16-byte rows)
+    const int t = threadIdx.x, j = t / (8 * Bk), i = (t >> 3) % Bk, c0 = E * (t & 7);
+    const int a0 = 2 * j * Bk, b0 = a0 + Bk;
+    float *mj = ms + j * Bk * MS;
+    float acc[E];
 #pragma unroll
-            for (int p = 7; p >= 0; --p) {
-                const float *nr = ns + (8 * b + p) * kGS + 8 * b;  // N[8 b + p][8 b .. 8 b + 7]
-                const float4 n0 = *reinterpret_cast<const float4 *>(nr);
-                const float4 n1 = *reinterpret_cast<const float4 *>(nr + 4);
-                const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+    for (int q = 0; q < E; ++q) acc[q] = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (i <= p) continue;
-                    tr[p] = __ffma2_rn(make_float2(-nv[i], -nv[i]), tr[i], tr[p]);
+    for (int k = 0; k < Bk; k += 4) {
+        const float4 n = *reinterpret_cast<const float4 *>(ts + (a0 + i) * kGS + b0 + k);
+        fma_row<E>(acc, n.x, ts + (b0 + k) * kGS + b0 + c0);
+        fma_row<E>(acc, n.y, ts + (b0 + k + 1) * kGS + b0 + c0);
+        fma_row<E>(acc, n.z, ts + (b0 + k + 2) * kGS + b0 + c0);
+        fma_row<E>(acc, n.w, ts + (b0 + k + 3) * kGS + b0 + c0);
+    }
+#pragma unroll
+    for (int q = 0; q < E; ++q) mj[i * MS + c0 + q] = acc[q];
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < E; ++q) acc[q] = 0.f;
+#pragma unroll
+    for (int k = 0; k < Bk; k += 4) {
+        const float4 ta = *reinterpret_cast<const float4 *>(ts + (a0 + i) * kGS + a0 + k);
+        fma_row<E>(acc, ta.x, mj + k * MS + c0);
+        fma_row<E>(acc, ta.y, mj + (k + 1) * MS + c0);
+        fma_row<E>(acc, ta.z, mj + (k + 2) * MS + c0);
+        fma_row<E>(acc, ta.w, mj + (k + 3) * MS + c0);
+    }
+#pragma unroll
+    for (int q = 0; q < E; ++q) ts[(a0 + i) * kGS + b0 + c0 + q] = -acc[q];
+    __syncthreads();
+}
+
+// The same level with 4 x 4 register blocks (used for Bk = 32, where the
+// products are large enough to pay for the idle warps): thread t <
+// (32 / Bk) (Bk / 4)^2 takes pair t / (Bk / 4)^2, rows 4 rg .. 4 rg + 3 and
+// columns 4 cg .. 4 cg + 3 (cg fastest, so a quarter-warp reads one row of the
+// right operand and broadcasts the left one) over the full sum; the other
+// threads only join the barriers.
+template <int Bk>
+__device__ __forceinline__ void tri_level_blk(float *ts, float *ms) {
+    constexpr int G = Bk / 4;       // row / column groups per block
+    constexpr int MS = Bk + 4;      // scratch row stride (16-byte rows)
+    const int t = threadIdx.x;
+    const bool act = t < (32 / Bk) * G * G;
+    const int j = t / (G * G), rg = (t / G) % G, cg = t % G;
+    const int a0 = 2 * j * Bk, b0 = a0 + Bk, r0 = 4 * rg, c0 = 4 * cg;
+    float *mj = ms + j * Bk * MS;
+    float2 acc[4][2];
+    if (act) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < Bk; k += 4) {
+            float4 n[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) n[r] = *reinterpret_cast<const float4 *>(ts + (a0 + r0 + r) * kGS + b0 + k);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 tb = *reinterpret_cast<const float4 *>(ts + (b0 + k + kk) * kGS + b0 + c0);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float m = kk == 0 ? n[r].x : kk == 1 ? n[r].y : kk == 2 ? n[r].z : n[r].w;
+                    acc[r][0] = __ffma2_rn(make_float2(m, m), make_float2(tb.x, tb.y), acc[r][0]);
+                    acc[r][1] = __ffma2_rn(make_float2(m, m), make_float2(tb.z, tb.w), acc[r][1]);
                 }
             }
-#pragma unroll
-            for (int p = 0; p < 8; ++p) *reinterpret_cast<float2 *>(pb + p * 64 + 2 * lane) = tr[p];
         }
-        __syncthreads();
-        if (warp < b) {
-            float2 pr[8];
 #pragma unroll
-            for (int p = 0; p < 8; ++p) pr[p] = *reinterpret_cast<const float2 *>(pb + p * 64 + 2 * lane);
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4 *>(mj + (r0 + r) * MS + c0) =
+                make_float4(acc[r][0].x, acc[r][0].y, acc[r][1].x, acc[r][1].y);
+    }
+    __syncthreads();
+    if (act) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float *nr = ns + (8 * warp + i) * kGS + 8 * b;  // N[8 warp + i][8 b .. 8 b + 7]
-                const float4 n0 = *reinterpret_cast<const float4 *>(nr);
-                const float4 n1 = *reinterpret_cast<const float4 *>(nr + 4);
-                const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+        for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int p = 0; p < 8; ++p) tr[i] = __ffma2_rn(make_float2(-nv[p], -nv[p]), pr[p], tr[i]);
+        for (int k = 0; k < Bk; k += 4) {
+            float4 ta[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) ta[r] = *reinterpret_cast<const float4 *>(ts + (a0 + r0 + r) * kGS + a0 + k);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 mk = *reinterpret_cast<const float4 *>(mj + (k + kk) * MS + c0);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float m = kk == 0 ? ta[r].x : kk == 1 ? ta[r].y : kk == 2 ? ta[r].z : ta[r].w;
+                    acc[r][0] = __ffma2_rn(make_float2(m, m), make_float2(mk.x, mk.y), acc[r][0]);
+                    acc[r][1] = __ffma2_rn(make_float2(m, m), make_float2(mk.z, mk.w), acc[r][1]);
+                }
             }
         }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4 *>(ts + (a0 + r0 + r) * kGS + b0 + c0) =
+                make_float4(-acc[r][0].x, -acc[r][0].y, -acc[r][1].x, -acc[r][1].y);
     }
-    __syncthreads();  // every read of ns is done (the output may alias it)
+    __syncthreads();
+}
+
+// T = (I + N)^{-1} for a strictly upper triangular 64 x 64 N by recursive
+// doubling on the block structure: the inverse of [[I + N_A, N_AB], [0,
+// I + N_B]] is [[T_A, -T_A N_AB T_B], [0, T_B]].  Each warp first inverts
+// its own 8 x 8 diagonal block (lane c < 8 solves column c by back
+// substitution, no barrier), then three levels join pairs of blocks
+// 8 -> 16 -> 32 -> 64 with small products spread over all threads.  T is
+// built in place over N.  256 threads; all must call.
+//   ns:   in N, then T (fp32, row s, stride kGS; below-diagonal entries zero)
+//   ms:   scratch, 32 x 36 floats (16-byte aligned)
+//   t_hi, t_lo: out, T as bf16 hi/lo tile pairs, tile row s = row s of T
+//               (an MN-major operand for products with T on the right); may
+//               alias ns
+__device__ __forceinline__ void tri_inv64(float *ns, float *ms, unsigned char *t_hi, unsigned char *t_lo) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    {   // diagonal block 8 warp .. 8 warp + 7: column c = lane of its inverse
+        const int c = lane & 7;
+        float col[8];
+#pragma unroll
+        for (int r = 7; r >= 0; --r) {
+            const float4 n0 = *reinterpret_cast<const float4 *>(ns + (8 * warp + r) * kGS + 8 * warp);
+            const float4 n1 = *reinterpret_cast<const float4 *>(ns + (8 * warp + r) * kGS + 8 * warp + 4);
+            const float nr[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+            float acc = (r == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int k = 7; k > r; --k) acc = fmaf(-nr[k], col[k], acc);  // col[r + 1] (the latest) last
+            col[r] = acc;
+        }
+        __syncwarp();  // every lane has read the block's N before it is overwritten
+        if (lane < 8) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) ns[(8 * warp + r) * kGS + 8 * warp + c] = col[r];
+        }
+    }
+    __syncthreads();
+    tri_level<8>(ns, ms);
+    tri_level<16>(ns, ms);
+    tri_level_blk<32>(ns, ms);
+    // rows 8 warp + i, columns 2 lane, 2 lane + 1, as bf16 hi/lo
+    float2 tr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tr[i] = *reinterpret_cast<const float2 *>(ns + (8 * warp + i) * kGS + 2 * lane);
+    __syncthreads();  // the output may alias ns
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = 8 * warp + i;
