@@ -6,7 +6,8 @@
 // Transformers"), and of the readout's n_t (section 2.3).
 //
 // Tiles of 64 tokens of u and k arrive by TMA tensor copies
-// (cp.async.bulk.tensor) in the 128-byte swizzle, four stages deep.  The
+// (cp.async.bulk.tensor) in the 128-byte swizzle, four stages deep (a stage
+// is refilled one iteration after its product was issued).  The
 // token-major u tile is both operands of the product, read MN-major (tile
 // rows = K = tokens), so no transposition is needed; bf16 x bf16 products
 // are exact in fp32 and only the accumulation (in TMEM) rounds.  Two
@@ -27,9 +28,10 @@ constexpr int kStages = 4;
 struct GrLayout {
     static constexpr size_t ctrl = 0;                     // full[4], done[4] mbarriers, TMEM slot, abort flag
     static constexpr size_t tiles = 1024;                 // [stage]: u tile, k tile (8 KB each)
-    static constexpr size_t nred = tiles + (size_t)kStages * 2 * kTile;  // [128 threads][33] fp32
-    static constexpr size_t total = nred + 128 * 33 * 4;
+    static constexpr size_t nred = tiles;                 // [128 threads][33] fp32, over the tiles once all are used
+    static constexpr size_t total = tiles + (size_t)kStages * 2 * kTile;
 };
+static_assert(128 * 33 * 4 <= kStages * 2 * kTile, "the reduction buffer fits over the tiles");
 
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
     asm volatile(
@@ -77,7 +79,7 @@ __global__ void __launch_bounds__(kGThreads) gram_tma_kernel(ChunkArgs a, const 
         tma_load_3d(su(b), &tm_u, 0, t0 + st * kSB, bh, &full[b]);
         tma_load_3d(sk(b), &tm_k, 0, t0 + st * kSB, bh, &full[b]);
     };
-    int issued = 0, committed = 0;
+    int issued = 0, committed = 0, landed = 0;  // (thread 0's bookkeeping)
     if (tid == 0) {
         for (int st = 0; st < kStages && st < nst; ++st) issue(st);
         issued = min(kStages, nst);
@@ -91,7 +93,10 @@ __global__ void __launch_bounds__(kGThreads) gram_tma_kernel(ChunkArgs a, const 
     bool ok = true;
     for (int st = 0; st < nst; ++st) {
         const int b = st % kStages;
-        if (!mbar_wait_bounded(&full[b], (uint32_t)((st / kStages) & 1), a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+        if (!mbar_wait_bounded(&full[b], (uint32_t)((st / kStages) & 1), a.p.wait_limit_ns, a.p.err))
+            *abort_flag = 1;
+        else
+            landed = st + 1;
         __syncthreads();
         if (*abort_flag) {
             ok = false;
@@ -120,13 +125,15 @@ __global__ void __launch_bounds__(kGThreads) gram_tma_kernel(ChunkArgs a, const 
             }
         }
         __syncthreads();  // everyone is done with the k tile
-        if (tid == 0 && st + kStages < nst) {
-            // the u tile is free once its product completed
-            if (!mbar_wait_bounded(&done[b], (uint32_t)((st / kStages) & 1), a.p.wait_limit_ns, a.p.err)) {
+        // refill the previous tile's stage: its product was issued an iteration
+        // ago (waiting on it does not stall on the one just issued)
+        if (tid == 0 && st >= 1 && st + kStages - 1 < nst) {
+            const int sp = st - 1;
+            if (!mbar_wait_bounded(&done[sp % kStages], (uint32_t)((sp / kStages) & 1), a.p.wait_limit_ns, a.p.err)) {
                 *abort_flag = 1;
             } else {
-                issue(st + kStages);
-                issued = st + kStages + 1;
+                issue(sp + kStages);
+                issued = sp + kStages + 1;
             }
         }
     }
@@ -140,10 +147,12 @@ __global__ void __launch_bounds__(kGThreads) gram_tma_kernel(ChunkArgs a, const 
     tc_fence_after();
     if (!ok || *abort_flag) {
         if (tid == 0) {  // let everything issued land before the CTA exits
-            for (int st = max(0, committed - kStages); st < committed; ++st)
-                (void)mbar_wait_bounded(&done[st % kStages], (uint32_t)((st / kStages) & 1), a.p.wait_limit_ns,
+            if (committed > 0) {  // (a commit covers every earlier product)
+                const int l = committed - 1;
+                (void)mbar_wait_bounded(&done[l % kStages], (uint32_t)((l / kStages) & 1), a.p.wait_limit_ns,
                                         a.p.err);
-            for (int st = committed; st < issued; ++st)
+            }
+            for (int st = landed; st < issued; ++st)
                 (void)mbar_wait_bounded(&full[st % kStages], (uint32_t)((st / kStages) & 1), a.p.wait_limit_ns,
                                         a.p.err);
         }
