@@ -980,6 +980,9 @@ __global__ void __launch_bounds__(RowsCfg<D, MODE>::NT) rows_kernel(ChunkArgs a)
 // Rows of S per chain CTA: few rows per CTA keep each step a single short dot
 // product per thread (one or two outputs), with many CTAs walking the chain
 // side by side; every CTA of a (b, h) reads the same chunk maps (L2 hits).
+// At d = 64 a thread instead applies one column of P_c to all 4 rows over a
+// quarter of the sum (each P element is read once, the rows of S broadcast),
+// and the four partial sums meet in shared memory.
 template <int D>
 constexpr int chain_rows() { return D == 32 ? 8 : 4; }
 
@@ -991,7 +994,8 @@ struct ChainSmem {
     static constexpr size_t P = 128;                                 // [NS][D][D]
     static constexpr size_t H = P + NS * (size_t)D * D * 4;          // [NS][RB][D]
     static constexpr size_t S = H + NS * (size_t)RB * D * 4;         // [RB][D]
-    static constexpr size_t total = S + (size_t)RB * D * 4;
+    static constexpr size_t red = S + (size_t)RB * D * 4;            // (d = 64) [4 quarters][RB][D] partial sums
+    static constexpr size_t total = red + (D == 64 ? 4 * (size_t)RB * D * 4 : 0);
 };
 
 template <int D>
@@ -1053,14 +1057,45 @@ __global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
         const float *P = sP + (size_t)buf * D * D;
         const float *Hh = sH + (size_t)buf * kRB * D;
         float acc[OPT];
+        if constexpr (D == 64) {
+            // column jj of P_c on all 4 rows, over the quarter k in [16 kq, 16 kq + 16)
+            float *red = reinterpret_cast<float *>(smem + Lo::red);
+            const int kq = tid >> 6, jj = tid & 63;
+            float part[kRB];
 #pragma unroll
-        for (int q = 0; q < OPT; ++q) acc[q] = Hh[r * D + j0 + q];
-        const float *srow = sS + r * D;
+            for (int q = 0; q < kRB; ++q) part[q] = 0.f;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int k0 = 16 * kq + 4 * g;
+                float4 sv[kRB];
+#pragma unroll
+                for (int q = 0; q < kRB; ++q) sv[q] = *reinterpret_cast<const float4 *>(sS + q * D + k0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const float pv = P[(k0 + kk) * D + jj];
+#pragma unroll
+                    for (int q = 0; q < kRB; ++q) {
+                        const float sk = kk == 0 ? sv[q].x : kk == 1 ? sv[q].y : kk == 2 ? sv[q].z : sv[q].w;
+                        part[q] = fmaf(sk, pv, part[q]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kRB; ++q) red[(kq * kRB + q) * D + jj] = part[q];
+            __syncthreads();
+            acc[0] = Hh[r * D + j0];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) acc[0] += red[(h * kRB + r) * D + j0];
+        } else {
+#pragma unroll
+            for (int q = 0; q < OPT; ++q) acc[q] = Hh[r * D + j0 + q];
+            const float *srow = sS + r * D;
 #pragma unroll 8
-        for (int k = 0; k < D; ++k) {
-            const float sk = srow[k];
+            for (int k = 0; k < D; ++k) {
+                const float sk = srow[k];
 #pragma unroll
-            for (int q = 0; q < OPT; ++q) acc[q] = fmaf(sk, P[k * D + j0 + q], acc[q]);
+                for (int q = 0; q < OPT; ++q) acc[q] = fmaf(sk, P[k * D + j0 + q], acc[q]);
+            }
         }
         __syncthreads();  // everyone done reading sS and this buffer
 #pragma unroll
