@@ -49,8 +49,8 @@ TRAFFIC = {
     # profiles/seq_kernel_long.md: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
     ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
     # profiles/chunk_tc_long.md: at T=16384 (same 16 heads), scaled x4 to T=65536
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (75.316736e6 + 16.904192e6), "src_sha": "685ab36485c7918b"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.224512e6 + 102.653952e6), "src_sha": "685ab36485c7918b"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (75.313664e6 + 17.085184e6), "src_sha": "918bfd7865dc27c5"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.54656e6 + 99.970816e6), "src_sha": "918bfd7865dc27c5"},
 }
 
 
