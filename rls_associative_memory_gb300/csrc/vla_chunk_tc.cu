@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     for (int j = 0; j < 32; ++j) x[j] = (xrow - 64 == 32 * hw + j) ? 1.f : 0.f;
     put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
 
-    // Inputs of the next sub-block, prefetched into registers (token pt,
-    // features 16 pq .. 16 pq + 15).
+    // Inputs of the next sub-block, prefetched into registers during rounds
+    // 2-3 of the current one (token pt, features 16 pq .. 16 pq + 15).
     uint4 rk[2], rv[2], rq[2];
     float4 ra[4];
     // (always a valid token row, clamped: no select waits on the loads here;
@@ -265,7 +265,6 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             dp += __shfl_xor_sync(0xffffffffu, dp, 16);
             if (pq == 0) s_rden[pt] = 1.f / (dp + kEps);
         }
-        load_in(sb + 1);
         if (!round_wait()) {
             ok = false;
             break;
@@ -313,6 +312,9 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                                     smem_u32(al_lo), id_64, false);
             umma_commit(bar);
         }
+        // the next sub-block's inputs: issued here, after the inverse, so that
+        // their registers are not live through it (rounds 2-3 hide the latency)
+        load_in(sb + 1);
         if (!round_wait()) {
             ok = false;
             break;

@@ -212,7 +212,6 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             mma_k64<false, false>(tbase + col_d1, smem_u32(uk), smem_u32(a_lo), idesc_bf16_f32(128, 64), true);
             umma_commit(bar);
         }
-        load_in(sb + 1);
         if (!round_wait()) {
             ok = false;
             break;
@@ -275,6 +274,9 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
                                    idesc_bf16_f32(64, 128), false, 16, kTile);
             umma_commit(bar);
         }
+        // the next sub-block's inputs: issued after the elimination, so that their
+        // registers are not live through it (rounds 3-4 hide the latency)
+        load_in(sb + 1);
         if (!round_wait()) {
             ok = false;
             break;
