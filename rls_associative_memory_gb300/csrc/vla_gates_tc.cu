@@ -107,9 +107,11 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     // ---- A at the chunk start ----
     // c > 0: A = (M^(c))^{-1} = L^{-T} D^{-1} L^{-1}: elimination of M^(c),
     // then one product E^T (diag(1/D) E) on the tensor cores.  c = 0: A0 or
-    // I / lambda0 as given.
-    float am[32];  // A[r64][32 hw .. 32 hw + 31]
+    // I / lambda0 as given.  A stays in fp32 in the TMEM columns of D5 (rows
+    // in the M = 64 lane layout) for the whole chunk: each sub-block's last
+    // product accumulates onto it.
     {
+        float am[32];  // A[r64][32 hw .. 32 hw + 31]
         const int gr = tid >> 2, gp = tid & 3;
         const float *src = nullptr;
         if (c > 0) src = ws_f(a, a.L.off_M) + ((size_t)bh * NCA + c) * kD * kD;
@@ -151,6 +153,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) am[j] = (32 * hw + j == r64) ? il : 0.f;
             }
+            tmem_st32(tq + col_d5 + 32 * hw, am);
+            tc_fence_before();
         }
         __syncthreads();
         if (act64) put_row32(a_hi, a_lo, r64, 32 * hw, am);
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             ok = false;
             break;
         }
-        // ---- Z^T, (beta Z)^T and E' tiles (rows s) ----
+        // ---- Z^T, -(beta Z)^T and E' tiles (rows s) ----
         {
             float v[32];
             tmem_ld32(tq + col_d2 + 32 * hw, v);  // z_s[i], i = 32 hw ..
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             if (act64) {
                 put_row32(zt_hi, zt_lo, r64, 32 * hw, v);
 #pragma unroll
-                for (int m = 0; m < 32; ++m) v[m] *= bs;
+                for (int m = 0; m < 32; ++m) v[m] *= -bs;
                 put_row32(bz_hi, bz_lo, r64, 32 * hw, v);
             }
             tmem_ld32(tq + col_d2 + 64 + 32 * hw, v);  // P[s][t] = z_s . k_hat_t, t = 32 hw ..
@@ -311,14 +315,14 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- R4: D1[k rows] += E'^T Z^T (A MN-major, atoms [(beta Z)^T | E']: M = 128,
-        // the first 64 rows land in D1's dead W rows); D5 = (Z diag(beta)) Z^T ----
+        // ---- R4: D1[k rows] += E'^T Z^T (A MN-major, atoms [-(beta Z)^T | E']: M = 128,
+        // the first 64 rows land in D1's dead W rows); A += -(Z diag(beta)) Z^T ----
         if (tid == 0) {
             tc_fence_after();
             mma_k64x3<true, true>(tbase + col_d1, smem_u32(bz_hi), smem_u32(bz_lo), smem_u32(zt_hi), smem_u32(zt_lo),
                                   idesc_bf16_f32(128, 64), true, kTile, 16);
             mma_k64x3<true, true>(tbase + col_d5, smem_u32(bz_hi), smem_u32(bz_lo), smem_u32(zt_hi), smem_u32(zt_lo),
-                                  idesc_bf16_f32(64, 64), false);
+                                  idesc_bf16_f32(64, 64), true);
             umma_commit(bar);
         }
         if (!round_wait()) {
@@ -337,12 +341,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
                 s_nrm[hw * 64 + t] = sq;
             }
             float v[32];
-            tmem_ld32(tq + col_d5 + 32 * hw, v);  // (Z diag(beta) Z^T)[r64][32 hw ..]
-            if (act64) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) am[j] -= v[j];
-                put_row32(a_hi, a_lo, r64, 32 * hw, am);
-            }
+            tmem_ld32(tq + col_d5 + 32 * hw, v);  // the updated A[r64][32 hw ..]
+            if (act64) put_row32(a_hi, a_lo, r64, 32 * hw, v);
             tc_fence_before();
             fence_proxy_async_smem();
             __syncthreads();
@@ -359,10 +359,14 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     }
     if (!ok) {
         if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
-    } else if (c == NCA - 1 && act64) {
-        float4 *dA = reinterpret_cast<float4 *>(a.p.A_T + (size_t)bh * kD * kD + (size_t)r64 * kD + 32 * hw);
+    } else if (c == NCA - 1) {
+        float am[32];
+        tmem_ld32(tq + col_d5 + 32 * hw, am);
+        if (act64) {
+            float4 *dA = reinterpret_cast<float4 *>(a.p.A_T + (size_t)bh * kD * kD + (size_t)r64 * kD + 32 * hw);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) dA[q] = make_float4(am[4 * q], am[4 * q + 1], am[4 * q + 2], am[4 * q + 3]);
+            for (int q = 0; q < 8; ++q) dA[q] = make_float4(am[4 * q], am[4 * q + 1], am[4 * q + 2], am[4 * q + 3]);
+        }
     }
     tc_fence_before();
     __syncthreads();
