@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     load_in(0);
     for (int sb = 0; sb < nsb; ++sb) {
         const int nt = min(kSB, ntok - sb * kSB);
-        float fq[16], fk[16];
+        float fq[16];
         // ---- stage the sub-block's operands ----
         if (pt >= nt) {  // past the chunk: zero inputs
             rk[0] = rk[1] = rv[0] = rv[1] = rq[0] = rq[1] = make_uint4(0, 0, 0, 0);
@@ -209,7 +209,29 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             split8(fq + 8, h4, l4);
             *reinterpret_cast<uint4 *>(ph_hi + toff(pt, 16 * pq + 8)) = h4;
             *reinterpret_cast<uint4 *>(ph_lo + toff(pt, 16 * pq + 8)) = l4;
-            // phi(k_hat): inclusive scan over this warp's 8 tokens (adjacent lanes)
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // ---- round 1: D1 = X K^T, D2 = K Al^T, DO = Phi X^T ----
+        if (tid == 0) {
+            tc_fence_after();
+            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x, false);
+            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x, true);
+            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
+            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
+            mma_k64x3<false, false>(tbase + col_do, smem_u32(ph_hi), smem_u32(ph_lo), smem_u32(xs_hi),
+                                    smem_u32(xs_lo), id_do, false);
+            umma_commit(bar);
+        }
+        // ---- readout denominators 1 / (phi(q_t) . n_t + eps), while round 1 runs ----
+        // phi(k_hat) of token pt (the raw keys from the K tile), scanned over this
+        // warp's 8 tokens (adjacent lanes)
+        float fk[16];
+        {
+            float kf[16];
+            unpack8(*reinterpret_cast<const uint4 *>(kb + toff(pt, 16 * pq)), kf);
+            unpack8(*reinterpret_cast<const uint4 *>(kb + toff(pt, 16 * pq + 8)), kf + 8);
+            const float ksc = s_ks[pt];
 #pragma unroll
             for (int m = 0; m < 16; ++m) fk[m] = pt < nt ? phi_fast(kf[m] * ksc) : 0.f;
 #pragma unroll
@@ -226,20 +248,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                 for (int h = 0; h < 4; ++h) dst[h] = make_float4(fk[4 * h], fk[4 * h + 1], fk[4 * h + 2], fk[4 * h + 3]);
             }
         }
-        fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 1: D1 = X K^T, D2 = K Al^T, DO = Phi X^T ----
-        if (tid == 0) {
-            tc_fence_after();
-            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x, false);
-            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x, true);
-            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
-            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
-            mma_k64x3<false, false>(tbase + col_do, smem_u32(ph_hi), smem_u32(ph_lo), smem_u32(xs_hi),
-                                    smem_u32(xs_lo), id_do, false);
-            umma_commit(bar);
-        }
-        // ---- readout denominators 1 / (phi(q_t) . n_t + eps) ----
         if (tid < 64) {  // per feature: n before each warp's tokens, and n after the sub-block
             float run = s_nrun[tid];
 #pragma unroll
