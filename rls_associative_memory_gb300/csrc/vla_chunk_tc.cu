@@ -21,15 +21,18 @@
 //   X_t phi(q_t) = X phi(q_t) + sum_{s <= t} r_s (alpha_s . phi(q_t))
 // where R = [r_1 .. r_c] holds the per-token residuals value_t - X_{t-1} k_hat_t
 // (the residual of token t is its value minus what the earlier tokens of
-// the sub-block left in the state, hence the triangular system).  A
-// sub-block is three rounds of tcgen05.mma plus one triangular inverse on
-// the CUDA cores (recursive doubling on the 8 x 8 block structure):
-//   1. D1 = X K^T,  D2 = K Al^T (= N^T),  DO = Phi X^T
+// the sub-block left in the state, hence the triangular system).  The
+// readout numerators are kept transposed, DO^T (rows = the 128 state rows,
+// columns = tokens), so that every product of a round shares its left
+// operand and the round is one wide product.  A sub-block is three rounds
+// of tcgen05.mma plus one triangular inverse on the CUDA cores (recursive
+// doubling on the 8 x 8 block structure):
+//   1. [DO^T | D1] = X [Phi; K]^T  (N = 128),  D2 = K Al^T (= N^T)
 //   2. R = E T_inv  (E = Vals - (X K) diag(1/|k|), T_inv = (I + N)^{-1}),
-//      and Qm^T = Phi Al^T  (Qm = upper-incl(Al^T Phi))
-//   3. X += R Al^T,  DO += Qm^T R^T
-// DO holds the readout numerators token-major (rows = tokens; columns = the
-// 128 state rows, h_t then y_t, before the division by den_t).
+//      and Qm = Al Phi^T  (upper-incl: Qm[s][t] = alpha_s . phi(q_t), s <= t)
+//   3. [X | DO^T] += R [Al | Qm]  (M = N = 128, accumulated in place)
+// X stays in fp32 in TMEM for the whole chunk; its bf16 hi/lo tiles are
+// rebuilt for each round 1.
 //
 // Precision: fp32 operands enter the tensor cores as bf16 pairs
 // x = hi + lo (hi = bf16(x), lo = bf16(x - hi)), and a product takes
@@ -50,21 +53,25 @@ struct TcLayout {
     // X / E / R tiles: 128 rows (0..63 the H rows, 64..127 the P rows), hi then lo
     static constexpr size_t xs_hi = 1024;
     static constexpr size_t xs_lo = xs_hi + 2 * kTile;
-    static constexpr size_t al_hi = xs_hi + 4 * kTile;       // gates (token rows), hi, lo
+    // gates (token rows) hi, lo; then the T_inv tiles, later Qm: [Al | Qm] is
+    // round 3's right operand, two MN-major atoms 16 KB apart
+    static constexpr size_t al_hi = xs_hi + 4 * kTile;
     static constexpr size_t al_lo = al_hi + kTile;
-    static constexpr size_t kb = al_hi + 2 * kTile;          // K (raw bf16, token rows)
-    static constexpr size_t ph_hi = kb + kTile;              // Phi = phi(Q) (token rows), then Qm^T; hi, lo
-    static constexpr size_t ph_lo = ph_hi + kTile;
-    static constexpr size_t ti = ph_hi + 2 * kTile;          // N fp32 (row stride kGS), then T_inv hi, lo
+    static constexpr size_t ti = al_hi + 2 * kTile;          // N fp32 (row stride kGS), then T_inv hi, lo, then Qm
+    static constexpr uint32_t kAtom = 2 * kTile;             // Al -> Qm distance
+    static constexpr size_t ph_hi = ti + 18 * 1024;          // Phi = phi(Q) hi, directly followed by
+    static constexpr size_t kb = ph_hi + kTile;              // K (raw bf16): [Phi_hi; K] is one 128-row operand
+    static constexpr size_t ph_lo = kb + kTile;              // Phi lo
     static constexpr int kVS = 72;                           // row stride (bf16) of the v tile
-    static constexpr size_t vt = ti + (size_t)64 * kGS * 4;  // v [t][i] bf16
+    static constexpr size_t vt = ph_lo + kTile;              // v [t][i] bf16
     static constexpr size_t ks = vt + (size_t)64 * kVS * 2;  // [64] 1 / max(|k|, eps)
     static constexpr size_t rden = ks + 256;                 // [64] 1 / (phi(q).n + eps)
     static constexpr size_t tot = rden + 256;                // [8][64] warp totals of phi(k_hat), then prefixes
     static constexpr size_t nrun = tot + 8 * 64 * 4;         // [64] n at the sub-block start
     static constexpr size_t total = nrun + 256;
 };
-static_assert(TcLayout::ti % 1024 == 0, "T_inv tiles must be 1024-byte aligned");
+static_assert(TcLayout::ti % 1024 == 0 && TcLayout::ph_hi % 1024 == 0, "operand tiles must be 1024-byte aligned");
+static_assert(TcLayout::ti + (size_t)64 * kGS * 4 <= TcLayout::ph_hi, "N fits before Phi");
 
 __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     using L = TcLayout;
@@ -78,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     unsigned char *kb = smem + L::kb, *ph_hi = smem + L::ph_hi, *ph_lo = smem + L::ph_lo;
     unsigned char *al_hi = smem + L::al_hi, *al_lo = smem + L::al_lo;
     float *ntb = reinterpret_cast<float *>(smem + L::ti);  // N, row stride kGS
-    unsigned char *ti_hi = smem + L::ti, *ti_lo = smem + L::ti + kTile;  // T_inv, tile row s = row s
+    unsigned char *ti_hi = smem + L::ti, *ti_lo = smem + L::ti + kTile;  // T_inv (tile row s = row s), then Qm
     __nv_bfloat16 *vt = reinterpret_cast<__nv_bfloat16 *>(smem + L::vt);
     float *s_ks = reinterpret_cast<float *>(smem + L::ks);
     float *s_rden = reinterpret_cast<float *>(smem + L::rden);
@@ -98,7 +105,8 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.p.v) + tok0;
     const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.p.q) + tok0;
     const float *gal = ws_f(a, a.L.off_alpha) + tok0;
-    // this chunk's readout coefficients: per sub-block [y hi | y lo | h hi | h lo] (token rows)
+    // this chunk's readout coefficients: per sub-block [y hi | y lo | h hi | h lo],
+    // tile row = state row (feature), columns = tokens
     unsigned char *gyh = static_cast<unsigned char *>(a.p.ws) + a.L.off_yh +
                          (size_t)(bh * NC + c) * (C / kSB) * (4 * kTile);
 
@@ -115,14 +123,22 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     tc_fence_after();
     const uint32_t tbase = *tslot;
     const uint32_t tq = tbase + ((uint32_t)(32 * qw) << 16);  // this warp's lane quarter
+    constexpr uint32_t col_x = 0;     // X (fp32 state, M = 128 rows)
+    constexpr uint32_t col_do = 64;   // DO^T (state rows x tokens), next to X and to D1
+    constexpr uint32_t col_d1 = 128;  // D1 = X K^T, then R
+    constexpr uint32_t col_d2 = 192;  // D2 = N^T, then Qm
 
-    // State row held in registers: row 32 qw + lane of [H; P], the 32 columns
-    // 32 hw .. this thread reads back from TMEM (M = 128).  H starts at 0, P at I.
+    // State row 32 qw + lane of [H; P], columns 32 hw .. (H starts at 0, P at I):
+    // into TMEM and, as hi/lo tiles, into the first round's operand.
     const int xrow = 32 * qw + lane;
-    float x[32];
+    {
+        float x[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = (xrow - 64 == 32 * hw + j) ? 1.f : 0.f;
-    put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
+        for (int j = 0; j < 32; ++j) x[j] = (xrow - 64 == 32 * hw + j) ? 1.f : 0.f;
+        tmem_st32(tq + col_x + 32 * hw, x);
+        put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
+        tc_fence_before();  // (the first round accumulates onto X after a barrier)
+    }
 
     // Inputs of the next sub-block, prefetched into registers during rounds
     // 2-3 of the current one (token pt, features 16 pq .. 16 pq + 15).
@@ -152,13 +168,10 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         tc_fence_after();
         return *abort_flag == 0;
     };
-    constexpr uint32_t id_x = idesc_bf16_f32(128, 64);   // products with the 128 state rows
+    constexpr uint32_t id_xw = idesc_bf16_f32(128, 128);  // the 128 state rows x 128 columns
+    constexpr uint32_t id_x = idesc_bf16_f32(128, 64);
     constexpr uint32_t id_64 = idesc_bf16_f32(64, 64);
-    constexpr uint32_t id_do = idesc_bf16_f32(64, 128);  // token rows x the 128 state rows
     constexpr int kVS = L::kVS;
-    constexpr uint32_t col_d4 = 0;    // D1 = X K^T, then Qm^T, then D4 = R Al^T
-    constexpr uint32_t col_d2 = 64;   // D2 = N^T, then D3 = R
-    constexpr uint32_t col_do = 128;  // readout numerators, token rows (128 columns)
 
     bool ok = true;
     load_in(0);
@@ -212,15 +225,15 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         }
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 1: D1 = X K^T, D2 = K Al^T, DO = Phi X^T ----
+        // ---- round 1: [DO^T | D1] = X [Phi; K]^T, D2 = K Al^T ----
         if (tid == 0) {
             tc_fence_after();
-            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_hi), smem_u32(kb), id_x, false);
-            mma_k64<false, false>(tbase + col_d4, smem_u32(xs_lo), smem_u32(kb), id_x, true);
+            // hi.hi and lo.hi for both (K is exact), then hi.lo for the Phi part
+            mma_k64<false, false>(tbase + col_do, smem_u32(xs_hi), smem_u32(ph_hi), id_xw, false);
+            mma_k64<false, false>(tbase + col_do, smem_u32(xs_lo), smem_u32(ph_hi), id_xw, true);
+            mma_k64<false, false>(tbase + col_do, smem_u32(xs_hi), smem_u32(ph_lo), id_x, true);
             mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
             mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
-            mma_k64x3<false, false>(tbase + col_do, smem_u32(ph_hi), smem_u32(ph_lo), smem_u32(xs_hi),
-                                    smem_u32(xs_lo), id_do, false);
             umma_commit(bar);
         }
         // ---- readout denominators 1 / (phi(q_t) . n_t + eps), while round 1 runs ----
@@ -291,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                     ntb[sr * kGS + t] = sr < t ? v[m] * kt : 0.f;
                 }
             }
-            tmem_ld32(tq + col_d4 + 32 * hw, v);  // X K, columns 32 hw ..
+            tmem_ld32(tq + col_d1 + 32 * hw, v);  // X K, columns 32 hw ..
             const float4 *ks4 = reinterpret_cast<const float4 *>(s_ks + 32 * hw);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -312,13 +325,13 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         tri_inv64(ntb, reinterpret_cast<float *>(kb), ti_hi, ti_lo);
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 2: R = E T_inv, Qm^T = Phi Al^T ----
+        // ---- round 2: R = E T_inv, Qm = Al Phi^T ----
         if (tid == 0) {
             tc_fence_after();
-            mma_k64x3<false, true>(tbase + col_d2, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi),
+            mma_k64x3<false, true>(tbase + col_d1, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(ti_hi),
                                    smem_u32(ti_lo), id_x, false);
-            mma_k64x3<false, false>(tbase + col_d4, smem_u32(ph_hi), smem_u32(ph_lo), smem_u32(al_hi),
-                                    smem_u32(al_lo), id_64, false);
+            mma_k64x3<false, false>(tbase + col_d2, smem_u32(al_hi), smem_u32(al_lo), smem_u32(ph_hi),
+                                    smem_u32(ph_lo), id_64, false);
             umma_commit(bar);
         }
         // the next sub-block's inputs: issued here, after the inverse, so that
@@ -328,30 +341,28 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             ok = false;
             break;
         }
-        // ---- R tiles; Qm^T tiles over Phi (round 2 has read it) ----
+        // ---- R tiles; Qm tiles over T_inv (round 2 has read it) ----
         {
             float v[32];
-            tmem_ld32(tq + col_d2 + 32 * hw, v);
+            tmem_ld32(tq + col_d1 + 32 * hw, v);
             put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
-            tmem_ld32(tq + col_d4 + 32 * hw, v);  // Qm^T row t = 16 qw + lane, columns s = 32 hw ..
+            tmem_ld32(tq + col_d2 + 32 * hw, v);  // Qm row s = 16 qw + lane, columns t = 32 hw ..
             if (lane < 16) {
-                const int t = 16 * qw + lane;
+                const int srow = 16 * qw + lane;
 #pragma unroll
                 for (int m = 0; m < 32; ++m)
-                    if (32 * hw + m > t) v[m] = 0.f;
-                put_row32(ph_hi, ph_lo, t, 32 * hw, v);
+                    if (32 * hw + m < srow) v[m] = 0.f;
+                put_row32(ti_hi, ti_lo, srow, 32 * hw, v);
             }
         }
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- round 3: X += R Al^T, DO += Qm^T R^T ----
+        // ---- round 3: [X | DO^T] += R [Al | Qm] (B MN-major, two atoms 16 KB apart) ----
         if (tid == 0) {
             tc_fence_after();
-            mma_k64x3<false, true>(tbase + col_d4, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi),
-                                   smem_u32(al_lo), id_x, false);
-            mma_k64x3<false, false>(tbase + col_do, smem_u32(ph_hi), smem_u32(ph_lo), smem_u32(xs_hi),
-                                    smem_u32(xs_lo), id_do, true);
+            mma_k64x3<false, true>(tbase + col_x, smem_u32(xs_hi), smem_u32(xs_lo), smem_u32(al_hi), smem_u32(al_lo),
+                                   id_xw, true, 16, L::kAtom);
             umma_commit(bar);
         }
         if (!round_wait()) {
@@ -360,27 +371,19 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         }
         {
             float v[32];
-            tmem_ld32(tq + col_d4 + 32 * hw, v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] += v[j];
-            put_row32(xs_hi, xs_lo, xrow, 32 * hw, x);
-            // readout coefficients of token t = 16 qw + lane: y_t (state rows
-            // 64..127) and h_t (rows 0..63), columns 32 hw .., divided by den_t
-            unsigned char *dst = gyh + (size_t)sb * (4 * kTile);
-            const int t = 16 * qw + lane;
-            const float rd = s_rden[t & 63];
-            tmem_ld32(tq + col_do + 64 + 32 * hw, v);
-            if (lane < 16) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= rd;
-                put_row32(dst, dst + kTile, t, 32 * hw, v);
-            }
+            tmem_ld32(tq + col_x + 32 * hw, v);  // the new X: next round 1's operand
+            put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
+            // readout coefficients of state row xrow for tokens 32 hw .., divided by
+            // den_t: y (rows 64..127, tile row xrow - 64) and h (rows 0..63)
             tmem_ld32(tq + col_do + 32 * hw, v);
-            if (lane < 16) {
+            const float4 *rd4 = reinterpret_cast<const float4 *>(s_rden + 32 * hw);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= rd;
-                put_row32(dst + 2 * kTile, dst + 3 * kTile, t, 32 * hw, v);
+            for (int q = 0; q < 8; ++q) {
+                const float4 r4 = rd4[q];
+                v[4 * q] *= r4.x; v[4 * q + 1] *= r4.y; v[4 * q + 2] *= r4.z; v[4 * q + 3] *= r4.w;
             }
+            unsigned char *dst = gyh + (size_t)sb * (4 * kTile) + (xrow < 64 ? 2 * kTile : 0);
+            put_row32(dst, dst + kTile, xrow & 63, 32 * hw, v);
         }
         tc_fence_before();
         fence_proxy_async_smem();
@@ -389,6 +392,8 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     if (!ok) {
         if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
     } else {  // rows 0..63 are H_c, rows 64..127 P_c
+        float x[32];
+        tmem_ld32(tq + col_x + 32 * hw, x);
         float4 *dst = reinterpret_cast<float4 *>(ws_f(a, xrow < 64 ? a.L.off_H : a.L.off_P) +
                                                  ((size_t)bh * NC + c) * kD * kD + (size_t)(xrow & 63) * kD + 32 * hw);
 #pragma unroll
@@ -486,11 +491,12 @@ __global__ void __launch_bounds__(kOutThreads) out_tc_kernel(ChunkArgs a) {
             if (w) {
                 landed = sb + 1;
                 tc_fence_after();
-                // D = Y S_c^T (hi/lo split) + H I^T
-                mma_k64x3<false, false>(tbase, smem_u32(yh), smem_u32(yh + kTile), smem_u32(sc_hi), smem_u32(sc_lo),
-                                        id_64, false);
-                mma_k64<false, false>(tbase, smem_u32(yh + 2 * kTile), smem_u32(eye), id_64, true);
-                mma_k64<false, false>(tbase, smem_u32(yh + 3 * kTile), smem_u32(eye), id_64, true);
+                // D = Y S_c^T (hi/lo split) + H I^T; the coefficient tiles hold a
+                // feature per row (MN-major: rows = K, columns = the tokens M)
+                mma_k64x3<true, false>(tbase, smem_u32(yh), smem_u32(yh + kTile), smem_u32(sc_hi), smem_u32(sc_lo),
+                                       id_64, false);
+                mma_k64<true, false>(tbase, smem_u32(yh + 2 * kTile), smem_u32(eye), id_64, true);
+                mma_k64<true, false>(tbase, smem_u32(yh + 3 * kTile), smem_u32(eye), id_64, true);
                 umma_commit(mbar);
                 w = mbar_wait_bounded(mbar, (uint32_t)(sb & 1), a.p.wait_limit_ns, a.p.err);
                 if (!w) mma_open = sb;
