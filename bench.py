@@ -462,14 +462,18 @@ def main():
         hn = torch.empty(n_T.shape, dtype=torch.float32).pin_memory()
 
         # a decode step returns o; its state stays resident on the device
-        results = ((ho, o),) if in_place else ((ho, o), (hS, S_T), (hA, A_T), (hn, n_T))
+
+        copy_stream = torch.cuda.Stream(dev)
+        ev_uk, ev_qv = torch.cuda.Event(), torch.cuda.Event()
 
         def e2e_step():
-            for dst, src in ((q, hq), (k, hk), (v, hv), (u, hu)):
-                dst.copy_(src, non_blocking=True)
-            step()
-            for dst, src in results:
-                dst.copy_(src, non_blocking=True)
+            # the public host-buffer entry: uploads u, k first on a second stream, q, v
+            # while the passes that read only u, k run, the results back after the kernels
+            st = (S_T, A_T, n_T) if in_place else (None, None, None)
+            hs = (None, None, None) if in_place else (hS, hA, hn)
+            vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, q, k, v, u, o, ho, S_T, A_T, n_T, hs[0], hs[1], hs[2],
+                                 S0=st[0], A0=st[1], n0=st[2], kernel=resolved, workspace=ws if need else None,
+                                 stream=stream, copy_stream=copy_stream, ev_uk=ev_uk, ev_qv=ev_qv)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()

@@ -87,6 +87,43 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
                 const float *n0, void *o, float *S_T, float *A_T, float *n_T, int kernel,
                 int chunk, void *workspace, size_t ws_bytes, void *stream);
 
+/*
+ * vla_forward_host -- vla_forward for inputs and outputs in host memory, with
+ * the uploads overlapped with the first passes.
+ *
+ * The recurrence reads u and k in its first passes (the chunk Grams, their
+ * prefix and the gates of sections 2.2-2.3 of "Variational Linear Attention:
+ * Stable Associative Memory for Long-Context Transformers") and q and v only
+ * from the state pass on.  So the call copies u and k to the device first on
+ * copy_stream (then records ev_uk), q and v next (then records ev_qv); the
+ * kernels on `stream` wait for ev_uk before the first launch and for ev_qv
+ * before the first pass that reads q or v (on the sequential and decode paths,
+ * before their one kernel).  The uploads start after the work queued on
+ * `stream` before the call.  o (and the final state for the non-NULL host
+ * pointers among hS_T, hA_T, hn_T) is copied back on `stream` after the last
+ * kernel.
+ *
+ * hq, hk, hv, hu  host [B,H,T,d] io_dtype, read; page-locked memory lets the
+ *                 copies run asynchronously (pageable memory still works).
+ * ho              host [B,H,T,d] io_dtype, written.
+ * hS_T, hA_T, hn_T  optional host copies of S_T, A_T, n_T (hn_T needs n_T).
+ * q, k, v, u, o   device staging buffers owned by the caller, as in
+ *                 vla_forward; q, k, v, u are overwritten by the uploads.
+ * S0 .. ws_bytes  as in vla_forward.
+ * stream          the compute stream; copy_stream a second stream (cudaStream_t
+ *                 as void*; the same stream works, without overlap).
+ * ev_uk, ev_qv    two cudaEvent_t (as void*) the call records; required.
+ * Asynchronous: the host buffers must stay valid until `stream` has passed
+ * the call's work.  Returns as vla_forward; on an argument error nothing is
+ * queued.
+ */
+int vla_forward_host(const void *hq, const void *hk, const void *hv, const void *hu, int io_dtype,
+                     float lambda0, int B, int H, int T, int d_h, const float *S0, const float *A0,
+                     const float *n0, void *q, void *k, void *v, void *u, void *o, void *ho, float *S_T,
+                     float *A_T, float *n_T, float *hS_T, float *hA_T, float *hn_T, int kernel, int chunk,
+                     void *workspace, size_t ws_bytes, void *stream, void *copy_stream, void *ev_uk,
+                     void *ev_qv);
+
 /* Workspace bytes vla_forward needs for these arguments (0 for the
  * sequential kernel).  Returns 0 for invalid arguments as well. */
 size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk);

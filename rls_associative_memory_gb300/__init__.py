@@ -28,6 +28,7 @@ from ._lib import (  # noqa: F401
     vla_backward_workspace_bytes,
     vla_debug_inject,
     vla_device_status,
+    vla_forward_host,
     vla_forward,
     vla_last_launch_count,
     vla_select_kernel,

@@ -184,10 +184,16 @@ int vla_device_status(void *stream) {
     return VLA_OK;
 }
 
-int vla_forward(const void *q, const void *k, const void *v, const void *u, int io_dtype, float lambda0,
-                int B, int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o,
-                float *S_T, float *A_T, float *n_T, int kernel, int chunk, void *workspace,
-                size_t ws_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// vla_forward's body; wait_qv (a cudaEvent_t or null) is waited for before the
+// first pass that reads q or v.
+int forward_impl(const void *q, const void *k, const void *v, const void *u, int io_dtype, float lambda0, int B,
+                 int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o, float *S_T,
+                 float *A_T, float *n_T, int kernel, int chunk, void *workspace, size_t ws_bytes, void *stream,
+                 void *wait_qv) {
     int rc = check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
     if (rc != VLA_OK) return rc;
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
@@ -229,15 +235,89 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
         const bool tc = (kk == VLA_KERNEL_CHUNK_TC);
         const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk, tc && io_dtype == VLA_BF16);
         p.rows_tc = tc;
+        p.wait_qv = wait_qv;
         e = vla::launch_chunk(p, L, st);
-    } else if (kk == VLA_KERNEL_DECODE) {
-        e = vla::launch_decode(p, st);
     } else {
-        // the sequential kernel also serves T == 0 (state copy) for either choice
-        e = vla::launch_seq(p, st);
+        // one kernel reads every input
+        if (wait_qv) e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(wait_qv), 0);
+        if (e == cudaSuccess) {
+            if (kk == VLA_KERNEL_DECODE) e = vla::launch_decode(p, st);
+            else e = vla::launch_seq(p, st);  // (also T == 0: the state copy, for either choice)
+        }
     }
     if (e != cudaSuccess) return cuda_fail(e);
     t_last_launches = launches;
+    return VLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int vla_forward(const void *q, const void *k, const void *v, const void *u, int io_dtype, float lambda0,
+                int B, int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o,
+                float *S_T, float *A_T, float *n_T, int kernel, int chunk, void *workspace,
+                size_t ws_bytes, void *stream) {
+    return forward_impl(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
+                        workspace, ws_bytes, stream, nullptr);
+}
+
+int vla_forward_host(const void *hq, const void *hk, const void *hv, const void *hu, int io_dtype, float lambda0,
+                     int B, int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *q,
+                     void *k, void *v, void *u, void *o, void *ho, float *S_T, float *A_T, float *n_T,
+                     float *hS_T, float *hA_T, float *hn_T, int kernel, int chunk, void *workspace,
+                     size_t ws_bytes, void *stream, void *copy_stream, void *ev_uk, void *ev_qv) {
+    int rc = check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
+    if (rc != VLA_OK) return rc;
+    if (!ev_uk || !ev_qv) return VLA_ERR_ARG;
+    const size_t n_io = (size_t)B * H * (size_t)T * d_h * (io_dtype == VLA_BF16 ? 2 : 4);
+    if (n_io > 0 && (!hq || !hk || !hv || !hu || !ho)) return VLA_ERR_ARG;
+    const void *hptrs[] = {hq, hk, hv, hu, ho, hS_T, hA_T, hn_T};
+    for (const void *p : hptrs)
+        if (p && !aligned16(p)) return VLA_ERR_ALIGN;
+    // the device call's own checks (pointers, alignment, workspace) before anything is queued
+    {
+        const long long BH = (long long)B * H;
+        if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
+        if (BH > 0 && (!S_T || !A_T)) return VLA_ERR_ARG;
+        if (BH > 0 && T > 0 && (!q || !k || !v || !u || !o)) return VLA_ERR_ARG;
+        const void *ptrs[] = {q, k, v, u, o, S0, A0, n0, S_T, A_T, n_T, workspace};
+        for (const void *p : ptrs)
+            if (p && !aligned16(p)) return VLA_ERR_ALIGN;
+        const int kk = resolve_kernel(B, H, T, d_h, kernel);
+        const size_t need = vla_workspace_bytes(B, H, T, d_h, io_dtype, kk, chunk);
+        if (need > 0 && (!workspace || ws_bytes < need)) return VLA_ERR_WORKSPACE;
+        if ((hn_T && !n_T)) return VLA_ERR_ARG;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+    cudaEvent_t e_uk = static_cast<cudaEvent_t>(ev_uk), e_qv = static_cast<cudaEvent_t>(ev_qv);
+    cudaError_t e;
+    // the uploads overwrite the staging buffers: after `stream`'s earlier work
+    if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return cuda_fail(e);
+    if (n_io > 0) {
+        // u and k first: the Grams, the prefix and the gates read only those
+        if ((e = cudaMemcpyAsync(u, hu, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(k, hk, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
+    }
+    if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return cuda_fail(e);
+    if (n_io > 0) {
+        if ((e = cudaMemcpyAsync(q, hq, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(v, hv, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
+    }
+    if ((e = cudaEventRecord(e_qv, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return cuda_fail(e);
+    rc = forward_impl(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
+                      workspace, ws_bytes, stream, ev_qv);
+    if (rc != VLA_OK) return rc;
+    const size_t n_dd = (size_t)B * H * d_h * d_h * 4, n_d = (size_t)B * H * d_h * 4;
+    if (n_io > 0 && (e = cudaMemcpyAsync(ho, o, n_io, cudaMemcpyDeviceToHost, st)) != cudaSuccess) return cuda_fail(e);
+    if (hS_T && n_dd && (e = cudaMemcpyAsync(hS_T, S_T, n_dd, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e);
+    if (hA_T && n_dd && (e = cudaMemcpyAsync(hA_T, A_T, n_dd, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e);
+    if (hn_T && n_d && (e = cudaMemcpyAsync(hn_T, n_T, n_d, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e);
     return VLA_OK;
 }
 

@@ -1184,6 +1184,9 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     }
     mark_launch(a.p, ++n, st);
     const bool tc = a.p.rows_tc && rows_tc_supported(a.p, a.L);
+    // the passes so far read u and k only; q and v may still be arriving
+    if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
+        return e;
     if (tc) {
         if ((e = launch_rows_tc(a, 0, st)) != cudaSuccess) return e;
     } else {

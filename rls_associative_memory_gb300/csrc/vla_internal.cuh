@@ -35,6 +35,8 @@ struct FwdParams {
     size_t ws_bytes;
     int chunk;                  // chunk length (chunked kernel)
     int rows_tc;                // chunked kernel: state passes on the tensor cores where supported
+    void *wait_qv;              // optional cudaEvent_t: the stream waits for it before the first pass
+                                // that reads q or v (the chunked path's state pass)
     void *const *events;        // measurement hook: cudaEvent_t handles, or null
     int n_events;
     int *launches;              // out: number of kernels launched

@@ -133,3 +133,24 @@ def test_debug_hook_is_host_state_only():
     assert vla.vla_debug_inject(2) == vla.VLA_ERR_ARG
     assert vla.vla_debug_inject(1, 1000) == vla.VLA_OK
     assert vla.vla_debug_inject(0) == vla.VLA_OK
+
+
+def test_host_entry_argument_checks():
+    """vla_forward_host rejects bad arguments before queuing any copy or
+    launch (no CUDA call is reached here)."""
+    L = vla.lib()
+    f = 1 << 20
+    dev = [f + 0x1000 * i for i in range(12)]  # aligned stand-ins, never dereferenced
+
+    def call(ev=(f, f + 16), hq=f + 0x100000, hn=None, n_T=None, io=vla.VLA_BF16, d=64, T=64):
+        return L.vla_forward_host(hq, hq, hq, hq, io, 1.0, 1, 1, T, d, None, None, None,
+                                  dev[0], dev[1], dev[2], dev[3], dev[4], hq, dev[5], dev[6], n_T,
+                                  None, None, hn, vla.VLA_KERNEL_SEQ, 0, None, 0, None, None, ev[0], ev[1])
+
+    assert call(ev=(None, f)) == vla.VLA_ERR_ARG
+    assert call(ev=(f, None)) == vla.VLA_ERR_ARG
+    assert call(hq=None) == vla.VLA_ERR_ARG
+    assert call(hq=f + 0x100000 + 4) == vla.VLA_ERR_ALIGN
+    assert call(hn=f + 0x200000) == vla.VLA_ERR_ARG  # a host n_T needs the device n_T
+    assert call(d=48) == vla.VLA_ERR_UNSUPPORTED_DIM
+    assert call(io=9) == vla.VLA_ERR_ARG
