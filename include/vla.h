@@ -95,11 +95,12 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * prefix and the gates of sections 2.2-2.3 of "Variational Linear Attention:
  * Stable Associative Memory for Long-Context Transformers") and q and v only
  * from the state pass on.  So the call copies u and k to the device first on
- * copy_stream (then records ev_uk), q and v next (then records ev_qv); the
- * kernels on `stream` wait for ev_uk before the first launch and for ev_qv
- * before the first pass that reads q or v (on the sequential and decode paths,
- * before their one kernel).  The uploads start after the work queued on
- * `stream` before the call.  o (and the final state for the non-NULL host
+ * copy_stream, then q and v in two halves of the (b, h) units; the kernels on
+ * `stream` wait for u and k before the first launch, and the tensor-core state
+ * pass runs in two launches, each after its half of q and v has landed (on the
+ * other paths every pass that reads q or v waits for all of them).  ev_uk and
+ * ev_qv carry these dependencies (ev_uk is recorded twice).  The uploads start
+ * after the work queued on `stream` before the call.  o (and the final state for the non-NULL host
  * pointers among hS_T, hA_T, hn_T) is copied back on `stream` after the last
  * kernel.
  *

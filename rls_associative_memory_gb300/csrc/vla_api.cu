@@ -189,11 +189,12 @@ int vla_device_status(void *stream) {
 namespace {
 
 // vla_forward's body; wait_qv (a cudaEvent_t or null) is waited for before the
-// first pass that reads q or v.
+// first pass that reads q or v; wait_qv2 (or null) before the state pass of the
+// units from qv_split on (every pass that reads q or v on the other paths).
 int forward_impl(const void *q, const void *k, const void *v, const void *u, int io_dtype, float lambda0, int B,
                  int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o, float *S_T,
                  float *A_T, float *n_T, int kernel, int chunk, void *workspace, size_t ws_bytes, void *stream,
-                 void *wait_qv) {
+                 void *wait_qv, void *wait_qv2, int qv_split) {
     int rc = check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
     if (rc != VLA_OK) return rc;
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
@@ -236,10 +237,13 @@ int forward_impl(const void *q, const void *k, const void *v, const void *u, int
         const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk, tc && io_dtype == VLA_BF16);
         p.rows_tc = tc;
         p.wait_qv = wait_qv;
+        p.wait_qv2 = wait_qv2;
+        p.qv_split = qv_split;
         e = vla::launch_chunk(p, L, st);
     } else {
         // one kernel reads every input
         if (wait_qv) e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(wait_qv), 0);
+        if (e == cudaSuccess && wait_qv2) e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(wait_qv2), 0);
         if (e == cudaSuccess) {
             if (kk == VLA_KERNEL_DECODE) e = vla::launch_decode(p, st);
             else e = vla::launch_seq(p, st);  // (also T == 0: the state copy, for either choice)
@@ -259,7 +263,7 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
                 float *S_T, float *A_T, float *n_T, int kernel, int chunk, void *workspace,
                 size_t ws_bytes, void *stream) {
     return forward_impl(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
-                        workspace, ws_bytes, stream, nullptr);
+                        workspace, ws_bytes, stream, nullptr, nullptr, 0);
 }
 
 int vla_forward_host(const void *hq, const void *hk, const void *hv, const void *hu, int io_dtype, float lambda0,
@@ -301,14 +305,31 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
         if ((e = cudaMemcpyAsync(k, hk, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
     }
     if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return cuda_fail(e);
-    if (n_io > 0) {
+    if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return cuda_fail(e);
+    // q and v in two halves of the (b, h) units: the state pass of the first half
+    // starts while the second uploads (ev_uk is reused: the wait above has taken
+    // its first record)
+    const long long BH = (long long)B * H;
+    const int split = BH >= 2 ? (int)(BH / 2) : 0;
+    const size_t unit = BH > 0 ? n_io / (size_t)BH : 0, first = unit * (size_t)split;
+    if (n_io > 0 && split > 0) {
+        const unsigned char *hq8 = static_cast<const unsigned char *>(hq), *hv8 = static_cast<const unsigned char *>(hv);
+        unsigned char *q8 = static_cast<unsigned char *>(q), *v8 = static_cast<unsigned char *>(v);
+        if ((e = cudaMemcpyAsync(q8, hq8, first, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(v8, hv8, first, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(q8 + first, hq8 + first, n_io - first, cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(v8 + first, hv8 + first, n_io - first, cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+            return cuda_fail(e);
+    } else if (n_io > 0) {
         if ((e = cudaMemcpyAsync(q, hq, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
         if ((e = cudaMemcpyAsync(v, hv, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
     }
     if ((e = cudaEventRecord(e_qv, cs)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return cuda_fail(e);
+    const bool two = n_io > 0 && split > 0;
     rc = forward_impl(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
-                      workspace, ws_bytes, stream, ev_qv);
+                      workspace, ws_bytes, stream, two ? ev_uk : ev_qv, two ? ev_qv : nullptr, two ? split : 0);
     if (rc != VLA_OK) return rc;
     const size_t n_dd = (size_t)B * H * d_h * d_h * 4, n_d = (size_t)B * H * d_h * 4;
     if (n_io > 0 && (e = cudaMemcpyAsync(ho, o, n_io, cudaMemcpyDeviceToHost, st)) != cudaSuccess) return cuda_fail(e);

@@ -1187,9 +1187,24 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     // the passes so far read u and k only; q and v may still be arriving
     if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
         return e;
-    if (tc) {
+    if (tc && a.p.wait_qv2 && a.p.qv_split > 0 && a.p.qv_split < a.p.BH) {
+        // the state pass in two launches: the units whose q, v have landed first
+        ChunkArgs h = a;
+        h.bh_lo = 0;
+        h.bh_n = a.p.qv_split;
+        if ((e = launch_rows_tc(h, 0, st)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess) return e;
+        mark_launch(a.p, ++n, st);
+        h.bh_lo = a.p.qv_split;
+        h.bh_n = a.p.BH - a.p.qv_split;
+        if ((e = launch_rows_tc(h, 0, st)) != cudaSuccess) return e;
+    } else if (tc) {
+        if (a.p.wait_qv2 && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess)
+            return e;
         if ((e = launch_rows_tc(a, 0, st)) != cudaSuccess) return e;
     } else {
+        if (a.p.wait_qv2 && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess)
+            return e;
         rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), RowsCfg<D, 0>::NT, RowsSmem<D, IO>::total, st>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

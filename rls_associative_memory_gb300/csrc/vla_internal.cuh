@@ -37,6 +37,8 @@ struct FwdParams {
     int rows_tc;                // chunked kernel: state passes on the tensor cores where supported
     void *wait_qv;              // optional cudaEvent_t: the stream waits for it before the first pass
                                 // that reads q or v (the chunked path's state pass)
+    void *wait_qv2;             // optional second event (tensor-core path): q, v of the units from
+    int qv_split;               // qv_split on; the state pass then runs in two launches
     void *const *events;        // measurement hook: cudaEvent_t handles, or null
     int n_events;
     int *launches;              // out: number of kernels launched
@@ -108,6 +110,7 @@ cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t 
 struct ChunkArgs {
     FwdParams p;
     ChunkLayout L;
+    int bh_lo = 0, bh_n = 0;  // (b, h) units of a state-pass launch (bh_n = 0: all)
 };
 __device__ __forceinline__ float *ws_f(const ChunkArgs &a, size_t off) {
     return reinterpret_cast<float *>(static_cast<unsigned char *>(a.p.ws) + off);
