@@ -191,10 +191,12 @@ namespace {
 // vla_forward's body; wait_qv (a cudaEvent_t or null) is waited for before the
 // first pass that reads q or v; wait_qv2 (or null) before the state pass of the
 // units from qv_split on (every pass that reads q or v on the other paths).
+// When the tensor-core path runs its later passes per half, done_first is
+// recorded after the first half's o is written and *did_split set to 1.
 int forward_impl(const void *q, const void *k, const void *v, const void *u, int io_dtype, float lambda0, int B,
                  int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o, float *S_T,
                  float *A_T, float *n_T, int kernel, int chunk, void *workspace, size_t ws_bytes, void *stream,
-                 void *wait_qv, void *wait_qv2, int qv_split) {
+                 void *wait_qv, void *wait_qv2, int qv_split, void *done_first, int *did_split) {
     int rc = check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
     if (rc != VLA_OK) return rc;
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
@@ -239,6 +241,8 @@ int forward_impl(const void *q, const void *k, const void *v, const void *u, int
         p.wait_qv = wait_qv;
         p.wait_qv2 = wait_qv2;
         p.qv_split = qv_split;
+        p.done_first = done_first;
+        p.did_split = did_split;
         e = vla::launch_chunk(p, L, st);
     } else {
         // one kernel reads every input
@@ -263,7 +267,7 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
                 float *S_T, float *A_T, float *n_T, int kernel, int chunk, void *workspace,
                 size_t ws_bytes, void *stream) {
     return forward_impl(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
-                        workspace, ws_bytes, stream, nullptr, nullptr, 0);
+                        workspace, ws_bytes, stream, nullptr, nullptr, 0, nullptr, nullptr);
 }
 
 int vla_forward_host(const void *hq, const void *hk, const void *hv, const void *hu, int io_dtype, float lambda0,
@@ -328,17 +332,32 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
     }
     if ((e = cudaEventRecord(e_qv, cs)) != cudaSuccess) return cuda_fail(e);
     const bool two = n_io > 0 && split > 0;
+    int did_split = 0;
     rc = forward_impl(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
-                      workspace, ws_bytes, stream, two ? ev_uk : ev_qv, two ? ev_qv : nullptr, two ? split : 0);
+                      workspace, ws_bytes, stream, two ? ev_uk : ev_qv, two ? ev_qv : nullptr, two ? split : 0, ev_uk,
+                      &did_split);
     if (rc != VLA_OK) return rc;
     const size_t n_dd = (size_t)B * H * d_h * d_h * 4, n_d = (size_t)B * H * d_h * 4;
-    if (n_io > 0 && (e = cudaMemcpyAsync(ho, o, n_io, cudaMemcpyDeviceToHost, st)) != cudaSuccess) return cuda_fail(e);
+    size_t o_from = 0;
+    if (did_split) {
+        // the first half's o leaves on copy_stream while the second half computes; `stream`
+        // then waits for that copy, so that it covers the whole call
+        if ((e = cudaStreamWaitEvent(cs, e_uk, 0)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaMemcpyAsync(ho, o, first, cudaMemcpyDeviceToHost, cs)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaEventRecord(e_qv, cs)) != cudaSuccess) return cuda_fail(e);
+        o_from = first;
+    }
+    if (n_io > o_from &&
+        (e = cudaMemcpyAsync(static_cast<unsigned char *>(ho) + o_from, static_cast<const unsigned char *>(o) + o_from,
+                             n_io - o_from, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e);
     if (hS_T && n_dd && (e = cudaMemcpyAsync(hS_T, S_T, n_dd, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
         return cuda_fail(e);
     if (hA_T && n_dd && (e = cudaMemcpyAsync(hA_T, A_T, n_dd, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
         return cuda_fail(e);
     if (hn_T && n_d && (e = cudaMemcpyAsync(hn_T, n_T, n_d, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
         return cuda_fail(e);
+    if (did_split && (e = cudaStreamWaitEvent(st, e_qv, 0)) != cudaSuccess) return cuda_fail(e);
     return VLA_OK;
 }
 

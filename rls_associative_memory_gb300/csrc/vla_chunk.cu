@@ -1010,7 +1010,7 @@ __global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
     float *sP = reinterpret_cast<float *>(smem + Lo::P);
     float *sH = reinterpret_cast<float *>(smem + Lo::H);
     float *sS = reinterpret_cast<float *>(smem + Lo::S);
-    const int rb = (int)(blockIdx.x % (D / kRB)), bh = (int)(blockIdx.x / (D / kRB));  // row block, unit
+    const int rb = (int)(blockIdx.x % (D / kRB)), bh = a.bh_lo + (int)(blockIdx.x / (D / kRB));  // row block, unit
     const int NC = a.L.NC;
     const int tid = threadIdx.x;
     const int r = tid / (D / OPT), j0 = (tid % (D / OPT)) * OPT;
@@ -1188,23 +1188,34 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
         return e;
     if (tc && a.p.wait_qv2 && a.p.qv_split > 0 && a.p.qv_split < a.p.BH) {
-        // the state pass in two launches: the units whose q, v have landed first
+        // two halves of the units, each through the state pass, the chain and the
+        // output pass (all per (b, h)): the first half runs while the second's q, v
+        // land, and its o can leave while the second half computes
+        if (a.p.did_split) *a.p.did_split = 1;
         ChunkArgs h = a;
-        h.bh_lo = 0;
-        h.bh_n = a.p.qv_split;
-        if ((e = launch_rows_tc(h, 0, st)) != cudaSuccess) return e;
-        if ((e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess) return e;
-        mark_launch(a.p, ++n, st);
-        h.bh_lo = a.p.qv_split;
-        h.bh_n = a.p.BH - a.p.qv_split;
-        if ((e = launch_rows_tc(h, 0, st)) != cudaSuccess) return e;
-    } else if (tc) {
-        if (a.p.wait_qv2 && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess)
-            return e;
+        for (int half = 0; half < 2; ++half) {
+            h.bh_lo = half ? a.p.qv_split : 0;
+            h.bh_n = half ? a.p.BH - a.p.qv_split : a.p.qv_split;
+            if (half && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess)
+                return e;
+            if ((e = launch_rows_tc(h, 0, st)) != cudaSuccess) return e;
+            mark_launch(a.p, ++n, st);
+            chain_kernel<D><<<(unsigned)((D / chain_rows<D>()) * h.bh_n), 256, ChainSmem<D>::total, st>>>(h);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            mark_launch(a.p, ++n, st);
+            if ((e = launch_rows_tc(h, 1, st)) != cudaSuccess) return e;
+            mark_launch(a.p, ++n, st);
+            if (!half && a.p.done_first &&
+                (e = cudaEventRecord(static_cast<cudaEvent_t>(a.p.done_first), st)) != cudaSuccess)
+                return e;
+        }
+        return cudaSuccess;
+    }
+    if (a.p.wait_qv2 && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess)
+        return e;
+    if (tc) {
         if ((e = launch_rows_tc(a, 0, st)) != cudaSuccess) return e;
     } else {
-        if (a.p.wait_qv2 && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess)
-            return e;
         rows_kernel<D, IO, 0><<<(unsigned)(NC * BH), RowsCfg<D, 0>::NT, RowsSmem<D, IO>::total, st>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kOutThreads) out_tc_kernel(ChunkArgs a) {
     unsigned char *st = smem + L::stage, *sc_hi = smem + L::sc_hi, *sc_lo = smem + L::sc_lo, *eye = smem + L::eye;
 
     const int NC = a.L.NC, C = a.L.C, T = a.p.T;
-    const int c = (int)(blockIdx.x % (unsigned)NC), bh = (int)(blockIdx.x / (unsigned)NC);
+    const int c = (int)(blockIdx.x % (unsigned)NC), bh = a.bh_lo + (int)(blockIdx.x / (unsigned)NC);
     const int t0 = c * C, ntok = min(C, T - t0), nsb = (ntok + kSB - 1) / kSB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned char *gyh = static_cast<const unsigned char *>(a.p.ws) + a.L.off_yh +
@@ -551,7 +551,7 @@ bool rows_tc_supported(const FwdParams &p, const ChunkLayout &L) {
 }
 
 cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream) {
-    const long long grid = (long long)a.L.NC * (mode == 0 && a.bh_n > 0 ? a.bh_n : a.p.BH);
+    const long long grid = (long long)a.L.NC * (a.bh_n > 0 ? a.bh_n : a.p.BH);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     cudaError_t e;
     if (mode == 0) {

@@ -38,7 +38,9 @@ struct FwdParams {
     void *wait_qv;              // optional cudaEvent_t: the stream waits for it before the first pass
                                 // that reads q or v (the chunked path's state pass)
     void *wait_qv2;             // optional second event (tensor-core path): q, v of the units from
-    int qv_split;               // qv_split on; the state pass then runs in two launches
+    int qv_split;               // qv_split on; the passes from the state pass on then run per half
+    void *done_first;           // optional event recorded after the first half's output pass
+    int *did_split;             // optional out: set to 1 when the passes ran per half
     void *const *events;        // measurement hook: cudaEvent_t handles, or null
     int n_events;
     int *launches;              // out: number of kernels launched
