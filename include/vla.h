@@ -99,10 +99,13 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * `stream` wait for u and k before the first launch, and the tensor-core state
  * pass runs in two launches, each after its half of q and v has landed (on the
  * other paths every pass that reads q or v waits for all of them).  ev_uk and
- * ev_qv carry these dependencies (ev_uk is recorded twice).  The uploads start
- * after the work queued on `stream` before the call.  o (and the final state for the non-NULL host
- * pointers among hS_T, hA_T, hn_T) is copied back on `stream` after the last
- * kernel.
+ * ev_qv carry these dependencies (each is recorded more than once).  The
+ * uploads start after the work queued on `stream` before the call.  On the
+ * tensor-core path the chain and the output pass also run per half, and the
+ * first half's o goes back on copy_stream while the second half computes; the
+ * rest of o (and the final state for the non-NULL host pointers among hS_T,
+ * hA_T, hn_T) goes back on `stream`, which finally waits for the first half's
+ * copy: everything the call queued is complete once `stream` is.
  *
  * hq, hk, hv, hu  host [B,H,T,d] io_dtype, read; page-locked memory lets the
  *                 copies run asynchronously (pageable memory still works).
