@@ -49,8 +49,8 @@ TRAFFIC = {
     # profiles/seq_kernel_long.md: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
     ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
     # profiles/chunk_tc_long.md: at T=16384 (same 16 heads), scaled x4 to T=65536
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (75.313664e6 + 17.085184e6), "src_sha": "918bfd7865dc27c5"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.54656e6 + 99.970816e6), "src_sha": "918bfd7865dc27c5"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (75.366144e6 + 17.920256e6), "src_sha": "f0f86301075d5492"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.76544e6 + 100.307712e6), "src_sha": "f0f86301075d5492"},
 }
 
 
