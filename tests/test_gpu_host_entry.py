@@ -39,3 +39,56 @@ def test_host_entry_matches_device_entry(kernel, T, dtype):
     assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
     got = {"o": ho.float().numpy(), "S_T": hS.numpy(), "A_T": hA.numpy(), "n_T": hn.numpy()}
     compare(got, oracle_ref(x), dtype)
+
+
+def _host_call(x, kernel, S0=None, A0=None, n0=None, in_place=False):
+    q, k, v, u = to_device(x)
+    B, H, T, d = q.shape
+    hq, hk, hv, hu = (t.cpu().pin_memory() for t in (q, k, v, u))
+    dq, dk, dv, du = (torch.empty_like(t) for t in (q, k, v, u))
+    o = torch.empty_like(q)
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    if in_place:
+        S_T, A_T, n_T = S0, A0, n0
+    else:
+        S_T = torch.empty((B, H, d, d), device="cuda")
+        A_T = torch.empty_like(S_T)
+        n_T = torch.empty((B, H, d), device="cuda")
+    hS, hA = torch.empty(S_T.shape).pin_memory(), torch.empty(A_T.shape).pin_memory()
+    hn = torch.empty(n_T.shape).pin_memory()
+    io = vla.VLA_BF16 if q.dtype == torch.bfloat16 else vla.VLA_F32
+    need = vla.vla_workspace_bytes(B, H, T, d, io, kernel)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, dq, dk, dv, du, o, ho, S_T, A_T, n_T, hS, hA, hn, S0=S0, A0=A0,
+                         n0=n0, kernel=kernel, workspace=ws, stream=stream, copy_stream=torch.cuda.Stream())
+    stream.synchronize()
+    return {"o": ho.float().numpy(), "S_T": hS.numpy(), "A_T": hA.numpy(), "n_T": hn.numpy()}
+
+
+@pytest.mark.parametrize("kernel", [vla.VLA_KERNEL_CHUNK_TC, vla.VLA_KERNEL_SEQ])
+def test_host_entry_given_initial_state(kernel):
+    """Streaming continuation through the host entry (A0 given adds the chunked
+    path's A0 inversion before the passes that read u and k)."""
+    pre = make_inputs(1, 3, 150, 64, "bf16", seed=71, lambda0=0.9, u_scale=0.5)
+    st = oracle_ref(pre)
+    x = make_inputs(1, 3, 1000, 64, "bf16", seed=72, lambda0=0.9, u_scale=0.5)
+    S0, A0, n0 = (torch.from_numpy(st[n]).float().cuda() for n in ("S_T", "A_T", "n_T"))
+    got = _host_call(x, kernel, S0=S0, A0=A0, n0=n0)
+    compare(got, oracle_ref(x, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"]), "bf16")
+
+
+def test_host_entry_single_unit():
+    """One (b, h) unit: no halves to split into."""
+    x = make_inputs(1, 1, 2000, 64, "bf16", seed=73, u_scale=0.5)
+    compare(_host_call(x, vla.VLA_KERNEL_CHUNK_TC), oracle_ref(x), "bf16")
+
+
+def test_host_entry_decode_in_place():
+    """Decode steps with the state updated in place on the device."""
+    pre = make_inputs(2, 4, 100, 64, "bf16", seed=74)
+    st = oracle_ref(pre)
+    x = make_inputs(2, 4, 2, 64, "bf16", seed=75)
+    S, A, n = (torch.from_numpy(st[k]).float().cuda().contiguous() for k in ("S_T", "A_T", "n_T"))
+    got = _host_call(x, vla.VLA_KERNEL_DECODE, S0=S, A0=A, n0=n, in_place=True)
+    compare(got, oracle_ref(x, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"]), "bf16")
