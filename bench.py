@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -49,8 +50,8 @@ TRAFFIC = {
     # profiles/seq_kernel_long.md: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
     ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
     # profiles/chunk_tc_long.md: at T=16384 (same 16 heads), scaled x4 to T=65536
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (75.366144e6 + 17.920256e6), "src_sha": "f0f86301075d5492"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.76544e6 + 100.307712e6), "src_sha": "f0f86301075d5492"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (75.366144e6 + 17.920256e6), "src_sha": "d7a37034f3620835"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.76544e6 + 100.307712e6), "src_sha": "d7a37034f3620835"},
 }
 
 
@@ -63,7 +64,11 @@ def kernel_src_hash(kernel_name: str) -> str:
         path = os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", fn)
         if not os.path.exists(path):
             return ""
-        h.update(open(path, "rb").read())
+        # the code only: comments and blank space do not invalidate a capture
+        src = open(path).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -24,11 +24,14 @@
 // Rows of S (and of [H; P]) evolve independently once the gates are known,
 // so the summary and output passes need no block-wide reduction per token.
 //
-// With VLA_KERNEL_CHUNK_TC at d = 64 and bf16 I/O (vla_chunk_tc.cu) the
-// summary pass also writes, per token, the readout of its [H; P] rows
-// (y_t = P_t phi(q_t) / den_t, h_t = H_t phi(q_t) / den_t; the state is affine
-// in S^(c) within a chunk), and the output pass is the product
-// o_t = S^(c) y_t + h_t, with no recurrence.
+// With VLA_KERNEL_CHUNK_TC at d = 64 and bf16 I/O every pass but the prefix
+// and the chain runs its products on the tensor cores: the Grams from TMA
+// tensor copies (vla_gram_tc.cu), the gates in block-Woodbury form
+// (vla_gates_tc.cu), and the summary pass in UT form (vla_chunk_tc.cu), which
+// also writes, per token, the readout of its [H; P] rows (y_t = P_t phi(q_t) /
+// den_t, h_t = H_t phi(q_t) / den_t; the state is affine in S^(c) within a
+// chunk), so that the output pass is the product o_t = S^(c) y_t + h_t, with
+// no recurrence.
 #include "vla_internal.cuh"
 
 namespace vla {
@@ -37,7 +40,7 @@ namespace {
 constexpr int kTT = 16;  // tokens per staged tile
 
 // VLA_KERNEL_CHUNK_TC takes the block-Woodbury gates of vla_gates_tc.cu
-// (measured 0.99 ms against 1.26 ms for the Sherman-Morrison gates here on the
+// (measured 0.90 ms against 1.26 ms for the Sherman-Morrison gates here on the
 // long stream, B = 1, H = 16, T = 65536, d = 64).
 constexpr bool kGatesOnTensorCores = true;
 

@@ -23,10 +23,12 @@
 //   R3  D3 = X^T [W | Y_hat]          Z^T and P = X^T Y_hat, Y_hat = Y diag(1/|k|)
 //   R4  D1[k rows] += E'^T Z^T        E'[s][t] = -beta_s P[s][t] |k_t| (s <= t):
 //                                      the rows become |k_t| A_t k_hat_t
-//       D5 = (Z diag(beta)) Z^T
-//   alpha_t = that row / |that row|,  A -= D5.
+//       A += -(Z diag(beta)) Z^T      (A held in fp32 in TMEM for the whole
+//                                      A-chunk; the product accumulates onto it)
+//   alpha_t = that row / |that row|, and the new A's operand tiles.
 // A starts each A-chunk from its definition (M^(c))^{-1}, M^(c) = lambda0 I +
-// the Grams of the earlier A-chunks (Gauss-Jordan), as in the SIMT gates.
+// the Grams of the earlier A-chunks: the same elimination on M^(c) gives
+// E = L^{-1} and D, then A = E^T D^{-1} E is one product on the tensor cores.
 #include "vla_tc_common.cuh"
 
 namespace vla {
