@@ -32,6 +32,8 @@
 // den_t, h_t = H_t phi(q_t) / den_t; the state is affine in S^(c) within a
 // chunk), so that the output pass is the product o_t = S^(c) y_t + h_t, with
 // no recurrence.
+#include <algorithm>
+
 #include "vla_internal.cuh"
 
 namespace vla {
@@ -1269,21 +1271,61 @@ int chunk_default_a(int BH, int T, int d, int C) {
     return best;
 }
 
-// A-chunk length for the tensor-core gates (d = 64): two CTAs per SM, each
-// sub-block of 64 tokens one unit of time and the Gauss-Jordan restart about
-// 0.4 of one.
-int chunk_default_a_tc(int BH, int T, int C) {
-    const long long resident = 152LL * 2;
-    int best = C;
-    long long best_cost = -1;
-    for (int CA = C; CA >= 64; CA /= 2) {
-        if (C % CA) continue;
-        const long long chunks = (long long)BH * ((T + CA - 1) / CA);
-        const long long waves = (chunks + resident - 1) / resident;
-        const long long cost = waves * (10 * (CA / 64) + 4);
-        if (best_cost < 0 || cost < best_cost) {
+// Wave model of the tensor-core passes (d = 64): each CTA walks its chunk one
+// 64-token sub-block after another, two CTAs resident per SM. The time of a
+// pass of `ctas` CTAs, each `len` sub-block times long: its full waves on the
+// 2 x 152 slots, then a partial one, which costs a whole CTA time if some SM
+// holds two of its CTAs and about 0.72 of one if none does (a CTA alone on an
+// SM runs that much faster, measured on the state pass).
+static double tc_pass_cost(long long ctas, double len) {
+    const long long slots = 2LL * 152;
+    const long long full = ctas / slots, rem = ctas % slots;
+    return len * ((double)full + (rem == 0 ? 0.0 : (rem <= 152 ? 0.72 : 1.0)));
+}
+
+// S-chunk length of the tensor-core path, a multiple of 64 (the long stream,
+// 16 units of 65536 tokens: 1728, two full waves of 27 sub-blocks, where 512
+// took seven waves of 8 with the last one part full). It minimises, in
+// sub-block times, the state pass over all units plus the same pass over each
+// half of the units (the host entry runs the halves one after the other, to
+// overlap the copies), plus the chain along the chunks, about 0.045 of a
+// sub-block per chunk (measured), counted for both.
+int chunk_default_tc(int BH, int T) {
+    static thread_local int last_BH = -1, last_T = -1, last_C = 64;
+    if (BH == last_BH && T == last_T) return last_C;
+    const int maxm = std::min((T + 63) / 64, 1024);
+    const long long h1 = BH / 2, h2 = BH - BH / 2;
+    int best = 64;
+    double best_cost = -1;
+    for (int m = 1; m <= maxm; ++m) {
+        const long long NC = (T + 64LL * m - 1) / (64LL * m);
+        const double full = tc_pass_cost(BH * NC, m);
+        const double halves = h1 > 0 ? tc_pass_cost(h1 * NC, m) + tc_pass_cost(h2 * NC, m) : full;
+        const double cost = full + halves + 2 * 0.045 * (double)NC;
+        if (best_cost < 0 || cost < best_cost - 1e-9) {
             best_cost = cost;
-            best = CA;
+            best = 64 * m;
+        }
+    }
+    last_BH = BH, last_T = T, last_C = best;
+    return best;
+}
+
+// A-chunk length of the tensor-core gates: a multiple of 64 that divides C
+// (each S-chunk starts on an A-chunk boundary), by the same wave model, each
+// A-chunk its sub-blocks plus the restart (the inverse of the prefix), about
+// 0.4 of a sub-block.
+int chunk_default_a_tc(int BH, int T, int C) {
+    const int m = C / 64;
+    int best = C;
+    double best_cost = -1;
+    for (int j = m; j >= 1; --j) {
+        if (m % j) continue;
+        const long long NCA = (T + 64LL * j - 1) / (64LL * j);
+        const double cost = tc_pass_cost(BH * NCA, j + 0.4);
+        if (best_cost < 0 || cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = 64 * j;
         }
     }
     return best;
@@ -1291,7 +1333,7 @@ int chunk_default_a_tc(int BH, int T, int C) {
 
 ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc_path) {
     ChunkLayout L{};
-    L.C = chunk > 0 ? chunk : chunk_default(BH, T);
+    L.C = chunk > 0 ? chunk : (tc_path && d == 64 ? chunk_default_tc(BH, T) : chunk_default(BH, T));
     const bool tc = tc_path && d == 64 && L.C % 64 == 0;
     L.CA = chunk > 0 ? chunk : (tc ? chunk_default_a_tc(BH, T, L.C) : chunk_default_a(BH, T, d, L.C));
     L.NC = (T + L.C - 1) / L.C;

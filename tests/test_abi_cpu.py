@@ -115,6 +115,22 @@ def test_workspace_query_and_kernel_selection():
     assert vla.vla_select_kernel(1, 16, 4096, 40) == vla.VLA_ERR_UNSUPPORTED_DIM
 
 
+def test_tensor_core_chunk_defaults():
+    """Default chunk lengths of the tensor-core path come from a wave model of
+    its passes (two CTAs per SM on 152 SMs): 16 units x 65536 tokens take
+    1728-token chunks (38 per unit, 608 CTAs: two full waves, and one full
+    wave for each half of the units), and 32 units x 4096 tokens 256. The
+    explicit length equal to the default needs the same workspace (same S- and
+    A-chunk counts)."""
+    ws = lambda BH, T, c: vla.vla_workspace_bytes(1, BH, T, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK_TC, c)  # noqa: E731
+    assert ws(16, 65536, 0) == ws(16, 65536, 1728)
+    assert ws(16, 65536, 0) != ws(16, 65536, 512)
+    assert ws(32, 4096, 0) == ws(32, 4096, 256)
+    # the float path keeps its own lengths
+    f32 = vla.vla_workspace_bytes(1, 16, 65536, 64, vla.VLA_F32, vla.VLA_KERNEL_CHUNK_TC, 0)
+    assert f32 == vla.vla_workspace_bytes(1, 16, 65536, 64, vla.VLA_F32, vla.VLA_KERNEL_CHUNK, 0)
+
+
 def test_backward_argument_checks():
     f = 1 << 20
     L = vla.lib()
