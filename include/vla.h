@@ -94,18 +94,22 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * The recurrence reads u and k in its first passes (the chunk Grams, their
  * prefix and the gates of sections 2.2-2.3 of "Variational Linear Attention:
  * Stable Associative Memory for Long-Context Transformers") and q and v only
- * from the state pass on.  So the call copies u and k to the device first on
- * copy_stream, then q and v in two halves of the (b, h) units; the kernels on
- * `stream` wait for u and k before the first launch, and the tensor-core state
- * pass runs in two launches, each after its half of q and v has landed (on the
- * other paths every pass that reads q or v waits for all of them).  ev_uk and
- * ev_qv carry these dependencies (each is recorded more than once).  The
- * uploads start after the work queued on `stream` before the call.  On the
- * tensor-core path the chain and the output pass also run per half, and the
- * first half's o goes back on copy_stream while the second half computes; the
- * rest of o (and the final state for the non-NULL host pointers among hS_T,
- * hA_T, hn_T) goes back on `stream`, which finally waits for the first half's
- * copy: everything the call queued is complete once `stream` is.
+ * from the state pass on, and every pass works per (b, h) unit.  On the
+ * tensor-core path (two or more units) the call therefore runs the passes in
+ * ranges of units as their inputs land: u and k go to the device on
+ * copy_stream in two halves of the units, each followed on `stream` by its
+ * Grams, prefix and gates; then q and v in two or three ranges, each
+ * followed by its state pass, chain and output pass.  The o of every range
+ * but the last comes back on copy_stream once all uploads are queued; the
+ * last range's o (and the final state for the non-NULL host pointers among
+ * hS_T, hA_T, hn_T) comes back on `stream`, which finally waits for
+ * copy_stream: everything the call queued is complete once `stream` is.  On
+ * the other paths u and k go first, the kernels wait for them before the
+ * first launch and for q and v before the first pass that reads them, and
+ * all outputs come back on `stream`.  ev_uk and ev_qv carry these
+ * dependencies (each is recorded more than once).  The uploads start after
+ * the work queued on `stream` before the call.  The results are those of
+ * vla_forward on the same data, bit for bit.
  *
  * hq, hk, hv, hu  host [B,H,T,d] io_dtype, read; page-locked memory lets the
  *                 copies run asynchronously (pageable memory still works).

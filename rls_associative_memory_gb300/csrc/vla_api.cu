@@ -188,15 +188,12 @@ int vla_device_status(void *stream) {
 
 namespace {
 
-// vla_forward's body; wait_qv (a cudaEvent_t or null) is waited for before the
-// first pass that reads q or v; wait_qv2 (or null) before the state pass of the
-// units from qv_split on (every pass that reads q or v on the other paths).
-// When the tensor-core path runs its later passes per half, done_first is
-// recorded after the first half's o is written and *did_split set to 1.
-int forward_impl(const void *q, const void *k, const void *v, const void *u, int io_dtype, float lambda0, int B,
-                 int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o, float *S_T,
-                 float *A_T, float *n_T, int kernel, int chunk, void *workspace, size_t ws_bytes, void *stream,
-                 void *wait_qv, void *wait_qv2, int qv_split, void *done_first, int *did_split) {
+// vla_forward's checks and parameter block. Returns VLA_OK with p (and, for
+// the chunked paths, L) filled in, or the error status; queues nothing.
+int prepare_forward(const void *q, const void *k, const void *v, const void *u, int io_dtype, float lambda0, int B,
+                    int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o, float *S_T,
+                    float *A_T, float *n_T, int kernel, int chunk, void *workspace, size_t ws_bytes,
+                    vla::FwdParams &p, vla::ChunkLayout &L, int &kk) {
     int rc = check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
     if (rc != VLA_OK) return rc;
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
@@ -206,17 +203,16 @@ int forward_impl(const void *q, const void *k, const void *v, const void *u, int
         if (T > 0 && (!q || !k || !v || !u || !o)) return VLA_ERR_ARG;
     }
     const void *ptrs[] = {q, k, v, u, o, S0, A0, n0, S_T, A_T, n_T, workspace};
-    for (const void *p : ptrs)
-        if (p && !aligned16(p)) return VLA_ERR_ALIGN;
-    const int kk = resolve_kernel(B, H, T, d_h, kernel);
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return VLA_ERR_ALIGN;
+    kk = resolve_kernel(B, H, T, d_h, kernel);
     const size_t need = vla_workspace_bytes(B, H, T, d_h, io_dtype, kk, chunk);
     if (need > 0 && (!workspace || ws_bytes < need)) return VLA_ERR_WORKSPACE;
+    p = vla::FwdParams{};
+    L = vla::ChunkLayout{};
     if (BH == 0) return VLA_OK;
-
     int *err = device_err_word();
     if (!err) return cuda_fail(cudaGetLastError());
-
-    vla::FwdParams p{};
     p.q = q; p.k = k; p.v = v; p.u = u; p.o = o;
     p.S0 = S0; p.A0 = A0; p.n0 = n0;
     p.S_T = S_T; p.A_T = A_T; p.n_T = n_T;
@@ -229,33 +225,30 @@ int forward_impl(const void *q, const void *k, const void *v, const void *u, int
     p.ws = workspace; p.ws_bytes = ws_bytes; p.chunk = chunk;
     p.events = g_n_events > 0 ? g_events : nullptr;
     p.n_events = g_n_events;
-    int launches = 0;
-    p.launches = &launches;
-
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaSuccess;
     if ((kk == VLA_KERNEL_CHUNK || kk == VLA_KERNEL_CHUNK_TC) && T > 0) {
         const bool tc = (kk == VLA_KERNEL_CHUNK_TC);
-        const vla::ChunkLayout L = vla::chunk_layout((int)BH, T, d_h, chunk, tc && io_dtype == VLA_BF16);
+        L = vla::chunk_layout((int)BH, T, d_h, chunk, tc && io_dtype == VLA_BF16);
         p.rows_tc = tc;
+    }
+    return VLA_OK;
+}
+
+// vla_forward's launches; wait_qv (a cudaEvent_t or null) is waited for before
+// the first pass that reads q or v.
+cudaError_t launch_forward(vla::FwdParams &p, const vla::ChunkLayout &L, int kk, cudaStream_t st, void *wait_qv) {
+    cudaError_t e = cudaSuccess;
+    if ((kk == VLA_KERNEL_CHUNK || kk == VLA_KERNEL_CHUNK_TC) && p.T > 0) {
         p.wait_qv = wait_qv;
-        p.wait_qv2 = wait_qv2;
-        p.qv_split = qv_split;
-        p.done_first = done_first;
-        p.did_split = did_split;
         e = vla::launch_chunk(p, L, st);
     } else {
         // one kernel reads every input
         if (wait_qv) e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(wait_qv), 0);
-        if (e == cudaSuccess && wait_qv2) e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(wait_qv2), 0);
         if (e == cudaSuccess) {
             if (kk == VLA_KERNEL_DECODE) e = vla::launch_decode(p, st);
             else e = vla::launch_seq(p, st);  // (also T == 0: the state copy, for either choice)
         }
     }
-    if (e != cudaSuccess) return cuda_fail(e);
-    t_last_launches = launches;
-    return VLA_OK;
+    return e;
 }
 
 }  // namespace
@@ -266,8 +259,18 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
                 int B, int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *o,
                 float *S_T, float *A_T, float *n_T, int kernel, int chunk, void *workspace,
                 size_t ws_bytes, void *stream) {
-    return forward_impl(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
-                        workspace, ws_bytes, stream, nullptr, nullptr, 0, nullptr, nullptr);
+    vla::FwdParams p;
+    vla::ChunkLayout L;
+    int kk = 0;
+    const int rc = prepare_forward(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel,
+                                   chunk, workspace, ws_bytes, p, L, kk);
+    if (rc != VLA_OK || p.BH == 0) return rc;
+    int launches = 0;
+    p.launches = &launches;
+    const cudaError_t e = launch_forward(p, L, kk, static_cast<cudaStream_t>(stream), nullptr);
+    if (e != cudaSuccess) return cuda_fail(e);
+    t_last_launches = launches;
+    return VLA_OK;
 }
 
 int vla_forward_host(const void *hq, const void *hk, const void *hv, const void *hu, int io_dtype, float lambda0,
@@ -281,83 +284,114 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
     const size_t n_io = (size_t)B * H * (size_t)T * d_h * (io_dtype == VLA_BF16 ? 2 : 4);
     if (n_io > 0 && (!hq || !hk || !hv || !hu || !ho)) return VLA_ERR_ARG;
     const void *hptrs[] = {hq, hk, hv, hu, ho, hS_T, hA_T, hn_T};
-    for (const void *p : hptrs)
-        if (p && !aligned16(p)) return VLA_ERR_ALIGN;
+    for (const void *ptr : hptrs)
+        if (ptr && !aligned16(ptr)) return VLA_ERR_ALIGN;
+    if (hn_T && !n_T) return VLA_ERR_ARG;
     // the device call's own checks (pointers, alignment, workspace) before anything is queued
-    {
-        const long long BH = (long long)B * H;
-        if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
-        if (BH > 0 && (!S_T || !A_T)) return VLA_ERR_ARG;
-        if (BH > 0 && T > 0 && (!q || !k || !v || !u || !o)) return VLA_ERR_ARG;
-        const void *ptrs[] = {q, k, v, u, o, S0, A0, n0, S_T, A_T, n_T, workspace};
-        for (const void *p : ptrs)
-            if (p && !aligned16(p)) return VLA_ERR_ALIGN;
-        const int kk = resolve_kernel(B, H, T, d_h, kernel);
-        const size_t need = vla_workspace_bytes(B, H, T, d_h, io_dtype, kk, chunk);
-        if (need > 0 && (!workspace || ws_bytes < need)) return VLA_ERR_WORKSPACE;
-        if ((hn_T && !n_T)) return VLA_ERR_ARG;
-    }
+    vla::FwdParams p;
+    vla::ChunkLayout L;
+    int kk = 0;
+    rc = prepare_forward(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
+                         workspace, ws_bytes, p, L, kk);
+    if (rc != VLA_OK) return rc;
+    const long long BH = (long long)B * H;
+    if (BH == 0) return VLA_OK;
+    int launches = 0;
+    p.launches = &launches;
+
     cudaStream_t st = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
     cudaEvent_t e_uk = static_cast<cudaEvent_t>(ev_uk), e_qv = static_cast<cudaEvent_t>(ev_qv);
+    const size_t unit = n_io / (size_t)BH;  // bytes of one (b, h) unit of an input
+    auto up = [&](void *dst, const void *src, long long lo, long long n) {
+        return cudaMemcpyAsync(static_cast<unsigned char *>(dst) + unit * (size_t)lo,
+                               static_cast<const unsigned char *>(src) + unit * (size_t)lo, unit * (size_t)n,
+                               cudaMemcpyHostToDevice, cs);
+    };
+    auto down_o = [&](long long lo, long long n, cudaStream_t s) {
+        return cudaMemcpyAsync(static_cast<unsigned char *>(ho) + unit * (size_t)lo,
+                               static_cast<const unsigned char *>(o) + unit * (size_t)lo, unit * (size_t)n,
+                               cudaMemcpyDeviceToHost, s);
+    };
+    auto fail = [&](cudaError_t e) { return cuda_fail(e); };
     cudaError_t e;
     // the uploads overwrite the staging buffers: after `stream`'s earlier work
-    if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return cuda_fail(e);
-    if (n_io > 0) {
-        // u and k first: the Grams, the prefix and the gates read only those
-        if ((e = cudaMemcpyAsync(u, hu, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
-        if ((e = cudaMemcpyAsync(k, hk, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return fail(e);
+    const bool staged = n_io > 0 && BH >= 2 && kk == VLA_KERNEL_CHUNK_TC && vla::chunk_tc_parts_supported(p, L);
+    long long o_lo = 0;  // o from this unit on comes back on `stream`
+    if (staged) {
+        // Every pass of the tensor-core path is per (b, h), so the call runs it in
+        // ranges of units as their inputs land on copy_stream: u and k in two
+        // halves, each followed by its front (Grams, prefix, gates); then q and v
+        // in two or three ranges, each followed by its back (state pass, chain,
+        // output pass). The o of all ranges but the last comes back on
+        // copy_stream once its uploads are all queued; the last range's o and
+        // the final state come back on `stream`, which at the end also waits
+        // for copy_stream. The two events are reused: each wait is queued right
+        // after the record it refers to, before that event is recorded again.
+        const long long h = BH / 2;
+        const long long g[3] = {0, h, BH};
+        const int nr = (BH - h >= 2) ? 3 : 2;
+        const long long r[4] = {0, h, nr == 3 ? h + (BH - h) / 2 : BH, BH};
+        for (int i = 0; i < 2; ++i) {
+            if ((e = up(u, hu, g[i], g[i + 1] - g[i])) != cudaSuccess) return fail(e);
+            if ((e = up(k, hk, g[i], g[i + 1] - g[i])) != cudaSuccess) return fail(e);
+            if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
+            if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
+            if ((e = vla::launch_chunk_tc_part(p, L, 0, (int)g[i], (int)(g[i + 1] - g[i]), st)) != cudaSuccess)
+                return fail(e);
+        }
+        for (int j = 0; j < nr; ++j) {
+            if ((e = up(q, hq, r[j], r[j + 1] - r[j])) != cudaSuccess) return fail(e);
+            if ((e = up(v, hv, r[j], r[j + 1] - r[j])) != cudaSuccess) return fail(e);
+            if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
+            if (j == nr - 1) {
+                // all uploads are queued: the earlier ranges' o leave on copy_stream
+                // (e_qv holds "range 0 done", recorded on `stream` after its back)
+                if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return fail(e);
+                if ((e = down_o(r[0], r[1] - r[0], cs)) != cudaSuccess) return fail(e);
+                if (nr == 3) {
+                    // `stream`'s last queued work is range 1's back
+                    if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
+                    if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return fail(e);
+                    if ((e = down_o(r[1], r[2] - r[1], cs)) != cudaSuccess) return fail(e);
+                }
+            }
+            if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
+            if ((e = vla::launch_chunk_tc_part(p, L, 1, (int)r[j], (int)(r[j + 1] - r[j]), st)) != cudaSuccess)
+                return fail(e);
+            if (j == 0 && (e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
+        }
+        // copy_stream's downloads done: `stream` waits for it after its own copies
+        if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
+        o_lo = r[nr - 1];
+    } else {
+        // u and k first: on the chunked paths the Grams, the prefix and the gates
+        // read only those; the kernels wait for q and v before their first pass
+        // that reads them
+        if (n_io > 0) {
+            if ((e = up(u, hu, 0, BH)) != cudaSuccess) return fail(e);
+            if ((e = up(k, hk, 0, BH)) != cudaSuccess) return fail(e);
+        }
+        if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
+        if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
+        if (n_io > 0) {
+            if ((e = up(q, hq, 0, BH)) != cudaSuccess) return fail(e);
+            if ((e = up(v, hv, 0, BH)) != cudaSuccess) return fail(e);
+        }
+        if ((e = cudaEventRecord(e_qv, cs)) != cudaSuccess) return fail(e);
+        if ((e = launch_forward(p, L, kk, st, ev_qv)) != cudaSuccess) return fail(e);
     }
-    if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return cuda_fail(e);
-    // q and v in two halves of the (b, h) units: the state pass of the first half
-    // starts while the second uploads (ev_uk is reused: the wait above has taken
-    // its first record)
-    const long long BH = (long long)B * H;
-    const int split = BH >= 2 ? (int)(BH / 2) : 0;
-    const size_t unit = BH > 0 ? n_io / (size_t)BH : 0, first = unit * (size_t)split;
-    if (n_io > 0 && split > 0) {
-        const unsigned char *hq8 = static_cast<const unsigned char *>(hq), *hv8 = static_cast<const unsigned char *>(hv);
-        unsigned char *q8 = static_cast<unsigned char *>(q), *v8 = static_cast<unsigned char *>(v);
-        if ((e = cudaMemcpyAsync(q8, hq8, first, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
-        if ((e = cudaMemcpyAsync(v8, hv8, first, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
-        if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return cuda_fail(e);
-        if ((e = cudaMemcpyAsync(q8 + first, hq8 + first, n_io - first, cudaMemcpyHostToDevice, cs)) != cudaSuccess)
-            return cuda_fail(e);
-        if ((e = cudaMemcpyAsync(v8 + first, hv8 + first, n_io - first, cudaMemcpyHostToDevice, cs)) != cudaSuccess)
-            return cuda_fail(e);
-    } else if (n_io > 0) {
-        if ((e = cudaMemcpyAsync(q, hq, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
-        if ((e = cudaMemcpyAsync(v, hv, n_io, cudaMemcpyHostToDevice, cs)) != cudaSuccess) return cuda_fail(e);
-    }
-    if ((e = cudaEventRecord(e_qv, cs)) != cudaSuccess) return cuda_fail(e);
-    const bool two = n_io > 0 && split > 0;
-    int did_split = 0;
-    rc = forward_impl(q, k, v, u, io_dtype, lambda0, B, H, T, d_h, S0, A0, n0, o, S_T, A_T, n_T, kernel, chunk,
-                      workspace, ws_bytes, stream, two ? ev_uk : ev_qv, two ? ev_qv : nullptr, two ? split : 0, ev_uk,
-                      &did_split);
-    if (rc != VLA_OK) return rc;
-    const size_t n_dd = (size_t)B * H * d_h * d_h * 4, n_d = (size_t)B * H * d_h * 4;
-    size_t o_from = 0;
-    if (did_split) {
-        // the first half's o leaves on copy_stream while the second half computes; `stream`
-        // then waits for that copy, so that it covers the whole call
-        if ((e = cudaStreamWaitEvent(cs, e_uk, 0)) != cudaSuccess) return cuda_fail(e);
-        if ((e = cudaMemcpyAsync(ho, o, first, cudaMemcpyDeviceToHost, cs)) != cudaSuccess) return cuda_fail(e);
-        if ((e = cudaEventRecord(e_qv, cs)) != cudaSuccess) return cuda_fail(e);
-        o_from = first;
-    }
-    if (n_io > o_from &&
-        (e = cudaMemcpyAsync(static_cast<unsigned char *>(ho) + o_from, static_cast<const unsigned char *>(o) + o_from,
-                             n_io - o_from, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-        return cuda_fail(e);
+    t_last_launches = launches;
+    const size_t n_dd = (size_t)BH * d_h * d_h * 4, n_d = (size_t)BH * d_h * 4;
+    if (n_io > 0 && o_lo < BH && (e = down_o(o_lo, BH - o_lo, st)) != cudaSuccess) return fail(e);
     if (hS_T && n_dd && (e = cudaMemcpyAsync(hS_T, S_T, n_dd, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-        return cuda_fail(e);
+        return fail(e);
     if (hA_T && n_dd && (e = cudaMemcpyAsync(hA_T, A_T, n_dd, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-        return cuda_fail(e);
+        return fail(e);
     if (hn_T && n_d && (e = cudaMemcpyAsync(hn_T, n_T, n_d, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-        return cuda_fail(e);
-    if (did_split && (e = cudaStreamWaitEvent(st, e_qv, 0)) != cudaSuccess) return cuda_fail(e);
+        return fail(e);
+    if (staged && (e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
     return VLA_OK;
 }
 

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(GramTc<D>::NT) gram_tc_kernel(ChunkArgs a) {
 template <int D>
 __global__ void __launch_bounds__(256) prefix_kernel(ChunkArgs a) {
     constexpr int NB = (D * D + D + 255) / 256;  // blocks per (b, h)
-    const int bh = (int)(blockIdx.x / NB);
+    const int bh = a.bh_lo + (int)(blockIdx.x / NB);
     const int e = (int)(blockIdx.x % NB) * 256 + threadIdx.x;
     const int NC = a.L.NCA;  // A-chunks
     if (e < D * D) {
@@ -1131,7 +1131,7 @@ template <int D>
 __global__ void __launch_bounds__(RowCfg<D>::NT) invert_a0_kernel(ChunkArgs a) {
     using R = RowCfg<D>;
     __shared__ __align__(16) float piv[2 * R::VLEN];
-    const int bh = blockIdx.x;
+    const int bh = a.bh_lo + (int)blockIdx.x;
     const int tid = threadIdx.x, row = tid / R::TPR, part = tid % R::TPR, c0 = part * 32;
     float x[32];
     const float *src = a.p.A0 + (size_t)bh * D * D + row * D + c0;
@@ -1148,6 +1148,54 @@ cudaError_t set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// The tensor-core path (d = 64, bf16 I/O) in two parts per range of units:
+// the front (the initial-A inverse when A0 is given, the Grams, their prefix
+// and the gates: reads u and k) and the back (the state pass, the chain and
+// the output pass: reads q, k, v and the gates). Launch boundaries are
+// numbered on from *p.launches.
+bool tc_parts_ok(const FwdParams &p, const ChunkLayout &L) {
+    return p.d == 64 && p.io_bf16 && p.rows_tc && kGatesOnTensorCores && gram_tma_supported(p, L) &&
+           gates_tc_supported(p, L) && rows_tc_supported(p, L);
+}
+
+cudaError_t tc_front(const ChunkArgs &a, cudaStream_t st) {
+    constexpr int D = 64;
+    using R = RowCfg<D>;
+    const long long n_units = a.bh_n > 0 ? a.bh_n : a.p.BH;
+    int n = a.p.launches ? *a.p.launches : 0;
+    if (n == 0) mark_launch(a.p, 0, st);
+    cudaError_t e;
+    if (a.p.A0) {
+        invert_a0_kernel<D><<<(unsigned)n_units, R::NT, 0, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        mark_launch(a.p, ++n, st);
+    }
+    if ((e = launch_gram_tma(a, st)) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    prefix_kernel<D><<<(unsigned)(((D * D + D + 255) / 256) * n_units), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    if ((e = launch_gates_tc(a, st)) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    return cudaSuccess;
+}
+
+cudaError_t tc_back(const ChunkArgs &a, cudaStream_t st) {
+    constexpr int D = 64;
+    const long long n_units = a.bh_n > 0 ? a.bh_n : a.p.BH;
+    int n = a.p.launches ? *a.p.launches : 0;
+    cudaError_t e;
+    if ((e = set_smem(chain_kernel<D>, ChainSmem<D>::total)) != cudaSuccess) return e;
+    if ((e = launch_rows_tc(a, 0, st)) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    chain_kernel<D><<<(unsigned)((D / chain_rows<D>()) * n_units), 256, ChainSmem<D>::total, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    if ((e = launch_rows_tc(a, 1, st)) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    return cudaSuccess;
+}
+
 template <int D, typename IO>
 cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     using R = RowCfg<D>;
@@ -1155,6 +1203,15 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     if (NCA * BH > 0x7fffffffLL || BH * ((D * D + D + 255) / 256) > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     cudaError_t e;
+    if constexpr (D == 64 && sizeof(IO) == 2) {
+        if (tc_parts_ok(a.p, a.L)) {
+            if ((e = tc_front(a, st)) != cudaSuccess) return e;
+            // the front reads u and k only; q and v may still be arriving
+            if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
+                return e;
+            return tc_back(a, st);
+        }
+    }
     if ((e = set_smem(gates_kernel<D, IO>, GatesSmem<D, IO>::total)) != cudaSuccess) return e;
     using G = GatesCfg<D>;
     if ((e = set_smem(rows_kernel<D, IO, 0>, RowsSmem<D, IO>::total)) != cudaSuccess) return e;
@@ -1191,32 +1248,6 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     const bool tc = a.p.rows_tc && rows_tc_supported(a.p, a.L);
     // the passes so far read u and k only; q and v may still be arriving
     if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
-        return e;
-    if (tc && a.p.wait_qv2 && a.p.qv_split > 0 && a.p.qv_split < a.p.BH) {
-        // two halves of the units, each through the state pass, the chain and the
-        // output pass (all per (b, h)): the first half runs while the second's q, v
-        // land, and its o can leave while the second half computes
-        if (a.p.did_split) *a.p.did_split = 1;
-        ChunkArgs h = a;
-        for (int half = 0; half < 2; ++half) {
-            h.bh_lo = half ? a.p.qv_split : 0;
-            h.bh_n = half ? a.p.BH - a.p.qv_split : a.p.qv_split;
-            if (half && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess)
-                return e;
-            if ((e = launch_rows_tc(h, 0, st)) != cudaSuccess) return e;
-            mark_launch(a.p, ++n, st);
-            chain_kernel<D><<<(unsigned)((D / chain_rows<D>()) * h.bh_n), 256, ChainSmem<D>::total, st>>>(h);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-            mark_launch(a.p, ++n, st);
-            if ((e = launch_rows_tc(h, 1, st)) != cudaSuccess) return e;
-            mark_launch(a.p, ++n, st);
-            if (!half && a.p.done_first &&
-                (e = cudaEventRecord(static_cast<cudaEvent_t>(a.p.done_first), st)) != cudaSuccess)
-                return e;
-        }
-        return cudaSuccess;
-    }
-    if (a.p.wait_qv2 && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv2), 0)) != cudaSuccess)
         return e;
     if (tc) {
         if ((e = launch_rows_tc(a, 0, st)) != cudaSuccess) return e;
@@ -1352,6 +1383,18 @@ ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc_path) {
     if (L.yh) off = align256(off + bh * nc * (size_t)(L.C / 64) * 32768);
     L.total = off;
     return L;
+}
+
+bool chunk_tc_parts_supported(const FwdParams &p, const ChunkLayout &L) { return tc_parts_ok(p, L); }
+
+cudaError_t launch_chunk_tc_part(const FwdParams &p, const ChunkLayout &L, int part, int bh_lo, int bh_n,
+                                 cudaStream_t stream) {
+    if (!tc_parts_ok(p, L) || bh_lo < 0 || bh_n <= 0 || bh_lo + bh_n > p.BH) return cudaErrorInvalidValue;
+    if ((long long)L.NCA * bh_n > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    ChunkArgs a{p, L};
+    a.bh_lo = bh_lo;
+    a.bh_n = bh_n;
+    return part == 0 ? tc_front(a, stream) : tc_back(a, stream);
 }
 
 cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream) {

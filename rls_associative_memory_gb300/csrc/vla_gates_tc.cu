@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     unsigned char *bz_lo = slot + 3 * kTile, *ep_lo = slot + 4 * kTile, *zt_lo = slot + 5 * kTile;
 
     const int NCA = a.L.NCA, CA = a.L.CA, T = a.p.T;
-    const int c = (int)(blockIdx.x % (unsigned)NCA), bh = (int)(blockIdx.x / (unsigned)NCA);
+    const int c = (int)(blockIdx.x % (unsigned)NCA), bh = a.bh_lo + (int)(blockIdx.x / (unsigned)NCA);
     const int t0 = c * CA, ntok = min(CA, T - t0), nsb = (ntok + kSB - 1) / kSB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int qw = warp & 3, hw = warp >> 2;  // TMEM lane quarter, column half
@@ -385,7 +385,7 @@ cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream) {
     constexpr size_t bytes = GtLayout::total + 1024;  // + alignment slack
     cudaError_t e = cudaFuncSetAttribute(gates_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    const long long grid = (long long)a.L.NCA * a.p.BH;
+    const long long grid = (long long)a.L.NCA * (a.bh_n > 0 ? a.bh_n : a.p.BH);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     gates_tc_kernel<<<(unsigned)grid, kThreads, bytes, stream>>>(a);
     return cudaGetLastError();

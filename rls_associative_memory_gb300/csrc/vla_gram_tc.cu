@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kGThreads) gram_tma_kernel(ChunkArgs a, const 
     float *nred = reinterpret_cast<float *>(smem + L::nred);
 
     const int NCA = a.L.NCA, CA = a.L.CA, T = a.p.T;
-    const int c = (int)(blockIdx.x % (unsigned)NCA), bh = (int)(blockIdx.x / (unsigned)NCA);
+    const int c = (int)(blockIdx.x % (unsigned)NCA), bh = a.bh_lo + (int)(blockIdx.x / (unsigned)NCA);
     const int t0 = c * CA, ntok = min(CA, T - t0), nst = (ntok + kSB - 1) / kSB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     auto su = [&](int b) { return smem + L::tiles + (size_t)b * 2 * kTile; };
@@ -232,7 +232,7 @@ cudaError_t launch_gram_tma(const ChunkArgs &a, cudaStream_t stream) {
     constexpr size_t bytes = GrLayout::total + 1024;  // + alignment slack
     cudaError_t e = cudaFuncSetAttribute(gram_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    const long long grid = (long long)a.L.NCA * a.p.BH;
+    const long long grid = (long long)a.L.NCA * (a.bh_n > 0 ? a.bh_n : a.p.BH);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     gram_tma_kernel<<<(unsigned)grid, kGThreads, bytes, stream>>>(a, tm_u, tm_k);
     return cudaGetLastError();

@@ -37,10 +37,6 @@ struct FwdParams {
     int rows_tc;                // chunked kernel: state passes on the tensor cores where supported
     void *wait_qv;              // optional cudaEvent_t: the stream waits for it before the first pass
                                 // that reads q or v (the chunked path's state pass)
-    void *wait_qv2;             // optional second event (tensor-core path): q, v of the units from
-    int qv_split;               // qv_split on; the passes from the state pass on then run per half
-    void *done_first;           // optional event recorded after the first half's output pass
-    int *did_split;             // optional out: set to 1 when the passes ran per half
     void *const *events;        // measurement hook: cudaEvent_t handles, or null
     int n_events;
     int *launches;              // out: number of kernels launched
@@ -107,6 +103,17 @@ int api_cuda_fail(cudaError_t e);
 ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc = false);
 // Chunk-parallel path (six launches).  Returns a cudaError_t.
 cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream);
+// The tensor-core path (d = 64, bf16 I/O, every pass on its tensor-core
+// kernel) for a range of units [bh_lo, bh_lo + bh_n), in two parts: part 0,
+// the front (the initial-A inverse when A0 is given, the Grams, their prefix
+// and the gates; reads u and k), and part 1, the back (the state pass, the
+// chain and the output pass; reads q, k, v and the front's gates). A caller
+// that overlaps the input uploads runs the fronts and the backs of its
+// ranges as the data lands; each back after its range's front. Launch
+// boundaries are numbered on from *p.launches.
+bool chunk_tc_parts_supported(const FwdParams &p, const ChunkLayout &L);
+cudaError_t launch_chunk_tc_part(const FwdParams &p, const ChunkLayout &L, int part, int bh_lo, int bh_n,
+                                 cudaStream_t stream);
 
 // Kernel argument of the chunk-parallel kernels.
 struct ChunkArgs {

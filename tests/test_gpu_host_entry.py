@@ -11,12 +11,24 @@ from vla_testutil import compare, oracle_ref, to_device
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kernel,T,dtype", [(vla.VLA_KERNEL_CHUNK_TC, 1000, "bf16"), (vla.VLA_KERNEL_SEQ, 77, "f32"),
-                                            (vla.VLA_KERNEL_CHUNK, 300, "bf16"), (vla.VLA_KERNEL_AUTO, 3, "bf16")])
-def test_host_entry_matches_device_entry(kernel, T, dtype):
-    x = make_inputs(1, 3, T, 64, dtype, seed=61 + T, u_scale=0.5)
+@pytest.mark.parametrize("kernel,B,H,T,dtype,init", [
+    (vla.VLA_KERNEL_CHUNK_TC, 1, 3, 1000, "bf16", False),  # ranges of units 1 | 1 | 1
+    (vla.VLA_KERNEL_CHUNK_TC, 1, 2, 700, "bf16", False),   # 1 | 1 (two ranges)
+    (vla.VLA_KERNEL_CHUNK_TC, 2, 4, 1000, "bf16", True),   # 4 | 2 | 2, A0 inverted per range
+    (vla.VLA_KERNEL_CHUNK_TC, 1, 5, 640, "bf16", False),   # 2 | 1 | 2
+    (vla.VLA_KERNEL_SEQ, 1, 3, 77, "f32", False), (vla.VLA_KERNEL_CHUNK, 1, 3, 300, "bf16", False),
+    (vla.VLA_KERNEL_AUTO, 1, 3, 3, "bf16", False)])
+def test_host_entry_matches_device_entry(kernel, B, H, T, dtype, init):
+    x = make_inputs(B, H, T, 64, dtype, seed=61 + T, u_scale=0.5)
     q, k, v, u = to_device(x)
-    o_ref, S_ref, A_ref, n_ref = vla.vla_forward(q, k, v, u, x.lambda0, kernel=kernel)
+    S0 = A0 = n0 = None
+    ref0 = {}
+    if init:
+        pre = make_inputs(B, H, 90, 64, dtype, seed=60 + T, u_scale=0.5)
+        st = oracle_ref(pre)
+        S0, A0, n0 = (torch.from_numpy(st[n]).float().cuda().contiguous() for n in ("S_T", "A_T", "n_T"))
+        ref0 = dict(S0=st["S_T"], A0=st["A_T"], n0=st["n_T"])
+    o_ref, S_ref, A_ref, n_ref = vla.vla_forward(q, k, v, u, x.lambda0, S0=S0, A0=A0, n0=n0, kernel=kernel)
     torch.cuda.synchronize()
 
     hq, hk, hv, hu = (t.cpu().pin_memory() for t in (q, k, v, u))
@@ -33,12 +45,12 @@ def test_host_entry_matches_device_entry(kernel, T, dtype):
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
     stream, copy_stream = torch.cuda.current_stream(), torch.cuda.Stream()
     vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, dq, dk, dv, du, o, ho, S_T, A_T, n_T, hS, hA, hn,
-                         kernel=kernel, workspace=ws, stream=stream, copy_stream=copy_stream)
+                         S0=S0, A0=A0, n0=n0, kernel=kernel, workspace=ws, stream=stream, copy_stream=copy_stream)
     stream.synchronize()
     assert torch.equal(ho, o_ref.cpu())
     assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
     got = {"o": ho.float().numpy(), "S_T": hS.numpy(), "A_T": hA.numpy(), "n_T": hn.numpy()}
-    compare(got, oracle_ref(x), dtype)
+    compare(got, oracle_ref(x, **ref0), dtype)
 
 
 def _host_call(x, kernel, S0=None, A0=None, n0=None, in_place=False):
