@@ -49,9 +49,9 @@ struct GtLayout {
     // pivot rows in slot 3 (sub-blocks) or slot 5
     // chunk start: M^(c) (fp32, 64 x kGS) in slots 0-2, then (1/D) L^{-1} hi, lo in slots 0, 1
     static constexpr size_t xt = slots + 6 * kTile;         // I + G (fp32, 64 x kGS), then X^T hi, lo
-    static constexpr size_t ksc = xt + (size_t)64 * kGS * 4;  // [64] 1 / max(|k|, eps)
-    static constexpr size_t kn = ksc + 256;                 // [64] max(|k|, eps)
-    static constexpr size_t beta = kn + 256;                // [64]
+    static constexpr size_t ksc = xt + (size_t)64 * kGS * 4;  // [2][64] 1 / max(|k|, eps) (by sub-block parity)
+    static constexpr size_t kn = ksc + 512;                 // [2][64] max(|k|, eps)
+    static constexpr size_t beta = kn + 512;                // [64]
     static constexpr size_t nrm = beta + 256;               // [2][64] halves of |row|^2
     static constexpr size_t total = nrm + 512;
 };
@@ -184,33 +184,39 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         return *abort_flag == 0;
     };
 
+    // [U; K] of sub-block sb into its operand tile and its key norms into the
+    // sb-parity half of s_kn, s_ks (the other half still serves sub-block sb - 1);
+    // the tile is read by the tensor cores after a proxy fence and a barrier
+    auto stage_in = [&](int sb) {
+        const int nt = min(kSB, ntok - sb * kSB);
+        if (pt >= nt) ru[0] = ru[1] = rk[0] = rk[1] = make_uint4(0, 0, 0, 0);  // past the chunk
+        float kf[16];
+        unpack8(rk[0], kf);
+        unpack8(rk[1], kf + 8);
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) ss = fmaf(kf[m], kf[m], ss);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+        const float kn = fmaxf(sqrtf(ss), kEps);
+        if (pq == 0) {
+            s_kn[64 * (sb & 1) + pt] = kn;
+            s_ks[64 * (sb & 1) + pt] = 1.f / kn;
+        }
+        *reinterpret_cast<uint4 *>(uk + toff(pt, 16 * pq)) = ru[0];
+        *reinterpret_cast<uint4 *>(uk + toff(pt, 16 * pq + 8)) = ru[1];
+        *reinterpret_cast<uint4 *>(uk + toff(64 + pt, 16 * pq)) = rk[0];
+        *reinterpret_cast<uint4 *>(uk + toff(64 + pt, 16 * pq + 8)) = rk[1];
+        fence_proxy_async_smem();
+    };
+
     bool ok = true;
     load_in(0);
+    if (nsb > 0) stage_in(0);
+    __syncthreads();
     for (int sb = 0; sb < nsb; ++sb) {
         const int nt = min(kSB, ntok - sb * kSB);
-        // ---- stage [U; K] and the key norms ----
-        if (pt >= nt) ru[0] = ru[1] = rk[0] = rk[1] = make_uint4(0, 0, 0, 0);  // past the chunk
-        {
-            float kf[16];
-            unpack8(rk[0], kf);
-            unpack8(rk[1], kf + 8);
-            float ss = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) ss = fmaf(kf[m], kf[m], ss);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-            const float kn = fmaxf(sqrtf(ss), kEps);
-            if (pq == 0) {
-                s_kn[pt] = kn;
-                s_ks[pt] = 1.f / kn;
-            }
-            *reinterpret_cast<uint4 *>(uk + toff(pt, 16 * pq)) = ru[0];
-            *reinterpret_cast<uint4 *>(uk + toff(pt, 16 * pq + 8)) = ru[1];
-            *reinterpret_cast<uint4 *>(uk + toff(64 + pt, 16 * pq)) = rk[0];
-            *reinterpret_cast<uint4 *>(uk + toff(64 + pt, 16 * pq + 8)) = rk[1];
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
+        const float *kn_sb = s_kn + 64 * (sb & 1), *ks_sb = s_ks + 64 * (sb & 1);
         // ---- R1: D1 = [U; K] A (M = 128) ----
         if (tid == 0) {
             tc_fence_after();
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             float v[32];
             tmem_ld32(tq + col_d2 + 32 * hw, v);  // Y[s][t], t = 32 hw ..
             if (act64) {
-                const float4 *k4 = reinterpret_cast<const float4 *>(s_ks + 32 * hw);
+                const float4 *k4 = reinterpret_cast<const float4 *>(ks_sb + 32 * hw);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float4 kv = k4[q];
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             }
             tmem_ld32(tq + col_d2 + 64 + 32 * hw, v);  // P[s][t] = z_s . k_hat_t, t = 32 hw ..
             if (act64) {
-                const float4 *n4 = reinterpret_cast<const float4 *>(s_kn + 32 * hw);
+                const float4 *n4 = reinterpret_cast<const float4 *>(kn_sb + 32 * hw);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float4 kv = n4[q];
@@ -327,6 +333,9 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
                                   idesc_bf16_f32(64, 64), true);
             umma_commit(bar);
         }
+        // the next sub-block's [U; K] while round 4 runs ([U; K] was last read by
+        // round 2; its loads were issued after round 3's issue)
+        if (sb + 1 < nsb) stage_in(sb + 1);
         if (!round_wait()) {
             ok = false;
             break;
@@ -351,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             if (qw >= 2 && t < nt) {
                 // alpha = g / max(|g|, eps) with g = row / |k_t|
                 const float nr = sqrtf(s_nrm[t] + s_nrm[64 + t]);
-                const float sc = 1.f / fmaxf(nr, kEps * s_kn[t]);
+                const float sc = 1.f / fmaxf(nr, kEps * kn_sb[t]);
                 float4 *dst = reinterpret_cast<float4 *>(galpha + (size_t)(sb * kSB + t) * kD + 32 * hw);
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
