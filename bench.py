@@ -50,8 +50,8 @@ TRAFFIC = {
     # profiles/seq_kernel_long.md: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
     ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
     # profiles/chunk_tc_long.md: at T=16384 (same 16 heads), scaled x4 to T=65536
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (76.625664e6 + 19.006208e6), "src_sha": "3fea45f876245715"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.706048e6 + 102.05568e6), "src_sha": "3fea45f876245715"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (76.668928e6 + 18.857984e6), "src_sha": "7937a7a93ac61e07"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.859648e6 + 102.140416e6), "src_sha": "7937a7a93ac61e07"},
 }
 
 
