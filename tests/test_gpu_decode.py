@@ -60,3 +60,31 @@ def test_decode_workload_full_size():
     ref = oracle_ref(x, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"])
     errs = compare(got, ref, "bf16")
     print("\ndecode full-size errs", errs)
+
+
+@pytest.mark.parametrize("given", ["both", "A0", "S0"])
+def test_decode_many_units_in_place(given):
+    """More units than resident CTAs (8 x 80 = 640): each CTA walks several
+    units while the next units' initial state lands in shared memory; the
+    state is updated in place, and with only A0 or only S0 given the other
+    starts from its default (I / lambda0, 0)."""
+    B, H, d, T = 8, 80, 64, 2
+    pre = make_inputs(B, H, 12, d, "bf16", seed=500, lambda0=0.8)
+    st = oracle_ref(pre)
+    x = make_inputs(B, H, T, d, "bf16", seed=501, lambda0=0.8)
+    q, k, v, u = to_device(x)
+    dev = q.device
+    S = torch.from_numpy(st["S_T"]).float().to(dev).contiguous() if given in ("both", "S0") else None
+    A = torch.from_numpy(st["A_T"]).float().to(dev).contiguous() if given in ("both", "A0") else None
+    n = torch.from_numpy(st["n_T"]).float().to(dev).contiguous()
+    S_T = S if S is not None else torch.empty(B, H, d, d, device=dev)
+    A_T = A if A is not None else torch.empty(B, H, d, d, device=dev)
+    o, S_out, A_out, n_out = vla.vla_forward(q, k, v, u, x.lambda0, S0=S, A0=A, n0=n, S_T=S_T, A_T=A_T, n_T=n,
+                                             kernel=vla.VLA_KERNEL_DECODE)
+    torch.cuda.synchronize()
+    assert vla.vla_device_status() == vla.VLA_OK
+    ref = oracle_ref(x, S0=st["S_T"] if S is not None else None, A0=st["A_T"] if A is not None else None,
+                     n0=st["n_T"])
+    got = {"o": o.float().cpu().numpy(), "S_T": S_out.cpu().numpy(), "A_T": A_out.cpu().numpy(),
+           "n_T": n_out.cpu().numpy()}
+    compare(got, ref, "bf16")
