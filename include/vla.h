@@ -123,7 +123,9 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * ev_uk, ev_qv    two cudaEvent_t (as void*) the call records; required.
  * Asynchronous: the host buffers must stay valid until `stream` has passed
  * the call's work.  Returns as vla_forward; on an argument error nothing is
- * queued.
+ * queued.  On VLA_ERR_CUDA (a failed copy, record or launch) the work queued
+ * before the failure may still run on both streams: synchronise both before
+ * reusing the buffers.
  */
 int vla_forward_host(const void *hq, const void *hk, const void *hv, const void *hu, int io_dtype,
                      float lambda0, int B, int H, int T, int d_h, const float *S0, const float *A0,
