@@ -104,3 +104,26 @@ def test_host_entry_decode_in_place():
     S, A, n = (torch.from_numpy(st[k]).float().cuda().contiguous() for k in ("S_T", "A_T", "n_T"))
     got = _host_call(x, vla.VLA_KERNEL_DECODE, S0=S, A0=A, n0=n, in_place=True)
     compare(got, oracle_ref(x, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"]), "bf16")
+
+
+def test_host_entry_one_stream():
+    """copy_stream == stream: the ranges run one after another, same results."""
+    x = make_inputs(1, 3, 700, 64, "bf16", seed=76, u_scale=0.5)
+    q, k, v, u = to_device(x)
+    o_ref, S_ref, A_ref, n_ref = vla.vla_forward(q, k, v, u, x.lambda0, kernel=vla.VLA_KERNEL_CHUNK_TC)
+    torch.cuda.synchronize()
+    hq, hk, hv, hu = (t.cpu().pin_memory() for t in (q, k, v, u))
+    dq, dk, dv, du = (torch.empty_like(t) for t in (q, k, v, u))
+    o = torch.empty_like(q)
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    S_T, A_T, n_T = torch.empty_like(S_ref), torch.empty_like(A_ref), torch.empty_like(n_ref)
+    hS, hA, hn = (torch.empty(t.shape).pin_memory() for t in (S_T, A_T, n_T))
+    B, H, T, d = q.shape
+    ws = torch.empty(vla.vla_workspace_bytes(B, H, T, d, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK_TC), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+    vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, dq, dk, dv, du, o, ho, S_T, A_T, n_T, hS, hA, hn,
+                         kernel=vla.VLA_KERNEL_CHUNK_TC, workspace=ws, stream=stream, copy_stream=stream)
+    stream.synchronize()
+    assert torch.equal(ho, o_ref.cpu())
+    assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
