@@ -124,7 +124,9 @@ size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kerne
 size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h) {
     if (check_common(VLA_F32, 1.f, B, H, T, d_h, VLA_KERNEL_AUTO) != VLA_OK) return 0;
     if (d_h != 32 && d_h != 64) return 0;
-    return vla::backward_workspace_floats(B * H, T, d_h) * sizeof(float);
+    const size_t seq = vla::backward_workspace_floats(B * H, T, d_h) * sizeof(float);
+    const size_t chunked = vla::backward_chunk_bytes(B * H, T, d_h);
+    return seq > chunked ? seq : chunked;
 }
 
 int vla_backward(const void *q, const void *k, const void *v, const void *u, const void *dO, int io_dtype,

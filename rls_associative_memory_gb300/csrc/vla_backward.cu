@@ -420,6 +420,10 @@ size_t backward_workspace_floats(int BH, int T, int d) {
 
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream) {
     if (p.BH == 0) return cudaSuccess;
+    // two or more of the chunked forward's S-chunks: in parallel over the chunks
+    bool chunked = false;
+    const cudaError_t ec = launch_backward_chunk(p, stream, &chunked);
+    if (ec != cudaSuccess || chunked) return ec;
     if (p.io_bf16) {
         switch (p.d) {
             case 32: return launch_backward_t<32, __nv_bfloat16>(p, stream);

@@ -65,6 +65,12 @@ struct BwdParams {
 };
 size_t backward_workspace_floats(int BH, int T, int d);
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
+// The backward in parallel over the chunked forward's S-chunks (vla_backward_chunk.cu):
+// its workspace bytes (the larger of the bf16 and fp32 layouts; 0 when fewer
+// than two chunks), and its launches (*used = false, nothing launched, when it
+// does not apply to the shape).
+size_t backward_chunk_bytes(int BH, int T, int d);
+cudaError_t launch_backward_chunk(const BwdParams &p, cudaStream_t stream, bool *used);
 
 // Decode step: one CTA per (b, h), state streamed from HBM.  Returns a cudaError_t.
 cudaError_t launch_decode(const FwdParams &p, cudaStream_t stream);
