@@ -302,7 +302,8 @@ def type_of(v):
 
 def run_backward(args):
     """--pass backward: gradients of sum <dO, o> for one batch of the workload
-    (vla_backward: forward recompute + reverse sweep in one launch)."""
+    (vla_backward: in parallel over the chunked forward's chunks when the
+    stream has two or more, else one sequential launch per step)."""
     import torch
     import rls_associative_memory_gb300 as vla
     dev = torch.device("cuda", 0)
@@ -323,6 +324,7 @@ def run_backward(args):
         vla.vla_backward(q, k, v, u, dO, x.lambda0, workspace=ws)
         en[i].record()
     torch.cuda.synchronize(dev)
+    launches = vla.vla_last_launch_count()
     ms = float(np.mean([a.elapsed_time(b) for a, b in zip(st, en)]))
     units = B * H * T
     # forward recompute (12 d^2) + reverse sweep (28 d^2: four matrix-vector
@@ -333,9 +335,11 @@ def run_backward(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "dtype": "f32", "data": "synthetic", "config": config_block(args.config, x, "backward"),
             "roofline": {"bound": "alu", "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                         "frac": tf / FP32_PEAK_TFLOPS, "traffic": None, "kernel": "backward_kernel<%d,%s>" % (d, x.dtype),
+                         "frac": tf / FP32_PEAK_TFLOPS, "traffic": None,
+                         "kernel": ("chunked backward (%d launches)" % launches if launches > 1
+                                    else "backward_kernel<%d,%s>" % (d, x.dtype)),
                          "algorithmic_flops": flops},
-            "gpu_launches": args.steps}
+            "gpu_launches": args.steps * launches}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -195,8 +195,15 @@ int vla_last_launch_count(void);
  *                 unsymmetrised adjoint of A_0.
  * d_h             32 or 64 (VLA_ERR_UNSUPPORTED_DIM otherwise).
  * workspace       at least vla_backward_workspace_bytes(B, H, T, d_h) bytes.
- * One CTA per (b, h) reruns the forward, storing per-token records and a
- * state checkpoint every 64 tokens, then sweeps the tokens in reverse.
+ * When the stream spans two or more chunks of the chunked forward
+ * (vla_forward's default chunk length), the call runs that forward for the
+ * chunk-start states and then works on all chunks in parallel: over a chunk
+ * the adjoint of S is an affine map with one d x d product (the chunk's
+ * transitions of section 3.1), the symmetric part of the adjoint of A (the
+ * only part that feeds back) a two-sided one, and the adjoint of n a sum, so
+ * short chains along the chunks give every chunk its end adjoints.  Shorter
+ * streams run one CTA per (b, h), which reruns the forward (records and a
+ * state checkpoint every 64 tokens) and sweeps the tokens in reverse.
  * Asynchronous on stream; returns VLA_OK or a VLA_ERR_* code.
  */
 int vla_backward(const void *q, const void *k, const void *v, const void *u, const void *dO,

@@ -150,9 +150,11 @@ int vla_backward(const void *q, const void *k, const void *v, const void *u, con
     p.dq = dq; p.dk = dk; p.dv = dv; p.du = du; p.dS0 = dS0; p.dA0 = dA0; p.dn0 = dn0;
     p.BH = (int)BH; p.T = T; p.d = d_h; p.io_bf16 = (io_dtype == VLA_BF16); p.lambda0 = lambda0;
     p.ws = static_cast<float *>(workspace);
+    int launches = 0;
+    p.launches = &launches;
     const cudaError_t e = vla::launch_backward(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
-    t_last_launches = 1;
+    t_last_launches = launches;
     return VLA_OK;
 }
 

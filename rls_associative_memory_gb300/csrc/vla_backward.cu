@@ -424,6 +424,7 @@ cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream) {
     bool chunked = false;
     const cudaError_t ec = launch_backward_chunk(p, stream, &chunked);
     if (ec != cudaSuccess || chunked) return ec;
+    if (p.launches) *p.launches = 1;
     if (p.io_bf16) {
         switch (p.d) {
             case 32: return launch_backward_t<32, __nv_bfloat16>(p, stream);

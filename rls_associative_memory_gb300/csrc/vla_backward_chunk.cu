@@ -773,8 +773,11 @@ cudaError_t launch_backward_chunk(const BwdParams &p, cudaStream_t st, bool *use
     f.ws_bytes = b.L.total;
     f.chunk = 0;
     f.rows_tc = (p.d == 64 && p.io_bf16) ? 1 : 0;
+    int nf = 0;
+    f.launches = &nf;
     cudaError_t e = launch_chunk(f, b.L, st);
     if (e != cudaSuccess) return e;
+    if (p.launches) *p.launches = nf + (p.dA0 ? 7 : 6);
     BcArgs a{};
     a.p = p;
     a.L = b.L;

@@ -62,6 +62,7 @@ struct BwdParams {
     int BH, T, d, io_bf16;
     float lambda0;
     float *ws;                                       // backward_workspace_floats(BH, T, d) floats
+    int *launches;                                   // out (optional): kernels launched
 };
 size_t backward_workspace_floats(int BH, int T, int d);
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
