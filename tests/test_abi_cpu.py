@@ -143,6 +143,12 @@ def test_backward_argument_checks():
     assert L.vla_backward(*args(k=f + 4)) == vla.VLA_ERR_ALIGN
     assert vla.vla_backward_workspace_bytes(1, 2, 16, 128) == 0
     assert vla.vla_backward_workspace_bytes(1, 2, 16, 64) == 2 * (16 * 260 + 1 * (2 * 64 * 64 + 64)) * 4
+    # streams of two or more forward chunks: the chunk-parallel backward carves the chunked
+    # forward's workspace, its o, the per-token records and dg / dk_hat parts, and the maps
+    BH, T, d = 16, 65536, 64
+    fwd = max(vla.vla_workspace_bytes(1, BH, T, d, io, vla.VLA_KERNEL_CHUNK_TC) for io in (vla.VLA_BF16, vla.VLA_F32))
+    need = vla.vla_backward_workspace_bytes(1, BH, T, d)
+    assert need >= fwd + BH * T * d * 2 + BH * T * ((4 * d + 4) + 2 * d) * 4
 
 
 def test_debug_hook_is_host_state_only():
