@@ -216,7 +216,10 @@ int vla_backward(const void *q, const void *k, const void *v, const void *u, con
 size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h);
 
 /* Size of the device scratch array built into the library for
- * vla_forward_noalloc (64 MiB on every GPU that loads the library). */
+ * vla_forward_noalloc.  It is a static device array: each GPU holds its
+ * 64 MiB from the moment the library's code is loaded on that GPU until the
+ * process exits.  Under CUDA's default lazy module loading that moment is
+ * the entry point's set-up (its first call on the GPU), not library load. */
 #define VLA_NOALLOC_SCRATCH_BYTES (64ull << 20)
 
 /*
@@ -238,6 +241,15 @@ size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h);
  * outputs are still the caller's device buffers.  The call allocates
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *
+ * Set-up: the array's device address is looked up (cudaGetSymbolAddress,
+ * with the device current) by the first call on each device, and again by
+ * the first call in a different driver context of that device (after a
+ * cudaDeviceReset, say); the address is kept per device together with the
+ * id of the context it belongs to.  Make that first call before any stream
+ * capture begins.  A call with B = 0 (every pointer may then be NULL) does
+ * the set-up and nothing else: a host that takes its memory budget at
+ * start-up should make it first, so that the 64 MiB are already held.
+ *
  * Limits and sharing:
  *   - Problems whose chunked workspace (vla_workspace_bytes with
  *     VLA_KERNEL_CHUNK and the same chunk) exceeds VLA_NOALLOC_SCRATCH_BYTES
@@ -248,9 +260,6 @@ size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h);
  *     is written earlier in the same call.  Calls that overlap on the GPU
  *     (different streams, or different host threads without ordering)
  *     race on the array and produce garbage; serialise them.
- *   - The first call on each device (with that device current) looks up the
- *     array's device address once; make that first call before any stream
- *     capture begins.
  * Returns VLA_OK or a VLA_ERR_* code.
  */
 int vla_forward_noalloc(const void *q, const void *k, const void *v, const void *u, int io_dtype,

@@ -9,7 +9,7 @@ import torch
 import oracle
 import rls_associative_memory_gb300 as vla
 from synthetic import make_config, make_inputs
-from vla_testutil import TOL, compare, oracle_ref, rel_fro, run_gpu, to_device
+from vla_testutil import TOL, compare, oracle_ref, rel_fro, run_gpu, to_device, window_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -188,6 +188,13 @@ def test_full_config_parity(kernel, name):
     sub = {key: flat(val)[heads] for key, val in got.items()}
     errs = compare(sub, ref, x.dtype)
     print("\n%s %s heads=%d errs=%s" % (name, _kid(kernel), len(heads), errs))
+    # o over windows of the stream (the late tokens carry little of the whole
+    # tensor's norm under the 1/t decay of the readout)
+    win = 4096 if T >= 8192 else max(64, T // 8)
+    wins, last = window_errors(sub["o"], ref["o"], win)
+    print("o per %d-token window: max %.3g (window %d), last %d tokens %.3g"
+          % (win, max(wins), int(np.argmax(wins)), win, last))
+    assert max(wins) <= TOL[x.dtype] and last <= TOL[x.dtype], (wins, last)
     if x.keys is not None:
         # recall measurement: |S_T key_i - value_i| from the GPU state vs the oracle's
         keys = flat(x.keys)[heads]

@@ -57,3 +57,14 @@ def compare(gpu, ref, dtype, keys=("o", "S_T", "A_T", "n_T")):
 
 def oracle_ref(x, **kw):
     return oracle.forward_inputs(x, **kw)
+
+
+def window_errors(o_gpu, o_ref, win):
+    """Relative Frobenius error of o over consecutive token windows of `win`
+    tokens (the last one ragged) and over the last `win` tokens: under the
+    readout's 1/t decay a whole-tensor ratio is dominated by the early
+    tokens, these show the late ones."""
+    T = o_ref.shape[-2]
+    wins = [rel_fro(o_gpu[..., a:min(T, a + win), :], o_ref[..., a:min(T, a + win), :]) for a in range(0, T, win)]
+    last = rel_fro(o_gpu[..., max(0, T - win):, :], o_ref[..., max(0, T - win):, :])
+    return wins, last
