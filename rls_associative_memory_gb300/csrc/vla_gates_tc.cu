@@ -13,22 +13,32 @@
 //   A_t k_hat_t = A k_hat_t - sum_{s <= t} beta_s z_s (z_s . k_hat_t),
 //     z_s . k_hat_t = (X^T U^T A K_hat)[s][t]
 //   A_end = A - Z diag(beta) Z^T
-// Per sub-block (tensor-core rounds R1..R4; tiles and products as in the
+// Per sub-block (tensor-core rounds R1, R2, R4; tiles and products as in the
 // state passes, bf16 hi/lo pairs for fp32 operands):
 //   R1  D1 = [U; K] A                 rows: w_t, A k_t
 //   R2  D2 = U [A K ; W]^T            Y = U^T A K, G = U^T W
-//   on the CUDA cores: elimination of [I + G | I] -> [D L^T | L^{-1}],
-//       L^{-1} = X^T and beta_s = 1 / pivot_s (the trailing block stays
+//   on the CUDA cores, in fp32: forward elimination of [I + G | W^T | Y_hat]
+//       (Y_hat = Y diag(1/|k|)) -> [D L^T | L^{-1} W^T | L^{-1} Y_hat]: the
+//       rows of L^{-1} W^T are z_s^T (X = L^{-T}), P = L^{-1} Y_hat holds
+//       z_s . k_hat_t, and beta_s = 1 / pivot_s (the trailing block stays
 //       symmetric, so the multipliers come from the pivot row)
-//   R3  D3 = X^T [W | Y_hat]          Z^T and P = X^T Y_hat, Y_hat = Y diag(1/|k|)
 //   R4  D1[k rows] += E'^T Z^T        E'[s][t] = -beta_s P[s][t] |k_t| (s <= t):
 //                                      the rows become |k_t| A_t k_hat_t
 //       A += -(Z diag(beta)) Z^T      (A held in fp32 in TMEM for the whole
-//                                      A-chunk; the product accumulates onto it)
+//                                      A-chunk; the product accumulates onto
+//                                      it with three-way bf16 splits)
 //   alpha_t = that row / |that row|, and the new A's operand tiles.
+// Precision: Z and P carry most of the cancellation when the sub-block's
+// penalty directions outweigh the penalty accumulated so far (A_t k_hat_t is
+// then a small difference of large terms; at the start of a stream, or with
+// large u or small lambda0).  They come out of the fp32 elimination, not
+// out of split products, and the downdate of A, which accumulates over the
+// A-chunk, takes three-way splits (x = x0 + x1 + x2, the six products with
+// i + j <= 2, about 2^-24 relative); the other products keep hi/lo pairs.
 // A starts each A-chunk from its definition (M^(c))^{-1}, M^(c) = lambda0 I +
-// the Grams of the earlier A-chunks: the same elimination on M^(c) gives
-// E = L^{-1} and D, then A = E^T D^{-1} E is one product on the tensor cores.
+// the Grams of the earlier A-chunks: the same elimination on M^(c) against
+// the identity gives E = L^{-1} and D, then A = E^T D^{-1} E is one product on
+// the tensor cores (a sum of positive semi-definite terms, no cancellation).
 #include "vla_tc_common.cuh"
 
 namespace vla {
@@ -42,19 +52,146 @@ struct GtLayout {
     static constexpr size_t ctrl = 0;                       // mbarrier, TMEM slot, abort flag
     static constexpr size_t uk = 1024;                      // [U; K] (128 rows, exact bf16)
     static constexpr size_t ah = uk + 2 * kTile;            // A hi, lo
-    static constexpr size_t slots = ah + 2 * kTile;         // six 8 KB slots:
-    // R1-R3: AK^T hi, W^T hi, Y_hat hi, AK^T lo, W^T lo, Y_hat lo
-    // R4:    (beta Z)^T hi, E' hi, Z^T hi, (beta Z)^T lo, E' lo, Z^T lo
-    // elimination: published pivot rows in slot 0 (sub-blocks) or slot 4, scaled
-    // pivot rows in slot 3 (sub-blocks) or slot 5
-    // chunk start: M^(c) (fp32, 64 x kGS) in slots 0-2, then (1/D) L^{-1} hi, lo in slots 0, 1
-    static constexpr size_t xt = slots + 6 * kTile;         // I + G (fp32, 64 x kGS), then X^T hi, lo
-    static constexpr size_t ksc = xt + (size_t)64 * kGS * 4;  // [2][64] 1 / max(|k|, eps) (by sub-block parity)
+    static constexpr size_t work = ah + 2 * kTile;          // 66 KB work area, by phase:
+    // R1 -> R2: AK^T hi @0, W^T hi @8K, AK^T lo @16K, W^T lo @24K (R2's B operand, two
+    //           64-row tiles stacked), W^T fp32 @kW32
+    // R2 -> elimination: Y_hat fp32 @0, I + G fp32 @kG32, W^T fp32 @kW32
+    // elimination: pivot rows @0 (2 x 8 x 192 floats), scaled pivot rows @kSrow
+    // R4: [-(beta Z)^T | E'] pairs of atoms @0 (parts 0) and @16K (parts 1), Z^T parts
+    //     0, 1, 2 @32K, 40K, 48K, -(beta Z)^T part 2 @56K
+    // chunk start: diag(1/D) E hi @0, lo @8K, E hi @16K, lo @24K, M^(c) fp32 @32K,
+    //     pivot rows @kCrow (2 x 8 x 128 floats), scaled pivot rows @kCsrow
+    static constexpr size_t kW32 = 4 * kTile;
+    static constexpr size_t kG32 = kW32 + (size_t)64 * kGS * 4;
+    static constexpr size_t kSrow = (size_t)2 * 8 * 192 * 4;
+    static constexpr size_t kCrow = kW32 + (size_t)64 * kGS * 4;
+    static constexpr size_t kCsrow = kCrow + (size_t)2 * 8 * 128 * 4;
+    static constexpr size_t work_bytes = kG32 + (size_t)64 * kGS * 4;
+    static constexpr size_t ksc = work + work_bytes;        // [2][64] 1 / max(|k|, eps) (by sub-block parity)
     static constexpr size_t kn = ksc + 512;                 // [2][64] max(|k|, eps)
     static constexpr size_t beta = kn + 512;                // [64]
     static constexpr size_t nrm = beta + 256;               // [2][64] halves of |row|^2
     static constexpr size_t total = nrm + 512;
 };
+static_assert(GtLayout::work % 1024 == 0, "operand tiles must be 1024-byte aligned");
+static_assert(GtLayout::kSrow + 2 * 8 * 64 * 4 <= GtLayout::kW32, "elimination scratch fits below W^T");
+static_assert(8 * kTile <= GtLayout::work_bytes, "R4 tiles fit the work area");
+static_assert(GtLayout::kCsrow + 2 * 8 * 64 * 4 <= GtLayout::work_bytes, "chunk-start scratch fits");
+
+// bf16 parts x = x0 + x1 + x2 of two fp32 values (each part the nearest bf16
+// of what the earlier parts leave), as packed pairs.
+__device__ __forceinline__ void split3_pair(float a, float b, uint32_t &p0, uint32_t &p1, uint32_t &p2) {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(a, b);
+    const float2 f0 = __bfloat1622float2(h0);
+    const float ra = a - f0.x, rb = b - f0.y;
+    const __nv_bfloat162 h1 = __floats2bfloat162_rn(ra, rb);
+    const float2 f1 = __bfloat1622float2(h1);
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(ra - f1.x, rb - f1.y);
+    p0 = bf2_bits(h0);
+    p1 = bf2_bits(h1);
+    p2 = bf2_bits(h2);
+}
+
+// Forward elimination of [I + G | W^T | Y_hat] (64 rows s, fp32, row stride
+// kGS) without pivoting, the block scheme of eliminate64 (warp w owns rows
+// 8 w .. 8 w + 7, lane l columns 2 l, 2 l + 1 of each block; the owner of a
+// block of 8 pivots eliminates it with shuffles and publishes its pivot rows
+// and the rows scaled by -1 / D_s; the next owner applies first), carrying
+// the two right-hand blocks instead of the identity.  Afterwards row s holds
+// z_s^T = (L^{-1} W^T)[s] and P[s] = (L^{-1} Y_hat)[s], and rpiv[s] = 1 / D_s.
+// It writes the operand tiles of round 4 (rows s): Z^T and -(beta Z)^T in
+// three bf16 parts, E'[s][t] = -beta_s P[s][t] |k_t| (s <= t, else 0) in two.
+// 256 threads; all must call.
+__device__ __forceinline__ void eliminate_rhs64(const float *gs, const float *w32, const float *y32, float *prow,
+                                                float *srow, float *rpiv, const float *kn, unsigned char *work) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float2 m[8], z[8], pp[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * warp + i;
+        m[i] = *reinterpret_cast<const float2 *>(gs + r * kGS + 2 * lane);
+        z[i] = *reinterpret_cast<const float2 *>(w32 + r * kGS + 2 * lane);
+        pp[i] = *reinterpret_cast<const float2 *>(y32 + r * kGS + 2 * lane);
+    }
+    __syncthreads();  // the staging may be overwritten once everyone has its rows
+#pragma unroll 1
+    for (int b = 0; b < 8; ++b) {
+        float *pb = prow + (b & 1) * 8 * 192;
+        float *sb = srow + (b & 1) * 8 * 64;
+        if (warp == b) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                // pivot M[s][s], s = 8 b + p: lane s / 2, component p mod 2
+                const float pv = __shfl_sync(0xffffffffu, (p & 1) ? m[p].y : m[p].x, 4 * b + (p >> 1));
+                // fast reciprocal: the pivots of I + G are >= 1 and its relative
+                // error (about 2^-22) is far below the parity bar downstream
+                const float rp = __fdividef(1.f, pv);
+                if (lane == 0) rpiv[8 * b + p] = rp;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (i <= p) continue;  // (constant trip count: the rows stay in registers)
+                    const float mv = __shfl_sync(0xffffffffu, (i & 1) ? m[p].y : m[p].x, 4 * b + (i >> 1));
+                    const float2 f = make_float2(-mv * rp, -mv * rp);
+                    m[i] = __ffma2_rn(f, m[p], m[i]);
+                    z[i] = __ffma2_rn(f, z[p], z[i]);
+                    pp[i] = __ffma2_rn(f, pp[p], pp[i]);
+                }
+                *reinterpret_cast<float2 *>(pb + p * 192 + 2 * lane) = m[p];
+                *reinterpret_cast<float2 *>(pb + p * 192 + 64 + 2 * lane) = z[p];
+                *reinterpret_cast<float2 *>(pb + p * 192 + 128 + 2 * lane) = pp[p];
+                *reinterpret_cast<float2 *>(sb + p * 64 + 2 * lane) = __fmul2_rn(m[p], make_float2(-rp, -rp));
+            }
+        }
+        __syncthreads();
+        if (warp > b) {
+            const uint32_t nbar = 32u * (uint32_t)(7 - b);
+            if (warp > b + 1) asm volatile("bar.sync 1, %0;" ::"r"(nbar) : "memory");
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const float4 fa = *reinterpret_cast<const float4 *>(sb + p * 64 + 8 * warp);
+                const float4 fb = *reinterpret_cast<const float4 *>(sb + p * 64 + 8 * warp + 4);
+                const float2 pm = *reinterpret_cast<const float2 *>(pb + p * 192 + 2 * lane);
+                const float2 pz = *reinterpret_cast<const float2 *>(pb + p * 192 + 64 + 2 * lane);
+                const float2 py = *reinterpret_cast<const float2 *>(pb + p * 192 + 128 + 2 * lane);
+                const float fr[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float2 fi = make_float2(fr[i], fr[i]);
+                    m[i] = __ffma2_rn(fi, pm, m[i]);
+                    z[i] = __ffma2_rn(fi, pz, z[i]);
+                    pp[i] = __ffma2_rn(fi, py, pp[i]);
+                }
+            }
+            if (warp == b + 1) asm volatile("bar.arrive 1, %0;" ::"r"(nbar) : "memory");
+        }
+    }
+    // round 4's tiles, rows s = 8 warp + i, columns 2 lane, 2 lane + 1 (the pivot
+    // scratch is no longer read by anyone once every warp has left the loop)
+    unsigned char *bz0 = work, *ep0 = work + kTile, *bz1 = work + 2 * kTile, *ep1 = work + 3 * kTile;
+    unsigned char *zt0 = work + 4 * kTile, *zt1 = work + 5 * kTile, *zt2 = work + 6 * kTile;
+    unsigned char *bz2 = work + 7 * kTile;
+    const float2 knt = *reinterpret_cast<const float2 *>(kn + 2 * lane);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int s = 8 * warp + i;
+        const float bs = rpiv[s];  // written by this warp as the owner of row s
+        const uint32_t o = toff(s, 2 * lane);
+        uint32_t w0, w1, w2;
+        split3_pair(z[i].x, z[i].y, w0, w1, w2);
+        *reinterpret_cast<uint32_t *>(zt0 + o) = w0;
+        *reinterpret_cast<uint32_t *>(zt1 + o) = w1;
+        *reinterpret_cast<uint32_t *>(zt2 + o) = w2;
+        split3_pair(-bs * z[i].x, -bs * z[i].y, w0, w1, w2);
+        *reinterpret_cast<uint32_t *>(bz0 + o) = w0;
+        *reinterpret_cast<uint32_t *>(bz1 + o) = w1;
+        *reinterpret_cast<uint32_t *>(bz2 + o) = w2;
+        const float ex = (2 * lane >= s) ? -bs * pp[i].x * knt.x : 0.f;
+        const float ey = (2 * lane + 1 >= s) ? -bs * pp[i].y * knt.y : 0.f;
+        split3_pair(ex, ey, w0, w1, w2);
+        *reinterpret_cast<uint32_t *>(ep0 + o) = w0;
+        *reinterpret_cast<uint32_t *>(ep1 + o) = w1;
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     using L = GtLayout;
@@ -65,19 +202,19 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
     unsigned char *uk = smem + L::uk;
     unsigned char *a_hi = smem + L::ah, *a_lo = smem + L::ah + kTile;
-    unsigned char *slot = smem + L::slots;  // slot(i) = slot + i * kTile
-    unsigned char *xt_hi = smem + L::xt, *xt_lo = smem + L::xt + kTile;
-    float *gs = reinterpret_cast<float *>(smem + L::xt);
-    float *stage = reinterpret_cast<float *>(slot);
+    unsigned char *work = smem + L::work;  // work + i * kTile: tile slot i
     float *s_ks = reinterpret_cast<float *>(smem + L::ksc);
     float *s_kn = reinterpret_cast<float *>(smem + L::kn);
     float *s_beta = reinterpret_cast<float *>(smem + L::beta);
     float *s_nrm = reinterpret_cast<float *>(smem + L::nrm);
-    // R1-R3 operands and R4 operands in the six slots
-    unsigned char *akt_hi = slot, *wt_hi = slot + kTile, *yh_hi = slot + 2 * kTile;
-    unsigned char *akt_lo = slot + 3 * kTile, *wt_lo = slot + 4 * kTile, *yh_lo = slot + 5 * kTile;
-    unsigned char *bz_hi = slot, *ep_hi = slot + kTile, *zt_hi = slot + 2 * kTile;
-    unsigned char *bz_lo = slot + 3 * kTile, *ep_lo = slot + 4 * kTile, *zt_lo = slot + 5 * kTile;
+    // R2's B operand [AK; W] (two stacked tiles, hi then lo) and the elimination's staging
+    unsigned char *akt_hi = work, *wt_hi = work + kTile, *akt_lo = work + 2 * kTile, *wt_lo = work + 3 * kTile;
+    float *w32 = reinterpret_cast<float *>(work + L::kW32);  // W^T rows (fp32)
+    float *g32 = reinterpret_cast<float *>(work + L::kG32);  // I + G (fp32)
+    float *y32 = reinterpret_cast<float *>(work);            // Y_hat rows (fp32), once R2 is done
+    // R4's operands (written by the elimination)
+    unsigned char *bz0 = work, *bz1 = work + 2 * kTile, *bz2 = work + 7 * kTile;
+    unsigned char *zt0 = work + 4 * kTile, *zt1 = work + 5 * kTile, *zt2 = work + 6 * kTile;
 
     const int NCA = a.L.NCA, CA = a.L.CA, T = a.p.T;
     const int c = (int)(blockIdx.x % (unsigned)NCA), bh = a.bh_lo + (int)(blockIdx.x / (unsigned)NCA);
@@ -104,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     tc_fence_after();
     const uint32_t tbase = *tslot;
     const uint32_t tq = tbase + ((uint32_t)(32 * qw) << 16);  // this warp's lane quarter
-    constexpr uint32_t col_d1 = 0, col_d5 = 64, col_d2 = 128;  // D2, then D3
+    constexpr uint32_t col_d1 = 0, col_d5 = 64, col_d2 = 128;
 
     // ---- A at the chunk start ----
     // c > 0: A = (M^(c))^{-1} = L^{-T} D^{-1} L^{-1}: elimination of M^(c),
@@ -119,19 +256,21 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         if (c > 0) src = ws_f(a, a.L.off_M) + ((size_t)bh * NCA + c) * kD * kD;
         else if (a.p.A0) src = a.p.A0 + (size_t)bh * kD * kD;
         if (c > 0) {
+            float *stage = reinterpret_cast<float *>(work + L::kW32);  // M^(c) (fp32)
             const float4 *g4 = reinterpret_cast<const float4 *>(src + gr * kD + 16 * gp);
             float4 *st = reinterpret_cast<float4 *>(stage + gr * kGS + 16 * gp);
 #pragma unroll
             for (int q = 0; q < 4; ++q) st[q] = g4[q];
             __syncthreads();
-            eliminate64(stage, reinterpret_cast<float *>(slot + 4 * kTile), reinterpret_cast<float *>(slot + 5 * kTile),
-                        s_beta, xt_hi, xt_lo, slot, slot + kTile);
+            // E = L^{-1} hi, lo @16K, 24K; diag(1/D) E hi, lo @0, 8K
+            eliminate64(stage, reinterpret_cast<float *>(work + L::kCrow), reinterpret_cast<float *>(work + L::kCsrow),
+                        s_beta, work + 2 * kTile, work + 3 * kTile, work, work + kTile);
             fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0) {
                 tc_fence_after();
-                mma_k64x3<true, true>(tbase + col_d5, smem_u32(slot), smem_u32(slot + kTile), smem_u32(xt_hi),
-                                      smem_u32(xt_lo), idesc_bf16_f32(64, 64), false);
+                mma_k64x3<true, true>(tbase + col_d5, smem_u32(work), smem_u32(work + kTile), smem_u32(work + 2 * kTile),
+                                      smem_u32(work + 3 * kTile), idesc_bf16_f32(64, 64), false);
                 umma_commit(bar);
             }
             const bool w = mbar_wait_bounded(bar, 0, a.p.wait_limit_ns, a.p.err);
@@ -228,12 +367,18 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             ok = false;
             break;
         }
-        // ---- W^T and (A K)^T tiles (token rows) ----
+        // ---- W^T and (A K)^T tiles (token rows); W^T in fp32 for the elimination ----
         {
             float v[32];
             tmem_ld32(tq + col_d1 + 32 * hw, v);
-            if (qw < 2) put_row32(wt_hi, wt_lo, r128, 32 * hw, v);
-            else put_row32(akt_hi, akt_lo, r128 - 64, 32 * hw, v);
+            if (qw < 2) {
+                put_row32(wt_hi, wt_lo, r128, 32 * hw, v);
+                float4 *dst = reinterpret_cast<float4 *>(w32 + r128 * kGS + 32 * hw);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+                put_row32(akt_hi, akt_lo, r128 - 64, 32 * hw, v);
+            }
         }
         tc_fence_before();
         fence_proxy_async_smem();
@@ -249,92 +394,57 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             ok = false;
             break;
         }
-        // ---- Y_hat tiles (rows s), I + G (fp32) for the elimination ----
+        // ---- Y_hat rows s and I + G (fp32) for the elimination ----
         {
             float v[32];
             tmem_ld32(tq + col_d2 + 32 * hw, v);  // Y[s][t], t = 32 hw ..
             if (act64) {
                 const float4 *k4 = reinterpret_cast<const float4 *>(ks_sb + 32 * hw);
+                float4 *dst = reinterpret_cast<float4 *>(y32 + r64 * kGS + 32 * hw);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float4 kv = k4[q];
-                    v[4 * q] *= kv.x; v[4 * q + 1] *= kv.y; v[4 * q + 2] *= kv.z; v[4 * q + 3] *= kv.w;
+                    dst[q] = make_float4(v[4 * q] * kv.x, v[4 * q + 1] * kv.y, v[4 * q + 2] * kv.z, v[4 * q + 3] * kv.w);
                 }
-                put_row32(yh_hi, yh_lo, r64, 32 * hw, v);
             }
             tmem_ld32(tq + col_d2 + 64 + 32 * hw, v);  // G[s][t]
             if (act64) {
 #pragma unroll
                 for (int m = 0; m < 32; ++m)
                     if (32 * hw + m == r64) v[m] += 1.f;
-                float4 *dst = reinterpret_cast<float4 *>(gs + r64 * kGS + 32 * hw);
+                float4 *dst = reinterpret_cast<float4 *>(g32 + r64 * kGS + 32 * hw);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
         tc_fence_before();
         __syncthreads();
-        // ---- elimination of I + G: X^T = L^{-1} and beta_s = 1 / D_s ----
-        eliminate64(gs, reinterpret_cast<float *>(akt_hi), reinterpret_cast<float *>(akt_lo), s_beta, xt_hi, xt_lo,
-                    nullptr, nullptr);
-        fence_proxy_async_smem();
-        __syncthreads();
-        // ---- R3: D3 = X^T [W | Y_hat] (B MN-major, two atoms 8 KB apart): Z^T | P ----
-        if (tid == 0) {
-            tc_fence_after();
-            mma_k64x3<false, true>(tbase + col_d2, smem_u32(xt_hi), smem_u32(xt_lo), smem_u32(wt_hi), smem_u32(wt_lo),
-                                   idesc_bf16_f32(64, 128), false, 16, kTile);
-            umma_commit(bar);
-        }
+        // ---- elimination of [I + G | W^T | Y_hat]: Z^T, P and beta, and round 4's tiles ----
+        eliminate_rhs64(g32, w32, y32, reinterpret_cast<float *>(work), reinterpret_cast<float *>(work + L::kSrow),
+                        s_beta, kn_sb, work);
         // the next sub-block's inputs: issued after the elimination, so that their
-        // registers are not live through it (rounds 3-4 hide the latency)
+        // registers are not live through it (round 4 hides the latency)
         load_in(sb + 1);
-        if (!round_wait()) {
-            ok = false;
-            break;
-        }
-        // ---- Z^T, -(beta Z)^T and E' tiles (rows s) ----
-        {
-            float v[32];
-            tmem_ld32(tq + col_d2 + 32 * hw, v);  // z_s[i], i = 32 hw ..
-            const float bs = act64 ? s_beta[r64] : 0.f;
-            if (act64) {
-                put_row32(zt_hi, zt_lo, r64, 32 * hw, v);
-#pragma unroll
-                for (int m = 0; m < 32; ++m) v[m] *= -bs;
-                put_row32(bz_hi, bz_lo, r64, 32 * hw, v);
-            }
-            tmem_ld32(tq + col_d2 + 64 + 32 * hw, v);  // P[s][t] = z_s . k_hat_t, t = 32 hw ..
-            if (act64) {
-                const float4 *n4 = reinterpret_cast<const float4 *>(kn_sb + 32 * hw);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 kv = n4[q];
-                    const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-                    for (int e4 = 0; e4 < 4; ++e4) {
-                        const int mm = 4 * q + e4;
-                        v[mm] = (32 * hw + mm >= r64) ? -bs * v[mm] * kk[e4] : 0.f;
-                    }
-                }
-                put_row32(ep_hi, ep_lo, r64, 32 * hw, v);
-            }
-        }
-        tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
         // ---- R4: D1[k rows] += E'^T Z^T (A MN-major, atoms [-(beta Z)^T | E']: M = 128,
-        // the first 64 rows land in D1's dead W rows); A += -(Z diag(beta)) Z^T ----
+        // the first 64 rows land in D1's dead W rows); A += -(Z diag(beta)) Z^T with
+        // three-way splits (parts i + j <= 2) ----
         if (tid == 0) {
             tc_fence_after();
-            mma_k64x3<true, true>(tbase + col_d1, smem_u32(bz_hi), smem_u32(bz_lo), smem_u32(zt_hi), smem_u32(zt_lo),
+            mma_k64x3<true, true>(tbase + col_d1, smem_u32(bz0), smem_u32(bz1), smem_u32(zt0), smem_u32(zt1),
                                   idesc_bf16_f32(128, 64), true, kTile, 16);
-            mma_k64x3<true, true>(tbase + col_d5, smem_u32(bz_hi), smem_u32(bz_lo), smem_u32(zt_hi), smem_u32(zt_lo),
-                                  idesc_bf16_f32(64, 64), true);
+            constexpr uint32_t id64 = idesc_bf16_f32(64, 64);
+            mma_k64<true, true>(tbase + col_d5, smem_u32(bz0), smem_u32(zt0), id64, true);
+            mma_k64<true, true>(tbase + col_d5, smem_u32(bz0), smem_u32(zt1), id64, true);
+            mma_k64<true, true>(tbase + col_d5, smem_u32(bz1), smem_u32(zt0), id64, true);
+            mma_k64<true, true>(tbase + col_d5, smem_u32(bz0), smem_u32(zt2), id64, true);
+            mma_k64<true, true>(tbase + col_d5, smem_u32(bz1), smem_u32(zt1), id64, true);
+            mma_k64<true, true>(tbase + col_d5, smem_u32(bz2), smem_u32(zt0), id64, true);
             umma_commit(bar);
         }
         // the next sub-block's [U; K] while round 4 runs ([U; K] was last read by
-        // round 2; its loads were issued after round 3's issue)
+        // round 2; its loads were issued after the elimination)
         if (sb + 1 < nsb) stage_in(sb + 1);
         if (!round_wait()) {
             ok = false;
