@@ -68,10 +68,25 @@ struct TcLayout {
     static constexpr size_t rden = ks + 256;                 // [64] 1 / (phi(q).n + eps)
     static constexpr size_t tot = rden + 256;                // [8][64] warp totals of phi(k_hat), then prefixes
     static constexpr size_t nrun = tot + 8 * 64 * 4;         // [64] n at the sub-block start
-    static constexpr size_t total = nrun + 256;
+    static constexpr size_t tms = nrun + 256;                // triangular-inverse scratch (32 x 36 floats)
+    static constexpr size_t total = tms + 32 * 36 * 4;
 };
 static_assert(TcLayout::ti % 1024 == 0 && TcLayout::ph_hi % 1024 == 0, "operand tiles must be 1024-byte aligned");
 static_assert(TcLayout::ti + (size_t)64 * kGS * 4 <= TcLayout::ph_hi, "N fits before Phi");
+static_assert(TcLayout::ti == TcLayout::al_hi + 2 * kTile && TcLayout::ti + 2 * kTile <= TcLayout::ph_hi,
+              "the readout coefficients of a sub-block are staged in [Al | T_inv] (32 KB)");
+static_assert(TcLayout::tms % 16 == 0, "scratch rows are 16-byte aligned");
+
+// Bulk copy shared -> global (bulk-group completion), its commit, and the
+// waits for the group's source reads / for its completion.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     using L = TcLayout;
@@ -81,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
+    uint64_t *bar_n = reinterpret_cast<uint64_t *>(smem + L::ctrl + 16);  // round 1's N^T product alone
     unsigned char *xs_hi = smem + L::xs_hi, *xs_lo = smem + L::xs_lo;
     unsigned char *kb = smem + L::kb, *ph_hi = smem + L::ph_hi, *ph_lo = smem + L::ph_lo;
     unsigned char *al_hi = smem + L::al_hi, *al_lo = smem + L::al_lo;
@@ -112,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
 
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar_n, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -159,9 +176,12 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         for (int h = 0; h < 4; ++h) ra[h] = reinterpret_cast<const float4 *>(gal + off)[h];
     };
 
-    uint32_t phase = 0;
+    // phase: next parity of bar (three commits per sub-block), phase_n of bar_n
+    // (one); pend: after an abort, the parity of bar's last commit
+    uint32_t phase = 0, phase_n = 0, pend = 0;
     auto round_wait = [&]() -> bool {
         const bool w = mbar_wait_bounded(bar, phase, a.p.wait_limit_ns, a.p.err);
+        pend = phase;
         phase ^= 1u;
         if (!w) *abort_flag = 1;
         __syncthreads();
@@ -229,11 +249,14 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         if (tid == 0) {
             tc_fence_after();
             // hi.hi and lo.hi for both (K is exact), then hi.lo for the Phi part
+            // N^T = K Al^T first, on its own barrier: the triangular inverse
+            // runs on the CUDA cores while the wide product is still going
+            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
+            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
+            umma_commit(bar_n);
             mma_k64<false, false>(tbase + col_do, smem_u32(xs_hi), smem_u32(ph_hi), id_xw, false);
             mma_k64<false, false>(tbase + col_do, smem_u32(xs_lo), smem_u32(ph_hi), id_xw, true);
             mma_k64<false, false>(tbase + col_do, smem_u32(xs_hi), smem_u32(ph_lo), id_x, true);
-            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_hi), id_64, false);
-            mma_k64<false, false>(tbase + col_d2, smem_u32(kb), smem_u32(al_lo), id_64, true);
             umma_commit(bar);
         }
         // ---- readout denominators 1 / (phi(q_t) . n_t + eps), while round 1 runs ----
@@ -287,11 +310,19 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             dp += __shfl_xor_sync(0xffffffffu, dp, 16);
             if (pq == 0) s_rden[pt] = 1.f / (dp + kEps);
         }
-        if (!round_wait()) {
-            ok = false;
-            break;
+        {
+            const bool w = mbar_wait_bounded(bar_n, phase_n, a.p.wait_limit_ns, a.p.err);
+            phase_n ^= 1u;
+            if (!w) *abort_flag = 1;
+            __syncthreads();
+            tc_fence_after();
+            if (*abort_flag) {
+                pend = phase;  // the wide product's commit is still outstanding
+                ok = false;
+                break;
+            }
         }
-        // ---- N (fp32, row-major, for the inverse), E tiles ----
+        // ---- N (fp32, row-major, for the inverse) ----
         {
             float v[32];
             tmem_ld32(tq + col_d2 + 32 * hw, v);  // D2 row t = 16 qw + lane (M = 64), columns s = 32 hw ..
@@ -304,6 +335,19 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                     ntb[sr * kGS + t] = sr < t ? v[m] * kt : 0.f;
                 }
             }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // ---- T_inv = (I + N)^{-1} (recursive doubling, in place over N), while the
+        // wide product of round 1 runs ----
+        tri_inv64(ntb, reinterpret_cast<float *>(smem + L::tms), ti_hi, ti_lo);
+        if (!round_wait()) {
+            ok = false;
+            break;
+        }
+        // ---- E tiles ----
+        {
+            float v[32];
             tmem_ld32(tq + col_d1 + 32 * hw, v);  // X K, columns 32 hw ..
             const float4 *ks4 = reinterpret_cast<const float4 *>(s_ks + 32 * hw);
 #pragma unroll
@@ -319,11 +363,8 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             }
             put_row32(xs_hi, xs_lo, xrow, 32 * hw, v);
         }
-        tc_fence_before();
-        __syncthreads();
-        // ---- T_inv = (I + N)^{-1} (recursive doubling, in place over N) ----
-        tri_inv64(ntb, reinterpret_cast<float *>(kb), ti_hi, ti_lo);
         fence_proxy_async_smem();
+        tc_fence_before();
         __syncthreads();
         // ---- round 2: R = E T_inv, Qm = Al Phi^T ----
         if (tid == 0) {
@@ -382,15 +423,23 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
                 const float4 r4 = rd4[q];
                 v[4 * q] *= r4.x; v[4 * q + 1] *= r4.y; v[4 * q + 2] *= r4.z; v[4 * q + 3] *= r4.w;
             }
-            unsigned char *dst = gyh + (size_t)sb * (4 * kTile) + (xrow < 64 ? 2 * kTile : 0);
+            // staged in [Al | T_inv] (free once round 3 is done) in the global
+            // layout [y hi | y lo | h hi | h lo], then one bulk copy
+            unsigned char *dst = al_hi + (xrow < 64 ? 2 * kTile : 0);
             put_row32(dst, dst + kTile, xrow & 63, 32 * hw, v);
         }
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(gyh + (size_t)sb * (4 * kTile), al_hi, 4 * kTile);
+            bulk_wait_read();  // the next sub-block's staging overwrites the source
+        }
+        __syncthreads();
     }
+    if (tid == 0) bulk_wait_all();  // the coefficient copies are complete before the CTA ends
     if (!ok) {
-        if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
+        if (tid == 0) (void)mbar_wait_bounded(bar, pend, a.p.wait_limit_ns, a.p.err);
     } else {  // rows 0..63 are H_c, rows 64..127 P_c
         float x[32];
         tmem_ld32(tq + col_x + 32 * hw, x);
