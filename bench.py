@@ -50,8 +50,8 @@ TRAFFIC = {
     # sequential kernel, long stream: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
     ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
     # tensor-core path, long stream: at T=16384 (same 16 heads), scaled x4 to T=65536
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (76.668928e6 + 18.857984e6), "src_sha": "7937a7a93ac61e07"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.859648e6 + 102.140416e6), "src_sha": "7937a7a93ac61e07"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (76.620544e6 + 15.288064e6), "src_sha": "56d72c88e7f36bb7"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.020224e6 + 101.082112e6), "src_sha": "56d72c88e7f36bb7"},
 }
 
 
