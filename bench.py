@@ -78,8 +78,9 @@ def kernel_src_hash(kernel_name: str) -> str:
 # transitions, the chain - counts zero), and so is every input and output
 # byte.  engine is the pipe the kernel's arithmetic runs on: "alu" (FP32 CUDA
 # cores) or "tensor" (bf16 tcgen05; its roofline takes the bf16 tensor peak).
-def kernel_plan(kname, d, io_dtype="bf16"):
-    """[(kernel, algorithmic flops, algorithmic bytes per token-head, engine)] in launch order."""
+def kernel_plan(kname, d, io_dtype="bf16", units=0):
+    """[(kernel, algorithmic flops, algorithmic bytes per token-head, engine)] in launch order
+    (units: the (b, h) units of the batch)."""
     io = 2 if io_dtype == "bf16" else 4
     full = 12 * d * d + 16 * d
     if kname == "seq":
@@ -96,6 +97,11 @@ def kernel_plan(kname, d, io_dtype="bf16"):
     # state pass does the state write and readout (a3-a4, reading q and v) for the
     # [H; P] rows of each chunk, and the output pass combines them with the chunk-start
     # state (o = S^(c) y + h, writing o)
+    # chunk_tc at d = 128 with bf16 I/O and one chunk per unit (enough units): the
+    # gates from A0, then the state pass on S itself, which writes o
+    if kname == "chunk_tc" and io_dtype == "bf16" and d == 128 and units >= 128:
+        return [("gates_tc128_kernel", half, 2 * d * io, "tensor"),
+                ("rows_tc128_kernel", half, 3 * d * io, "tensor")]
     if kname == "chunk_tc" and io_dtype == "bf16" and d == 64:
         return [("gram_tma_kernel", 0, 0, "tensor"), ("prefix_kernel", 0, 0, "alu"),
                 ("gates_tc_kernel", half, 2 * d * io, "tensor"), ("rows_tc_kernel", half, 2 * d * io, "tensor"),
@@ -388,7 +394,8 @@ def main():
     io_bytes = 2 if x.dtype == "bf16" else 4
     hq, hk, hv, hu = to_torch_host(x)
     q, k, v, u = (t.to(dev) for t in (hq, hk, hv, hu))
-    resolved = kernel if kernel != vla.VLA_KERNEL_AUTO else vla.vla_select_kernel(B, H, T, d)
+    resolved = kernel if kernel != vla.VLA_KERNEL_AUTO else vla.vla_select_kernel(
+        B, H, T, d, vla.VLA_BF16 if x.dtype == "bf16" else vla.VLA_F32)
     kname = {vla.VLA_KERNEL_SEQ: "seq", vla.VLA_KERNEL_CHUNK: "chunk", vla.VLA_KERNEL_CHUNK_TC: "chunk_tc",
              vla.VLA_KERNEL_DECODE: "decode"}[resolved]
     o = torch.empty_like(q)
@@ -413,7 +420,7 @@ def main():
         vla.vla_forward(q, k, v, u, x.lambda0, S0=st[0], A0=st[1], n0=st[2], o=o, S_T=S_T, A_T=A_T, n_T=n_T,
                         kernel=resolved, workspace=ws if need else None, stream=stream)
 
-    plan = kernel_plan(kname, d, x.dtype)
+    plan = kernel_plan(kname, d, x.dtype, B * H)
     nb = len(plan) + 1  # launch boundaries per step
     bounds = [[torch.cuda.Event(enable_timing=True) for _ in range(nb)] for _ in range(args.steps)]
     for evs in bounds:
@@ -597,7 +604,13 @@ def precision_block(kname, io_dtype, d):
     """What the step computes in: I/O, state and accumulation types, and how the
     tensor-core products take their fp32 operands."""
     blk = {"io": io_dtype, "state": "f32", "accumulate": "f32"}
-    if kname == "chunk_tc" and io_dtype == "bf16" and d == 64:
+    if kname == "chunk_tc" and io_dtype == "bf16" and d == 128:
+        blk["tensor_products"] = ("tcgen05 kind::f16, fp32 operands as bf16 parts: A, AK, W and the "
+                                  "downdate's Z in three (about 2^-24 relative), the rest as hi/lo pairs "
+                                  "(hi*hi + hi*lo + lo*hi, about 2^-16); fp32 accumulation; the bf16 inputs "
+                                  "enter exactly")
+        blk["cuda_core"] = "f32 (eliminations, triangular inverses, norms)"
+    elif kname == "chunk_tc" and io_dtype == "bf16" and d == 64:
         blk["tensor_products"] = ("tcgen05 kind::f16, fp32 operands as bf16 hi/lo pairs, products "
                                   "hi*hi + hi*lo + lo*hi (about 2^-16 relative), fp32 accumulation; "
                                   "the bf16 inputs enter exactly")

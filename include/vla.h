@@ -55,9 +55,12 @@ extern "C" {
 #define VLA_KERNEL_SEQ 1   /* one CTA per (b, h), token-sequential, no workspace */
 #define VLA_KERNEL_CHUNK 2 /* chunk-parallel over T, needs workspace */
 #define VLA_KERNEL_DECODE 3 /* a few tokens per call (decode step), state streamed from HBM */
-#define VLA_KERNEL_CHUNK_TC 4 /* VLA_KERNEL_CHUNK with the state passes as tcgen05 UT-transform
-                               * products (d_h = 64, bf16 I/O, chunk a multiple of 64; other
-                               * shapes run exactly as VLA_KERNEL_CHUNK); same workspace */
+#define VLA_KERNEL_CHUNK_TC 4 /* VLA_KERNEL_CHUNK with the gates and the state passes on the
+                               * tcgen05 tensor cores (block Woodbury, UT transform): d_h = 64
+                               * with bf16 I/O and chunks a multiple of 64 tokens, and d_h = 128
+                               * with bf16 I/O and one chunk per (b, h) unit (the default
+                               * chunk length there when B*H >= 128); other shapes run exactly
+                               * as VLA_KERNEL_CHUNK.  Workspace from vla_workspace_bytes */
 
 /*
  * vla_forward -- run the recurrence over T tokens for all B*H units.
@@ -75,7 +78,8 @@ extern "C" {
  * S_T, A_T     [B,H,d,d] fp32, written (required).
  * n_T          [B,H,d] fp32, written when non-NULL.
  * kernel       VLA_KERNEL_AUTO / _SEQ / _CHUNK / _CHUNK_TC / _DECODE.  AUTO takes DECODE for
- *              T <= 4, CHUNK_TC when B*H < 304 and T >= 1024, SEQ otherwise.
+ *              T <= 4; CHUNK_TC at d_h = 128 with bf16 I/O when B*H >= 128 and T >= 256,
+ *              and for any d_h when B*H < 304 and T >= 1024; SEQ otherwise.
  * chunk        chunk length for VLA_KERNEL_CHUNK and _CHUNK_TC (0 = library default).
  * workspace    device scratch of at least vla_workspace_bytes(...) bytes
  *              (may be NULL when that is 0).  Contents on entry are ignored.
@@ -138,10 +142,10 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
  * sequential kernel).  Returns 0 for invalid arguments as well. */
 size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk);
 
-/* Which kernel VLA_KERNEL_AUTO resolves to for this shape (VLA_KERNEL_SEQ,
- * VLA_KERNEL_CHUNK_TC or VLA_KERNEL_DECODE), or a VLA_ERR_* code for invalid
- * arguments. */
-int vla_select_kernel(int B, int H, int T, int d_h);
+/* Which kernel VLA_KERNEL_AUTO resolves to for this shape and I/O type
+ * (VLA_KERNEL_SEQ, VLA_KERNEL_CHUNK_TC or VLA_KERNEL_DECODE), or a VLA_ERR_*
+ * code for invalid arguments. */
+int vla_select_kernel(int B, int H, int T, int d_h, int io_dtype);
 
 /* Static, human-readable text for a status code. */
 const char *vla_status_str(int status);

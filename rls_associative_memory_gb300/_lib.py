@@ -43,7 +43,7 @@ _SIGS = {
     "vla_forward": (_i, [_vp, _vp, _vp, _vp, _i, ctypes.c_float, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                          _vp, _vp, _vp, _i, _i, _vp, ctypes.c_size_t, _vp]),
     "vla_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
-    "vla_select_kernel": (_i, [_i, _i, _i, _i]),
+    "vla_select_kernel": (_i, [_i, _i, _i, _i, _i]),
     "vla_status_str": (ctypes.c_char_p, [_i]),
     "vla_last_cuda_error": (_i, []),
     "vla_device_status": (_i, [_vp]),
@@ -101,8 +101,8 @@ def vla_workspace_bytes(B, H, T, d_h, io_dtype=VLA_BF16, kernel=VLA_KERNEL_AUTO,
     return int(lib().vla_workspace_bytes(B, H, T, d_h, io_dtype, kernel, chunk))
 
 
-def vla_select_kernel(B, H, T, d_h) -> int:
-    return int(lib().vla_select_kernel(B, H, T, d_h))
+def vla_select_kernel(B, H, T, d_h, io_dtype=VLA_BF16) -> int:
+    return int(lib().vla_select_kernel(B, H, T, d_h, io_dtype))
 
 
 def vla_device_status(stream=None) -> int:

@@ -49,15 +49,16 @@ int check_common(int io_dtype, float lambda0, int B, int H, int T, int d_h, int 
     return VLA_OK;
 }
 
-// AUTO: the decode step for a handful of tokens; the chunk-parallel path
-// (with the tensor-core state passes where they apply) when there are too
-// few (b, h) units to fill the GPU with one CTA each and the stream is long
-// enough to cut; otherwise the sequential kernel.
-int resolve_kernel(int B, int H, int T, int d_h, int kernel) {
-    (void)d_h;
+// AUTO: the decode step for a handful of tokens; at d = 128 with bf16 I/O and
+// enough units to fill the GPU, the tensor-core path with one chunk per unit;
+// the chunk-parallel path (with the tensor-core passes where they apply) when
+// there are too few (b, h) units to fill the GPU with one CTA each and the
+// stream is long enough to cut; otherwise the sequential kernel.
+int resolve_kernel(int B, int H, int T, int d_h, int io_dtype, int kernel) {
     if (kernel != VLA_KERNEL_AUTO) return kernel;
     const long long BH = (long long)B * H;
     if (T >= 1 && T <= 4) return VLA_KERNEL_DECODE;
+    if (d_h == 128 && io_dtype == VLA_BF16 && BH >= 128 && T >= 256) return VLA_KERNEL_CHUNK_TC;
     if (BH < 2 * 152 && T >= 1024) return VLA_KERNEL_CHUNK_TC;
     return VLA_KERNEL_SEQ;
 }
@@ -107,16 +108,16 @@ int vla_set_launch_events(void *const *events, int n) {
 
 int vla_last_launch_count(void) { return t_last_launches; }
 
-int vla_select_kernel(int B, int H, int T, int d_h) {
-    const int rc = check_common(VLA_F32, 1.f, B, H, T, d_h, VLA_KERNEL_AUTO);
+int vla_select_kernel(int B, int H, int T, int d_h, int io_dtype) {
+    const int rc = check_common(io_dtype, 1.f, B, H, T, d_h, VLA_KERNEL_AUTO);
     if (rc != VLA_OK) return rc;
-    return resolve_kernel(B, H, T, d_h, VLA_KERNEL_AUTO);
+    return resolve_kernel(B, H, T, d_h, io_dtype, VLA_KERNEL_AUTO);
 }
 
 size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk) {
     if (check_common(io_dtype, 1.f, B, H, T, d_h, kernel) != VLA_OK) return 0;
     if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return 0;
-    const int kk = resolve_kernel(B, H, T, d_h, kernel);
+    const int kk = resolve_kernel(B, H, T, d_h, io_dtype, kernel);
     if ((kk != VLA_KERNEL_CHUNK && kk != VLA_KERNEL_CHUNK_TC) || T == 0 || (long long)B * H == 0) return 0;
     return vla::chunk_layout(B * H, T, d_h, chunk, kk == VLA_KERNEL_CHUNK_TC && io_dtype == VLA_BF16).total;
 }
@@ -209,7 +210,7 @@ int prepare_forward(const void *q, const void *k, const void *v, const void *u, 
     const void *ptrs[] = {q, k, v, u, o, S0, A0, n0, S_T, A_T, n_T, workspace};
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return VLA_ERR_ALIGN;
-    kk = resolve_kernel(B, H, T, d_h, kernel);
+    kk = resolve_kernel(B, H, T, d_h, io_dtype, kernel);
     const size_t need = vla_workspace_bytes(B, H, T, d_h, io_dtype, kk, chunk);
     if (need > 0 && (!workspace || ws_bytes < need)) return VLA_ERR_WORKSPACE;
     p = vla::FwdParams{};

@@ -1203,6 +1203,19 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     if (NCA * BH > 0x7fffffffLL || BH * ((D * D + D + 255) / 256) > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     cudaError_t e;
+    if constexpr (D == 128 && sizeof(IO) == 2) {
+        if (a.p.rows_tc && a.L.NC == 1 && a.L.NCA == 1) {
+            // one chunk per unit: the gates from A0, then the state pass on S itself (writes o)
+            mark_launch(a.p, 0, st);
+            if ((e = launch_gates_tc128(a, st)) != cudaSuccess) return e;
+            mark_launch(a.p, 1, st);
+            if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
+                return e;
+            if ((e = launch_rows_tc128(a, st)) != cudaSuccess) return e;
+            mark_launch(a.p, 2, st);
+            return cudaSuccess;
+        }
+    }
     if constexpr (D == 64 && sizeof(IO) == 2) {
         if (tc_parts_ok(a.p, a.L)) {
             if ((e = tc_front(a, st)) != cudaSuccess) return e;
@@ -1362,11 +1375,18 @@ int chunk_default_a_tc(int BH, int T, int C) {
     return best;
 }
 
+// The tensor-core path at d = 128 runs one chunk per unit, one CTA per unit
+// and pass at one CTA per SM: the default when the units alone fill the GPU.
+constexpr int kTc128MinUnits = 128;
+
 ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc_path) {
     ChunkLayout L{};
-    L.C = chunk > 0 ? chunk : (tc_path && d == 64 ? chunk_default_tc(BH, T) : chunk_default(BH, T));
+    const bool single = chunk == 0 && tc_path && d == 128 && BH >= kTc128MinUnits;
+    L.C = chunk > 0 ? chunk
+                    : (single ? (T + 63) / 64 * 64
+                              : (tc_path && d == 64 ? chunk_default_tc(BH, T) : chunk_default(BH, T)));
     const bool tc = tc_path && d == 64 && L.C % 64 == 0;
-    L.CA = chunk > 0 ? chunk : (tc ? chunk_default_a_tc(BH, T, L.C) : chunk_default_a(BH, T, d, L.C));
+    L.CA = chunk > 0 || single ? L.C : (tc ? chunk_default_a_tc(BH, T, L.C) : chunk_default_a(BH, T, d, L.C));
     L.NC = (T + L.C - 1) / L.C;
     L.NCA = (T + L.CA - 1) / L.CA;
     const size_t bh = (size_t)BH, nc = (size_t)L.NC, nca = (size_t)L.NCA, dd = (size_t)d * d;

@@ -142,6 +142,11 @@ cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream);
 // A-chunks a multiple of 64 tokens.  Defined in vla_gates_tc.cu.
 bool gates_tc_supported(const FwdParams &p, const ChunkLayout &L);
 cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream);
+// d = 128 with bf16 I/O and one chunk per (b, h) unit (L.NC == L.NCA == 1):
+// the gates (block Woodbury from A0, vla_gates_tc128.cu) and the state pass
+// that runs S itself and writes o (vla_rows_tc128.cu), one CTA per unit each.
+cudaError_t launch_gates_tc128(const ChunkArgs &a, cudaStream_t stream);
+cudaError_t launch_rows_tc128(const ChunkArgs &a, cudaStream_t stream);
 // Chunk Grams with TMA tensor loads (vla_gram_tc.cu), same shapes.
 bool gram_tma_supported(const FwdParams &p, const ChunkLayout &L);
 cudaError_t launch_gram_tma(const ChunkArgs &a, cudaStream_t stream);

@@ -105,7 +105,12 @@ def test_workspace_query_and_kernel_selection():
     assert vla.vla_workspace_bytes(1, 16, 4096, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK, 24) == 0
     assert vla.vla_workspace_bytes(1, 16, 0, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK) == 0
     assert vla.vla_select_kernel(1, 16, 65536, 64) == vla.VLA_KERNEL_CHUNK_TC
-    assert vla.vla_select_kernel(256, 4, 512, 32) == vla.VLA_KERNEL_SEQ
+    assert vla.vla_select_kernel(256, 4, 512, 32, vla.VLA_F32) == vla.VLA_KERNEL_SEQ
+    # d = 128: the tensor-core path (one chunk per unit) with bf16 I/O and enough units,
+    # the sequential kernel with fp32 I/O or few units on short streams
+    assert vla.vla_select_kernel(32, 16, 2048, 128, vla.VLA_BF16) == vla.VLA_KERNEL_CHUNK_TC
+    assert vla.vla_select_kernel(32, 16, 2048, 128, vla.VLA_F32) == vla.VLA_KERNEL_SEQ
+    assert vla.vla_select_kernel(2, 16, 512, 128, vla.VLA_BF16) == vla.VLA_KERNEL_SEQ
     assert vla.vla_select_kernel(32, 64, 1, 64) == vla.VLA_KERNEL_DECODE
     assert vla.vla_select_kernel(32, 64, 4, 64) == vla.VLA_KERNEL_DECODE
     assert vla.vla_select_kernel(32, 64, 5, 64) == vla.VLA_KERNEL_SEQ
@@ -113,6 +118,18 @@ def test_workspace_query_and_kernel_selection():
     assert vla.vla_workspace_bytes(1, 16, 4096, 48, vla.VLA_BF16, vla.VLA_KERNEL_SEQ) == 0
     assert vla.vla_select_kernel(1, 16, 4096, 64) in (vla.VLA_KERNEL_SEQ, vla.VLA_KERNEL_CHUNK_TC)
     assert vla.vla_select_kernel(1, 16, 4096, 40) == vla.VLA_ERR_UNSUPPORTED_DIM
+    assert vla.vla_select_kernel(1, 16, 4096, 64, 7) == vla.VLA_ERR_ARG
+
+
+def test_single_chunk_layout_at_d128():
+    """d = 128 with the tensor-core path and enough units: one chunk per unit, so
+    the workspace is the unit gates plus a few d x d matrices per unit."""
+    B, H, T, d = 32, 16, 2048, 128
+    ws = vla.vla_workspace_bytes(B, H, T, d, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK_TC)
+    gates = B * H * T * d * 4
+    assert gates <= ws <= gates + B * H * 8 * d * d * 4 + (1 << 20)
+    # the same shape on the plain chunked path keeps its multi-chunk default
+    assert vla.vla_workspace_bytes(B, H, T, d, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK) > ws
 
 
 def test_tensor_core_chunk_defaults():
