@@ -1400,7 +1400,7 @@ ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc_path) {
     L.off_S = off; off = align256(off + bh * nc * dd * 4);
     L.off_yh = off;
     L.yh = tc ? 1 : 0;
-    if (L.yh) off = align256(off + bh * nc * (size_t)(L.C / 64) * 32768);
+    if (L.yh) off = align256(off + bh * nc * (size_t)(L.C / 64) * 16384);
     L.total = off;
     return L;
 }

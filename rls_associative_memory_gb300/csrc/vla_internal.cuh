@@ -91,9 +91,9 @@ struct ChunkLayout {
     size_t off_P;        // [BH][NC][d][d]  chunk transition P_c
     size_t off_H;        // [BH][NC][d][d]  chunk offset H_c
     size_t off_S;        // [BH][NC][d][d]  chunk-start states S^(c)
-    size_t off_yh;       // [BH][NC][C/64][4][64][64] bf16: readout coefficients y_t, h_t (hi, lo
-                         // operand tiles) of every 64-token sub-block, written by the
-                         // tensor-core state pass for the output pass
+    size_t off_yh;       // [BH][NC][C/64][2][64][64] bf16: readout coefficients y_t, h_t (operand
+                         // tiles) of every 64-token sub-block, written by the tensor-core
+                         // state pass for the output pass
     int yh;              // 1 when the off_yh region is reserved
     size_t total;
 };
