@@ -52,12 +52,18 @@ TRAFFIC = {
     # tensor-core path, long stream: at T=16384 (same 16 heads), scaled x4 to T=65536
     ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (76.620544e6 + 15.288064e6), "src_sha": "56d72c88e7f36bb7"},
     ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.020224e6 + 101.082112e6), "src_sha": "56d72c88e7f36bb7"},
+    # d = 128, one chunk per unit, batched workload: at B=8 (128 units, one wave), scaled x4 to B=32
+    ("chunk_tc", "batched", "gates_tc128_kernel"): {"bytes": 4 * (134.438144e6 + 91.868928e6),
+                                                    "src_sha": "2c5aeb91ecce2aab"},
+    ("chunk_tc", "batched", "rows_tc128_kernel"): {"bytes": 4 * (335.677440e6 + 54.724608e6),
+                                                   "src_sha": "2c5aeb91ecce2aab"},
 }
 
 
 def kernel_src_hash(kernel_name: str) -> str:
     fns = {"seq": ["vla_seq.cu"], "chunk": ["vla_chunk.cu"],
-           "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu", "vla_gates_tc.cu", "vla_gram_tc.cu", "vla_tc_common.cuh"],
+           "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu", "vla_gates_tc.cu", "vla_gram_tc.cu", "vla_tc_common.cuh",
+                        "vla_gates_tc128.cu", "vla_rows_tc128.cu"],
            "decode": ["vla_decode.cu"]}[kernel_name]
     h = hashlib.sha256()
     for fn in fns:
