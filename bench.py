@@ -49,9 +49,9 @@ FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
 TRAFFIC = {
     # sequential kernel, long stream: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
     ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
-    # tensor-core path, long stream: at T=16384 (same 16 heads), scaled x4 to T=65536
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 4 * (76.620544e6 + 15.288064e6), "src_sha": "56d72c88e7f36bb7"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 4 * (168.020224e6 + 101.082112e6), "src_sha": "56d72c88e7f36bb7"},
+    # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.238720e6 + 218.703104e6, "src_sha": "2c5aeb91ecce2aab"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 671.352576e6 + 250.816256e6, "src_sha": "2c5aeb91ecce2aab"},
     # d = 128, one chunk per unit, batched workload: at B=8 (128 units, one wave), scaled x4 to B=32
     ("chunk_tc", "batched", "gates_tc128_kernel"): {"bytes": 4 * (134.438144e6 + 91.868928e6),
                                                     "src_sha": "2c5aeb91ecce2aab"},
