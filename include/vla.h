@@ -107,8 +107,11 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * but the last comes back on copy_stream once all uploads are queued; the
  * last range's o (and the final state for the non-NULL host pointers among
  * hS_T, hA_T, hn_T) comes back on `stream`, which finally waits for
- * copy_stream: everything the call queued is complete once `stream` is.  On
- * the other paths u and k go first, the kernels wait for them before the
+ * copy_stream: everything the call queued is complete once `stream` is.  At
+ * d_h = 128 with one chunk per unit the ranges are waves of at most 152 units
+ * (up to four): u and k range by range, each followed by its gates; then q
+ * and v range by range, each followed by its state pass and, on `stream`,
+ * the download of its o.  On the other paths u and k go first, the kernels wait for them before the
  * first launch and for q and v before the first pass that reads them, and
  * all outputs come back on `stream`.  ev_uk and ev_qv carry these
  * dependencies (each is recorded more than once).  The uploads start after

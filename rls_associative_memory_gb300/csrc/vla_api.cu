@@ -323,8 +323,39 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
     if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return fail(e);
     const bool staged = n_io > 0 && BH >= 2 && kk == VLA_KERNEL_CHUNK_TC && vla::chunk_tc_parts_supported(p, L);
+    const bool staged128 = n_io > 0 && BH >= 2 && kk == VLA_KERNEL_CHUNK_TC && vla::chunk_tc128_parts_supported(p, L);
     long long o_lo = 0;  // o from this unit on comes back on `stream`
-    if (staged) {
+    if (staged128) {
+        // d = 128, one chunk per unit: both passes are per unit, one CTA per unit at
+        // one CTA per SM, so the ranges are waves of 152 units (at most four
+        // ranges). u and k go up range by range, each followed by its gates; then
+        // q and v, each range followed by its state pass and the download of its
+        // o, all on `stream`: the downloads run against the later uploads (the
+        // link carries both directions at once), and a range's state pass waits
+        // for its q and v longer than the previous range's o takes to come back.
+        long long nr = (BH + 151) / 152;
+        if (nr > 4) nr = 4;
+        long long r[5];
+        for (long long i = 0; i <= nr; ++i) r[i] = BH * i / nr;
+        for (long long i = 0; i < nr; ++i) {
+            if ((e = up(u, hu, r[i], r[i + 1] - r[i])) != cudaSuccess) return fail(e);
+            if ((e = up(k, hk, r[i], r[i + 1] - r[i])) != cudaSuccess) return fail(e);
+            if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
+            if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
+            if ((e = vla::launch_chunk_tc128_part(p, L, 0, (int)r[i], (int)(r[i + 1] - r[i]), st)) != cudaSuccess)
+                return fail(e);
+        }
+        for (long long j = 0; j < nr; ++j) {
+            if ((e = up(q, hq, r[j], r[j + 1] - r[j])) != cudaSuccess) return fail(e);
+            if ((e = up(v, hv, r[j], r[j + 1] - r[j])) != cudaSuccess) return fail(e);
+            if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
+            if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
+            if ((e = vla::launch_chunk_tc128_part(p, L, 1, (int)r[j], (int)(r[j + 1] - r[j]), st)) != cudaSuccess)
+                return fail(e);
+            if (j + 1 < nr && (e = down_o(r[j], r[j + 1] - r[j], st)) != cudaSuccess) return fail(e);
+        }
+        o_lo = r[nr - 1];
+    } else if (staged) {
         // Every pass of the tensor-core path is per (b, h), so the call runs it in
         // ranges of units as their inputs land on copy_stream: u and k in two
         // halves, each followed by its front (Grams, prefix, gates); then q and v

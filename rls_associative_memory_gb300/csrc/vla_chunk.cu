@@ -1407,6 +1407,25 @@ ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc_path) {
 
 bool chunk_tc_parts_supported(const FwdParams &p, const ChunkLayout &L) { return tc_parts_ok(p, L); }
 
+bool chunk_tc128_parts_supported(const FwdParams &p, const ChunkLayout &L) {
+    return p.d == 128 && p.io_bf16 && p.rows_tc && L.NC == 1 && L.NCA == 1;
+}
+
+cudaError_t launch_chunk_tc128_part(const FwdParams &p, const ChunkLayout &L, int part, int bh_lo, int bh_n,
+                                    cudaStream_t stream) {
+    if (!chunk_tc128_parts_supported(p, L) || bh_lo < 0 || bh_n <= 0 || bh_lo + bh_n > p.BH)
+        return cudaErrorInvalidValue;
+    ChunkArgs a{p, L};
+    a.bh_lo = bh_lo;
+    a.bh_n = bh_n;
+    int n = p.launches ? *p.launches : 0;
+    if (n == 0) mark_launch(p, 0, stream);
+    const cudaError_t e = part == 0 ? launch_gates_tc128(a, stream) : launch_rows_tc128(a, stream);
+    if (e != cudaSuccess) return e;
+    mark_launch(p, ++n, stream);
+    return cudaSuccess;
+}
+
 cudaError_t launch_chunk_tc_part(const FwdParams &p, const ChunkLayout &L, int part, int bh_lo, int bh_n,
                                  cudaStream_t stream) {
     if (!tc_parts_ok(p, L) || bh_lo < 0 || bh_n <= 0 || bh_lo + bh_n > p.BH) return cudaErrorInvalidValue;

@@ -147,6 +147,12 @@ cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream);
 // that runs S itself and writes o (vla_rows_tc128.cu), one CTA per unit each.
 cudaError_t launch_gates_tc128(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_rows_tc128(const ChunkArgs &a, cudaStream_t stream);
+// The same for a range of units [bh_lo, bh_lo + bh_n): part 0 the gates (reads u
+// and k), part 1 the state pass (reads q, k, v and the gates; writes o, S_T,
+// n_T).  Launch boundaries are numbered on from *p.launches.
+bool chunk_tc128_parts_supported(const FwdParams &p, const ChunkLayout &L);
+cudaError_t launch_chunk_tc128_part(const FwdParams &p, const ChunkLayout &L, int part, int bh_lo, int bh_n,
+                                    cudaStream_t stream);
 // Chunk Grams with TMA tensor loads (vla_gram_tc.cu), same shapes.
 bool gram_tma_supported(const FwdParams &p, const ChunkLayout &L);
 cudaError_t launch_gram_tma(const ChunkArgs &a, cudaStream_t stream);

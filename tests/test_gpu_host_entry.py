@@ -127,3 +127,36 @@ def test_host_entry_one_stream():
     stream.synchronize()
     assert torch.equal(ho, o_ref.cpu())
     assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
+
+
+@pytest.mark.parametrize("B,H,T", [(1, 2, 200), (2, 80, 130), (5, 64, 70)])
+def test_host_entry_d128_one_chunk_per_unit(B, H, T):
+    """d = 128 with one chunk per unit: ranges of at most 152 units (one wave),
+    u and k up first with each range's gates, then q and v with each range's
+    state pass; bit-identical to vla_forward."""
+    x = make_inputs(B, H, T, 128, "bf16", seed=90 + T, lambda0=0.5)
+    q, k, v, u = to_device(x)
+    chunk = (T + 63) // 64 * 64
+    kern = vla.VLA_KERNEL_CHUNK_TC
+    o_ref, S_ref, A_ref, n_ref = vla.vla_forward(q, k, v, u, x.lambda0, kernel=kern, chunk=chunk)
+    torch.cuda.synchronize()
+    assert vla.vla_last_launch_count() == 2
+    hq, hk, hv, hu = (t.cpu().pin_memory() for t in (q, k, v, u))
+    dq, dk, dv, du = (torch.empty_like(t) for t in (q, k, v, u))
+    o = torch.empty_like(q)
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    d = 128
+    S_T = torch.empty((B, H, d, d), device="cuda")
+    A_T = torch.empty_like(S_T)
+    n_T = torch.empty((B, H, d), device="cuda")
+    hS, hA = torch.empty(S_T.shape).pin_memory(), torch.empty(A_T.shape).pin_memory()
+    hn = torch.empty(n_T.shape).pin_memory()
+    ws = torch.empty(vla.vla_workspace_bytes(B, H, T, d, vla.VLA_BF16, kern, chunk), dtype=torch.uint8, device="cuda")
+    stream, copy_stream = torch.cuda.current_stream(), torch.cuda.Stream()
+    vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, dq, dk, dv, du, o, ho, S_T, A_T, n_T, hS, hA, hn, kernel=kern,
+                         chunk=chunk, workspace=ws, stream=stream, copy_stream=copy_stream)
+    stream.synchronize()
+    nr = min(4, (B * H + 151) // 152)
+    assert vla.vla_last_launch_count() == 2 * nr
+    assert torch.equal(ho, o_ref.cpu())
+    assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
