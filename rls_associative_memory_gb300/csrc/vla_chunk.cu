@@ -1251,14 +1251,17 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     prefix_kernel<D><<<(unsigned)(((D * D + D + 255) / 256) * BH), 256, 0, st>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     mark_launch(a.p, ++n, st);
-    if (kGatesOnTensorCores && a.p.rows_tc && gates_tc_supported(a.p, a.L)) {
+    const bool gtc = kGatesOnTensorCores && a.p.rows_tc && gates_tc_supported(a.p, a.L);
+    if (gtc) {
         if ((e = launch_gates_tc(a, st)) != cudaSuccess) return e;
     } else {
         gates_kernel<D, IO><<<(unsigned)(NCA * BH), G::NT, GatesSmem<D, IO>::total, st>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     mark_launch(a.p, ++n, st);
-    const bool tc = a.p.rows_tc && rows_tc_supported(a.p, a.L);
+    // the tensor-core state pass reads the gates in the fp16 form that only the
+    // tensor-core gates write
+    const bool tc = gtc && rows_tc_supported(a.p, a.L);
     // the passes so far read u and k only; q and v may still be arriving
     if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
         return e;

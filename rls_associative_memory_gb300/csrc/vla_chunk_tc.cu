@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
     const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.p.k) + tok0;
     const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.p.v) + tok0;
     const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.p.q) + tok0;
-    const float *gal = ws_f(a, a.L.off_alpha) + tok0;
+    const __half *gal = reinterpret_cast<const __half *>(static_cast<const unsigned char *>(a.p.ws) + a.L.off_alpha) + tok0;
     // this chunk's readout coefficients: per sub-block [y | h] (bf16), tile row =
     // state row (feature), columns = tokens
     unsigned char *gyh = static_cast<unsigned char *>(a.p.ws) + a.L.off_yh +
@@ -170,8 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
 
     // Inputs of the next sub-block, prefetched into registers during rounds
     // 2-3 of the current one (token pt, features 16 pq .. 16 pq + 15).
-    uint4 rk[2], rv[2], rq[2];
-    float4 ra[4];
+    uint4 rk[2], rv[2], rq[2], ra[2];
     // (always a valid token row, clamped: no select waits on the loads here;
     // tokens past the chunk are zeroed where the values are used)
     auto load_in = [&](int sb) {
@@ -184,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             rq[h] = reinterpret_cast<const uint4 *>(gq + off)[h];
         }
 #pragma unroll
-        for (int h = 0; h < 4; ++h) ra[h] = reinterpret_cast<const float4 *>(gal + off)[h];
+        for (int h = 0; h < 2; ++h) ra[h] = reinterpret_cast<const uint4 *>(gal + off)[h];
     };
 
     // phase: next parity of bar (three commits per sub-block), phase_n of bar_n
@@ -211,9 +210,7 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
         float fq[16];
         // ---- stage the sub-block's operands ----
         if (pt >= nt) {  // past the chunk: zero inputs
-            rk[0] = rk[1] = rv[0] = rv[1] = rq[0] = rq[1] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) ra[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            rk[0] = rk[1] = rv[0] = rv[1] = rq[0] = rq[1] = ra[0] = ra[1] = make_uint4(0, 0, 0, 0);
         }
         {
             float kf[16];
@@ -231,10 +228,8 @@ __global__ void __launch_bounds__(kThreads, 2) rows_tc_kernel(ChunkArgs a) {
             *reinterpret_cast<uint4 *>(vt + pt * kVS + 16 * pq) = rv[0];
             *reinterpret_cast<uint4 *>(vt + pt * kVS + 16 * pq + 8) = rv[1];
             float af[16];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                af[4 * h] = ra[h].x; af[4 * h + 1] = ra[h].y; af[4 * h + 2] = ra[h].z; af[4 * h + 3] = ra[h].w;
-            }
+            unpack8_h(ra[0], af);
+            unpack8_h(ra[1], af + 8);
             uint4 h4, l4;
             split8(af, h4, l4);
             *reinterpret_cast<uint4 *>(al_hi + toff(pt, 16 * pq)) = h4;

@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     const size_t tok0 = ((size_t)bh * T + t0) * kD;
     const __nv_bfloat16 *gu = static_cast<const __nv_bfloat16 *>(a.p.u) + tok0;
     const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.p.k) + tok0;
-    float *galpha = ws_f(a, a.L.off_alpha) + tok0;
+    __half *galpha = reinterpret_cast<__half *>(static_cast<unsigned char *>(a.p.ws) + a.L.off_alpha) + tok0;
 
     if (tid == 0) {
         mbar_init(bar, 1);
@@ -471,10 +471,14 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
                 // alpha = g / max(|g|, eps) with g = row / |k_t|
                 const float nr = sqrtf(s_nrm[t] + s_nrm[64 + t]);
                 const float sc = 1.f / fmaxf(nr, kEps * kn_sb[t]);
-                float4 *dst = reinterpret_cast<float4 *>(galpha + (size_t)(sb * kSB + t) * kD + 32 * hw);
+                uint4 *dst = reinterpret_cast<uint4 *>(galpha + (size_t)(sb * kSB + t) * kD + 32 * hw);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = make_float4(g[4 * q] * sc, g[4 * q + 1] * sc, g[4 * q + 2] * sc, g[4 * q + 3] * sc);
+                for (int q = 0; q < 4; ++q) {
+                    float e[8];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) e[m] = g[8 * q + m] * sc;
+                    dst[q] = pack8_h(e);
+                }
             }
         }
     }

@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) gates_tc128_kernel(ChunkArgs a) {
     const size_t tok0 = (size_t)bh * T * kD2;
     const __nv_bfloat16 *gu = static_cast<const __nv_bfloat16 *>(a.p.u) + tok0;
     const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.p.k) + tok0;
-    float *galpha = ws_f(a, a.L.off_alpha) + tok0;
+    __half *galpha = reinterpret_cast<__half *>(static_cast<unsigned char *>(a.p.ws) + a.L.off_alpha) + tok0;
 
     if (tid == 0) {
         mbar_init(bar, 1);
@@ -466,13 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1) gates_tc128_kernel(ChunkArgs a) {
             if (qw >= 2 && t < nt) {
                 const float nr = sqrtf(s_nrm[t] + s_nrm[64 + t]);
                 const float sc = 1.f / fmaxf(nr, kEps * kn_sb[t]);
-                float4 *dst = reinterpret_cast<float4 *>(galpha + (size_t)(sb * kSB + t) * kD2 + 64 * hw);
+                uint4 *dst = reinterpret_cast<uint4 *>(galpha + (size_t)(sb * kSB + t) * kD2 + 64 * hw);
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        dst[8 * half + q] = make_float4(g[half][4 * q] * sc, g[half][4 * q + 1] * sc,
-                                                        g[half][4 * q + 2] * sc, g[half][4 * q + 3] * sc);
+                    for (int q = 0; q < 4; ++q) {
+                        float e[8];
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) e[m] = g[half][8 * q + m] * sc;
+                        dst[4 * half + q] = pack8_h(e);
+                    }
             }
         }
     }

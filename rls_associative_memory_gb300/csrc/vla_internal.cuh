@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -87,7 +88,7 @@ struct ChunkLayout {
     size_t off_M;        // [BH][NCA][d][d]  A-chunk Grams, then exclusive prefix M^(c)
     size_t off_n;        // [BH][NCA+1][d]   A-chunk sums of phi(k_hat), then exclusive prefix n^(c)
     size_t off_M0;       // [BH][d][d]      inverse of A0 (only when A0 is given)
-    size_t off_alpha;    // [BH][T][d]      unit gates alpha_t
+    size_t off_alpha;    // [BH][T][d]      unit gates alpha_t (fp32; fp16 on the tensor-core passes)
     size_t off_P;        // [BH][NC][d][d]  chunk transition P_c
     size_t off_H;        // [BH][NC][d][d]  chunk offset H_c
     size_t off_S;        // [BH][NC][d][d]  chunk-start states S^(c)

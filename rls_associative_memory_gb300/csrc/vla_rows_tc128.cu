@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
     const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.p.v) + tok0;
     const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.p.q) + tok0;
     __nv_bfloat16 *go = static_cast<__nv_bfloat16 *>(a.p.o) + tok0;
-    const float *gal = ws_f(a, a.L.off_alpha) + tok0;
+    const __half *gal = reinterpret_cast<const __half *>(static_cast<const unsigned char *>(a.p.ws) + a.L.off_alpha) + tok0;
 
     if (tid == 0) {
         mbar_init(bar, 1);
@@ -137,8 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
         tc_fence_before();
     }
 
-    uint4 rk[4], rv[4], rq[4];
-    float4 ra[8];
+    uint4 rk[4], rv[4], rq[4], ra[4];
     auto load_in = [&](int sb) {
         const int t = min(sb * kSB + pt, T - 1);
         const size_t off = (size_t)t * kD2 + 32 * pq;
@@ -149,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
             rq[h] = reinterpret_cast<const uint4 *>(gq + off)[h];
         }
 #pragma unroll
-        for (int h = 0; h < 8; ++h) ra[h] = reinterpret_cast<const float4 *>(gal + off)[h];
+        for (int h = 0; h < 4; ++h) ra[h] = reinterpret_cast<const uint4 *>(gal + off)[h];
     };
 
     // phase: next parity of bar (three commits per sub-block), phase_n of bar_n
@@ -177,9 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
         // ---- stage the sub-block's operands ----
         if (pt >= nt) {
 #pragma unroll
-            for (int h = 0; h < 4; ++h) rk[h] = rv[h] = rq[h] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int h = 0; h < 8; ++h) ra[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int h = 0; h < 4; ++h) rk[h] = rv[h] = rq[h] = ra[h] = make_uint4(0, 0, 0, 0);
         }
         {
             float ss = 0.f;
@@ -200,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
             for (int h = 0; h < 4; ++h) {
                 *reinterpret_cast<uint4 *>(pk + toff(64 + pt, kc + 8 * h)) = rk[h];
                 *reinterpret_cast<uint4 *>(vt + pt * kVS2 + 32 * pq + 8 * h) = rv[h];
-                float af[8] = {ra[2 * h].x, ra[2 * h].y, ra[2 * h].z, ra[2 * h].w,
-                               ra[2 * h + 1].x, ra[2 * h + 1].y, ra[2 * h + 1].z, ra[2 * h + 1].w};
+                float af[8];
+                unpack8_h(ra[h], af);
                 uint4 h4, l4;
                 split8(af, h4, l4);
                 *reinterpret_cast<uint4 *>(ah_ + toff(pt, kc + 8 * h)) = h4;

@@ -52,6 +52,30 @@ __device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// The unit gates between the gates and the state pass travel as fp16: their
+// components lie in [-1, 1], where fp16 keeps 11 significant bits (bf16: 8),
+// and an fp16 value is exactly a bf16 pair (hi, lo), so the state pass's split
+// products see the stored gate without further rounding.
+__device__ __forceinline__ uint4 pack8_h(const float *x) {
+    uint32_t h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __half2 v = __floats2half2_rn(x[2 * e], x[2 * e + 1]);
+        h[e] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+__device__ __forceinline__ void unpack8_h(uint4 w, float *x) {
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&a[e]));
+        x[2 * e] = f.x;
+        x[2 * e + 1] = f.y;
+    }
+}
+
 __device__ __forceinline__ void unpack8(uint4 w, float *x) {
     const uint32_t a[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll

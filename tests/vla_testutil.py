@@ -50,6 +50,7 @@ def rel_fro(a, b):
 def compare(gpu, ref, dtype, keys=("o", "S_T", "A_T", "n_T")):
     errs = {k: rel_fro(gpu[k], ref[k]) for k in keys}
     tol = TOL[dtype]
+    print("parity errors (tol %g): %s" % (tol, " ".join("%s %.3g" % kv for kv in errs.items())))
     bad = {k: e for k, e in errs.items() if not (e <= tol)}
     assert not bad, "parity failed (tol %g): %s" % (tol, errs)
     return errs
