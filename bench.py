@@ -90,7 +90,7 @@ def kernel_plan(kname, d, io_dtype="bf16", units=0):
     io = 2 if io_dtype == "bf16" else 4
     full = 12 * d * d + 16 * d
     if kname == "seq":
-        return [("seq_kernel", full, 5 * d * io, "alu")]
+        return [("seq32_kernel" if d == 32 else "seq_kernel", full, 5 * d * io, "alu")]
     if kname == "decode":
         # one token per call: the state read and written back dominates (added by the caller)
         return [("decode_kernel", full, 5 * d * io, "alu")]

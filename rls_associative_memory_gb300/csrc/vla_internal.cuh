@@ -53,6 +53,8 @@ inline void mark_launch(const FwdParams &p, int i, cudaStream_t st) {
 
 // Sequential kernel: one CTA per (b, h).  Returns a cudaError_t.
 cudaError_t launch_seq(const FwdParams &p, cudaStream_t stream);
+// Its d = 32 form: three warps per (b, h) (inputs, A chain, S chain).
+cudaError_t launch_seq32(const FwdParams &p, cudaStream_t stream);
 
 // Backward pass (gradients of the recurrence); one CTA per (b, h).
 struct BwdParams {

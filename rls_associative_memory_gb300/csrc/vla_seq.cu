@@ -1,4 +1,5 @@
-// vla_seq.cu -- token-sequential VLA forward kernel: one CTA per (batch, head).
+// vla_seq.cu -- token-sequential VLA forward kernel: one CTA per (batch, head)
+// (d_h = 64 and 128; d_h = 32 has its own kernel in vla_seq32.cu).
 //
 // Recurrence ("Variational Linear Attention: Stable Associative Memory for
 // Long-Context Transformers", sections 2.2-2.3), per token t:
@@ -388,15 +389,14 @@ cudaError_t launch_seq_t(const FwdParams &p, cudaStream_t stream) {
 
 cudaError_t launch_seq(const FwdParams &p, cudaStream_t stream) {
     if (p.BH == 0) return cudaSuccess;
+    if (p.d == 32) return launch_seq32(p, stream);  // three warps a (b, h): vla_seq32.cu
     if (p.io_bf16) {
         switch (p.d) {
-            case 32: return launch_seq_t<32, __nv_bfloat16>(p, stream);
             case 64: return launch_seq_t<64, __nv_bfloat16>(p, stream);
             case 128: return launch_seq_t<128, __nv_bfloat16>(p, stream);
         }
     } else {
         switch (p.d) {
-            case 32: return launch_seq_t<32, float>(p, stream);
             case 64: return launch_seq_t<64, float>(p, stream);
             case 128: return launch_seq_t<128, float>(p, stream);
         }
