@@ -22,8 +22,8 @@
 // Each slot has three mbarriers: inputs ready (warp 2 -> 0, 1), gates ready
 // (warp 0 -> 1), slot free (warp 1 -> 2); every wait is bounded.
 //
-// A is updated as A -= beta * (z_i z_j): the product z_i z_j is symmetric in
-// (i, j), so A stays exactly symmetric in fp32.
+// A is updated as A -= w w^T with w = sqrt(beta) z, one FMA per entry: the
+// product inside an FMA is exact, so A stays exactly symmetric in fp32.
 #include "vla_internal.cuh"
 
 namespace vla {
@@ -41,7 +41,7 @@ struct S32Layout {
     static constexpr int slot = 5 * kTT * 32 + kTT;  // floats
     static constexpr size_t bars = 0;                // full_in[kNB], full_g[kNB], empty[kNB]
     static constexpr size_t flag = 3 * kNB * 8;      // abort flag
-    static constexpr size_t zbuf = 128;              // [2][32]: z of the A chain, by token parity
+    static constexpr size_t zbuf = 128;              // [2][32]: w of the A chain, by token parity
     static constexpr size_t slots = zbuf + 2 * 32 * 4;
     static constexpr size_t total = slots + (size_t)kNB * slot * 4;
 };
@@ -57,16 +57,32 @@ __device__ __forceinline__ void prefetch_l2(const void *ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase
+// completes or about `hint_ns` pass, instead of spinning on the issue slots
+// that the chain warps of the SM need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // All 32 lanes wait for phase `parity` of `bar`.  A lane gives up once another
 // warp has aborted, or after limit_ns (then it sets the device error word and
 // the abort flag).  The warp goes on only if every lane saw the phase.
 __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           const FwdParams &p) {
+    constexpr uint32_t kHintNs = 20000;
     bool ok = mbar_try_wait(bar, parity);
     if (!ok) {
         const unsigned long long t0 = globaltimer_ns();
         for (;;) {
-            if (mbar_try_wait(bar, parity)) {
+            if (mbar_try_wait_sleep(bar, parity, kHintNs)) {
                 ok = true;
                 break;
             }
@@ -90,6 +106,57 @@ __device__ __forceinline__ float2 warp_sum2(float x, float y) {
     for (int o = 8; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
     return make_float2(__shfl_sync(0xffffffffu, a, 0), __shfl_sync(0xffffffffu, a, 16));
 }
+
+// The four sums over the warp of (x0, x1, x2, x3), returned to every lane: the
+// first two exchanges halve the values each lane carries (6 shuffles, then 4
+// broadcasts).
+__device__ __forceinline__ float4 warp_sum4(float x0, float x1, float x2, float x3) {
+    const int lane = threadIdx.x & 31;
+    const bool b4 = lane & 16, b3 = lane & 8;
+    const float a0 = (b4 ? x2 : x0) + __shfl_xor_sync(0xffffffffu, b4 ? x0 : x2, 16);
+    const float a1 = (b4 ? x3 : x1) + __shfl_xor_sync(0xffffffffu, b4 ? x1 : x3, 16);
+    float c = (b3 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, b3 ? a0 : a1, 8);  // sum 2 b4 + b3
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    return make_float4(__shfl_sync(0xffffffffu, c, 0), __shfl_sync(0xffffffffu, c, 8),
+                       __shfl_sync(0xffffffffu, c, 16), __shfl_sync(0xffffffffu, c, 24));
+}
+
+// The eight sums over the warp of v[0..7]; lane l ends with the sum of
+// v[l / 4] (the first three exchanges halve the values each lane carries:
+// 4 + 2 + 1 + 2 shuffles for the eight).
+__device__ __forceinline__ float warp_sum8(const float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float a[4], b[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a[j] = (b4 ? v[4 + j] : v[j]) + __shfl_xor_sync(0xffffffffu, b4 ? v[j] : v[4 + j], 16);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) b[j] = (b3 ? a[2 + j] : a[j]) + __shfl_xor_sync(0xffffffffu, b3 ? a[j] : a[2 + j], 8);
+    float c = (b2 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, b2 ? b[0] : b[1], 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    return c;
+}
+
+// Row `lane` of a matrix (16 fp32 pairs) times two vectors in shared memory.
+__device__ __forceinline__ void row_dot2(const float2 (&a)[16], const float *x, const float *y, float &ax,
+                                        float &ay) {
+    const float4 *xp = reinterpret_cast<const float4 *>(x), *yp = reinterpret_cast<const float4 *>(y);
+    float2 xa = f2(0.f), xb = f2(0.f), ya = f2(0.f), yb = f2(0.f);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float4 xx = xp[c], yy = yp[c];
+        xa = fma2(a[2 * c], lo2(xx), xa);
+        xb = fma2(a[2 * c + 1], hi2(xx), xb);
+        ya = fma2(a[2 * c], lo2(yy), ya);
+        yb = fma2(a[2 * c + 1], hi2(yy), yb);
+    }
+    ax = hsum2(add2(xa, xb));
+    ay = hsum2(add2(ya, yb));
+}
+
+static_assert(kTT == 8, "the input warp reduces a slot's eight tokens at once");
 
 template <typename IO>
 __global__ void __launch_bounds__(kNT32, 7) seq32_kernel(FwdParams p) {
@@ -150,10 +217,14 @@ __global__ void __launch_bounds__(kNT32, 7) seq32_kernel(FwdParams p) {
                 u[tt] = io_to_f32(gu[off]);
             }
             float *sl = slots + (size_t)s * L::slot;
+            // |k_t|^2 of the slot's tokens in one reduction; lane 4 tt holds token tt's
+            float e[kTT];
+#pragma unroll
+            for (int tt = 0; tt < kTT; ++tt) e[tt] = k[tt] * k[tt];
+            const float ksl = 1.f / fmaxf(sqrtf(warp_sum8(e)), kEps);
 #pragma unroll
             for (int tt = 0; tt < kTT; ++tt) {
-                const float ss = warp_sum(k[tt] * k[tt]);
-                const float kh = k[tt] * (1.f / fmaxf(sqrtf(ss), kEps));
+                const float kh = k[tt] * __shfl_sync(0xffffffffu, ksl, 4 * tt);
                 if (tt < nt) {  // n_t includes token t
                     const float y = phi_elu1(kh) - ncomp;
                     const float tk = nrun + y;
@@ -161,13 +232,15 @@ __global__ void __launch_bounds__(kNT32, 7) seq32_kernel(FwdParams p) {
                     nrun = tk;
                 }
                 const float fq = phi_elu1(q[tt]);
-                const float den = warp_sum(fq * nrun);
+                e[tt] = fq * nrun;
                 sl[L::kKh + tt * 32 + lane] = kh;
                 sl[L::kU + tt * 32 + lane] = u[tt];
                 sl[L::kF + tt * 32 + lane] = fq;
                 sl[L::kV + tt * 32 + lane] = v[tt];
-                if (lane == 0) sl[L::kDen + tt] = 1.f / (den + kEps);
             }
+            // phi(q_t) . n_t of the slot's tokens, likewise
+            const float dl = warp_sum8(e);
+            if ((lane & 3) == 0) sl[L::kDen + (lane >> 2)] = 1.f / (dl + kEps);
             __syncwarp();
             mbar_arrive(&full_in[s]);
         }
@@ -192,53 +265,64 @@ __global__ void __launch_bounds__(kNT32, 7) seq32_kernel(FwdParams p) {
             for (int j = 0; j < 16; ++j)
                 a[j] = make_float2(2 * j == lane ? il : 0.f, 2 * j + 1 == lane ? il : 0.f);
         }
-        // the update of the previous token, applied in the next token's pass:
-        // A -= beta_p z_p z_p^T (z_p in zbuf[(t - 1) & 1], zero before token 0)
-        float beta_p = 0.f, z_p = 0.f;
+        // One token of lookahead keeps the products with A off the serial chain:
+        // with z_t = A_{t-1} u_t and y_t = A_{t-1} k_hat_t known,
+        //   z_{t+1} = A_{t-1} u_{t+1} - beta_t z_t (z_t . u_{t+1}),
+        //   y_{t+1} = A_{t-1} k_hat_{t+1} - beta_t z_t (z_t . k_hat_{t+1}),
+        // so the products with A_{t-1} run beside token t's one reduction (of
+        // u_t . z_t, k_hat_t . z_t, z_t . u_{t+1}, z_t . k_hat_{t+1}), and the chain
+        // per token is that reduction, a reciprocal square root and an FMA.
+        // A_t = A_{t-1} - w w^T with w = sqrt(beta_t) z_t: the product inside an
+        // FMA is exact, so w_i w_j = w_j w_i and A stays exactly symmetric.
+        float z = 0.f, y = 0.f;
+        if (ntiles > 0) {
+            if (!wait_warp(&full_in[0], 0u, abort_flag, p)) return;
+            row_dot2(a, slots + L::kU, slots + L::kKh, z, y);
+        }
         int t = 0;
         for (int m = 0; m < ntiles; ++m) {
             const int s = m % kNB;
-            if (!wait_warp(&full_in[s], (uint32_t)((m / kNB) & 1), abort_flag, p)) return;
             float *sl = slots + (size_t)s * L::slot;
             const int nt = min(kTT, T - m * kTT);
             for (int tt = 0; tt < nt; ++tt, ++t) {
-                const float4 *zp = reinterpret_cast<const float4 *>(zbuf + ((t + 1) & 1) * 32);
-                const float4 *up = reinterpret_cast<const float4 *>(sl + L::kU + tt * 32);
-                const float4 *kp = reinterpret_cast<const float4 *>(sl + L::kKh + tt * 32);
-                const float2 mb = f2(-beta_p), zi = f2(z_p);
-                float2 za = f2(0.f), zb = f2(0.f), ya = f2(0.f), yb = f2(0.f);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float4 zz = zp[c], uu = up[c], kk = kp[c];
-                    a[2 * c] = fma2(mb, mul2(zi, lo2(zz)), a[2 * c]);
-                    a[2 * c + 1] = fma2(mb, mul2(zi, hi2(zz)), a[2 * c + 1]);
-                    za = fma2(a[2 * c], lo2(uu), za);
-                    zb = fma2(a[2 * c + 1], hi2(uu), zb);
-                    ya = fma2(a[2 * c], lo2(kk), ya);
-                    yb = fma2(a[2 * c + 1], hi2(kk), yb);
+                // token t + 1: in this slot, or first in the next one
+                const bool more = t + 1 < T;
+                const float *sn = sl;
+                int tn = tt + 1;
+                if (tn == kTT) {
+                    const int mn = m + 1;
+                    sn = slots + (size_t)(mn % kNB) * L::slot;
+                    tn = 0;
+                    if (more && !wait_warp(&full_in[mn % kNB], (uint32_t)((mn / kNB) & 1), abort_flag, p)) return;
                 }
-                const float z = hsum2(add2(za, zb)), y = hsum2(add2(ya, yb));  // (A_{t-1} u)_i, (A_{t-1} k_hat)_i
-                zbuf[(t & 1) * 32 + lane] = z;
-                // u^T z and k_hat^T z
-                const float2 pr = warp_sum2(sl[L::kU + tt * 32 + lane] * z, sl[L::kKh + tt * 32 + lane] * z);
-                const float beta = 1.f / (1.f + pr.x);
-                sl[L::kG + tt * 32 + lane] = fmaf(-beta * pr.y, z, y);  // (A_t k_hat)_i
-                beta_p = beta;
-                z_p = z;
-                __syncwarp();  // z_t in zbuf for everyone before the next pass
+                float zn = 0.f, yn = 0.f, un = 0.f, kn = 0.f;
+                if (more) {
+                    row_dot2(a, sn + L::kU + tn * 32, sn + L::kKh + tn * 32, zn, yn);  // with A_{t-1}
+                    un = sn[L::kU + tn * 32 + lane];
+                    kn = sn[L::kKh + tn * 32 + lane];
+                }
+                const float4 pr = warp_sum4(sl[L::kU + tt * 32 + lane] * z, sl[L::kKh + tt * 32 + lane] * z,
+                                            un * z, kn * z);
+                const float sb = rsqrtf(1.f + pr.x);  // sqrt(beta_t)
+                const float beta = sb * sb;
+                sl[L::kG + tt * 32 + lane] = fmaf(-beta * pr.y, z, y);  // (A_t k_hat_t)_i
+                const float w = sb * z;
+                zbuf[(t & 1) * 32 + lane] = w;
+                __syncwarp();
+                const float4 *wp = reinterpret_cast<const float4 *>(zbuf + (t & 1) * 32);
+                const float2 mw = f2(-w);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // A_t = A_{t-1} - w w^T
+                    const float4 ww = wp[c];
+                    a[2 * c] = fma2(mw, lo2(ww), a[2 * c]);
+                    a[2 * c + 1] = fma2(mw, hi2(ww), a[2 * c + 1]);
+                }
+                const float zt = z;
+                z = fmaf(-beta * pr.z, zt, zn);
+                y = fmaf(-beta * pr.w, zt, yn);
             }
             __syncwarp();
             mbar_arrive(&full_g[s]);
-        }
-        {  // the last token's update
-            const float4 *zp = reinterpret_cast<const float4 *>(zbuf + ((t + 1) & 1) * 32);
-            const float2 mb = f2(-beta_p), zi = f2(z_p);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 zz = zp[c];
-                a[2 * c] = fma2(mb, mul2(zi, lo2(zz)), a[2 * c]);
-                a[2 * c + 1] = fma2(mb, mul2(zi, hi2(zz)), a[2 * c + 1]);
-            }
         }
         float4 *dst = reinterpret_cast<float4 *>(p.A_T + moff);
 #pragma unroll
