@@ -295,12 +295,13 @@ __global__ void __launch_bounds__(kNT32, 7) seq32_kernel(FwdParams p) {
                     tn = 0;
                     if (more && !wait_warp(&full_in[mn % kNB], (uint32_t)((mn / kNB) & 1), abort_flag, p)) return;
                 }
-                float zn = 0.f, yn = 0.f, un = 0.f, kn = 0.f;
-                if (more) {
-                    row_dot2(a, sn + L::kU + tn * 32, sn + L::kKh + tn * 32, zn, yn);  // with A_{t-1}
-                    un = sn[L::kU + tn * 32 + lane];
-                    kn = sn[L::kKh + tn * 32 + lane];
-                }
+                // (past the stream's end: this token's vectors, the results unused; no
+                // branch, so that these products and the reduction below interleave)
+                sn = more ? sn : sl;
+                tn = more ? tn : tt;
+                float zn, yn;
+                row_dot2(a, sn + L::kU + tn * 32, sn + L::kKh + tn * 32, zn, yn);  // with A_{t-1}
+                const float un = sn[L::kU + tn * 32 + lane], kn = sn[L::kKh + tn * 32 + lane];
                 const float4 pr = warp_sum4(sl[L::kU + tt * 32 + lane] * z, sl[L::kKh + tt * 32 + lane] * z,
                                             un * z, kn * z);
                 const float sb = rsqrtf(1.f + pr.x);  // sqrt(beta_t)
