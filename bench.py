@@ -47,21 +47,23 @@ FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
 # workload).  Reported only while the kernel source still hashes to the value
 # it was captured from; otherwise null.
 TRAFFIC = {
-    # sequential kernel, long stream: 134.4 + 18.6 MB at T=16384, scaled x4 to T=65536
-    ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.439936e6 + 18.616064e6), "src_sha": "40d37f7eec08ea9c"},
+    # sequential kernel, long stream: 134.4 + 18.9 MB at T=16384, scaled x4 to T=65536
+    ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.394112e6 + 18.881792e6), "src_sha": "60489ee668b38996"},
+    # sequential kernel at d = 32, recall8 workload: one full-size launch (one ncu pass)
+    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.476160e6 + 51.005184e6, "src_sha": "60489ee668b38996"},
     # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.238720e6 + 218.703104e6, "src_sha": "2c5aeb91ecce2aab"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 671.352576e6 + 250.816256e6, "src_sha": "2c5aeb91ecce2aab"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.211072e6 + 101.667328e6, "src_sha": "7e71eeed733c4469"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.463296e6 + 246.771456e6, "src_sha": "7e71eeed733c4469"},
     # d = 128, one chunk per unit, batched workload: at B=8 (128 units, one wave), scaled x4 to B=32
-    ("chunk_tc", "batched", "gates_tc128_kernel"): {"bytes": 4 * (134.438144e6 + 91.868928e6),
-                                                    "src_sha": "2c5aeb91ecce2aab"},
-    ("chunk_tc", "batched", "rows_tc128_kernel"): {"bytes": 4 * (335.677440e6 + 54.724608e6),
-                                                   "src_sha": "2c5aeb91ecce2aab"},
+    ("chunk_tc", "batched", "gates_tc128_kernel"): {"bytes": 4 * (134.330624e6 + 37.467392e6),
+                                                    "src_sha": "7e71eeed733c4469"},
+    ("chunk_tc", "batched", "rows_tc128_kernel"): {"bytes": 4 * (268.697856e6 + 48.734464e6),
+                                                   "src_sha": "7e71eeed733c4469"},
 }
 
 
 def kernel_src_hash(kernel_name: str) -> str:
-    fns = {"seq": ["vla_seq.cu"], "chunk": ["vla_chunk.cu"],
+    fns = {"seq": ["vla_seq.cu", "vla_seq32.cu"], "chunk": ["vla_chunk.cu"],
            "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu", "vla_gates_tc.cu", "vla_gram_tc.cu", "vla_tc_common.cuh",
                         "vla_gates_tc128.cu", "vla_rows_tc128.cu"],
            "decode": ["vla_decode.cu"]}[kernel_name]
