@@ -772,7 +772,11 @@ cudaError_t launch_backward_chunk(const BwdParams &p, cudaStream_t st, bool *use
     f.ws = ws;
     f.ws_bytes = b.L.total;
     f.chunk = 0;
-    f.rows_tc = (p.d == 64 && p.io_bf16) ? 1 : 0;
+    // the SIMT passes: their fp32 gates keep the chunk-start states, from which the
+    // sweeps below rebuild every token's state, at fp32 accuracy (the tensor-core
+    // passes hand fp16 gates on, which is within the forward's bf16 bar but shows
+    // in the gradients)
+    f.rows_tc = 0;
     int nf = 0;
     f.launches = &nf;
     cudaError_t e = launch_chunk(f, b.L, st);
