@@ -56,14 +56,14 @@ struct GtLayout {
     // R1 -> R2: AK^T hi @0, W^T hi @8K, AK^T lo @16K, W^T lo @24K (R2's B operand, two
     //           64-row tiles stacked), W^T fp32 @kW32
     // R2 -> elimination: Y_hat fp32 @0, I + G fp32 @kG32, W^T fp32 @kW32
-    // elimination: pivot rows @0 (2 x 8 x 192 floats), scaled pivot rows @kSrow
+    // elimination: 8 KB a block of 8 pivots @0 .. 64K (I + G pivot rows, scaled rows,
+    //     W^T and Y_hat pivot rows, 8 x 64 floats each)
     // R4: [-(beta Z)^T | E'] pairs of atoms @0 (parts 0) and @16K (parts 1), Z^T parts
     //     0, 1, 2 @32K, 40K, 48K, -(beta Z)^T part 2 @56K
     // chunk start: diag(1/D) E hi @0, lo @8K, E hi @16K, lo @24K, M^(c) fp32 @32K,
     //     pivot rows @kCrow (2 x 8 x 128 floats), scaled pivot rows @kCsrow
     static constexpr size_t kW32 = 4 * kTile;
     static constexpr size_t kG32 = kW32 + (size_t)64 * kGS * 4;
-    static constexpr size_t kSrow = (size_t)2 * 8 * 192 * 4;
     static constexpr size_t kCrow = kW32 + (size_t)64 * kGS * 4;
     static constexpr size_t kCsrow = kCrow + (size_t)2 * 8 * 128 * 4;
     static constexpr size_t work_bytes = kG32 + (size_t)64 * kGS * 4;
@@ -74,7 +74,7 @@ struct GtLayout {
     static constexpr size_t total = nrm + 512;
 };
 static_assert(GtLayout::work % 1024 == 0, "operand tiles must be 1024-byte aligned");
-static_assert(GtLayout::kSrow + 2 * 8 * 64 * 4 <= GtLayout::kW32, "elimination scratch fits below W^T");
+static_assert(8 * 8 * 4 * 64 * 4 <= GtLayout::work_bytes, "the elimination's publication buffers fit");
 static_assert(8 * kTile <= GtLayout::work_bytes, "R4 tiles fit the work area");
 static_assert(GtLayout::kCsrow + 2 * 8 * 64 * 4 <= GtLayout::work_bytes, "chunk-start scratch fits");
 
@@ -93,17 +93,30 @@ __device__ __forceinline__ void split3_pair(float a, float b, uint32_t &p0, uint
 }
 
 // Forward elimination of [I + G | W^T | Y_hat] (64 rows s, fp32, row stride
-// kGS) without pivoting, the block scheme of eliminate64 (warp w owns rows
-// 8 w .. 8 w + 7, lane l columns 2 l, 2 l + 1 of each block; the owner of a
-// block of 8 pivots eliminates it with shuffles and publishes its pivot rows
-// and the rows scaled by -1 / D_s; the next owner applies first), carrying
-// the two right-hand blocks instead of the identity.  Afterwards row s holds
-// z_s^T = (L^{-1} W^T)[s] and P[s] = (L^{-1} Y_hat)[s], and rpiv[s] = 1 / D_s.
-// It writes the operand tiles of round 4 (rows s): Z^T and -(beta Z)^T in
-// three bf16 parts, E'[s][t] = -beta_s P[s][t] |k_t| (s <= t, else 0) in two.
-// 256 threads; all must call.
-__device__ __forceinline__ void eliminate_rhs64(const float *gs, const float *w32, const float *y32, float *prow,
-                                                float *srow, float *rpiv, const float *kn, unsigned char *work) {
+// kGS) without pivoting.  Warp w owns rows 8 w .. 8 w + 7 and lane l columns
+// 2 l, 2 l + 1 of each block; the owner of a block of 8 pivots eliminates it
+// with shuffles.  Only the I + G part is on the serial chain: the owner runs
+// its pivots on I + G alone and publishes their rows and the rows scaled by
+// -1 / D_s (whose entries are the multipliers of the later rows), so that the
+// next owner can apply them to its I + G rows and start its own pivots at
+// once.  The right-hand blocks follow off the chain: each warp applies the
+// earlier blocks' pivots to its W^T and Y_hat rows, then its own (multipliers
+// read back from its scaled rows), and publishes its pivot rows of those.
+// Every element takes the same FMAs in the same pivot order as in a single
+// sweep, so the result does not depend on the split.  Each block has its own
+// publication buffers in `pub` (8 KB a block: I + G pivot rows, scaled rows,
+// W^T and Y_hat pivot rows) and two mbarriers, ebar[b] (the I + G part of
+// block b published) and ebar[8 + b] (its right-hand part), each completed by
+// the owner's 32 lanes once per call (phase parity `ephase`); every wait is
+// bounded, and after a failed one the warp sets the abort flag and waits no
+// more (it still publishes and arrives, so nobody else is held).
+// Afterwards row s holds z_s^T = (L^{-1} W^T)[s] and P[s] = (L^{-1} Y_hat)[s],
+// and rpiv[s] = 1 / D_s.  It writes the operand tiles of round 4 (rows s): Z^T
+// and -(beta Z)^T in three bf16 parts, E'[s][t] = -beta_s P[s][t] |k_t|
+// (s <= t, else 0) in two.  256 threads; all must call.
+__device__ __forceinline__ void eliminate_rhs64(const float *gs, const float *w32, const float *y32, float *pub,
+                                                float *rpiv, const float *kn, unsigned char *work, uint64_t *ebar,
+                                                uint32_t ephase, const ChunkArgs &a, volatile int *abort_flag) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float2 m[8], z[8], pp[8];
 #pragma unroll
@@ -114,59 +127,109 @@ __device__ __forceinline__ void eliminate_rhs64(const float *gs, const float *w3
         pp[i] = *reinterpret_cast<const float2 *>(y32 + r * kGS + 2 * lane);
     }
     __syncthreads();  // the staging may be overwritten once everyone has its rows
-#pragma unroll 1
-    for (int b = 0; b < 8; ++b) {
-        float *pb = prow + (b & 1) * 8 * 192;
-        float *sb = srow + (b & 1) * 8 * 64;
-        if (warp == b) {
+    // block b's buffers: I + G pivot rows, scaled rows, W^T and Y_hat pivot rows (8 x 64 each)
+    auto pm = [&](int b) { return pub + b * 2048; };
+    auto ps = [&](int b) { return pub + b * 2048 + 512; };
+    auto pz = [&](int b) { return pub + b * 2048 + 1024; };
+    auto py = [&](int b) { return pub + b * 2048 + 1536; };
+    bool live = true;
+    auto wait = [&](uint64_t *bar) {
+        if (live && !mbar_wait_bounded(bar, ephase, a.p.wait_limit_ns, a.p.err)) {
+            live = false;
+            *abort_flag = 1;
+        }
+    };
+    // block b's pivots applied to this warp's rows of I + G, or of W^T and Y_hat
+    auto apply_m = [&](int b) {
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                // pivot M[s][s], s = 8 b + p: lane s / 2, component p mod 2
-                const float pv = __shfl_sync(0xffffffffu, (p & 1) ? m[p].y : m[p].x, 4 * b + (p >> 1));
-                // fast reciprocal: the pivots of I + G are >= 1 and its relative
-                // error (about 2^-22) is far below the parity bar downstream
-                const float rp = __fdividef(1.f, pv);
-                if (lane == 0) rpiv[8 * b + p] = rp;
+        for (int p = 0; p < 8; ++p) {
+            const float4 fa = *reinterpret_cast<const float4 *>(ps(b) + p * 64 + 8 * warp);
+            const float4 fb = *reinterpret_cast<const float4 *>(ps(b) + p * 64 + 8 * warp + 4);
+            const float2 pv = *reinterpret_cast<const float2 *>(pm(b) + p * 64 + 2 * lane);
+            const float fr[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (i <= p) continue;  // (constant trip count: the rows stay in registers)
-                    const float mv = __shfl_sync(0xffffffffu, (i & 1) ? m[p].y : m[p].x, 4 * b + (i >> 1));
-                    const float2 f = make_float2(-mv * rp, -mv * rp);
-                    m[i] = __ffma2_rn(f, m[p], m[i]);
-                    z[i] = __ffma2_rn(f, z[p], z[i]);
-                    pp[i] = __ffma2_rn(f, pp[p], pp[i]);
-                }
-                *reinterpret_cast<float2 *>(pb + p * 192 + 2 * lane) = m[p];
-                *reinterpret_cast<float2 *>(pb + p * 192 + 64 + 2 * lane) = z[p];
-                *reinterpret_cast<float2 *>(pb + p * 192 + 128 + 2 * lane) = pp[p];
-                *reinterpret_cast<float2 *>(sb + p * 64 + 2 * lane) = __fmul2_rn(m[p], make_float2(-rp, -rp));
+            for (int i = 0; i < 8; ++i) m[i] = __ffma2_rn(make_float2(fr[i], fr[i]), pv, m[i]);
+        }
+    };
+    auto apply_zp = [&](int b) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const float4 fa = *reinterpret_cast<const float4 *>(ps(b) + p * 64 + 8 * warp);
+            const float4 fb = *reinterpret_cast<const float4 *>(ps(b) + p * 64 + 8 * warp + 4);
+            const float2 pzv = *reinterpret_cast<const float2 *>(pz(b) + p * 64 + 2 * lane);
+            const float2 pyv = *reinterpret_cast<const float2 *>(py(b) + p * 64 + 2 * lane);
+            const float fr[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 fi = make_float2(fr[i], fr[i]);
+                z[i] = __ffma2_rn(fi, pzv, z[i]);
+                pp[i] = __ffma2_rn(fi, pyv, pp[i]);
             }
         }
-        __syncthreads();
-        if (warp > b) {
-            const uint32_t nbar = 32u * (uint32_t)(7 - b);
-            if (warp > b + 1) asm volatile("bar.sync 1, %0;" ::"r"(nbar) : "memory");
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const float4 fa = *reinterpret_cast<const float4 *>(sb + p * 64 + 8 * warp);
-                const float4 fb = *reinterpret_cast<const float4 *>(sb + p * 64 + 8 * warp + 4);
-                const float2 pm = *reinterpret_cast<const float2 *>(pb + p * 192 + 2 * lane);
-                const float2 pz = *reinterpret_cast<const float2 *>(pb + p * 192 + 64 + 2 * lane);
-                const float2 py = *reinterpret_cast<const float2 *>(pb + p * 192 + 128 + 2 * lane);
-                const float fr[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float2 fi = make_float2(fr[i], fr[i]);
-                    m[i] = __ffma2_rn(fi, pm, m[i]);
-                    z[i] = __ffma2_rn(fi, pz, z[i]);
-                    pp[i] = __ffma2_rn(fi, py, pp[i]);
-                }
-            }
-            if (warp == b + 1) asm volatile("bar.arrive 1, %0;" ::"r"(nbar) : "memory");
+    };
+    // the earlier blocks: I + G as soon as published; the right-hand part of
+    // all but the last one in between (the last one's comes after this warp's
+    // own pivots, which are on the chain)
+#pragma unroll 1
+    for (int b = 0; b < warp; ++b) {
+        wait(&ebar[b]);
+        apply_m(b);
+        if (b + 1 < warp) {
+            wait(&ebar[8 + b]);
+            apply_zp(b);
         }
     }
-    // round 4's tiles, rows s = 8 warp + i, columns 2 lane, 2 lane + 1 (the pivot
-    // scratch is no longer read by anyone once every warp has left the loop)
+    // this warp's block: pivots s = 8 warp + p on I + G
+    {
+        float *bm = pm(warp), *bs = ps(warp);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            // pivot M[s][s], s = 8 warp + p: lane s / 2, component p mod 2
+            const float pv = __shfl_sync(0xffffffffu, (p & 1) ? m[p].y : m[p].x, 4 * warp + (p >> 1));
+            // fast reciprocal: the pivots of I + G are >= 1 and its relative
+            // error (about 2^-22) is far below the parity bar downstream
+            const float rp = __fdividef(1.f, pv);
+            if (lane == 0) rpiv[8 * warp + p] = rp;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i <= p) continue;  // (constant trip count: the rows stay in registers)
+                const float mv = __shfl_sync(0xffffffffu, (i & 1) ? m[p].y : m[p].x, 4 * warp + (i >> 1));
+                m[i] = __ffma2_rn(make_float2(-mv * rp, -mv * rp), m[p], m[i]);
+            }
+            *reinterpret_cast<float2 *>(bm + p * 64 + 2 * lane) = m[p];
+            *reinterpret_cast<float2 *>(bs + p * 64 + 2 * lane) = __fmul2_rn(m[p], make_float2(-rp, -rp));
+        }
+        mbar_arrive(&ebar[warp]);
+    }
+    // the right-hand part: the previous block's pivots, then this block's (their
+    // multipliers are the scaled rows just published: entry 8 warp + i of row p)
+    if (warp > 0) {
+        wait(&ebar[8 + warp - 1]);
+        apply_zp(warp - 1);
+    }
+    __syncwarp();
+    {
+        const float *bs = ps(warp);
+        float *bz = pz(warp), *by = py(warp);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const float4 fa = *reinterpret_cast<const float4 *>(bs + p * 64 + 8 * warp);
+            const float4 fb = *reinterpret_cast<const float4 *>(bs + p * 64 + 8 * warp + 4);
+            const float fr[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i <= p) continue;
+                const float2 fi = make_float2(fr[i], fr[i]);
+                z[i] = __ffma2_rn(fi, z[p], z[i]);
+                pp[i] = __ffma2_rn(fi, pp[p], pp[i]);
+            }
+            *reinterpret_cast<float2 *>(bz + p * 64 + 2 * lane) = z[p];
+            *reinterpret_cast<float2 *>(by + p * 64 + 2 * lane) = pp[p];
+        }
+        mbar_arrive(&ebar[8 + warp]);
+    }
+    __syncthreads();  // every block applied: the buffers may be overwritten
+    // round 4's tiles, rows s = 8 warp + i, columns 2 lane, 2 lane + 1
     unsigned char *bz0 = work, *ep0 = work + kTile, *bz1 = work + 2 * kTile, *ep1 = work + 3 * kTile;
     unsigned char *zt0 = work + 4 * kTile, *zt1 = work + 5 * kTile, *zt2 = work + 6 * kTile;
     unsigned char *bz2 = work + 7 * kTile;
@@ -200,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
+    uint64_t *ebar = reinterpret_cast<uint64_t *>(smem + L::ctrl + 64);  // the elimination's 16 mbarriers
     unsigned char *uk = smem + L::uk;
     unsigned char *a_hi = smem + L::ah, *a_lo = smem + L::ah + kTile;
     unsigned char *work = smem + L::work;  // work + i * kTile: tile slot i
@@ -232,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
 
     if (tid == 0) {
         mbar_init(bar, 1);
+        for (int b = 0; b < 16; ++b) mbar_init(&ebar[b], 32);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -420,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         tc_fence_before();
         __syncthreads();
         // ---- elimination of [I + G | W^T | Y_hat]: Z^T, P and beta, and round 4's tiles ----
-        eliminate_rhs64(g32, w32, y32, reinterpret_cast<float *>(work), reinterpret_cast<float *>(work + L::kSrow),
-                        s_beta, kn_sb, work);
+        eliminate_rhs64(g32, w32, y32, reinterpret_cast<float *>(work), s_beta, kn_sb, work, ebar,
+                        (uint32_t)(sb & 1), a, abort_flag);
         // the next sub-block's inputs: issued after the elimination, so that their
         // registers are not live through it (round 4 hides the latency)
         load_in(sb + 1);

@@ -48,11 +48,6 @@ struct S32Layout {
 static_assert(S32Layout::flag + 4 <= S32Layout::zbuf, "control block");
 static_assert(S32Layout::slot % 4 == 0 && S32Layout::slots % 16 == 0, "16-byte aligned vectors");
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
