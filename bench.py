@@ -487,7 +487,7 @@ def main():
 
         # a decode step returns o; its state stays resident on the device
 
-        copy_stream = torch.cuda.Stream(dev)
+        copy_stream, download_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev_uk, ev_qv = torch.cuda.Event(), torch.cuda.Event()
 
         def e2e_step():
@@ -497,7 +497,8 @@ def main():
             hs = (None, None, None) if in_place else (hS, hA, hn)
             vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, q, k, v, u, o, ho, S_T, A_T, n_T, hs[0], hs[1], hs[2],
                                  S0=st[0], A0=st[1], n0=st[2], kernel=resolved, workspace=ws if need else None,
-                                 stream=stream, copy_stream=copy_stream, ev_uk=ev_uk, ev_qv=ev_qv)
+                                 stream=stream, copy_stream=copy_stream, ev_uk=ev_uk, ev_qv=ev_qv,
+                                 download_stream=download_stream)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()

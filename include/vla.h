@@ -111,7 +111,10 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * d_h = 128 with one chunk per unit the ranges are waves of at most 152 units
  * (up to four): u and k range by range, each followed by its gates; then q
  * and v range by range, each followed by its state pass and, on `stream`,
- * the download of its o.  On the other paths u and k go first, the kernels wait for them before the
+ * the download of its o.  With a download_stream, on both staged paths every
+ * range's o comes back on it as soon as the range's passes are done, beside
+ * the later uploads and passes (the link carries both directions at once),
+ * and `stream` finally waits for it.  On the other paths u and k go first, the kernels wait for them before the
  * first launch and for q and v before the first pass that reads them, and
  * all outputs come back on `stream`.  ev_uk and ev_qv carry these
  * dependencies (each is recorded more than once).  The uploads start after
@@ -127,11 +130,13 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * S0 .. ws_bytes  as in vla_forward.
  * stream          the compute stream; copy_stream a second stream (cudaStream_t
  *                 as void*; the same stream works, without overlap).
+ * download_stream optional third stream for the downloads of o on the staged
+ *                 paths (NULL: as described above; ignored on the other paths).
  * ev_uk, ev_qv    two cudaEvent_t (as void*) the call records; required.
  * Asynchronous: the host buffers must stay valid until `stream` has passed
  * the call's work.  Returns as vla_forward; on an argument error nothing is
  * queued.  On VLA_ERR_CUDA (a failed copy, record or launch) the work queued
- * before the failure may still run on both streams: synchronise both before
+ * before the failure may still run on every stream given: synchronise them before
  * reusing the buffers.
  */
 int vla_forward_host(const void *hq, const void *hk, const void *hv, const void *hu, int io_dtype,
@@ -139,7 +144,7 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
                      const float *n0, void *q, void *k, void *v, void *u, void *o, void *ho, float *S_T,
                      float *A_T, float *n_T, float *hS_T, float *hA_T, float *hn_T, int kernel, int chunk,
                      void *workspace, size_t ws_bytes, void *stream, void *copy_stream, void *ev_uk,
-                     void *ev_qv);
+                     void *ev_qv, void *download_stream);
 
 /* Workspace bytes vla_forward needs for these arguments (0 for the
  * sequential kernel).  Returns 0 for invalid arguments as well. */

@@ -52,7 +52,7 @@ _SIGS = {
     "vla_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, ctypes.c_float, _i, _i, _i, _i, _vp, _vp, _vp,
                                  _vp, _vp, _vp, _vp, _i, _vp]),
     "vla_forward_host": (_i, [_vp, _vp, _vp, _vp, _i, ctypes.c_float, _i, _i, _i, _i, _vp, _vp, _vp]
-                         + [_vp] * 12 + [_i, _i, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
+                         + [_vp] * 12 + [_i, _i, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp, _vp]),
     "vla_last_launch_count": (_i, []),
     "vla_backward": (_i, [_vp] * 5 + [_i, ctypes.c_float, _i, _i, _i, _i] + [_vp] * 14 + [ctypes.c_size_t, _vp]),
     "vla_backward_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
@@ -231,13 +231,16 @@ def vla_forward(q, k, v, u, lambda0: float, S0=None, A0=None, n0=None, o=None, S
 
 def vla_forward_host(hq, hk, hv, hu, lambda0: float, q, k, v, u, o, ho, S_T, A_T, n_T=None, hS_T=None,
                      hA_T=None, hn_T=None, S0=None, A0=None, n0=None, kernel: int = VLA_KERNEL_AUTO,
-                     chunk: int = 0, workspace=None, stream=None, copy_stream=None, ev_uk=None, ev_qv=None):
+                     chunk: int = 0, workspace=None, stream=None, copy_stream=None, ev_uk=None, ev_qv=None,
+                     download_stream=None):
     """vla_forward on host inputs: copies hq, hk, hv, hu (CPU tensors, ideally
     pinned) into the device buffers q, k, v, u (u and k first on
     ``copy_stream``, overlapped with the passes that read only them), runs the
     recurrence on ``stream`` and copies o (and the final state for the given
     host tensors) back.  ``ev_uk``, ``ev_qv``: torch.cuda.Event objects the call
-    records (created here when None).  Asynchronous; returns None."""
+    records (created here when None).  ``download_stream``: optional third
+    stream on which o comes back range by range on the staged paths.
+    Asynchronous; returns None."""
     import torch
     B, H, T, d = q.shape
     for t in (hq, hk, hv, hu, ho):
@@ -259,6 +262,7 @@ def vla_forward_host(hq, hk, hv, hu, lambda0: float, q, k, v, u, o, ho, S_T, A_T
                                 _ptr(ho), _ptr(S_T), _ptr(A_T), _ptr(n_T), _ptr(hS_T), _ptr(hA_T), _ptr(hn_T),
                                 int(kernel), int(chunk), _ptr(workspace), ws_bytes,
                                 ctypes.c_void_p(s.cuda_stream), ctypes.c_void_p(cs.cuda_stream),
-                                ctypes.c_void_p(evs[0].cuda_event), ctypes.c_void_p(evs[1].cuda_event))
+                                ctypes.c_void_p(evs[0].cuda_event), ctypes.c_void_p(evs[1].cuda_event),
+                                ctypes.c_void_p(None if download_stream is None else download_stream.cuda_stream))
     if rc != VLA_OK:
         raise VLAError(rc, "vla_forward_host")

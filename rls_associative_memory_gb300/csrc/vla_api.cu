@@ -282,7 +282,8 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
                      int B, int H, int T, int d_h, const float *S0, const float *A0, const float *n0, void *q,
                      void *k, void *v, void *u, void *o, void *ho, float *S_T, float *A_T, float *n_T,
                      float *hS_T, float *hA_T, float *hn_T, int kernel, int chunk, void *workspace,
-                     size_t ws_bytes, void *stream, void *copy_stream, void *ev_uk, void *ev_qv) {
+                     size_t ws_bytes, void *stream, void *copy_stream, void *ev_uk, void *ev_qv,
+                     void *download_stream) {
     int rc = check_common(io_dtype, lambda0, B, H, T, d_h, kernel);
     if (rc != VLA_OK) return rc;
     if (!ev_uk || !ev_qv) return VLA_ERR_ARG;
@@ -305,6 +306,7 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
     p.launches = &launches;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream), cs = static_cast<cudaStream_t>(copy_stream);
+    cudaStream_t ds = static_cast<cudaStream_t>(download_stream);  // may be NULL
     cudaEvent_t e_uk = static_cast<cudaEvent_t>(ev_uk), e_qv = static_cast<cudaEvent_t>(ev_qv);
     const size_t unit = n_io / (size_t)BH;  // bytes of one (b, h) unit of an input
     auto up = [&](void *dst, const void *src, long long lo, long long n) {
@@ -352,9 +354,15 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
             if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
             if ((e = vla::launch_chunk_tc128_part(p, L, 1, (int)r[j], (int)(r[j + 1] - r[j]), st)) != cudaSuccess)
                 return fail(e);
-            if (j + 1 < nr && (e = down_o(r[j], r[j + 1] - r[j], st)) != cudaSuccess) return fail(e);
+            if (ds) {  // the range's o on download_stream, beside the later passes
+                if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
+                if ((e = cudaStreamWaitEvent(ds, e_qv, 0)) != cudaSuccess) return fail(e);
+                if ((e = down_o(r[j], r[j + 1] - r[j], ds)) != cudaSuccess) return fail(e);
+            } else if (j + 1 < nr && (e = down_o(r[j], r[j + 1] - r[j], st)) != cudaSuccess) {
+                return fail(e);
+            }
         }
-        o_lo = r[nr - 1];
+        o_lo = ds ? BH : r[nr - 1];
     } else if (staged) {
         // Every pass of the tensor-core path is per (b, h), so the call runs it in
         // ranges of units as their inputs land on copy_stream: u and k in two
@@ -381,7 +389,7 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
             if ((e = up(q, hq, r[j], r[j + 1] - r[j])) != cudaSuccess) return fail(e);
             if ((e = up(v, hv, r[j], r[j + 1] - r[j])) != cudaSuccess) return fail(e);
             if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
-            if (j == nr - 1) {
+            if (j == nr - 1 && !ds) {
                 // all uploads are queued: the earlier ranges' o leave on copy_stream
                 // (e_qv holds "range 0 done", recorded on `stream` after its back)
                 if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return fail(e);
@@ -396,11 +404,19 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
             if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
             if ((e = vla::launch_chunk_tc_part(p, L, 1, (int)r[j], (int)(r[j + 1] - r[j]), st)) != cudaSuccess)
                 return fail(e);
-            if (j == 0 && (e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
+            if (ds) {  // the range's o on download_stream, beside the later passes
+                if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
+                if ((e = cudaStreamWaitEvent(ds, e_qv, 0)) != cudaSuccess) return fail(e);
+                if ((e = down_o(r[j], r[j + 1] - r[j], ds)) != cudaSuccess) return fail(e);
+            } else if (j == 0 && (e = cudaEventRecord(e_qv, st)) != cudaSuccess) {
+                return fail(e);
+            }
         }
         // copy_stream's downloads done: `stream` waits for it after its own copies
-        if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
-        o_lo = r[nr - 1];
+        // (with download_stream, copy_stream's last work, an upload, is already
+        // behind `stream`)
+        if (!ds && (e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
+        o_lo = ds ? BH : r[nr - 1];
     } else {
         // u and k first: on the chunked paths the Grams, the prefix and the gates
         // read only those; the kernels wait for q and v before their first pass
@@ -427,7 +443,11 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
         return fail(e);
     if (hn_T && n_d && (e = cudaMemcpyAsync(hn_T, n_T, n_d, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
         return fail(e);
-    if (staged && (e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
+    if (staged && !ds && (e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
+    if (ds && (staged || staged128)) {  // download_stream's copies done before `stream` is
+        if ((e = cudaEventRecord(e_qv, ds)) != cudaSuccess) return fail(e);
+        if ((e = cudaStreamWaitEvent(st, e_qv, 0)) != cudaSuccess) return fail(e);
+    }
     return VLA_OK;
 }
 

@@ -184,7 +184,7 @@ def test_host_entry_argument_checks():
     def call(ev=(f, f + 16), hq=f + 0x100000, hn=None, n_T=None, io=vla.VLA_BF16, d=64, T=64):
         return L.vla_forward_host(hq, hq, hq, hq, io, 1.0, 1, 1, T, d, None, None, None,
                                   dev[0], dev[1], dev[2], dev[3], dev[4], hq, dev[5], dev[6], n_T,
-                                  None, None, hn, vla.VLA_KERNEL_SEQ, 0, None, 0, None, None, ev[0], ev[1])
+                                  None, None, hn, vla.VLA_KERNEL_SEQ, 0, None, 0, None, None, ev[0], ev[1], None)
 
     assert call(ev=(None, f)) == vla.VLA_ERR_ARG
     assert call(ev=(f, None)) == vla.VLA_ERR_ARG

@@ -1,5 +1,6 @@
 """vla_forward_host: the same kernels as vla_forward on staged copies, so the
-results are bit-identical; its uploads run on a second stream."""
+results are bit-identical; its uploads run on a second stream, and o comes
+back on the compute or copy stream, or on a third one when given."""
 
 import pytest
 import torch
@@ -18,7 +19,8 @@ pytestmark = pytest.mark.gpu
     (vla.VLA_KERNEL_CHUNK_TC, 1, 5, 640, "bf16", False),   # 2 | 1 | 2
     (vla.VLA_KERNEL_SEQ, 1, 3, 77, "f32", False), (vla.VLA_KERNEL_CHUNK, 1, 3, 300, "bf16", False),
     (vla.VLA_KERNEL_AUTO, 1, 3, 3, "bf16", False)])
-def test_host_entry_matches_device_entry(kernel, B, H, T, dtype, init):
+@pytest.mark.parametrize("download", [False, True], ids=["two_streams", "download_stream"])
+def test_host_entry_matches_device_entry(kernel, B, H, T, dtype, init, download):
     x = make_inputs(B, H, T, 64, dtype, seed=61 + T, u_scale=0.5)
     q, k, v, u = to_device(x)
     S0 = A0 = n0 = None
@@ -45,7 +47,8 @@ def test_host_entry_matches_device_entry(kernel, B, H, T, dtype, init):
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
     stream, copy_stream = torch.cuda.current_stream(), torch.cuda.Stream()
     vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, dq, dk, dv, du, o, ho, S_T, A_T, n_T, hS, hA, hn,
-                         S0=S0, A0=A0, n0=n0, kernel=kernel, workspace=ws, stream=stream, copy_stream=copy_stream)
+                         S0=S0, A0=A0, n0=n0, kernel=kernel, workspace=ws, stream=stream, copy_stream=copy_stream,
+                         download_stream=torch.cuda.Stream() if download else None)
     stream.synchronize()
     assert torch.equal(ho, o_ref.cpu())
     assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
@@ -130,7 +133,8 @@ def test_host_entry_one_stream():
 
 
 @pytest.mark.parametrize("B,H,T", [(1, 2, 200), (2, 80, 130), (5, 64, 70)])
-def test_host_entry_d128_one_chunk_per_unit(B, H, T):
+@pytest.mark.parametrize("download", [False, True], ids=["two_streams", "download_stream"])
+def test_host_entry_d128_one_chunk_per_unit(B, H, T, download):
     """d = 128 with one chunk per unit: ranges of at most 152 units (one wave),
     u and k up first with each range's gates, then q and v with each range's
     state pass; bit-identical to vla_forward."""
@@ -154,7 +158,8 @@ def test_host_entry_d128_one_chunk_per_unit(B, H, T):
     ws = torch.empty(vla.vla_workspace_bytes(B, H, T, d, vla.VLA_BF16, kern, chunk), dtype=torch.uint8, device="cuda")
     stream, copy_stream = torch.cuda.current_stream(), torch.cuda.Stream()
     vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, dq, dk, dv, du, o, ho, S_T, A_T, n_T, hS, hA, hn, kernel=kern,
-                         chunk=chunk, workspace=ws, stream=stream, copy_stream=copy_stream)
+                         chunk=chunk, workspace=ws, stream=stream, copy_stream=copy_stream,
+                         download_stream=torch.cuda.Stream() if download else None)
     stream.synchronize()
     nr = min(4, (B * H + 151) // 152)
     assert vla.vla_last_launch_count() == 2 * nr
