@@ -54,18 +54,13 @@ TRAFFIC = {
     # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
     ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.211072e6 + 101.667328e6, "src_sha": "7e71eeed733c4469"},
     ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.463296e6 + 246.771456e6, "src_sha": "7e71eeed733c4469"},
-    # d = 128, one chunk per unit, batched workload: at B=8 (128 units, one wave), scaled x4 to B=32
-    ("chunk_tc", "batched", "gates_tc128_kernel"): {"bytes": 4 * (134.330624e6 + 37.467392e6),
-                                                    "src_sha": "7e71eeed733c4469"},
-    ("chunk_tc", "batched", "rows_tc128_kernel"): {"bytes": 4 * (268.697856e6 + 48.734464e6),
-                                                   "src_sha": "7e71eeed733c4469"},
 }
 
 
 def kernel_src_hash(kernel_name: str) -> str:
     fns = {"seq": ["vla_seq.cu", "vla_seq32.cu"], "chunk": ["vla_chunk.cu"],
            "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu", "vla_gates_tc.cu", "vla_gram_tc.cu", "vla_tc_common.cuh",
-                        "vla_gates_tc128.cu", "vla_rows_tc128.cu"],
+                        "vla_gates_tc128.cuh", "vla_rows_tc128.cuh", "vla_tc128.cu"],
            "decode": ["vla_decode.cu"]}[kernel_name]
     h = hashlib.sha256()
     for fn in fns:
@@ -108,8 +103,8 @@ def kernel_plan(kname, d, io_dtype="bf16", units=0):
     # chunk_tc at d = 128 with bf16 I/O and one chunk per unit (enough units): the
     # gates from A0, then the state pass on S itself, which writes o
     if kname == "chunk_tc" and io_dtype == "bf16" and d == 128 and units >= 128:
-        return [("gates_tc128_kernel", half, 2 * d * io, "tensor"),
-                ("rows_tc128_kernel", half, 3 * d * io, "tensor")]
+        # both passes of every unit in one persistent launch (a job queue)
+        return [("tc128_queue_kernel", full, 5 * d * io, "tensor")]
     if kname == "chunk_tc" and io_dtype == "bf16" and d == 64:
         return [("gram_tma_kernel", 0, 0, "tensor"), ("prefix_kernel", 0, 0, "alu"),
                 ("gates_tc_kernel", half, 2 * d * io, "tensor"), ("rows_tc_kernel", half, 2 * d * io, "tensor"),

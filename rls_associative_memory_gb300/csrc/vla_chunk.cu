@@ -1205,8 +1205,14 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     cudaError_t e;
     if constexpr (D == 128 && sizeof(IO) == 2) {
         if (a.p.rows_tc && a.L.NC == 1 && a.L.NCA == 1) {
-            // one chunk per unit: the gates from A0, then the state pass on S itself (writes o)
+            // one chunk per unit: the gates from A0, then the state pass on S itself
+            // (writes o); both in one queue launch unless q and v are still arriving
             mark_launch(a.p, 0, st);
+            if (!a.p.wait_qv) {
+                if ((e = launch_tc128_queue(a, st)) != cudaSuccess) return e;
+                mark_launch(a.p, 1, st);
+                return cudaSuccess;
+            }
             if ((e = launch_gates_tc128(a, st)) != cudaSuccess) return e;
             mark_launch(a.p, 1, st);
             if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
@@ -1404,6 +1410,7 @@ ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc_path) {
     L.off_yh = off;
     L.yh = tc ? 1 : 0;
     if (L.yh) off = align256(off + bh * nc * (size_t)(L.C / 64) * 16384);
+    L.off_q = off; off = align256(off + (bh + 1) * 4);
     L.total = off;
     return L;
 }

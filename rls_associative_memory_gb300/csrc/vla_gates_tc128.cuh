@@ -1,4 +1,4 @@
-// vla_gates_tc128.cu -- the unit gates of "Variational Linear Attention:
+// vla_gates_tc128.cuh -- the unit gates of "Variational Linear Attention:
 // Stable Associative Memory for Long-Context Transformers" (section 2.2's
 // inverse penalty A, kept by Sherman-Morrison, and section 2.3's gate
 // alpha_t = A_t k_hat_t / |A_t k_hat_t|) on the tensor cores for d = 128 with
@@ -30,10 +30,13 @@
 // AK and W in R2, Z in the downdate) are therefore split in three bf16 parts
 // (about 2^-24 relative, with U and K exact); E' and Z in R4's gate product
 // keep two.
+// The body of one CTA's work for one unit, included by vla_tc128.cu.
+#pragma once
+
 #include "vla_tc_common.cuh"
 
 namespace vla {
-namespace {
+namespace g128 {
 
 using namespace tc;
 
@@ -203,9 +206,10 @@ __device__ __forceinline__ void eliminate_rhs128(const float *gs, const float *w
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gates_tc128_kernel(ChunkArgs a) {
+// The gates of unit bh, by one CTA of kThreads threads with G2Layout::total +
+// 1024 bytes of dynamic shared memory at smem_raw.
+__device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, unsigned char *smem_raw) {
     using L = G2Layout;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
@@ -226,7 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1) gates_tc128_kernel(ChunkArgs a) {
     unsigned char *const ep[2] = {work + 4 * kTile, work + 6 * kTile};
 
     const int T = a.p.T;
-    const int bh = a.bh_lo + (int)blockIdx.x;
     const int nsb = (T + kSB - 1) / kSB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int qw = warp & 3, hw = warp >> 2;                // TMEM lane quarter, column half
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) gates_tc128_kernel(ChunkArgs a) {
         *abort_flag = 0;
         fence_mbarrier_init();
     }
-    if (warp == 0) tmem_alloc(tslot, 512);
+    if (warp == 0) tmem_alloc(tslot, 512, false);  // (one CTA per SM; a queue CTA allocates per job)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -495,17 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) gates_tc128_kernel(ChunkArgs a) {
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 512);
+    if (tid == 0) mbar_inval(bar);  // (a later job of this CTA may lay out its memory otherwise)
 }
 
-}  // namespace
-
-cudaError_t launch_gates_tc128(const ChunkArgs &a, cudaStream_t stream) {
-    constexpr size_t bytes = G2Layout::total + 1024;  // + alignment slack
-    cudaError_t e = cudaFuncSetAttribute(gates_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e != cudaSuccess) return e;
-    const int n = a.bh_n > 0 ? a.bh_n : a.p.BH;
-    gates_tc128_kernel<<<(unsigned)n, kThreads, bytes, stream>>>(a);
-    return cudaGetLastError();
-}
-
+}  // namespace g128
 }  // namespace vla

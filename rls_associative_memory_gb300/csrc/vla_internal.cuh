@@ -98,6 +98,7 @@ struct ChunkLayout {
                          // tiles) of every 64-token sub-block, written by the tensor-core
                          // state pass for the output pass
     int yh;              // 1 when the off_yh region is reserved
+    size_t off_q;        // [BH + 1] u32: the job queue of the d = 128 single-chunk launch
     size_t total;
 };
 
@@ -150,6 +151,9 @@ cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream);
 // that runs S itself and writes o (vla_rows_tc128.cu), one CTA per unit each.
 cudaError_t launch_gates_tc128(const ChunkArgs &a, cudaStream_t stream);
 cudaError_t launch_rows_tc128(const ChunkArgs &a, cudaStream_t stream);
+// Both in one persistent launch over all units, a CTA per SM taking the units'
+// passes from a queue in the workspace (vla_tc128.cu).
+cudaError_t launch_tc128_queue(const ChunkArgs &a, cudaStream_t stream);
 // The same for a range of units [bh_lo, bh_lo + bh_n): part 0 the gates (reads u
 // and k), part 1 the state pass (reads q, k, v and the gates; writes o, S_T,
 // n_T).  Launch boundaries are numbered on from *p.launches.
@@ -186,6 +190,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
         "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
         "r"(bytes)
         : "memory");
+}
+
+// Ends an mbarrier's life, so that its bytes may serve another purpose.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // One arrival (release semantics at CTA scope: this thread's earlier writes are
@@ -261,11 +270,14 @@ __host__ __device__ __forceinline__ uint32_t kmajor_off_bf16(int r, int k, int K
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {  // whole warp
+// (relinquish: the CTA gives up its permit to allocate again, which lets other
+// CTAs on the SM allocate sooner; a CTA that allocates once per job of a
+// persistent loop keeps it)
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols, bool relinquish = true) {  // whole warp
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
                  "r"(ncols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (relinquish) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // whole warp
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");

@@ -1,4 +1,4 @@
-// vla_rows_tc128.cu -- the state write and ELU+1 readout of "Variational
+// vla_rows_tc128.cuh -- the state write and ELU+1 readout of "Variational
 // Linear Attention: Stable Associative Memory for Long-Context Transformers"
 // (section 2.3, step 3 and the readout) on the tensor cores for d = 128 with
 // bf16 I/O, when every (b, h) unit is one chunk: one CTA runs a unit's state
@@ -22,10 +22,13 @@
 // operands are bf16 hi/lo pairs (hi*hi + hi*lo + lo*hi); k, v, q are exact
 // bf16.  TMEM 320 columns (512 allocated), ~212 KB of shared memory: one CTA
 // per SM.
+// The body of one CTA's work for one unit, included by vla_tc128.cu.
+#pragma once
+
 #include "vla_tc_common.cuh"
 
 namespace vla {
-namespace {
+namespace r128 {
 
 using namespace tc;
 
@@ -67,9 +70,10 @@ __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t by
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
+// The state pass of unit bh, by one CTA of kThreads threads with
+// R2Layout::total + 1024 bytes of dynamic shared memory at smem_raw.
+__device__ __forceinline__ void rows_tc128_body(const ChunkArgs &a, int bh, unsigned char *smem_raw) {
     using L = R2Layout;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
@@ -87,7 +91,6 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
     unsigned char *qm_hi = alq + 4 * kTile, *qm_lo = alq + 5 * kTile;
 
     const int T = a.p.T;
-    const int bh = a.bh_lo + (int)blockIdx.x;
     const int nsb = (T + kSB - 1) / kSB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int qw = warp & 3, hw = warp >> 2;                // TMEM lane quarter, column half
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
         fence_mbarrier_init();
     }
     if (tid < kD2) s_nrun[tid] = a.p.n0 ? a.p.n0[(size_t)bh * kD2 + tid] : 0.f;
-    if (warp == 0) tmem_alloc(tslot, 512);
+    if (warp == 0) tmem_alloc(tslot, 512, false);  // (one CTA per SM; a queue CTA allocates per job)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -423,17 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1) rows_tc128_kernel(ChunkArgs a) {
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 512);
+    if (tid == 0) {  // (a later job of this CTA may lay out its memory otherwise)
+        mbar_inval(bar);
+        mbar_inval(bar_n);
+    }
 }
 
-}  // namespace
-
-cudaError_t launch_rows_tc128(const ChunkArgs &a, cudaStream_t stream) {
-    constexpr size_t bytes = R2Layout::total + 1024;  // + alignment slack
-    cudaError_t e = cudaFuncSetAttribute(rows_tc128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e != cudaSuccess) return e;
-    const int n = a.bh_n > 0 ? a.bh_n : a.p.BH;
-    rows_tc128_kernel<<<(unsigned)n, kThreads, bytes, stream>>>(a);
-    return cudaGetLastError();
-}
-
+}  // namespace r128
 }  // namespace vla

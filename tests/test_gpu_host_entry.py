@@ -144,7 +144,7 @@ def test_host_entry_d128_one_chunk_per_unit(B, H, T, download):
     kern = vla.VLA_KERNEL_CHUNK_TC
     o_ref, S_ref, A_ref, n_ref = vla.vla_forward(q, k, v, u, x.lambda0, kernel=kern, chunk=chunk)
     torch.cuda.synchronize()
-    assert vla.vla_last_launch_count() == 2
+    assert vla.vla_last_launch_count() == 1  # the queue kernel; the ranges below run the two passes apart
     hq, hk, hv, hu = (t.cpu().pin_memory() for t in (q, k, v, u))
     dq, dk, dv, du = (torch.empty_like(t) for t in (q, k, v, u))
     o = torch.empty_like(q)
