@@ -111,7 +111,10 @@ int vla_forward(const void *q, const void *k, const void *v, const void *u, int 
  * d_h = 128 with one chunk per unit the ranges are waves of at most 152 units
  * (up to four): u and k range by range, each followed by its gates; then q
  * and v range by range, each followed by its state pass and, on `stream`,
- * the download of its o.  With a download_stream, on both staged paths every
+ * the download of its o.  The sequential kernel (two or more units, T > 0) is
+ * staged the same way: q, k, v, u of at most four ranges of units in turn, each
+ * followed by the kernel over the range and, on `stream`, its o.  With a
+ * download_stream, on every staged path every
  * range's o comes back on it as soon as the range's passes are done, beside
  * the later uploads and passes (the link carries both directions at once),
  * and `stream` finally waits for it.  On the other paths u and k go first, the kernels wait for them before the

@@ -326,8 +326,54 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
     if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return fail(e);
     const bool staged = n_io > 0 && BH >= 2 && kk == VLA_KERNEL_CHUNK_TC && vla::chunk_tc_parts_supported(p, L);
     const bool staged128 = n_io > 0 && BH >= 2 && kk == VLA_KERNEL_CHUNK_TC && vla::chunk_tc128_parts_supported(p, L);
+    const bool staged_seq = n_io > 0 && BH >= 2 && p.T > 0 && kk == VLA_KERNEL_SEQ;
     long long o_lo = 0;  // o from this unit on comes back on `stream`
-    if (staged128) {
+    if (staged_seq) {
+        // the sequential kernel reads every input of a unit in one pass and works
+        // per unit, so it runs in ranges of units (at most four) as their inputs land:
+        // q, k, v, u of a range on copy_stream, then its launch on `stream` over
+        // the range's slices of every tensor; its o comes back on download_stream
+        // when one is given, else on `stream` after the range's pass
+        long long nr = BH < 4 ? BH : 4;
+        long long r[5];
+        for (long long i = 0; i <= nr; ++i) r[i] = BH * i / nr;
+        const size_t dd = (size_t)d_h * d_h;
+        for (long long j = 0; j < nr; ++j) {
+            const long long lo = r[j], n = r[j + 1] - r[j];
+            if ((e = up(q, hq, lo, n)) != cudaSuccess) return fail(e);
+            if ((e = up(k, hk, lo, n)) != cudaSuccess) return fail(e);
+            if ((e = up(v, hv, lo, n)) != cudaSuccess) return fail(e);
+            if ((e = up(u, hu, lo, n)) != cudaSuccess) return fail(e);
+            if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
+            if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
+            vla::FwdParams pr = p;
+            const size_t ub = unit * (size_t)lo, sb = dd * (size_t)lo, nb = (size_t)d_h * (size_t)lo;
+            pr.q = static_cast<const unsigned char *>(p.q) + ub;
+            pr.k = static_cast<const unsigned char *>(p.k) + ub;
+            pr.v = static_cast<const unsigned char *>(p.v) + ub;
+            pr.u = static_cast<const unsigned char *>(p.u) + ub;
+            pr.o = static_cast<unsigned char *>(p.o) + ub;
+            if (p.S0) pr.S0 = p.S0 + sb;
+            if (p.A0) pr.A0 = p.A0 + sb;
+            if (p.n0) pr.n0 = p.n0 + nb;
+            pr.S_T = p.S_T + sb;
+            pr.A_T = p.A_T + sb;
+            if (p.n_T) pr.n_T = p.n_T + nb;
+            pr.BH = (int)n;
+            int lc = 0;
+            pr.launches = &lc;
+            if ((e = vla::launch_seq(pr, st)) != cudaSuccess) return fail(e);
+            launches += lc;
+            if (ds) {
+                if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
+                if ((e = cudaStreamWaitEvent(ds, e_qv, 0)) != cudaSuccess) return fail(e);
+                if ((e = down_o(lo, n, ds)) != cudaSuccess) return fail(e);
+            } else if (j + 1 < nr && (e = down_o(lo, n, st)) != cudaSuccess) {
+                return fail(e);
+            }
+        }
+        o_lo = ds ? BH : r[nr - 1];
+    } else if (staged128) {
         // d = 128, one chunk per unit: both passes are per unit, one CTA per unit at
         // one CTA per SM, so the ranges are waves of 152 units (at most four
         // ranges). u and k go up range by range, each followed by its gates; then
@@ -444,7 +490,7 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
     if (hn_T && n_d && (e = cudaMemcpyAsync(hn_T, n_T, n_d, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
         return fail(e);
     if (staged && !ds && (e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
-    if (ds && (staged || staged128)) {  // download_stream's copies done before `stream` is
+    if (ds && (staged || staged128 || staged_seq)) {  // download_stream's copies done before `stream` is
         if ((e = cudaEventRecord(e_qv, ds)) != cudaSuccess) return fail(e);
         if ((e = cudaStreamWaitEvent(st, e_qv, 0)) != cudaSuccess) return fail(e);
     }

@@ -165,3 +165,35 @@ def test_host_entry_d128_one_chunk_per_unit(B, H, T, download):
     assert vla.vla_last_launch_count() == 2 * nr
     assert torch.equal(ho, o_ref.cpu())
     assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
+
+
+@pytest.mark.parametrize("download", [False, True], ids=["two_streams", "download_stream"])
+@pytest.mark.parametrize("B,H,T", [(8, 4, 130), (1, 2, 40)])
+def test_host_entry_sequential_ranges(B, H, T, download):
+    """The sequential kernel (d = 32 here) staged in ranges of units: each
+    range's inputs up, its launch over the range's slices, its o back;
+    bit-identical to vla_forward."""
+    x = make_inputs(B, H, T, 32, "f32", seed=95 + T, lambda0=0.8)
+    q, k, v, u = to_device(x)
+    kern = vla.VLA_KERNEL_SEQ
+    o_ref, S_ref, A_ref, n_ref = vla.vla_forward(q, k, v, u, x.lambda0, kernel=kern)
+    torch.cuda.synchronize()
+    hq, hk, hv, hu = (t.cpu().pin_memory() for t in (q, k, v, u))
+    dq, dk, dv, du = (torch.empty_like(t) for t in (q, k, v, u))
+    o = torch.empty_like(q)
+    ho = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    d = 32
+    S_T = torch.empty((B, H, d, d), device="cuda")
+    A_T = torch.empty_like(S_T)
+    n_T = torch.empty((B, H, d), device="cuda")
+    hS, hA = torch.empty(S_T.shape).pin_memory(), torch.empty(A_T.shape).pin_memory()
+    hn = torch.empty(n_T.shape).pin_memory()
+    stream, copy_stream = torch.cuda.current_stream(), torch.cuda.Stream()
+    vla.vla_forward_host(hq, hk, hv, hu, x.lambda0, dq, dk, dv, du, o, ho, S_T, A_T, n_T, hS, hA, hn, kernel=kern,
+                         stream=stream, copy_stream=copy_stream,
+                         download_stream=torch.cuda.Stream() if download else None)
+    stream.synchronize()
+    assert vla.vla_last_launch_count() == min(4, B * H)
+    assert torch.equal(ho, o_ref.cpu())
+    assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
+    compare({"o": ho.numpy(), "S_T": hS.numpy(), "A_T": hA.numpy(), "n_T": hn.numpy()}, oracle_ref(x), "f32")
