@@ -47,13 +47,17 @@ FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
 # workload).  Reported only while the kernel source still hashes to the value
 # it was captured from; otherwise null.
 TRAFFIC = {
-    # sequential kernel, long stream: 134.4 + 18.9 MB at T=16384, scaled x4 to T=65536
-    ("seq", "long", "seq_kernel"): {"bytes": 4 * (134.394112e6 + 18.881792e6), "src_sha": "60489ee668b38996"},
+    # sequential kernel, long stream: 135.3 + 18.9 MB at T=16384, scaled x4 to T=65536
+    ("seq", "long", "seq_kernel"): {"bytes": 4 * (135.331840e6 + 18.873600e6), "src_sha": "e3b0113e3167d722"},
     # sequential kernel at d = 32, recall8 workload: one full-size launch (one ncu pass)
-    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.476160e6 + 51.005184e6, "src_sha": "60489ee668b38996"},
+    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.589312e6 + 50.995200e6, "src_sha": "e3b0113e3167d722"},
     # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.211072e6 + 101.667328e6, "src_sha": "7e71eeed733c4469"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.463296e6 + 246.771456e6, "src_sha": "7e71eeed733c4469"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.248960e6 + 101.725184e6, "src_sha": "4b06033623916710"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.119488e6 + 246.631936e6, "src_sha": "4b06033623916710"},
+    # d = 128 queue launch, batched workload: at B=8 (128 units), scaled x4 to B=32 (the bytes
+    # of a unit's two passes do not depend on how many units a launch holds)
+    ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.733312e6 + 126.918144e6),
+                                                    "src_sha": "4b06033623916710"},
 }
 
 

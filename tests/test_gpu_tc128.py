@@ -96,3 +96,25 @@ def test_auto_takes_the_tensor_core_path_for_many_units():
     got = {"o": o.float().cpu().numpy(), "S_T": S_T.cpu().numpy(), "A_T": A_T.cpu().numpy(),
            "n_T": n_T.cpu().numpy()}
     compare(got, oracle_ref(x), "bf16")
+
+
+@pytest.mark.parametrize("T,init", [(1, False), (70, False), (130, True)])
+def test_queue_launch_many_units(T, init):
+    """300 units: more jobs than the 152 queue CTAs, so most CTAs run several
+    units' passes one after another (gates first, then state passes that wait
+    on their unit's flag).  Sampled units against the oracle."""
+    B, H = 75, 4
+    x = make_inputs(B, H, T, 128, "bf16", seed=77 + T, lambda0=0.6)
+    S0 = A0 = n0 = None
+    if init:  # a state from a short earlier stream (the oracle's, for every unit)
+        full = oracle_ref(make_inputs(B, H, 40, 128, "bf16", seed=78, lambda0=0.6))
+        S0, A0, n0 = full["S_T"], full["A_T"], full["n_T"]
+    got = _run(x, S0=S0, A0=A0, n0=n0)
+    for i in np.linspace(0, B * H - 1, 12).round().astype(int):
+        b, h = divmod(int(i), H)
+        sub = x.slice_heads(slice(b, b + 1), slice(h, h + 1))
+        kw = {}
+        if init:
+            kw = dict(S0=S0[b:b + 1, h:h + 1], A0=A0[b:b + 1, h:h + 1], n0=n0[b:b + 1, h:h + 1])
+        ref = oracle_ref(sub, **kw)
+        compare({k: v[b:b + 1, h:h + 1] for k, v in got.items()}, ref, "bf16")
