@@ -489,13 +489,20 @@ __global__ void __launch_bounds__(kOutThreads) out_tc_kernel(ChunkArgs a) {
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 28);
     unsigned char *st = smem + L::stage, *sc_hi = smem + L::sc_hi, *sc_lo = smem + L::sc_lo, *eye = smem + L::eye;
 
+    // two CTAs a chunk, each over half of its sub-blocks (the output pass has no
+    // recurrence left in it; more, shorter CTAs fill the waves better)
     const int NC = a.L.NC, C = a.L.C, T = a.p.T;
-    const int c = (int)(blockIdx.x % (unsigned)NC), bh = a.bh_lo + (int)(blockIdx.x / (unsigned)NC);
-    const int t0 = c * C, ntok = min(C, T - t0), nsb = (ntok + kSB - 1) / kSB;
+    const unsigned blk = blockIdx.x >> 1;
+    const int c = (int)(blk % (unsigned)NC), bh = a.bh_lo + (int)(blk / (unsigned)NC);
+    const int t0 = c * C, ntok = min(C, T - t0), nsb_chunk = (ntok + kSB - 1) / kSB;
+    const int half = (nsb_chunk + 1) / 2, sb0 = (int)(blockIdx.x & 1u) * half;
+    const int nsb = min(nsb_chunk, sb0 + half) - sb0;  // this CTA's sub-blocks sb0 .. sb0 + nsb - 1
+    if (nsb <= 0) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned char *gyh = static_cast<const unsigned char *>(a.p.ws) + a.L.off_yh +
-                               (size_t)(bh * NC + c) * (C / kSB) * (2 * kTile);
-    __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.p.o) + ((size_t)bh * T + t0) * kD;
+                               ((size_t)(bh * NC + c) * (C / kSB) + (size_t)sb0) * (2 * kTile);
+    __nv_bfloat16 *gout = static_cast<__nv_bfloat16 *>(a.p.o) + ((size_t)bh * T + t0 + (size_t)sb0 * kSB) * kD;
+    const int ntok_cta = ntok - sb0 * kSB;  // tokens from this CTA's first sub-block on
 
     if (tid == 0) {
         mbar_init(&full[0], 1);
@@ -570,7 +577,7 @@ __global__ void __launch_bounds__(kOutThreads) out_tc_kernel(ChunkArgs a) {
         if (*abort_flag) break;
         // o rows: token t = 16 warp + lane (lanes 0..15 hold the M = 64 rows)
         const int t = 16 * warp + lane;
-        const bool act = lane < 16 && sb * kSB + t < ntok;
+        const bool act = lane < 16 && sb * kSB + t < ntok_cta;
         uint4 *dst = reinterpret_cast<uint4 *>(gout + (size_t)(sb * kSB + (t & 63)) * kD);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -621,7 +628,8 @@ cudaError_t launch_rows_tc(const ChunkArgs &a, int mode, cudaStream_t stream) {
         if ((e = cudaFuncSetAttribute(out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes)) !=
             cudaSuccess)
             return e;
-        out_tc_kernel<<<(unsigned)grid, kOutThreads, bytes, stream>>>(a);
+        if (2 * grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        out_tc_kernel<<<(unsigned)(2 * grid), kOutThreads, bytes, stream>>>(a);  // two CTAs a chunk
     }
     return cudaGetLastError();
 }

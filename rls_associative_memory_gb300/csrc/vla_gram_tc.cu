@@ -6,7 +6,7 @@
 // Transformers"), and of the readout's n_t (section 2.3).
 //
 // Tiles of 64 tokens of u and k arrive by TMA tensor copies
-// (cp.async.bulk.tensor) in the 128-byte swizzle, four stages deep (a stage
+// (cp.async.bulk.tensor) in the 128-byte swizzle, three stages deep (a stage
 // is refilled one iteration after its product was issued).  The
 // token-major u tile is both operands of the product, read MN-major (tile
 // rows = K = tokens), so no transposition is needed; bf16 x bf16 products
@@ -23,7 +23,7 @@ namespace {
 using namespace tc;
 
 constexpr int kGThreads = 128;
-constexpr int kStages = 4;
+constexpr int kStages = 3;  // 50 KB a CTA: four CTAs per SM (608 Grams of the long stream in one wave)
 
 struct GrLayout {
     static constexpr size_t ctrl = 0;                     // full[4], done[4] mbarriers, TMEM slot, abort flag
