@@ -48,24 +48,33 @@ FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
 # it was captured from; otherwise null.
 TRAFFIC = {
     # sequential kernel, long stream: 135.3 + 18.9 MB at T=16384, scaled x4 to T=65536
-    ("seq", "long", "seq_kernel"): {"bytes": 4 * (135.331840e6 + 18.873600e6), "src_sha": "e3b0113e3167d722"},
+    ("seq", "long", "seq_kernel"): {"bytes": 4 * (135.331840e6 + 18.873600e6), "src_sha": "3e83f00723bacc5a"},
     # sequential kernel at d = 32, recall8 workload: one full-size launch (one ncu pass)
-    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.589312e6 + 50.995200e6, "src_sha": "e3b0113e3167d722"},
+    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.589312e6 + 50.995200e6, "src_sha": "cf4c667cff68449b"},
     # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.214144e6 + 98.598144e6, "src_sha": "f84e7406bd48151c"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.107456e6 + 246.773504e6, "src_sha": "f84e7406bd48151c"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.214144e6 + 98.598144e6, "src_sha": "b286e1a97adfb166"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.107456e6 + 246.773504e6, "src_sha": "6bc72c4621acfc2f"},
     # d = 128 queue launch, batched workload: at B=8 (128 units), scaled x4 to B=32 (the bytes
     # of a unit's two passes do not depend on how many units a launch holds)
     ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.733312e6 + 126.918144e6),
-                                                    "src_sha": "d874b62b8fa949e6"},
+                                                    "src_sha": "69029427c86670d5"},
+}
+
+
+# The sources of each kernel a traffic record is kept for (with the headers
+# every kernel includes): a capture stays valid while they are unchanged.
+KERNEL_SOURCES = {
+    "seq_kernel": ["vla_seq.cu"],
+    "seq32_kernel": ["vla_seq32.cu"],
+    "gates_tc_kernel": ["vla_gates_tc.cu", "vla_tc_common.cuh"],
+    "rows_tc_kernel": ["vla_chunk_tc.cu", "vla_tc_common.cuh"],
+    "tc128_queue_kernel": ["vla_gates_tc128.cuh", "vla_rows_tc128.cuh", "vla_tc128.cu", "vla_tc_common.cuh"],
 }
 
 
 def kernel_src_hash(kernel_name: str) -> str:
-    fns = {"seq": ["vla_seq.cu", "vla_seq32.cu"], "chunk": ["vla_chunk.cu"],
-           "chunk_tc": ["vla_chunk.cu", "vla_chunk_tc.cu", "vla_gates_tc.cu", "vla_gram_tc.cu", "vla_tc_common.cuh"],
-           "chunk_tc128": ["vla_gates_tc128.cuh", "vla_rows_tc128.cuh", "vla_tc128.cu", "vla_tc_common.cuh"],
-           "decode": ["vla_decode.cu"]}[kernel_name]
+    """Hash of a kernel's sources, code only (comments and blank space stripped)."""
+    fns = KERNEL_SOURCES[kernel_name] + ["vla_internal.cuh"]
     h = hashlib.sha256()
     for fn in fns:
         path = os.path.join(ROOT, "rls_associative_memory_gb300", "csrc", fn)
@@ -525,9 +534,7 @@ def main():
     kernel_ms = per_kernel_ms[dom]
     k_name, k_fpt, k_bpt, k_eng = plan[dom]
     tr = TRAFFIC.get((kname, args.config, k_name))
-    # the d = 128 tensor-core kernels have sources of their own
-    fam = "chunk_tc128" if kname == "chunk_tc" and "tc128" in k_name else kname
-    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash(fam) else None
+    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_hash(k_name) else None
     k_flops = units * k_fpt
     k_bytes = byts if len(plan) == 1 else units * k_bpt  # a one-kernel path owns all bytes (state included)
     hbm = measured_hbm_gbs()
