@@ -54,6 +54,26 @@ __device__ __forceinline__ void kahan_add(float &sum, float &comp, float x) {
     sum = t;
 }
 
+// The exclusive Kahan prefix of x[c * stride], c < n, in place, starting from
+// run; returns the total.  The loads go eight chunks at a time, ahead of the
+// stores, so that a thread waits on one latency per eight chunks.
+__device__ __forceinline__ float kahan_prefix_inplace(float *x, size_t stride, int n, float run) {
+    float comp = 0.f;
+    for (int c0 = 0; c0 < n; c0 += 8) {
+        float g[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = (c0 + j < n) ? x[(size_t)(c0 + j) * stride] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (c0 + j < n) {
+                x[(size_t)(c0 + j) * stride] = run;
+                kahan_add(run, comp, g[j]);
+            }
+        }
+    }
+    return run;
+}
+
 // ---------------------------------------------------------------------------
 // gram: chunk Gram matrices of u and chunk sums of phi(k_hat)
 // ---------------------------------------------------------------------------
@@ -324,24 +344,12 @@ __global__ void __launch_bounds__(256) prefix_kernel(ChunkArgs a) {
     const int NC = a.L.NCA;  // A-chunks
     if (e < D * D) {
         const int i = e / D, j = e % D;
-        float run = a.p.A0 ? ws_f(a, a.L.off_M0)[(size_t)bh * D * D + e] : (i == j ? a.p.lambda0 : 0.f);
-        float comp = 0.f;
-        float *M = ws_f(a, a.L.off_M) + (size_t)bh * NC * D * D + e;
-        for (int c = 0; c < NC; ++c) {
-            const float g = M[(size_t)c * D * D];
-            M[(size_t)c * D * D] = run;
-            kahan_add(run, comp, g);
-        }
+        const float run = a.p.A0 ? ws_f(a, a.L.off_M0)[(size_t)bh * D * D + e] : (i == j ? a.p.lambda0 : 0.f);
+        (void)kahan_prefix_inplace(ws_f(a, a.L.off_M) + (size_t)bh * NC * D * D + e, (size_t)D * D, NC, run);
     } else if (e < D * D + D) {
         const int j = e - D * D;
-        float run = a.p.n0 ? a.p.n0[(size_t)bh * D + j] : 0.f;
-        float comp = 0.f;
         float *n = ws_f(a, a.L.off_n) + (size_t)bh * (NC + 1) * D + j;
-        for (int c = 0; c < NC; ++c) {
-            const float g = n[(size_t)c * D];
-            n[(size_t)c * D] = run;
-            kahan_add(run, comp, g);
-        }
+        const float run = kahan_prefix_inplace(n, D, NC, a.p.n0 ? a.p.n0[(size_t)bh * D + j] : 0.f);
         n[(size_t)NC * D] = run;
         if (a.p.n_T) a.p.n_T[(size_t)bh * D + j] = run;
     }
