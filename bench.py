@@ -359,7 +359,8 @@ def run_backward(args):
             "roofline": {"bound": "alu", "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                          "frac": tf / FP32_PEAK_TFLOPS, "traffic": None,
                          "kernel": ("chunked backward (%d launches)" % launches if launches > 1
-                                    else "backward_kernel<%d,%s>" % (d, x.dtype)),
+                                    else ("backward128_kernel<%s>" % x.dtype if d == 128
+                                          else "backward_kernel<%d,%s>" % (d, x.dtype))),
                          "algorithmic_flops": flops},
             "gpu_launches": args.steps * launches}
     print(json.dumps(line), flush=True)

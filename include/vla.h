@@ -208,9 +208,9 @@ int vla_last_launch_count(void);
  * dS0, dA0, dn0   gradients of the initial state ([B,H,d,d], [B,H,d,d],
  *                 [B,H,d] fp32), written when non-NULL.  dA0 is the full,
  *                 unsymmetrised adjoint of A_0.
- * d_h             32 or 64 (VLA_ERR_UNSUPPORTED_DIM otherwise).
+ * d_h             32, 64 or 128 (VLA_ERR_UNSUPPORTED_DIM otherwise).
  * workspace       at least vla_backward_workspace_bytes(B, H, T, d_h) bytes.
- * When the stream spans two or more chunks of the chunked forward
+ * At d_h = 32 and 64, when the stream spans two or more chunks of the chunked forward
  * (vla_forward's default chunk length), the call runs that forward for the
  * chunk-start states and then works on all chunks in parallel: over a chunk
  * the adjoint of S is an affine map with one d x d product (the chunk's
@@ -218,7 +218,9 @@ int vla_last_launch_count(void);
  * only part that feeds back) a two-sided one, and the adjoint of n a sum, so
  * short chains along the chunks give every chunk its end adjoints.  Shorter
  * streams run one CTA per (b, h), which reruns the forward (records and a
- * state checkpoint every 64 tokens) and sweeps the tokens in reverse.
+ * state checkpoint every 64 tokens) and sweeps the tokens in reverse.  At
+ * d_h = 128 every stream takes that sequential form, with S and its adjoint
+ * in shared memory (A and its adjoint in registers).
  * Asynchronous on stream; returns VLA_OK or a VLA_ERR_* code.
  */
 int vla_backward(const void *q, const void *k, const void *v, const void *u, const void *dO,

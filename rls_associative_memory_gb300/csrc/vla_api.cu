@@ -124,7 +124,6 @@ size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kerne
 
 size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h) {
     if (check_common(VLA_F32, 1.f, B, H, T, d_h, VLA_KERNEL_AUTO) != VLA_OK) return 0;
-    if (d_h != 32 && d_h != 64) return 0;
     const size_t seq = vla::backward_workspace_floats(B * H, T, d_h) * sizeof(float);
     const size_t chunked = vla::backward_chunk_bytes(B * H, T, d_h);
     return seq > chunked ? seq : chunked;
@@ -136,7 +135,6 @@ int vla_backward(const void *q, const void *k, const void *v, const void *u, con
                  float *du, float *dS0, float *dA0, float *dn0, void *workspace, size_t ws_bytes, void *stream) {
     int rc = check_common(io_dtype, lambda0, B, H, T, d_h, VLA_KERNEL_AUTO);
     if (rc != VLA_OK) return rc;
-    if (d_h != 32 && d_h != 64) return VLA_ERR_UNSUPPORTED_DIM;
     const long long BH = (long long)B * H;
     if (BH > 0 && T > 0 && (!q || !k || !v || !u || !dO)) return VLA_ERR_ARG;
     const void *ptrs[] = {q, k, v, u, dO, S0, A0, n0, dS_T, dA_T, dn_T, dq, dk, dv, du, dS0, dA0, dn0, workspace};

@@ -26,13 +26,14 @@
 //   key      dk = (dk_hat - k_hat (k_hat . dk_hat)) / |k|
 // Rows of S, A, dS, dA live in registers of row-owner threads; the
 // transposed products S^T x, dS'^T r and dA'^T z are column sums through
-// shared memory.  d in {32, 64} (four d x d register states).
+// shared memory.  d in {32, 64} (four d x d register states; d = 128 has a
+// kernel of its own, vla_backward128.cu).
 #include "vla_internal.cuh"
 
 namespace vla {
 namespace {
 
-constexpr int kCk = 64;  // tokens between state checkpoints
+constexpr int kCk = kBwdCk;  // tokens between state checkpoints
 
 template <int D>
 struct BwdCfg {
@@ -425,6 +426,7 @@ cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream) {
     const cudaError_t ec = launch_backward_chunk(p, stream, &chunked);
     if (ec != cudaSuccess || chunked) return ec;
     if (p.launches) *p.launches = 1;
+    if (p.d == 128) return launch_backward128(p, stream);
     if (p.io_bf16) {
         switch (p.d) {
             case 32: return launch_backward_t<32, __nv_bfloat16>(p, stream);

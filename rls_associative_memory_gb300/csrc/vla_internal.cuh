@@ -68,6 +68,12 @@ struct BwdParams {
     int *launches;                                   // out (optional): kernels launched
 };
 size_t backward_workspace_floats(int BH, int T, int d);
+// Tokens between the state checkpoints of the sequential backward (its
+// workspace holds, per (b, h), T records of 4 d + 4 floats, then one (S, A,
+// n) checkpoint of 2 d^2 + d floats per kBwdCk tokens).
+constexpr int kBwdCk = 64;
+// The sequential backward at d = 128 (vla_backward128.cu): S and dS in shared memory.
+cudaError_t launch_backward128(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_backward(const BwdParams &p, cudaStream_t stream);
 // The backward in parallel over the chunked forward's S-chunks (vla_backward_chunk.cu):
 // its workspace bytes (the larger of the bf16 and fp32 layouts; 0 when fewer

@@ -154,11 +154,15 @@ def test_backward_argument_checks():
     args = lambda **kw: [kw.get(n, f) for n in ("q", "k", "v", "u", "dO")] + [  # noqa: E731
         kw.get("io", vla.VLA_BF16), 1.0, 1, 2, 16, kw.get("d", 64)] + [None] * 6 + [f] * 7 + [
         kw.get("ws", None), kw.get("wsb", 0), None]
-    assert L.vla_backward(*args(d=128)) == vla.VLA_ERR_UNSUPPORTED_DIM
+    assert L.vla_backward(*args(d=96)) == vla.VLA_ERR_UNSUPPORTED_DIM
     assert L.vla_backward(*args()) == vla.VLA_ERR_WORKSPACE
+    assert L.vla_backward(*args(d=128)) == vla.VLA_ERR_WORKSPACE
     assert L.vla_backward(*args(dO=None)) == vla.VLA_ERR_ARG
     assert L.vla_backward(*args(k=f + 4)) == vla.VLA_ERR_ALIGN
-    assert vla.vla_backward_workspace_bytes(1, 2, 16, 128) == 0
+    assert vla.vla_backward_workspace_bytes(1, 2, 16, 96) == 0
+    # d = 128: always the sequential form (records and one checkpoint per 64 tokens)
+    assert vla.vla_backward_workspace_bytes(1, 2, 16, 128) == 2 * (16 * 516 + 1 * (2 * 128 * 128 + 128)) * 4
+    assert vla.vla_backward_workspace_bytes(2, 3, 200, 128) == 6 * (200 * 516 + 4 * (2 * 128 * 128 + 128)) * 4
     assert vla.vla_backward_workspace_bytes(1, 2, 16, 64) == 2 * (16 * 260 + 1 * (2 * 64 * 64 + 64)) * 4
     # streams of two or more forward chunks: the chunk-parallel backward carves the chunked
     # forward's workspace, its o, the per-token records and dg / dk_hat parts, and the maps

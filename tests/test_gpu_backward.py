@@ -48,7 +48,7 @@ def _dO_exact(dO, dtype):
     return t.double().numpy()
 
 
-@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("T", [1, 17, 100, 200])
 def test_backward_small(d, dtype, T):
@@ -61,7 +61,7 @@ def test_backward_small(d, dtype, T):
     assert all(e <= GTOL for e in errs.values()), errs
 
 
-@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("d", [32, 64, 128])
 def test_backward_with_state_and_state_gradients(d):
     pre = make_inputs(1, 2, 30, d, "f32", seed=510, lambda0=1.3)
     import oracle
@@ -89,3 +89,38 @@ def test_backward_long_stream_sampled_heads():
         errs = {key: rel_fro(got[key][b, h], ref[key]) for key in KEYS}
         print("\nbackward 4x8x4096 unit (%d,%d) %s" % (b, h, {k_: "%.2e" % e for k_, e in errs.items()}))
         assert all(e <= GTOL for e in errs.values()), errs
+
+
+def test_backward_d128_many_units_sampled():
+    """d = 128 (the sequential form with S and dS in shared memory): 2 x 4 x 300
+    bf16 streams (300 tokens cross four checkpoints and end mid-interval); the
+    oracle checks two of the eight units."""
+    x = make_inputs(2, 4, 300, 128, "bf16", seed=530, lambda0=0.7)
+    dO = _dO_exact(_rand(x.q.shape, 531, 1), "bf16")
+    got = _run(x, dO)
+    for (b, h) in ((0, 1), (1, 3)):
+        ref = ob.backward(x.as_f64("q")[b, h], x.as_f64("k")[b, h], x.as_f64("v")[b, h], x.as_f64("u")[b, h],
+                          x.lambda0, dO[b, h])
+        errs = {key: rel_fro(got[key][b, h], ref[key]) for key in KEYS}
+        print("\nbackward d=128 2x4x300 unit (%d,%d) %s" % (b, h, {k_: "%.2e" % e for k_, e in errs.items()}))
+        assert all(e <= GTOL for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("case", ["zero_keys", "u0", "u10", "lambda0_small"])
+def test_backward_d128_edge_inputs(case):
+    """The method's special cases at d = 128: keys at and below the norm guard,
+    no penalty updates (u = 0: A stays lambda0^-1 I), strong penalty
+    directions, and a small lambda0."""
+    kw = {"u0": dict(u_scale=0.0), "u10": dict(u_scale=10.0)}.get(case, {})
+    lam = 0.05 if case == "lambda0_small" else 1.0
+    x = make_inputs(1, 2, 90, 128, "f32", seed=540, lambda0=lam, **kw)
+    if case == "zero_keys":
+        for t in (0, 5, 64, 89):
+            x.k[:, :, t, :] = 0.0
+        x.k[:, :, 30, :] *= 1e-8
+    dO = _rand(x.q.shape, 541, 1)
+    got = _run(x, dO)
+    ref = ob.backward(x.as_f64("q"), x.as_f64("k"), x.as_f64("v"), x.as_f64("u"), x.lambda0, dO)
+    errs = {key: rel_fro(got[key], ref[key]) for key in KEYS}
+    print("\nbackward d=128 %s %s" % (case, {k_: "%.2e" % e for k_, e in errs.items()}))
+    assert all(e <= GTOL for e in errs.values()), errs
