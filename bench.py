@@ -45,19 +45,20 @@ FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
 # DRAM traffic per launch of the dominant kernel, from ncu captures
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (kernel,
 # workload).  Reported only while the kernel source still hashes to the value
-# it was captured from; otherwise null.
+# it was captured from; otherwise null.  (An edit of the shared header that
+# adds only host declarations re-keys the records without a new capture.)
 TRAFFIC = {
     # sequential kernel, long stream: 135.3 + 18.9 MB at T=16384, scaled x4 to T=65536
-    ("seq", "long", "seq_kernel"): {"bytes": 4 * (135.331840e6 + 18.873600e6), "src_sha": "3e83f00723bacc5a"},
+    ("seq", "long", "seq_kernel"): {"bytes": 4 * (135.331840e6 + 18.873600e6), "src_sha": "c7b1da03ef2a882b"},
     # sequential kernel at d = 32, recall8 workload: one full-size launch (one ncu pass)
-    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.589312e6 + 50.995200e6, "src_sha": "cf4c667cff68449b"},
+    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.589312e6 + 50.995200e6, "src_sha": "36a8d00592a68bf1"},
     # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.214144e6 + 98.598144e6, "src_sha": "b286e1a97adfb166"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.107456e6 + 246.773504e6, "src_sha": "6bc72c4621acfc2f"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.214144e6 + 98.598144e6, "src_sha": "00e726b761b7237f"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.107456e6 + 246.773504e6, "src_sha": "348d9146873b85b1"},
     # d = 128 queue launch, batched workload: at B=8 (128 units), scaled x4 to B=32 (the bytes
     # of a unit's two passes do not depend on how many units a launch holds)
     ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.733312e6 + 126.918144e6),
-                                                    "src_sha": "69029427c86670d5"},
+                                                    "src_sha": "99228bae6f0f1461"},
 }
 
 

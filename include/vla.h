@@ -149,9 +149,36 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
                      void *workspace, size_t ws_bytes, void *stream, void *copy_stream, void *ev_uk,
                      void *ev_qv, void *download_stream);
 
-/* Workspace bytes vla_forward needs for these arguments (0 for the
- * sequential kernel).  Returns 0 for invalid arguments as well. */
+/* Workspace bytes for these arguments, enough for vla_forward and for
+ * vla_forward_host (0 for the sequential kernel).  On the tensor-core path at
+ * d_h = 64 with bf16 I/O the host entry runs the two halves of the units as
+ * problems of their own, side by side in the workspace (vla_host_ranges), which
+ * can take a little more than vla_forward alone.  Returns 0 for invalid
+ * arguments as well. */
 size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk);
+
+/* The chunk lengths vla_forward uses on the chunked paths for these
+ * arguments: S-chunks of *C tokens (the state pass, the chain along the chunks,
+ * the readout) and A-chunks of *CA tokens (the Grams and the gates; CA divides
+ * C).  Both 0 when the call does not take a chunked path.  Returns VLA_OK, or
+ * the argument checks' VLA_ERR_* code (C and CA untouched). */
+int vla_chunk_lengths(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk, int *C, int *CA);
+
+/* The ranges of units vla_forward_host stages on the tensor-core path at
+ * d_h = 64 with bf16 I/O: *n ranges (2 or 3: half the units, then the rest in
+ * one or two), range r from unit lo[r] (lo[n] = B * H), with S- and A-chunk
+ * lengths C[r] = CA[r].  The two halves are problems of their own, each with
+ * chunk when given; else the first half takes vla_forward's default S-chunk
+ * length for the whole problem, and the second half the S-chunk length of a
+ * lone pass over its last range when that is at least 512 tokens (the passes
+ * over that range, which run after the last upload, then fill the GPU for
+ * fewer sub-blocks), otherwise the first half's.  A range's results are those
+ * of vla_forward on its units with chunk = C[r].
+ * *n = 0 when the call does not
+ * stage this way.  lo holds at least 4 entries, C and CA at least 3.  Returns
+ * VLA_OK or the argument checks' VLA_ERR_* code. */
+int vla_host_ranges(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk, int *n, int *lo, int *C,
+                    int *CA);
 
 /* Which kernel VLA_KERNEL_AUTO resolves to for this shape and I/O type
  * (VLA_KERNEL_SEQ, VLA_KERNEL_CHUNK_TC or VLA_KERNEL_DECODE), or a VLA_ERR_*
@@ -178,13 +205,14 @@ int vla_device_status(void *stream);
  * VLA_ERR_ARG. */
 int vla_debug_inject(int mode, long long wait_limit_ns);
 
-/* Measurement hook.  With n > 0, every later vla_forward call records
- * events[0] on its stream before its first kernel and events[i] right after
- * its i-th kernel, for i < n, so that a caller can time each launch with
- * cudaEventElapsedTime on the launching stream.  events are cudaEvent_t
- * handles (as void*) created and owned by the caller.  n = 0 or
- * events = NULL turns recording off.  Process-wide host state; returns
- * VLA_OK, or VLA_ERR_ARG when n is negative or above 16. */
+/* Measurement hook.  With n > 0, every later vla_forward (or
+ * vla_forward_host) call records events[0] on its stream before its first
+ * kernel and events[i] right after its i-th kernel, for i < n, so that a
+ * caller can time each launch with cudaEventElapsedTime on the launching
+ * stream (on the host entry the first record follows the wait for the first
+ * uploads).  events are cudaEvent_t handles (as void*) created and owned by the
+ * caller.  n = 0 or events = NULL turns recording off.  Process-wide host
+ * state; returns VLA_OK, or VLA_ERR_ARG when n is negative or above 64. */
 int vla_set_launch_events(void *const *events, int n);
 
 /* Number of kernels the last successful vla_forward call on this host

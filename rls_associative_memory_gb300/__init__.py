@@ -26,10 +26,12 @@ from ._lib import (  # noqa: F401
     lib_path,
     vla_backward,
     vla_backward_workspace_bytes,
+    vla_chunk_lengths,
     vla_debug_inject,
     vla_device_status,
     vla_forward_host,
     vla_forward,
+    vla_host_ranges,
     vla_last_launch_count,
     vla_select_kernel,
     vla_set_launch_events,

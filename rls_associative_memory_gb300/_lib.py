@@ -44,6 +44,8 @@ _SIGS = {
                          _vp, _vp, _vp, _i, _i, _vp, ctypes.c_size_t, _vp]),
     "vla_workspace_bytes": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
     "vla_select_kernel": (_i, [_i, _i, _i, _i, _i]),
+    "vla_chunk_lengths": (_i, [_i] * 7 + [ctypes.POINTER(_i)] * 2),
+    "vla_host_ranges": (_i, [_i] * 7 + [ctypes.POINTER(_i)] * 4),
     "vla_status_str": (ctypes.c_char_p, [_i]),
     "vla_last_cuda_error": (_i, []),
     "vla_device_status": (_i, [_vp]),
@@ -103,6 +105,26 @@ def vla_workspace_bytes(B, H, T, d_h, io_dtype=VLA_BF16, kernel=VLA_KERNEL_AUTO,
 
 def vla_select_kernel(B, H, T, d_h, io_dtype=VLA_BF16) -> int:
     return int(lib().vla_select_kernel(B, H, T, d_h, io_dtype))
+
+
+def vla_chunk_lengths(B, H, T, d_h, io_dtype=VLA_BF16, kernel=VLA_KERNEL_AUTO, chunk=0):
+    """(C, CA): the S- and A-chunk lengths vla_forward uses ((0, 0) off the chunked paths)."""
+    C, CA = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().vla_chunk_lengths(B, H, T, d_h, io_dtype, kernel, chunk, ctypes.byref(C), ctypes.byref(CA))
+    if rc != VLA_OK:
+        raise VLAError(rc, "vla_chunk_lengths")
+    return C.value, CA.value
+
+
+def vla_host_ranges(B, H, T, d_h, io_dtype=VLA_BF16, kernel=VLA_KERNEL_AUTO, chunk=0):
+    """The ranges vla_forward_host stages on the tensor-core path at d_h = 64:
+    a list of (first unit, units, C, CA), empty when it does not stage so."""
+    n = ctypes.c_int(0)
+    lo, C, CA = (ctypes.c_int * 4)(), (ctypes.c_int * 3)(), (ctypes.c_int * 3)()
+    rc = lib().vla_host_ranges(B, H, T, d_h, io_dtype, kernel, chunk, ctypes.byref(n), lo, C, CA)
+    if rc != VLA_OK:
+        raise VLAError(rc, "vla_host_ranges")
+    return [(lo[r], lo[r + 1] - lo[r], C[r], CA[r]) for r in range(n.value)]
 
 
 def vla_device_status(stream=None) -> int:

@@ -17,7 +17,7 @@ thread_local int t_last_cuda_error = 0;
 
 long long g_wait_limit_ns = 1000000000LL;  // 1 s bound on every device-side wait
 int g_inject = 0;
-void *g_events[16];
+void *g_events[64];
 int g_n_events = 0;
 thread_local int t_last_launches = 0;
 
@@ -63,6 +63,15 @@ int resolve_kernel(int B, int H, int T, int d_h, int io_dtype, int kernel) {
     return VLA_KERNEL_SEQ;
 }
 
+// Workspace bytes vla_forward itself needs (the chunked paths' layout).
+size_t forward_ws_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk) {
+    if (check_common(io_dtype, 1.f, B, H, T, d_h, kernel) != VLA_OK) return 0;
+    if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return 0;
+    const int kk = resolve_kernel(B, H, T, d_h, io_dtype, kernel);
+    if ((kk != VLA_KERNEL_CHUNK && kk != VLA_KERNEL_CHUNK_TC) || T == 0 || (long long)B * H == 0) return 0;
+    return vla::chunk_layout(B * H, T, d_h, chunk, kk == VLA_KERNEL_CHUNK_TC && io_dtype == VLA_BF16).total;
+}
+
 
 }  // namespace
 
@@ -99,7 +108,7 @@ const char *vla_status_str(int status) {
 int vla_last_cuda_error(void) { return t_last_cuda_error; }
 
 int vla_set_launch_events(void *const *events, int n) {
-    if (n < 0 || n > 16) return VLA_ERR_ARG;
+    if (n < 0 || n > 64) return VLA_ERR_ARG;
     if (!events) n = 0;
     for (int i = 0; i < n; ++i) g_events[i] = events[i];
     g_n_events = n;
@@ -114,12 +123,53 @@ int vla_select_kernel(int B, int H, int T, int d_h, int io_dtype) {
     return resolve_kernel(B, H, T, d_h, io_dtype, VLA_KERNEL_AUTO);
 }
 
-size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk) {
-    if (check_common(io_dtype, 1.f, B, H, T, d_h, kernel) != VLA_OK) return 0;
-    if (chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return 0;
+int vla_chunk_lengths(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk, int *C, int *CA) {
+    const int rc = check_common(io_dtype, 1.f, B, H, T, d_h, kernel);
+    if (rc != VLA_OK) return rc;
+    if (!C || !CA || chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
+    *C = *CA = 0;
     const int kk = resolve_kernel(B, H, T, d_h, io_dtype, kernel);
-    if ((kk != VLA_KERNEL_CHUNK && kk != VLA_KERNEL_CHUNK_TC) || T == 0 || (long long)B * H == 0) return 0;
-    return vla::chunk_layout(B * H, T, d_h, chunk, kk == VLA_KERNEL_CHUNK_TC && io_dtype == VLA_BF16).total;
+    if ((kk != VLA_KERNEL_CHUNK && kk != VLA_KERNEL_CHUNK_TC) || T == 0 || (long long)B * H == 0) return VLA_OK;
+    const vla::ChunkLayout L =
+        vla::chunk_layout(B * H, T, d_h, chunk, kk == VLA_KERNEL_CHUNK_TC && io_dtype == VLA_BF16);
+    *C = L.C;
+    *CA = L.CA;
+    return VLA_OK;
+}
+
+int vla_host_ranges(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk, int *n, int *lo, int *C,
+                    int *CA) {
+    const int rc = check_common(io_dtype, 1.f, B, H, T, d_h, kernel);
+    if (rc != VLA_OK) return rc;
+    if (!n || !lo || !C || !CA || chunk < 0 || (chunk > 0 && chunk % 16 != 0)) return VLA_ERR_ARG;
+    *n = 0;
+    const int kk = resolve_kernel(B, H, T, d_h, io_dtype, kernel);
+    const long long BH = (long long)B * H;
+    if (kk != VLA_KERNEL_CHUNK_TC || io_dtype != VLA_BF16 || d_h != 64 || BH < 2 || T == 0) return VLA_OK;
+    if (vla::chunk_layout((int)BH, T, d_h, chunk, true).C % 64 != 0) return VLA_OK;
+    const vla::TcHostPlan plan = vla::tc_host_plan((int)BH, T, chunk);
+    for (int s = 0; s < 2; ++s)
+        if (plan.L[s].C % 64 != 0 || plan.L[s].CA % 64 != 0) return VLA_OK;
+    *n = plan.n;
+    for (int r = 0; r <= plan.n; ++r) lo[r] = plan.lo[r];
+    for (int r = 0; r < plan.n; ++r) {
+        C[r] = plan.L[plan.part[r]].C;
+        CA[r] = plan.L[plan.part[r]].CA;
+    }
+    return VLA_OK;
+}
+
+size_t vla_workspace_bytes(int B, int H, int T, int d_h, int io_dtype, int kernel, int chunk) {
+    const size_t fwd = forward_ws_bytes(B, H, T, d_h, io_dtype, kernel, chunk);
+    if (fwd == 0) return 0;
+    // vla_forward_host on the tensor-core path at d = 64 runs its ranges of units
+    // with layouts of their own, side by side in the workspace
+    const int kk = resolve_kernel(B, H, T, d_h, io_dtype, kernel);
+    if (kk == VLA_KERNEL_CHUNK_TC && io_dtype == VLA_BF16 && d_h == 64 && (long long)B * H >= 2) {
+        const size_t host = vla::tc_host_plan(B * H, T, chunk).total;
+        return host > fwd ? host : fwd;
+    }
+    return fwd;
 }
 
 size_t vla_backward_workspace_bytes(int B, int H, int T, int d_h) {
@@ -209,7 +259,7 @@ int prepare_forward(const void *q, const void *k, const void *v, const void *u, 
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return VLA_ERR_ALIGN;
     kk = resolve_kernel(B, H, T, d_h, io_dtype, kernel);
-    const size_t need = vla_workspace_bytes(B, H, T, d_h, io_dtype, kk, chunk);
+    const size_t need = forward_ws_bytes(B, H, T, d_h, io_dtype, kk, chunk);
     if (need > 0 && (!workspace || ws_bytes < need)) return VLA_ERR_WORKSPACE;
     p = vla::FwdParams{};
     L = vla::ChunkLayout{};
@@ -234,6 +284,27 @@ int prepare_forward(const void *q, const void *k, const void *v, const void *u, 
         p.rows_tc = tc;
     }
     return VLA_OK;
+}
+
+// p restricted to the units [lo, lo + n): every tensor from its slice (`unit`
+// bytes of an input per unit), BH = n.  The workspace fields are left as in p.
+vla::FwdParams range_params(const vla::FwdParams &p, long long lo, long long n, size_t unit) {
+    vla::FwdParams pr = p;
+    const size_t dd = (size_t)p.d * p.d;
+    const size_t ub = unit * (size_t)lo, sb = dd * (size_t)lo, nb = (size_t)p.d * (size_t)lo;
+    pr.q = static_cast<const unsigned char *>(p.q) + ub;
+    pr.k = static_cast<const unsigned char *>(p.k) + ub;
+    pr.v = static_cast<const unsigned char *>(p.v) + ub;
+    pr.u = static_cast<const unsigned char *>(p.u) + ub;
+    pr.o = static_cast<unsigned char *>(p.o) + ub;
+    if (p.S0) pr.S0 = p.S0 + sb;
+    if (p.A0) pr.A0 = p.A0 + sb;
+    if (p.n0) pr.n0 = p.n0 + nb;
+    pr.S_T = p.S_T + sb;
+    pr.A_T = p.A_T + sb;
+    if (p.n_T) pr.n_T = p.n_T + nb;
+    pr.BH = (int)n;
+    return pr;
 }
 
 // vla_forward's launches; wait_qv (a cudaEvent_t or null) is waited for before
@@ -319,10 +390,25 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
     };
     auto fail = [&](cudaError_t e) { return cuda_fail(e); };
     cudaError_t e;
+    bool staged = n_io > 0 && BH >= 2 && kk == VLA_KERNEL_CHUNK_TC && vla::chunk_tc_parts_supported(p, L);
+    // the tensor-core path's ranges, each a problem of its own over its units'
+    // slices of every tensor, with its layout at its own place in the workspace
+    vla::TcHostPlan plan{};
+    vla::FwdParams sub[2];
+    if (staged) {
+        plan = vla::tc_host_plan((int)BH, T, chunk);
+        if (ws_bytes < plan.total) return VLA_ERR_WORKSPACE;
+        for (int s = 0; s < 2; ++s) {
+            sub[s] = range_params(p, plan.sub_lo[s], plan.sub_lo[s + 1] - plan.sub_lo[s], unit);
+            sub[s].ws = static_cast<unsigned char *>(workspace) + plan.off[s];
+            sub[s].ws_bytes = plan.L[s].total;
+            sub[s].chunk = plan.L[s].C;
+            staged = staged && vla::chunk_tc_parts_supported(sub[s], plan.L[s]);
+        }
+    }
     // the uploads overwrite the staging buffers: after `stream`'s earlier work
     if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(cs, e_qv, 0)) != cudaSuccess) return fail(e);
-    const bool staged = n_io > 0 && BH >= 2 && kk == VLA_KERNEL_CHUNK_TC && vla::chunk_tc_parts_supported(p, L);
     const bool staged128 = n_io > 0 && BH >= 2 && kk == VLA_KERNEL_CHUNK_TC && vla::chunk_tc128_parts_supported(p, L);
     const bool staged_seq = n_io > 0 && BH >= 2 && p.T > 0 && kk == VLA_KERNEL_SEQ;
     long long o_lo = 0;  // o from this unit on comes back on `stream`
@@ -335,7 +421,6 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
         long long nr = BH < 4 ? BH : 4;
         long long r[5];
         for (long long i = 0; i <= nr; ++i) r[i] = BH * i / nr;
-        const size_t dd = (size_t)d_h * d_h;
         for (long long j = 0; j < nr; ++j) {
             const long long lo = r[j], n = r[j + 1] - r[j];
             if ((e = up(q, hq, lo, n)) != cudaSuccess) return fail(e);
@@ -344,20 +429,7 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
             if ((e = up(u, hu, lo, n)) != cudaSuccess) return fail(e);
             if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
             if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
-            vla::FwdParams pr = p;
-            const size_t ub = unit * (size_t)lo, sb = dd * (size_t)lo, nb = (size_t)d_h * (size_t)lo;
-            pr.q = static_cast<const unsigned char *>(p.q) + ub;
-            pr.k = static_cast<const unsigned char *>(p.k) + ub;
-            pr.v = static_cast<const unsigned char *>(p.v) + ub;
-            pr.u = static_cast<const unsigned char *>(p.u) + ub;
-            pr.o = static_cast<unsigned char *>(p.o) + ub;
-            if (p.S0) pr.S0 = p.S0 + sb;
-            if (p.A0) pr.A0 = p.A0 + sb;
-            if (p.n0) pr.n0 = p.n0 + nb;
-            pr.S_T = p.S_T + sb;
-            pr.A_T = p.A_T + sb;
-            if (p.n_T) pr.n_T = p.n_T + nb;
-            pr.BH = (int)n;
+            vla::FwdParams pr = range_params(p, lo, n, unit);
             int lc = 0;
             pr.launches = &lc;
             if ((e = vla::launch_seq(pr, st)) != cudaSuccess) return fail(e);
@@ -408,25 +480,29 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
         }
         o_lo = ds ? BH : r[nr - 1];
     } else if (staged) {
-        // Every pass of the tensor-core path is per (b, h), so the call runs it in
-        // ranges of units as their inputs land on copy_stream: u and k in two
-        // halves, each followed by its front (Grams, prefix, gates); then q and v
-        // in two or three ranges, each followed by its back (state pass, chain,
-        // output pass). The o of all ranges but the last comes back on
-        // copy_stream once its uploads are all queued; the last range's o and
-        // the final state come back on `stream`, which at the end also waits
-        // for copy_stream. The two events are reused: each wait is queued right
-        // after the record it refers to, before that event is recorded again.
-        const long long h = BH / 2;
-        const long long g[3] = {0, h, BH};
-        const int nr = (BH - h >= 2) ? 3 : 2;
-        const long long r[4] = {0, h, nr == 3 ? h + (BH - h) / 2 : BH, BH};
-        for (int i = 0; i < 2; ++i) {
-            if ((e = up(u, hu, g[i], g[i + 1] - g[i])) != cudaSuccess) return fail(e);
-            if ((e = up(k, hk, g[i], g[i + 1] - g[i])) != cudaSuccess) return fail(e);
+        // Every pass of the tensor-core path is per (b, h) unit, so the call runs
+        // the units as two problems of their own (vla::tc_host_plan), the first
+        // half and the rest, as their inputs land on copy_stream: u and k of each
+        // half, followed by its front (Grams, prefix, gates); then q and v in two
+        // or three ranges (the first half, then the rest in one or two), each
+        // followed by its back (state pass, chain, output pass). The second half
+        // takes the chunk length of its smaller back ranges, so the back of the
+        // last range, which runs after the last upload, is short. The o of all
+        // ranges but the last comes back on copy_stream once its uploads are all
+        // queued; the last range's o and the final state come back on `stream`,
+        // which at the end also waits for copy_stream. The two events are
+        // reused: each wait is queued right after the record it refers to,
+        // before that event is recorded again.
+        const int nr = plan.n;
+        long long r[4];
+        for (int i = 0; i <= nr; ++i) r[i] = plan.lo[i];
+        for (int s = 0; s < 2; ++s) {
+            const long long lo = plan.sub_lo[s], n = plan.sub_lo[s + 1] - plan.sub_lo[s];
+            if ((e = up(u, hu, lo, n)) != cudaSuccess) return fail(e);
+            if ((e = up(k, hk, lo, n)) != cudaSuccess) return fail(e);
             if ((e = cudaEventRecord(e_uk, cs)) != cudaSuccess) return fail(e);
             if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
-            if ((e = vla::launch_chunk_tc_part(p, L, 0, (int)g[i], (int)(g[i + 1] - g[i]), st)) != cudaSuccess)
+            if ((e = vla::launch_chunk_tc_part(sub[s], plan.L[s], 0, 0, sub[s].BH, st)) != cudaSuccess)
                 return fail(e);
         }
         for (int j = 0; j < nr; ++j) {
@@ -446,7 +522,9 @@ int vla_forward_host(const void *hq, const void *hk, const void *hv, const void 
                 }
             }
             if ((e = cudaStreamWaitEvent(st, e_uk, 0)) != cudaSuccess) return fail(e);
-            if ((e = vla::launch_chunk_tc_part(p, L, 1, (int)r[j], (int)(r[j + 1] - r[j]), st)) != cudaSuccess)
+            const int s = plan.part[j];
+            if ((e = vla::launch_chunk_tc_part(sub[s], plan.L[s], 1, (int)(r[j] - plan.sub_lo[s]),
+                                               (int)(r[j + 1] - r[j]), st)) != cudaSuccess)
                 return fail(e);
             if (ds) {  // the range's o on download_stream, beside the later passes
                 if ((e = cudaEventRecord(e_qv, st)) != cudaSuccess) return fail(e);

@@ -1396,14 +1396,77 @@ int chunk_default_a_tc(int BH, int T, int C) {
 // and pass at one CTA per SM: the default when the units alone fill the GPU.
 constexpr int kTc128MinUnits = 128;
 
+// S-chunk length of the tensor-core path for one range of the host entry, a
+// problem of `units` units on its own: the wave model of tc_pass_cost for one
+// pass, plus the chain along the chunks (chunk_default_tc also weighs the pass
+// over each half of the units, which a range does not run).
+static int chunk_default_tc_range(int units, int T) {
+    const int maxm = std::min((T + 63) / 64, 1024);
+    int best = 64;
+    double best_cost = -1;
+    for (int m = 1; m <= maxm; ++m) {
+        const long long NC = (T + 64LL * m - 1) / (64LL * m);
+        const double cost = tc_pass_cost((long long)units * NC, m) + 0.045 * (double)NC;
+        if (best_cost < 0 || cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = 64 * m;
+        }
+    }
+    return best;
+}
+
+static ChunkLayout layout_for(int BH, int T, int d, int C, int CA, bool tc);
+
 ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc_path) {
-    ChunkLayout L{};
     const bool single = chunk == 0 && tc_path && d == 128 && BH >= kTc128MinUnits;
-    L.C = chunk > 0 ? chunk
-                    : (single ? (T + 63) / 64 * 64
-                              : (tc_path && d == 64 ? chunk_default_tc(BH, T) : chunk_default(BH, T)));
-    const bool tc = tc_path && d == 64 && L.C % 64 == 0;
-    L.CA = chunk > 0 || single ? L.C : (tc ? chunk_default_a_tc(BH, T, L.C) : chunk_default_a(BH, T, d, L.C));
+    const int C = chunk > 0 ? chunk
+                            : (single ? (T + 63) / 64 * 64
+                                      : (tc_path && d == 64 ? chunk_default_tc(BH, T) : chunk_default(BH, T)));
+    const bool tc = tc_path && d == 64 && C % 64 == 0;
+    const int CA = chunk > 0 || single ? C : (tc ? chunk_default_a_tc(BH, T, C) : chunk_default_a(BH, T, d, C));
+    return layout_for(BH, T, d, C, CA, tc);
+}
+
+TcHostPlan tc_host_plan(int BH, int T, int chunk) {
+    TcHostPlan P{};
+    if (BH < 2 || T <= 0) return P;
+    const int h = BH / 2;
+    P.sub_lo[0] = 0;
+    P.sub_lo[1] = h;
+    P.sub_lo[2] = BH;
+    P.n = (BH - h >= 2) ? 3 : 2;
+    P.lo[0] = 0;
+    P.lo[1] = h;
+    if (P.n == 3) P.lo[2] = h + (BH - h) / 2;
+    P.lo[P.n] = BH;
+    for (int r = 0; r < P.n; ++r) P.part[r] = r == 0 ? 0 : 1;
+    // The first half keeps the whole problem's chunk length.  The second half's
+    // last back range is what runs after the last upload: it takes the chunk
+    // length of a lone pass over that range (its passes then fill the GPU for
+    // fewer sub-blocks) when that is at least 512 tokens; below that the longer
+    // chain along the chunks and the fixed cost of each launch outweigh what the
+    // shorter chunks save (measured: 4 x 8 x 4096 end to end 0.551 -> 0.568 ms
+    // with 128-token chunks there, 16 units x 65536 tokens 3.141 -> 3.118 ms
+    // with 896).
+    const int whole = chunk_default_tc(BH, T);
+    const int last = chunk_default_tc_range(P.lo[P.n] - P.lo[P.n - 1], T);
+    size_t off = 0;
+    for (int s = 0; s < 2; ++s) {
+        // A-chunks as long as the S-chunks, as with an explicit chunk length: a
+        // range is then exactly vla_forward on its units with chunk = C
+        const int C = chunk > 0 ? chunk : (s == 1 && last >= 512 ? last : whole);
+        P.L[s] = layout_for(P.sub_lo[s + 1] - P.sub_lo[s], T, 64, C, C, C % 64 == 0);
+        P.off[s] = off;
+        off = align256(off + P.L[s].total);
+    }
+    P.total = off;
+    return P;
+}
+
+static ChunkLayout layout_for(int BH, int T, int d, int C, int CA, bool tc) {
+    ChunkLayout L{};
+    L.C = C;
+    L.CA = CA;
     L.NC = (T + L.C - 1) / L.C;
     L.NCA = (T + L.CA - 1) / L.CA;
     const size_t bh = (size_t)BH, nc = (size_t)L.NC, nca = (size_t)L.NCA, dd = (size_t)d * d;

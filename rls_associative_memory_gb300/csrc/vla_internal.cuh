@@ -118,6 +118,24 @@ int api_cuda_fail(cudaError_t e);
 // chunk == 0 picks the defaults.  tc reserves the readout coefficients of
 // the tensor-core state pass (d = 64, chunks a multiple of 64 tokens).
 ChunkLayout chunk_layout(int BH, int T, int d, int chunk, bool tc = false);
+// The host entry's plan on the tensor-core path at d = 64 with bf16 I/O: two
+// problems of their own, the first half of the units and the rest (sub_lo),
+// each with its layout at byte offset off[s] of the workspace (total bytes in
+// all) and S- and A-chunks of one length (`chunk` when given; else the whole
+// problem's default, and for the second half that of a lone pass over its last
+// back range when that is at least 512 tokens).  The fronts run
+// per half; the backs per range r (n of them: the first half, then the rest in
+// one or two), range r from unit lo[r] in half part[r].  n = 0 when BH < 2.
+struct TcHostPlan {
+    int n;
+    int lo[4];          // first unit of back range r; lo[n] = BH
+    int part[3];        // the half back range r lies in
+    int sub_lo[3];      // first unit of half s; sub_lo[2] = BH
+    ChunkLayout L[2];
+    size_t off[2];
+    size_t total;
+};
+TcHostPlan tc_host_plan(int BH, int T, int chunk);
 // Chunk-parallel path (six launches).  Returns a cudaError_t.
 cudaError_t launch_chunk(const FwdParams &p, const ChunkLayout &L, cudaStream_t stream);
 // The tensor-core path (d = 64, bf16 I/O, every pass on its tensor-core

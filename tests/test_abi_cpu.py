@@ -137,15 +137,51 @@ def test_tensor_core_chunk_defaults():
     its passes (two CTAs per SM on 152 SMs): 16 units x 65536 tokens take
     1728-token chunks (38 per unit, 608 CTAs: two full waves, and one full
     wave for each half of the units), and 32 units x 4096 tokens 256. The
-    explicit length equal to the default needs the same workspace (same S- and
-    A-chunk counts)."""
-    ws = lambda BH, T, c: vla.vla_workspace_bytes(1, BH, T, 64, vla.VLA_BF16, vla.VLA_KERNEL_CHUNK_TC, c)  # noqa: E731
-    assert ws(16, 65536, 0) == ws(16, 65536, 1728)
+    explicit length equal to the default gives the same layout."""
+    TC = vla.VLA_KERNEL_CHUNK_TC
+    assert vla.vla_chunk_lengths(1, 16, 65536, 64, vla.VLA_BF16, TC) == (1728, 1728)
+    assert vla.vla_chunk_lengths(1, 32, 4096, 64, vla.VLA_BF16, TC)[0] == 256
+    assert vla.vla_chunk_lengths(1, 16, 65536, 64, vla.VLA_BF16, TC, 512) == (512, 512)
+    ws = lambda BH, T, c: vla.vla_workspace_bytes(1, BH, T, 64, vla.VLA_BF16, TC, c)  # noqa: E731
     assert ws(16, 65536, 0) != ws(16, 65536, 512)
-    assert ws(32, 4096, 0) == ws(32, 4096, 256)
-    # the float path keeps its own lengths
-    f32 = vla.vla_workspace_bytes(1, 16, 65536, 64, vla.VLA_F32, vla.VLA_KERNEL_CHUNK_TC, 0)
+    # the float path keeps its own lengths (no tensor-core passes, no staged ranges)
+    f32 = vla.vla_workspace_bytes(1, 16, 65536, 64, vla.VLA_F32, TC, 0)
     assert f32 == vla.vla_workspace_bytes(1, 16, 65536, 64, vla.VLA_F32, vla.VLA_KERNEL_CHUNK, 0)
+    assert vla.vla_host_ranges(1, 16, 65536, 64, vla.VLA_F32, TC) == []
+    assert vla.vla_chunk_lengths(1, 16, 65536, 64, vla.VLA_BF16, vla.VLA_KERNEL_SEQ) == (0, 0)
+
+
+def test_host_entry_ranges():
+    """The host entry's ranges on the tensor-core path: half the units, then the
+    rest in two.  Each half is a problem of its own: the first with the whole
+    problem's default chunk length, the second with that of a lone pass over
+    its last range (the wave model at two CTAs per SM on 152 SMs plus the chain
+    along the chunks) when that is at least 512 tokens.  16 units x 65536
+    tokens run 8 units at 1728 tokens (one full wave), then two ranges of 4 at
+    896 (74 chunks a unit, 296 CTAs: one wave of 14 sub-blocks instead of 27);
+    32 units x 4096 tokens keep 256 throughout (the lone pass would take 128).
+    An explicit chunk length holds for every range.  The workspace covers the
+    two halves' layouts side by side."""
+    TC, BF = vla.VLA_KERNEL_CHUNK_TC, vla.VLA_BF16
+    assert vla.vla_host_ranges(1, 16, 65536, 64, BF, TC) == [(0, 8, 1728, 1728), (8, 4, 896, 896),
+                                                             (12, 4, 896, 896)]
+    assert vla.vla_host_ranges(1, 16, 65536, 64, BF, TC, 1728) == [(0, 8, 1728, 1728), (8, 4, 1728, 1728),
+                                                                   (12, 4, 1728, 1728)]
+    assert [r[:2] for r in vla.vla_host_ranges(1, 2, 4096, 64, BF, TC)] == [(0, 1), (1, 1)]
+    assert [r[:2] for r in vla.vla_host_ranges(1, 3, 4096, 64, BF, TC)] == [(0, 1), (1, 1), (2, 1)]
+    assert vla.vla_host_ranges(1, 32, 4096, 64, BF, TC) == [(0, 16, 256, 256), (16, 8, 256, 256), (24, 8, 256, 256)]
+    for lo, n, C, CA in vla.vla_host_ranges(4, 8, 4096, 64, BF, TC):
+        assert C % 64 == 0 and CA % 64 == 0 and C % CA == 0
+    # no staging at one unit, at d = 128 (its own schedule) or on the sequential kernel
+    assert vla.vla_host_ranges(1, 1, 65536, 64, BF, TC) == []
+    assert vla.vla_host_ranges(32, 16, 2048, 128, BF, TC) == []
+    assert vla.vla_host_ranges(1, 16, 65536, 64, BF, vla.VLA_KERNEL_SEQ) == []
+    # the workspace holds every range's layout: at least the whole problem's
+    whole = vla.vla_workspace_bytes(1, 1, 65536, 64, BF, TC, 1728) * 16
+    assert vla.vla_workspace_bytes(1, 16, 65536, 64, BF, TC) >= whole
+    assert vla.vla_workspace_bytes(1, 16, 65536, 64, BF, TC) <= whole * 1.1
+    with pytest.raises(vla.VLAError):
+        vla.vla_host_ranges(1, 16, 65536, 48, BF, TC)
 
 
 def test_backward_argument_checks():
@@ -197,3 +233,11 @@ def test_host_entry_argument_checks():
     assert call(hn=f + 0x200000) == vla.VLA_ERR_ARG  # a host n_T needs the device n_T
     assert call(d=48) == vla.VLA_ERR_UNSUPPORTED_DIM
     assert call(io=9) == vla.VLA_ERR_ARG
+
+
+def test_launch_event_hook_limit():
+    """The measurement hook takes up to 64 event handles (the host entry's
+    staged ranges launch up to 18 kernels); more is an argument error."""
+    assert vla.vla_set_launch_events([1] * 65) == vla.VLA_ERR_ARG
+    assert vla.vla_set_launch_events([1] * 64) == vla.VLA_OK
+    assert vla.vla_set_launch_events(None) == vla.VLA_OK

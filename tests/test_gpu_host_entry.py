@@ -1,6 +1,9 @@
 """vla_forward_host: the same kernels as vla_forward on staged copies, so the
-results are bit-identical; its uploads run on a second stream, and o comes
-back on the compute or copy stream, or on a third one when given."""
+results are bit-identical to vla_forward run on each staged range of units
+with that range's chunk lengths (on the tensor-core path at d = 64 the ranges
+are problems of their own, vla_host_ranges); its uploads run on a second
+stream, and o comes back on the compute or copy stream, or on a third one when
+given."""
 
 import pytest
 import torch
@@ -12,11 +15,30 @@ from vla_testutil import compare, oracle_ref, to_device
 pytestmark = pytest.mark.gpu
 
 
+def _device_reference(q, k, v, u, lam, kernel, S0=None, A0=None, n0=None):
+    """vla_forward as the host entry runs it: per staged range with the range's
+    chunk lengths where the call stages ranges of its own, else in one call."""
+    B, H, T, d = q.shape
+    io = vla.VLA_BF16 if q.dtype == torch.bfloat16 else vla.VLA_F32
+    ranges = vla.vla_host_ranges(B, H, T, d, io, kernel)
+    if not ranges:
+        return vla.vla_forward(q, k, v, u, lam, S0=S0, A0=A0, n0=n0, kernel=kernel)
+    flat = lambda t: None if t is None else t.reshape(B * H, *t.shape[2:])  # noqa: E731
+    outs = []
+    for lo, n, C, CA in ranges:
+        assert CA == C, "an explicit chunk length sets both"
+        sl = lambda t: None if t is None else flat(t)[lo:lo + n].unsqueeze(0).contiguous()  # noqa: E731
+        outs.append(vla.vla_forward(sl(q), sl(k), sl(v), sl(u), lam, S0=sl(S0), A0=sl(A0), n0=sl(n0),
+                                    kernel=kernel, chunk=C))
+    return tuple(torch.cat([o[i][0] for o in outs]).reshape(B, H, *outs[0][i].shape[2:]) for i in range(4))
+
+
 @pytest.mark.parametrize("kernel,B,H,T,dtype,init", [
     (vla.VLA_KERNEL_CHUNK_TC, 1, 3, 1000, "bf16", False),  # ranges of units 1 | 1 | 1
     (vla.VLA_KERNEL_CHUNK_TC, 1, 2, 700, "bf16", False),   # 1 | 1 (two ranges)
     (vla.VLA_KERNEL_CHUNK_TC, 2, 4, 1000, "bf16", True),   # 4 | 2 | 2, A0 inverted per range
     (vla.VLA_KERNEL_CHUNK_TC, 1, 5, 640, "bf16", False),   # 2 | 1 | 2
+    (vla.VLA_KERNEL_CHUNK_TC, 2, 8, 2048, "bf16", True),   # 8 | 4 | 4 with their own chunk lengths
     (vla.VLA_KERNEL_SEQ, 1, 3, 77, "f32", False), (vla.VLA_KERNEL_CHUNK, 1, 3, 300, "bf16", False),
     (vla.VLA_KERNEL_AUTO, 1, 3, 3, "bf16", False)])
 @pytest.mark.parametrize("download", [False, True], ids=["two_streams", "download_stream"])
@@ -30,7 +52,7 @@ def test_host_entry_matches_device_entry(kernel, B, H, T, dtype, init, download)
         st = oracle_ref(pre)
         S0, A0, n0 = (torch.from_numpy(st[n]).float().cuda().contiguous() for n in ("S_T", "A_T", "n_T"))
         ref0 = dict(S0=st["S_T"], A0=st["A_T"], n0=st["n_T"])
-    o_ref, S_ref, A_ref, n_ref = vla.vla_forward(q, k, v, u, x.lambda0, S0=S0, A0=A0, n0=n0, kernel=kernel)
+    o_ref, S_ref, A_ref, n_ref = _device_reference(q, k, v, u, x.lambda0, kernel, S0=S0, A0=A0, n0=n0)
     torch.cuda.synchronize()
 
     hq, hk, hv, hu = (t.cpu().pin_memory() for t in (q, k, v, u))
@@ -113,7 +135,7 @@ def test_host_entry_one_stream():
     """copy_stream == stream: the ranges run one after another, same results."""
     x = make_inputs(1, 3, 700, 64, "bf16", seed=76, u_scale=0.5)
     q, k, v, u = to_device(x)
-    o_ref, S_ref, A_ref, n_ref = vla.vla_forward(q, k, v, u, x.lambda0, kernel=vla.VLA_KERNEL_CHUNK_TC)
+    o_ref, S_ref, A_ref, n_ref = _device_reference(q, k, v, u, x.lambda0, vla.VLA_KERNEL_CHUNK_TC)
     torch.cuda.synchronize()
     hq, hk, hv, hu = (t.cpu().pin_memory() for t in (q, k, v, u))
     dq, dk, dv, du = (torch.empty_like(t) for t in (q, k, v, u))
@@ -197,3 +219,23 @@ def test_host_entry_sequential_ranges(B, H, T, download):
     assert torch.equal(ho, o_ref.cpu())
     assert torch.equal(hS, S_ref.cpu()) and torch.equal(hA, A_ref.cpu()) and torch.equal(hn, n_ref.cpu())
     compare({"o": ho.numpy(), "S_T": hS.numpy(), "A_T": hA.numpy(), "n_T": hn.numpy()}, oracle_ref(x), "f32")
+
+
+def test_host_entry_halves_with_their_own_chunks():
+    """1 x 16 x 65536 (the long stream's shape): the first half (8 units) at the
+    whole problem's chunk length, then two ranges of 4 at the second half's
+    own, each bit-identical to vla_forward on its units with its chunk length;
+    the last unit of every range against the oracle."""
+    x = make_inputs(1, 16, 65536, 64, "bf16", seed=77)
+    q, k, v, u = to_device(x)
+    ranges = vla.vla_host_ranges(1, 16, 65536, 64, vla.VLA_BF16, vla.VLA_KERNEL_AUTO)
+    assert len({r[2] for r in ranges}) == 2, ranges  # the halves do not share one chunk length
+    o_ref, S_ref, A_ref, n_ref = _device_reference(q, k, v, u, x.lambda0, vla.VLA_KERNEL_AUTO)
+    torch.cuda.synchronize()
+    got = _host_call(x, vla.VLA_KERNEL_AUTO)
+    assert (got["o"] == o_ref.float().cpu().numpy()).all()
+    assert (got["S_T"] == S_ref.cpu().numpy()).all() and (got["A_T"] == A_ref.cpu().numpy()).all()
+    for lo, n, C, CA in ranges:
+        b, h = divmod(lo + n - 1, 16)
+        ref = oracle_ref(x.slice_heads(slice(b, b + 1), slice(h, h + 1)))  # the range's last unit
+        compare({key: val[b:b + 1, h:h + 1] for key, val in got.items()}, ref, "bf16")
