@@ -57,6 +57,8 @@ TRAFFIC = {
     ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.107456e6 + 246.773504e6, "src_sha": "348d9146873b85b1"},
     # d = 128 queue launch, batched workload: at B=8 (128 units), scaled x4 to B=32 (the bytes
     # of a unit's two passes do not depend on how many units a launch holds)
+    # decode step, state in place: one launch at full size (one ncu pass of the full set)
+    ("decode", "decode", "decode_kernel"): {"bytes": 68.699136e6 + 13.662208e6, "src_sha": "fa5b569b82b39c4d"},
     ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.733312e6 + 126.918144e6),
                                                     "src_sha": "99228bae6f0f1461"},
 }
@@ -70,6 +72,7 @@ KERNEL_SOURCES = {
     "gates_tc_kernel": ["vla_gates_tc.cu", "vla_tc_common.cuh"],
     "rows_tc_kernel": ["vla_chunk_tc.cu", "vla_tc_common.cuh"],
     "tc128_queue_kernel": ["vla_gates_tc128.cuh", "vla_rows_tc128.cuh", "vla_tc128.cu", "vla_tc_common.cuh"],
+    "decode_kernel": ["vla_decode.cu"],
 }
 
 
