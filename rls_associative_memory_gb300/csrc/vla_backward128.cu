@@ -106,6 +106,18 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
     float nj = (tid < D && p.n0) ? p.n0[(size_t)bh * D + tid] : 0.f;
 
     // ---------------- phase 1: forward with records and checkpoints ----------------
+    // a token's inputs are loaded one token ahead, so their latency overlaps a token's work
+    float nq = 0.f, nk = 0.f, nv = 0.f, nu = 0.f;
+    auto fetch_in = [&](int t) {
+        if (tid < D && t < T) {
+            const size_t tok = ((size_t)bh * T + t) * D;
+            nq = io_to_f32(static_cast<const IO *>(p.q)[tok + tid]);
+            nk = io_to_f32(static_cast<const IO *>(p.k)[tok + tid]);
+            nv = io_to_f32(static_cast<const IO *>(p.v)[tok + tid]);
+            nu = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
+        }
+    };
+    fetch_in(0);
     for (int t = 0; t < T; ++t) {
         if (t % kBwdCk == 0) {
             float *ck = ckp + (size_t)(t / kBwdCk) * CKF;
@@ -118,15 +130,9 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
             }
             if (tid < D) ck[2 * D * D + tid] = nj;
         }
-        const size_t tok = ((size_t)bh * T + t) * D;
         float *rt = rec + (size_t)t * REC;
-        float qj = 0.f, kj = 0.f, vj = 0.f, uj = 0.f;
-        if (tid < D) {
-            qj = io_to_f32(static_cast<const IO *>(p.q)[tok + tid]);
-            kj = io_to_f32(static_cast<const IO *>(p.k)[tok + tid]);
-            vj = io_to_f32(static_cast<const IO *>(p.v)[tok + tid]);
-            uj = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
-        }
+        const float qj = nq, kj = nk, vj = nv, uj = nu;
+        fetch_in(t + 1);
         const float4 r1 = block_sum4<NW>(kj * kj, 0.f, 0.f, 0.f, s_red);
         const float knorm = sqrtf(r1.x);
         const float ks = 1.f / fmaxf(knorm, kEps);
@@ -217,6 +223,25 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
     float dnj = (tid < D && p.dn_T) ? p.dn_T[(size_t)bh * D + tid] : 0.f;
     __syncthreads();
 
+    // a token's record and inputs are loaded one token ahead, so their latency
+    // overlaps a token's work
+    float pkh = 0.f, pz = 0.f, pal = 0.f, pr = 0.f, pu = 0.f, pq = 0.f, pdO = 0.f, psc = 0.f;
+    auto fetch_rec = [&](int t) {
+        if (t < 0) return;
+        const size_t tok = ((size_t)bh * T + t) * D;
+        const float *rt = rec + (size_t)t * REC;
+        if (tid < D) {
+            pkh = rt[tid];
+            pz = rt[D + tid];
+            pal = rt[2 * D + tid];
+            pr = rt[3 * D + tid];
+            pu = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
+            pq = io_to_f32(static_cast<const IO *>(p.q)[tok + tid]);
+            pdO = io_to_f32(static_cast<const IO *>(p.dO)[tok + tid]);
+        }
+        if (tid < 4) psc = rt[4 * D + tid];
+    };
+    fetch_rec(T - 1);
     for (int t = T - 1; t >= 0; --t) {
         if ((t + 1) % kBwdCk == 0 && t + 1 < T) {  // re-anchor: state after token t
             const float *ck = ckp + (size_t)((t + 1) / kBwdCk) * CKF;
@@ -231,24 +256,18 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
             if (tid < D) nj = ck[2 * D * D + tid];
         }
         const size_t tok = ((size_t)bh * T + t) * D;
-        const float *rt = rec + (size_t)t * REC;
-        float khj = 0.f, zj = 0.f, alj = 0.f, uj = 0.f, qj = 0.f, fqj = 0.f;
+        const float khj = pkh, zj = pz, alj = pal, uj = pu, qj = pq, fqj = phi_elu1(qj);
         if (tid < D) {
-            khj = rt[tid];
-            zj = rt[D + tid];
-            alj = rt[2 * D + tid];
-            uj = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
-            qj = io_to_f32(static_cast<const IO *>(p.q)[tok + tid]);
-            fqj = phi_elu1(qj);
             v_kh[vidx(tid)] = khj;
             v_z[vidx(tid)] = zj;
             v_al[vidx(tid)] = alj;
             v_u[vidx(tid)] = uj;
             v_fq[vidx(tid)] = fqj;
-            s_r[tid] = rt[3 * D + tid];
-            s_dO[tid] = io_to_f32(static_cast<const IO *>(p.dO)[tok + tid]);
+            s_r[tid] = pr;
+            s_dO[tid] = pdO;
         }
-        if (tid < 4) s_sc[tid] = rt[4 * D + tid];
+        if (tid < 4) s_sc[tid] = psc;
+        fetch_rec(t - 1);
         __syncthreads();
         const float knorm = s_sc[0], beta = s_sc[1], gnorm = s_sc[2], rden = s_sc[3];
         const float4 *kp = reinterpret_cast<const float4 *>(v_kh + vo);

@@ -186,6 +186,20 @@ __global__ void __launch_bounds__(Bc<D>::NT) bc_fwd_maps_kernel(BcArgs a) {
     }
     float nj = tid < D ? ckp[(size_t)(t0 / kCkB) * CKF + 2 * D * D + tid] : 0.f;
     float dn_acc = 0.f;  // thread j < D: sum over the chunk of dden_t phi(q_t)_j
+    // the inputs are loaded one token ahead, so their latency overlaps a token's work
+    float nq = 0.f, nk = 0.f, nv = 0.f, nu = 0.f, ndO = 0.f;
+    auto fetch = [&](int t) {
+        if (t >= t1) return;
+        const size_t tok = ((size_t)bh * T + t) * D;
+        if (tid < D) {
+            nq = io_to_f32(static_cast<const IO *>(p.q)[tok + tid]);
+            nk = io_to_f32(static_cast<const IO *>(p.k)[tok + tid]);
+            nv = io_to_f32(static_cast<const IO *>(p.v)[tok + tid]);
+            nu = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
+        }
+        ndO = io_to_f32(static_cast<const IO *>(p.dO)[tok + row]);
+    };
+    fetch(t0);
     for (int t = t0; t < t1; ++t) {
         if (t % kCkB == 0 && t != t0) {
             float *ck = ckp + (size_t)(t / kCkB) * CKF;
@@ -193,15 +207,9 @@ __global__ void __launch_bounds__(Bc<D>::NT) bc_fwd_maps_kernel(BcArgs a) {
             st_row(ck + (size_t)D * D + moff, am);
             if (tid < D) ck[2 * D * D + tid] = nj;
         }
-        const size_t tok = ((size_t)bh * T + t) * D;
         float *rt = rec + (size_t)t * REC;
-        float qj = 0.f, kj = 0.f, vj = 0.f, uj = 0.f;
-        if (tid < D) {
-            qj = io_to_f32(static_cast<const IO *>(p.q)[tok + tid]);
-            kj = io_to_f32(static_cast<const IO *>(p.k)[tok + tid]);
-            vj = io_to_f32(static_cast<const IO *>(p.v)[tok + tid]);
-            uj = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
-        }
+        const float qj = nq, kj = nk, vj = nv, uj = nu, dOi = ndO;
+        fetch(t + 1);
         const float4 r1 = block_sum4<NW>(kj * kj, 0.f, 0.f, 0.f, s_red[0]);
         const float knorm = sqrtf(r1.x);
         const float ks = 1.f / fmaxf(knorm, kEps);
@@ -222,7 +230,6 @@ __global__ void __launch_bounds__(Bc<D>::NT) bc_fwd_maps_kernel(BcArgs a) {
         const float y = dot_row<TPR>(am, v_kh + vo);
         const float sk = dot_row<TPR>(s, v_kh + vo);
         const float sq = dot_row<TPR>(s, v_fq + vo);
-        const float dOi = io_to_f32(static_cast<const IO *>(p.dO)[tok + row]);
         float p1 = 0.f, p2 = 0.f, p4 = 0.f;
         if (part == 0) {
             p1 = v_u[vidx(row)] * z;
@@ -350,6 +357,25 @@ __global__ void __launch_bounds__(Bc<D>::NT) bc_spart_kernel(BcArgs a) {
     float dnj = tid < D ? a.dn_end[((size_t)bh * NC + c) * D + tid] : 0.f;
     set_diag(X, row, c0, 0.f);
 
+    // the token's record and inputs are loaded one token ahead, so their latency
+    // overlaps a token's work
+    float nkh = 0.f, nz = 0.f, nal = 0.f, nr = 0.f, nq = 0.f, nu = 0.f, ndO = 0.f, nsc = 0.f;
+    auto fetch = [&](int t) {
+        if (t < t0) return;
+        const size_t tok = ((size_t)bh * T + t) * D;
+        const float *rt = rec + (size_t)t * REC;
+        if (tid < D) {
+            nkh = rt[tid];
+            nz = rt[D + tid];
+            nal = rt[2 * D + tid];
+            nr = rt[3 * D + tid];
+            nq = io_to_f32(static_cast<const IO *>(p.q)[tok + tid]);
+            nu = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
+            ndO = io_to_f32(static_cast<const IO *>(p.dO)[tok + tid]);
+        }
+        if (tid < 4) nsc = rt[4 * D + tid];
+    };
+    fetch(t1 - 1);
     for (int t = t1 - 1; t >= t0; --t) {
         if ((t + 1) % kCkB == 0 && t + 1 < t1) {  // re-anchor: the state after token t
             const float *ck = ckp + (size_t)((t + 1) / kCkB) * CKF;
@@ -357,22 +383,18 @@ __global__ void __launch_bounds__(Bc<D>::NT) bc_spart_kernel(BcArgs a) {
             if (tid < D) nj = ck[2 * D * D + tid];
         }
         const size_t tok = ((size_t)bh * T + t) * D;
-        const float *rt = rec + (size_t)t * REC;
-        float khj = 0.f, alj = 0.f, qj = 0.f, fqj = 0.f;
+        const float khj = nkh, alj = nal, qj = nq, fqj = phi_elu1(qj);
         if (tid < D) {
-            khj = rt[tid];
-            alj = rt[2 * D + tid];
-            qj = io_to_f32(static_cast<const IO *>(p.q)[tok + tid]);
-            fqj = phi_elu1(qj);
             v_kh[vidx(tid)] = khj;
-            v_z[vidx(tid)] = rt[D + tid];
+            v_z[vidx(tid)] = nz;
             v_al[vidx(tid)] = alj;
-            v_u[vidx(tid)] = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
+            v_u[vidx(tid)] = nu;
             v_fq[vidx(tid)] = fqj;
-            s_r[tid] = rt[3 * D + tid];
-            s_dO[tid] = io_to_f32(static_cast<const IO *>(p.dO)[tok + tid]);
+            s_r[tid] = nr;
+            s_dO[tid] = ndO;
         }
-        if (tid < 4) s_sc[tid] = rt[4 * D + tid];
+        if (tid < 4) s_sc[tid] = nsc;
+        fetch(t - 1);
         __syncthreads();
         const float beta = s_sc[1], gnorm = s_sc[2], rden = s_sc[3];
         const float4 *kp = reinterpret_cast<const float4 *>(v_kh + vo);
@@ -586,21 +608,37 @@ __global__ void __launch_bounds__(Bc<D>::NT) bc_final_kernel(BcArgs a) {
     ld_row(X, a.xs_end + ((size_t)bh * NC + c) * D * D + moff);
     set_diag(as, row, c0, 0.f);
 
+    // the token's record, u and gate terms are loaded one token ahead, so their
+    // latency overlaps a token's work
+    float nkh = 0.f, nz = 0.f, nu = 0.f, ndg = 0.f, ndk = 0.f, nsc = 0.f;
+    auto fetch = [&](int t) {
+        if (t < t0) return;
+        const size_t tok = ((size_t)bh * T + t) * D;
+        const float *rt = rec + (size_t)t * REC;
+        if (tid < D) {
+            nkh = rt[tid];
+            nz = rt[D + tid];
+            nu = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
+            ndg = tokv[(size_t)t * 2 * D + tid];
+            ndk = tokv[(size_t)t * 2 * D + D + tid];
+        }
+        if (tid < 4) nsc = rt[4 * D + tid];
+    };
+    fetch(t1 - 1);
     for (int t = t1 - 1; t >= t0; --t) {
         if ((t + 1) % kCkB == 0 && t + 1 < t1)  // re-anchor: A after token t
             ld_row(am, ckp + (size_t)((t + 1) / kCkB) * CKF + (size_t)D * D + moff);
         const size_t tok = ((size_t)bh * T + t) * D;
-        const float *rt = rec + (size_t)t * REC;
-        float khj = 0.f;
+        const float khj = nkh;
         if (tid < D) {
-            khj = rt[tid];
             v_kh[vidx(tid)] = khj;
-            v_z[vidx(tid)] = rt[D + tid];
-            v_u[vidx(tid)] = io_to_f32(static_cast<const IO *>(p.u)[tok + tid]);
-            v_dg[vidx(tid)] = tokv[(size_t)t * 2 * D + tid];
-            s_dkh[tid] = tokv[(size_t)t * 2 * D + D + tid];
+            v_z[vidx(tid)] = nz;
+            v_u[vidx(tid)] = nu;
+            v_dg[vidx(tid)] = ndg;
+            s_dkh[tid] = ndk;
         }
-        if (tid < 4) s_sc[tid] = rt[4 * D + tid];
+        if (tid < 4) s_sc[tid] = nsc;
+        fetch(t - 1);
         __syncthreads();
         const float knorm = s_sc[0], beta = s_sc[1];
         const float dgi = v_dg[vidx(row)], khi = v_kh[vidx(row)], zi = v_z[vidx(row)], ui = v_u[vidx(row)];
