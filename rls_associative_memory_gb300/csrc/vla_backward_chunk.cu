@@ -45,6 +45,8 @@ struct Bc {
     static constexpr int NT = D * TPR;
     static constexpr int NW = NT / 32;
     static constexpr int VLEN = TPR * kPart;
+    // resident CTAs per SM the reverse sweeps are built for (d = 64: 168 registers)
+    static constexpr int MINB = D == 64 ? 3 : 1;
     static constexpr int REC = 4 * D + 4;      // per token: k_hat, z, alpha, r, |k|, beta, |g|, 1/den
     static constexpr int CKF = 2 * D * D + D;  // checkpoint: S, A, n
     static constexpr int LDC = D + 4;          // row stride of the column-sum buffers
@@ -330,7 +332,7 @@ __device__ __forceinline__ const float *end_slot(const BcArgs &a, const float *c
 // dq, dv, dg_t and the S and n parts of dk_hat; Omega_c
 // ---------------------------------------------------------------------------
 template <int D, typename IO>
-__global__ void __launch_bounds__(Bc<D>::NT) bc_spart_kernel(BcArgs a) {
+__global__ void __launch_bounds__(Bc<D>::NT, Bc<D>::MINB) bc_spart_kernel(BcArgs a) {
     using K = Bc<D>;
     constexpr int TPR = K::TPR, VLEN = K::VLEN, NW = K::NW, REC = K::REC, CKF = K::CKF, LDC = K::LDC;
     __shared__ __align__(16) float v_kh[VLEN], v_u[VLEN], v_fq[VLEN], v_z[VLEN], v_al[VLEN], v_dg[VLEN];
@@ -586,7 +588,7 @@ __global__ void __launch_bounds__(Bc<D>::NT) bc_chain_x_kernel(BcArgs a) {
 // du, dk (with the stored S and n parts of dk_hat), the antisymmetric sum
 // ---------------------------------------------------------------------------
 template <int D, typename IO>
-__global__ void __launch_bounds__(Bc<D>::NT) bc_final_kernel(BcArgs a) {
+__global__ void __launch_bounds__(Bc<D>::NT, Bc<D>::MINB) bc_final_kernel(BcArgs a) {
     using K = Bc<D>;
     constexpr int TPR = K::TPR, VLEN = K::VLEN, NW = K::NW, REC = K::REC, CKF = K::CKF;
     __shared__ __align__(16) float v_kh[VLEN], v_z[VLEN], v_u[VLEN], v_dg[VLEN], v_dz[VLEN];
@@ -753,10 +755,31 @@ struct BcLayout {
            xs_end = 0, xs0 = 0, asum = 0, tokv = 0, total = 0;
 };
 
+// The backward's chunk length.  Each of its three sweeps runs one C-token
+// chain per CTA, three CTAs per SM at d = 64 (about eight at d = 32), on 152
+// SMs: the fewest waves of the shortest chains, plus the chains along the
+// chunks (about six token steps a chunk).  For 16 units of 65536 tokens that
+// is 28 chunks of 2368 tokens, one wave, where the forward's 38 chunks of 1728
+// take two.
+int bc_chunk(int BH, int T, int d) {
+    const long long slots = 152LL * (d == 64 ? 3 : 8);
+    int best = 64;
+    long long best_cost = -1;
+    for (int m = 1; m <= (T + 63) / 64; ++m) {
+        const long long C = 64LL * m, NC = (T + C - 1) / C;
+        const long long cost = ((long long)BH * NC + slots - 1) / slots * C + 6 * NC;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = (int)C;
+        }
+    }
+    return best;
+}
+
 BcLayout bc_layout(int BH, int T, int d, bool bf16) {
     BcLayout b;
     if (BH <= 0 || T <= 0 || (d != 32 && d != 64)) return b;
-    b.L = chunk_layout(BH, T, d, 0, bf16 && d == 64);
+    b.L = chunk_layout(BH, T, d, bc_chunk(BH, T, d), bf16 && d == 64);
     if (b.L.NC < 2 || b.L.C % kCkB != 0 || b.L.C % b.L.CA != 0) return b;
     const size_t bh = (size_t)BH, t = (size_t)T, dd = (size_t)d * d, nc = (size_t)b.L.NC;
     b.NCK = (T + kCkB - 1) / kCkB;
@@ -809,7 +832,7 @@ cudaError_t launch_backward_chunk(const BwdParams &p, cudaStream_t st, bool *use
     f.wait_limit_ns = api_wait_limit_ns();
     f.ws = ws;
     f.ws_bytes = b.L.total;
-    f.chunk = 0;
+    f.chunk = b.L.C;
     // the SIMT passes: their fp32 gates keep the chunk-start states, from which the
     // sweeps below rebuild every token's state, at fp32 accuracy (the tensor-core
     // passes hand fp16 gates on, which is within the forward's bf16 bar but shows
