@@ -751,7 +751,7 @@ struct BcLayout {
     ChunkLayout L{};
     int NCK = 0;
     bool ok = false;
-    size_t o = 0, sT = 0, aT = 0, nT = 0, rec = 0, ckp = 0, maps = 0, dnsum = 0, dn_end = 0, dS_end = 0, om = 0,
+    size_t sT = 0, aT = 0, nT = 0, rec = 0, ckp = 0, maps = 0, dnsum = 0, dn_end = 0, dS_end = 0, om = 0,
            xs_end = 0, xs0 = 0, asum = 0, tokv = 0, total = 0;
 };
 
@@ -784,7 +784,6 @@ BcLayout bc_layout(int BH, int T, int d, bool bf16) {
     const size_t bh = (size_t)BH, t = (size_t)T, dd = (size_t)d * d, nc = (size_t)b.L.NC;
     b.NCK = (T + kCkB - 1) / kCkB;
     size_t off = al256(b.L.total);
-    b.o = off; off = al256(off + bh * t * d * (bf16 ? 2 : 4));
     b.sT = off; off = al256(off + bh * dd * 4);
     b.aT = off; off = al256(off + bh * dd * 4);
     b.nT = off; off = al256(off + bh * d * 4);
@@ -822,7 +821,7 @@ cudaError_t launch_backward_chunk(const BwdParams &p, cudaStream_t st, bool *use
     // the chunked forward: chunk-start states S^(c), M^(c), n^(c) in its workspace
     FwdParams f{};
     f.q = p.q; f.k = p.k; f.v = p.v; f.u = p.u;
-    f.o = ws + b.o;
+    f.o = nullptr;  // the output pass is skipped
     f.S0 = p.S0; f.A0 = p.A0; f.n0 = p.n0;
     f.S_T = reinterpret_cast<float *>(ws + b.sT);
     f.A_T = reinterpret_cast<float *>(ws + b.aT);
@@ -838,6 +837,7 @@ cudaError_t launch_backward_chunk(const BwdParams &p, cudaStream_t st, bool *use
     // passes hand fp16 gates on, which is within the forward's bf16 bar but shows
     // in the gradients)
     f.rows_tc = 0;
+    f.skip_out = 1;  // the sweeps recompute what they need of the readout
     int nf = 0;
     f.launches = &nf;
     cudaError_t e = launch_chunk(f, b.L, st);

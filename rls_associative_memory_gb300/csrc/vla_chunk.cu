@@ -1291,9 +1291,11 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     mark_launch(a.p, ++n, st);
     if (tc) {
         if ((e = launch_rows_tc(a, 1, st)) != cudaSuccess) return e;
-    } else {
+    } else if (!a.p.skip_out) {
         rows_kernel<D, IO, 1><<<(unsigned)(NC * BH), RowsCfg<D, 1>::NT, RowsSmem<D, IO>::total, st>>>(a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    } else {
+        return cudaSuccess;
     }
     mark_launch(a.p, ++n, st);
     return cudaSuccess;

@@ -36,6 +36,8 @@ struct FwdParams {
     size_t ws_bytes;
     int chunk;                  // chunk length (chunked kernel)
     int rows_tc;                // chunked kernel: state passes on the tensor cores where supported
+    int skip_out;               // chunked kernel, SIMT passes: no output pass (o not written); the
+                                // backward's forward, which needs only the chunk-start states
     void *wait_qv;              // optional cudaEvent_t: the stream waits for it before the first pass
                                 // that reads q or v (the chunked path's state pass)
     void *const *events;        // measurement hook: cudaEvent_t handles, or null
