@@ -63,6 +63,27 @@ __device__ __forceinline__ int elt(int i, int j) { return chk(i, j >> 2) + (j & 
 
 __device__ __forceinline__ float dphi(float x) { return x > 0.f ? 1.f : expf(x); }
 
+// Block-wide sum of four values over the 16 warps; every thread gets the four
+// totals.  Each warp reads the 16 warp partials once (lane l takes component
+// l mod 4 of partials l / 4 and l / 4 + 8) and finishes with shuffles: two
+// shared-memory passes and seven shuffles a warp, where reading all 16 float4
+// partials in every thread took 64 passes a warp.  red: 16 float4, not reused
+// before the next block barrier.
+__device__ __forceinline__ float4 block_sum4_w16(float v0, float v1, float v2, float v3, float4 *red) {
+    static_assert(NW == 16, "16 warps");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float r = warp_reduce4(v0, v1, v2, v3);
+    if ((lane & 7) == 0) reinterpret_cast<float *>(red)[warp * 4 + (lane >> 3)] = r;
+    __syncthreads();
+    const float *rf = reinterpret_cast<const float *>(red);
+    float x = rf[lane] + rf[32 + lane];  // component lane & 3 of partials lane / 4 and lane / 4 + 8
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 8);
+    x += __shfl_xor_sync(0xffffffffu, x, 16);
+    return make_float4(__shfl_sync(0xffffffffu, x, 0), __shfl_sync(0xffffffffu, x, 1),
+                       __shfl_sync(0xffffffffu, x, 2), __shfl_sync(0xffffffffu, x, 3));
+}
+
 template <typename IO>
 __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
     using L = Bw128;
@@ -133,7 +154,7 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
         float *rt = rec + (size_t)t * REC;
         const float qj = nq, kj = nk, vj = nv, uj = nu;
         fetch_in(t + 1);
-        const float4 r1 = block_sum4<NW>(kj * kj, 0.f, 0.f, 0.f, s_red);
+        const float4 r1 = block_sum4_w16(kj * kj, 0.f, 0.f, 0.f, s_red);
         const float knorm = sqrtf(r1.x);
         const float ks = 1.f / fmaxf(knorm, kEps);
         float fq = 0.f;
@@ -172,11 +193,11 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
             v_z[vidx(row)] = z;
             rt[D + row] = z;
         }
-        const float4 r2 = block_sum4<NW>(p1, p2, tid < D ? fq * nj : 0.f, 0.f, s_red + NW);
+        const float4 r2 = block_sum4_w16(p1, p2, tid < D ? fq * nj : 0.f, 0.f, s_red + NW);
         const float beta = 1.f / (1.f + r2.x);
         const float rden = 1.f / (r2.z + kEps);
         const float g = y - beta * r2.y * z;
-        const float4 r3 = block_sum4<NW>(part == 0 ? g * g : 0.f, 0.f, 0.f, 0.f, s_red + 2 * NW);
+        const float4 r3 = block_sum4_w16(part == 0 ? g * g : 0.f, 0.f, 0.f, 0.f, s_red + 2 * NW);
         const float gnorm = sqrtf(r3.x);
         const float inv = 1.f / fmaxf(gnorm, kEps);
         const float r = s_v[row] - sk;
@@ -302,7 +323,7 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
             if (p.dv) p.dv[tok + row] = dr;
         }
         const float o_i = num * rden;
-        const float4 R1 = block_sum4<NW>(part == 0 ? dOi * o_i : 0.f, part == 0 ? ri * dr : 0.f, 0.f, 0.f,
+        const float4 R1 = block_sum4_w16(part == 0 ? dOi * o_i : 0.f, part == 0 ? ri * dr : 0.f, 0.f, 0.f,
                                          s_red + 3 * NW);
         // ---- S2 (column order): S'^T dnum, dS'^T r, S^T(-dr); undo the state write; dS ----
         {
@@ -374,7 +395,7 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
             const float2 lo = mul2(zr2, da[2 * c]), hi = mul2(zr2, da[2 * c + 1]);
             rowc(sbuf, c) = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
-        const float4 R3 = block_sum4<NW>(part == 0 ? zrow * w : 0.f, 0.f, 0.f, 0.f, s_red + 4 * NW);
+        const float4 R3 = block_sum4_w16(part == 0 ? zrow * w : 0.f, 0.f, 0.f, 0.f, s_red + 4 * NW);
         // ---- P4 (columns): dA'^T z, dbeta, dz ----
         {
             float acc = 0.f;
@@ -418,7 +439,7 @@ __global__ void __launch_bounds__(NT, 1) backward128_kernel(BwdParams p) {
             if (p.du) p.du[tok + tid] = du_part + s_adz[tid];
             dkh = s_dkh[tid];
         }
-        const float4 R4 = block_sum4<NW>(tid < D ? khj * dkh : 0.f, 0.f, 0.f, 0.f, s_red + 5 * NW);
+        const float4 R4 = block_sum4_w16(tid < D ? khj * dkh : 0.f, 0.f, 0.f, 0.f, s_red + 5 * NW);
         if (tid < D && p.dk)
             p.dk[tok + tid] = knorm > kEps ? (dkh - khj * R4.x) / knorm : dkh / kEps;
         __syncthreads();  // the next token overwrites the shared vectors and partials
