@@ -39,7 +39,7 @@
 // the Grams of the earlier A-chunks: the same elimination on M^(c) against
 // the identity gives E = L^{-1} and D, then A = E^T D^{-1} E is one product on
 // the tensor cores (a sum of positive semi-definite terms, no cancellation).
-#include "vla_tc_common.cuh"
+#include "vla_tma.cuh"
 
 namespace vla {
 namespace {
@@ -49,7 +49,7 @@ using namespace tc;
 constexpr int kThreads = 256;
 
 struct GtLayout {
-    static constexpr size_t ctrl = 0;                       // mbarrier, TMEM slot, abort flag
+    static constexpr size_t ctrl = 0;                       // mbarriers, TMEM slot, abort flag
     static constexpr size_t uk = 1024;                      // [U; K] (128 rows, exact bf16)
     static constexpr size_t ah = uk + 2 * kTile;            // A hi, lo
     static constexpr size_t work = ah + 2 * kTile;          // 66 KB work area, by phase:
@@ -256,7 +256,8 @@ __device__ __forceinline__ void eliminate_rhs64(const float *gs, const float *w3
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a, const __grid_constant__ CUtensorMap tm_u,
+                                                               const __grid_constant__ CUtensorMap tm_k) {
     using L = GtLayout;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -264,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
     uint64_t *ebar = reinterpret_cast<uint64_t *>(smem + L::ctrl + 64);  // the elimination's 16 mbarriers
+    uint64_t *tbar = reinterpret_cast<uint64_t *>(smem + L::ctrl + 256);  // [U; K] tensor copies
     unsigned char *uk = smem + L::uk;
     unsigned char *a_hi = smem + L::ah, *a_lo = smem + L::ah + kTile;
     unsigned char *work = smem + L::work;  // work + i * kTile: tile slot i
@@ -290,13 +292,12 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     const bool act64 = lane < 16;
     const int r128 = 32 * qw + lane;                        // row in an M = 128 accumulator
     const size_t tok0 = ((size_t)bh * T + t0) * kD;
-    const __nv_bfloat16 *gu = static_cast<const __nv_bfloat16 *>(a.p.u) + tok0;
-    const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.p.k) + tok0;
     __half *galpha = reinterpret_cast<__half *>(static_cast<unsigned char *>(a.p.ws) + a.L.off_alpha) + tok0;
 
     if (tid == 0) {
         mbar_init(bar, 1);
         for (int b = 0; b < 16; ++b) mbar_init(&ebar[b], 32);
+        mbar_init(tbar, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -307,6 +308,19 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     const uint32_t tbase = *tslot;
     const uint32_t tq = tbase + ((uint32_t)(32 * qw) << 16);  // this warp's lane quarter
     constexpr uint32_t col_d1 = 0, col_d5 = 64, col_d2 = 128;
+
+    // [U; K] of sub-block sb by two tensor copies into the operand tile (U rows,
+    // then K rows; the maps fill tokens past T with zeros, and every A-chunk but
+    // the stream's last is whole sub-blocks).  Thread 0 issues; the copy of
+    // sub-block sb completes phase sb mod 2 of tbar.
+    int tma_issued = -1;  // (thread 0's bookkeeping) the last sub-block whose copy was issued
+    auto issue_in = [&](int sb) {
+        mbar_arrive_expect_tx(tbar, 2 * kTile);
+        tma_load_3d(uk, &tm_u, 0, t0 + sb * kSB, bh, tbar);
+        tma_load_3d(uk + kTile, &tm_k, 0, t0 + sb * kSB, bh, tbar);
+        tma_issued = sb;
+    };
+    if (tid == 0 && nsb > 0) issue_in(0);  // lands while the chunk-start A is formed
 
     // ---- A at the chunk start ----
     // c > 0: A = (M^(c))^{-1} = L^{-T} D^{-1} L^{-1}: elimination of M^(c),
@@ -366,18 +380,6 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         if (act64) put_row32(a_hi, a_lo, r64, 32 * hw, am);
     }
 
-    uint4 ru[2], rk[2];  // inputs of the next sub-block (token pt, features 16 pq ..)
-    // (always a valid token row, clamped: no select waits on the loads here;
-    // tokens past the chunk are zeroed where the values are used)
-    auto load_in = [&](int sb) {
-        const int t = min(sb * kSB + pt, ntok - 1);
-        const size_t off = (size_t)t * kD + 16 * pq;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            ru[h] = reinterpret_cast<const uint4 *>(gu + off)[h];
-            rk[h] = reinterpret_cast<const uint4 *>(gk + off)[h];
-        }
-    };
     uint32_t phase = (c > 0) ? 1u : 0u;  // the chunk-start product used phase 0
     auto round_wait = [&]() -> bool {
         const bool w = mbar_wait_bounded(bar, phase, a.p.wait_limit_ns, a.p.err);
@@ -388,15 +390,16 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         return *abort_flag == 0;
     };
 
-    // [U; K] of sub-block sb into its operand tile and its key norms into the
-    // sb-parity half of s_kn, s_ks (the other half still serves sub-block sb - 1);
-    // the tile is read by the tensor cores after a proxy fence and a barrier
-    auto stage_in = [&](int sb) {
-        const int nt = min(kSB, ntok - sb * kSB);
-        if (pt >= nt) ru[0] = ru[1] = rk[0] = rk[1] = make_uint4(0, 0, 0, 0);  // past the chunk
+    // the key norms of sub-block sb, from its K rows once its copy has landed,
+    // into the sb-parity half of s_kn, s_ks (the other half still serves
+    // sub-block sb - 1)
+    auto norms_in = [&](int sb) {
+        if (!mbar_wait_bounded(tbar, (uint32_t)(sb & 1), a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+        const uint4 k0 = *reinterpret_cast<const uint4 *>(uk + toff(64 + pt, 16 * pq));
+        const uint4 k1 = *reinterpret_cast<const uint4 *>(uk + toff(64 + pt, 16 * pq + 8));
         float kf[16];
-        unpack8(rk[0], kf);
-        unpack8(rk[1], kf + 8);
+        unpack8(k0, kf);
+        unpack8(k1, kf + 8);
         float ss = 0.f;
 #pragma unroll
         for (int m = 0; m < 16; ++m) ss = fmaf(kf[m], kf[m], ss);
@@ -407,16 +410,10 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             s_kn[64 * (sb & 1) + pt] = kn;
             s_ks[64 * (sb & 1) + pt] = 1.f / kn;
         }
-        *reinterpret_cast<uint4 *>(uk + toff(pt, 16 * pq)) = ru[0];
-        *reinterpret_cast<uint4 *>(uk + toff(pt, 16 * pq + 8)) = ru[1];
-        *reinterpret_cast<uint4 *>(uk + toff(64 + pt, 16 * pq)) = rk[0];
-        *reinterpret_cast<uint4 *>(uk + toff(64 + pt, 16 * pq + 8)) = rk[1];
-        fence_proxy_async_smem();
     };
 
     bool ok = true;
-    load_in(0);
-    if (nsb > 0) stage_in(0);
+    if (nsb > 0) norms_in(0);
     __syncthreads();
     for (int sb = 0; sb < nsb; ++sb) {
         const int nt = min(kSB, ntok - sb * kSB);
@@ -459,6 +456,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             ok = false;
             break;
         }
+        // round 2 has read [U; K]: the next sub-block's copy lands during the elimination
+        if (tid == 0 && sb + 1 < nsb) issue_in(sb + 1);
         // ---- Y_hat rows s and I + G (fp32) for the elimination ----
         {
             float v[32];
@@ -487,9 +486,6 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
         // ---- elimination of [I + G | W^T | Y_hat]: Z^T, P and beta, and round 4's tiles ----
         eliminate_rhs64(g32, w32, y32, reinterpret_cast<float *>(work), s_beta, kn_sb, work, ebar,
                         (uint32_t)(sb & 1), a, abort_flag);
-        // the next sub-block's inputs: issued after the elimination, so that their
-        // registers are not live through it (round 4 hides the latency)
-        load_in(sb + 1);
         fence_proxy_async_smem();
         __syncthreads();
         // ---- R4: D1[k rows] += E'^T Z^T (A MN-major, atoms [-(beta Z)^T | E']: M = 128,
@@ -508,9 +504,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
             mma_k64<true, true>(tbase + col_d5, smem_u32(bz2), smem_u32(zt0), id64, true);
             umma_commit(bar);
         }
-        // the next sub-block's [U; K] while round 4 runs ([U; K] was last read by
-        // round 2; its loads were issued after the elimination)
-        if (sb + 1 < nsb) stage_in(sb + 1);
+        // the next sub-block's key norms while round 4 runs (its copy has landed by now)
+        if (sb + 1 < nsb) norms_in(sb + 1);
         if (!round_wait()) {
             ok = false;
             break;
@@ -549,6 +544,8 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
     }
     if (!ok) {
         if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
+        // a copy issued for a sub-block that was never reached lands before the CTA ends
+        if (tid == 0 && tma_issued >= 0) (void)mbar_wait_bounded(tbar, (uint32_t)(tma_issued & 1), a.p.wait_limit_ns, a.p.err);
     } else if (c == NCA - 1) {
         float am[32];
         tmem_ld32(tq + col_d5 + 32 * hw, am);
@@ -566,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 2) gates_tc_kernel(ChunkArgs a) {
 }  // namespace
 
 bool gates_tc_supported(const FwdParams &p, const ChunkLayout &L) {
-    return p.d == kD && p.io_bf16 && L.CA % kSB == 0 && L.yh;
+    return p.d == kD && p.io_bf16 && L.CA % kSB == 0 && L.yh && tile_maps_available();
 }
 
 cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream) {
@@ -575,7 +572,10 @@ cudaError_t launch_gates_tc(const ChunkArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long long grid = (long long)a.L.NCA * (a.bh_n > 0 ? a.bh_n : a.p.BH);
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    gates_tc_kernel<<<(unsigned)grid, kThreads, bytes, stream>>>(a);
+    CUtensorMap tm_u, tm_k;
+    if (!make_tile_map(&tm_u, a.p.u, a.p.BH, a.p.T) || !make_tile_map(&tm_k, a.p.k, a.p.BH, a.p.T))
+        return cudaErrorInvalidValue;
+    gates_tc_kernel<<<(unsigned)grid, kThreads, bytes, stream>>>(a, tm_u, tm_k);
     return cudaGetLastError();
 }
 

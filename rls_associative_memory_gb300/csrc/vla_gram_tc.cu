@@ -13,9 +13,7 @@
 // are exact in fp32 and only the accumulation (in TMEM) rounds.  Two
 // threads a token (32 features each) sum phi(k_hat) on the CUDA cores.  The 3-D
 // tensor maps (features, tokens, b*h) fill tokens past T with zeros.
-#include <cuda.h>
-
-#include "vla_tc_common.cuh"
+#include "vla_tma.cuh"
 
 namespace vla {
 namespace {
@@ -32,14 +30,6 @@ struct GrLayout {
     static constexpr size_t total = tiles + (size_t)kStages * 2 * kTile;
 };
 static_assert(128 * 33 * 4 <= kStages * 2 * kTile, "the reduction buffer fits over the tiles");
-
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
 
 __global__ void __launch_bounds__(kGThreads) gram_tma_kernel(ChunkArgs a, const __grid_constant__ CUtensorMap tm_u,
                                                             const __grid_constant__ CUtensorMap tm_k) {
@@ -206,9 +196,11 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D map of a [BH][T][64] bf16 tensor: boxes of 64 tokens x 64 features of
-// one (b, h), 128-byte swizzle, zeros past T.
-bool make_map(CUtensorMap *m, const void *base, int BH, int T) {
+}  // namespace
+
+bool tile_maps_available() { return encode_fn() != nullptr; }
+
+bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)T, (cuuint64_t)BH};
@@ -220,15 +212,14 @@ bool make_map(CUtensorMap *m, const void *base, int BH, int T) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
 bool gram_tma_supported(const FwdParams &p, const ChunkLayout &L) {
     return p.d == kD && p.io_bf16 && L.CA % kSB == 0 && L.yh && encode_fn() != nullptr;
 }
 
 cudaError_t launch_gram_tma(const ChunkArgs &a, cudaStream_t stream) {
     CUtensorMap tm_u, tm_k;
-    if (!make_map(&tm_u, a.p.u, a.p.BH, a.p.T) || !make_map(&tm_k, a.p.k, a.p.BH, a.p.T)) return cudaErrorInvalidValue;
+    if (!make_tile_map(&tm_u, a.p.u, a.p.BH, a.p.T) || !make_tile_map(&tm_k, a.p.k, a.p.BH, a.p.T))
+        return cudaErrorInvalidValue;
     constexpr size_t bytes = GrLayout::total + 1024;  // + alignment slack
     cudaError_t e = cudaFuncSetAttribute(gram_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
