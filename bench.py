@@ -71,7 +71,7 @@ KERNEL_SOURCES = {
     "seq32_kernel": ["vla_seq32.cu"],
     "gates_tc_kernel": ["vla_gates_tc.cu", "vla_tc_common.cuh", "vla_tma.cuh"],
     "rows_tc_kernel": ["vla_chunk_tc.cu", "vla_tc_common.cuh"],
-    "tc128_queue_kernel": ["vla_gates_tc128.cuh", "vla_rows_tc128.cuh", "vla_tc128.cu", "vla_tc_common.cuh"],
+    "tc128_queue_kernel": ["vla_gates_tc128.cuh", "vla_rows_tc128.cuh", "vla_tc128.cu", "vla_tc_common.cuh", "vla_tma.cuh"],
     "decode_kernel": ["vla_decode.cu"],
 }
 

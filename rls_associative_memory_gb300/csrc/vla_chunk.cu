@@ -37,6 +37,10 @@
 #include "vla_internal.cuh"
 
 namespace vla {
+
+// Whether the driver's tensor-map encoder could be found (vla_gram_tc.cu): the
+// tensor-core passes stage their inputs by tiled tensor copies.
+bool tile_maps_available();
 namespace {
 
 constexpr int kTT = 16;  // tokens per staged tile
@@ -413,7 +417,6 @@ template <int D>
 struct RowCfg {
     static constexpr int TPR = D / 32;
     static constexpr int NT = D * TPR;
-    static constexpr int NW = NT / 32;
     static constexpr int VLEN = TPR * kPart;
 };
 
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(GatesCfg<D>::NT) gates_kernel(ChunkArgs a) {
     using R = GatesCfg<D>;
     using Lo = GatesSmem<D, IO>;
     constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW, CPT = R::CPT, RPT = R::RPT, RS = R::RSTRIDE;
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 16);
     IO *raw = reinterpret_cast<IO *>(smem + Lo::raw);
@@ -726,7 +729,7 @@ __global__ void __launch_bounds__(RowsCfg<D, MODE>::NT) rows_kernel(ChunkArgs a)
     constexpr int TPR = R::TPR, VLEN = R::VLEN, NW = R::NW, RPT = R::RPT;
     constexpr int ROW2 = D / 2;  // second row of a thread in MODE 1 with RPT = 2
     constexpr int NIO = (MODE == 0) ? 2 : 3;  // k, v (+ q)
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 16);
     IO *raw = reinterpret_cast<IO *>(smem + Lo::raw);
@@ -1017,7 +1020,7 @@ __global__ void __launch_bounds__(256) chain_kernel(ChunkArgs a) {
     constexpr int NS = Lo::NS, kRB = Lo::RB;
     constexpr int OPT = kRB * D / 256;  // outputs per thread: one row, OPT consecutive columns
     static_assert(OPT >= 1, "at least one output per thread");
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lo::bars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Lo::bars + 8 * NS);
     float *sP = reinterpret_cast<float *>(smem + Lo::P);
@@ -1212,7 +1215,7 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
         return cudaErrorInvalidConfiguration;
     cudaError_t e;
     if constexpr (D == 128 && sizeof(IO) == 2) {
-        if (a.p.rows_tc && a.L.NC == 1 && a.L.NCA == 1) {
+        if (a.p.rows_tc && a.L.NC == 1 && a.L.NCA == 1 && tile_maps_available()) {
             // one chunk per unit: the gates from A0, then the state pass on S itself
             // (writes o); both in one queue launch unless q and v are still arriving
             mark_launch(a.p, 0, st);
@@ -1491,7 +1494,7 @@ static ChunkLayout layout_for(int BH, int T, int d, int C, int CA, bool tc) {
 bool chunk_tc_parts_supported(const FwdParams &p, const ChunkLayout &L) { return tc_parts_ok(p, L); }
 
 bool chunk_tc128_parts_supported(const FwdParams &p, const ChunkLayout &L) {
-    return p.d == 128 && p.io_bf16 && p.rows_tc && L.NC == 1 && L.NCA == 1;
+    return p.d == 128 && p.io_bf16 && p.rows_tc && L.NC == 1 && L.NCA == 1 && tile_maps_available();
 }
 
 cudaError_t launch_chunk_tc128_part(const FwdParams &p, const ChunkLayout &L, int part, int bh_lo, int bh_n,

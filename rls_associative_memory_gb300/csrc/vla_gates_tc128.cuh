@@ -33,7 +33,7 @@
 // The body of one CTA's work for one unit, included by vla_tc128.cu.
 #pragma once
 
-#include "vla_tc_common.cuh"
+#include "vla_tma.cuh"
 
 namespace vla {
 namespace g128 {
@@ -208,10 +208,12 @@ __device__ __forceinline__ void eliminate_rhs128(const float *gs, const float *w
 
 // The gates of unit bh, by one CTA of kThreads threads with G2Layout::total +
 // 1024 bytes of dynamic shared memory at smem_raw.
-__device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, unsigned char *smem_raw) {
+__device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, unsigned char *smem_raw,
+                                                 const CUtensorMap *tm_u, const CUtensorMap *tm_k) {
     using L = G2Layout;
     unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::ctrl);
+    uint64_t *tbar = reinterpret_cast<uint64_t *>(smem + L::ctrl + 64);  // [U; K] tensor copies
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + L::ctrl + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::ctrl + 12);
     unsigned char *uk = smem + L::uk;  // + 2 kTile * h: features 64 h ..
@@ -238,12 +240,11 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
     const bool act64 = lane < 16;
     const int r128 = 32 * qw + lane;                        // row in an M = 128 accumulator
     const size_t tok0 = (size_t)bh * T * kD2;
-    const __nv_bfloat16 *gu = static_cast<const __nv_bfloat16 *>(a.p.u) + tok0;
-    const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(a.p.k) + tok0;
     __half *galpha = reinterpret_cast<__half *>(static_cast<unsigned char *>(a.p.ws) + a.L.off_alpha) + tok0;
 
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(tbar, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -254,6 +255,22 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
     const uint32_t tbase = *tslot;
     const uint32_t tq = tbase + ((uint32_t)(32 * qw) << 16);  // this warp's lane quarter
     constexpr uint32_t col_a = 0, col_d1 = 128, col_d2 = 256;
+
+    // [U; K] of sub-block sb by four tiled tensor copies (U, then K, of features
+    // 0..63, then of 64..127) into the two feature tiles; the maps fill tokens
+    // past T with zeros.  Thread 0 issues; the copies of sub-block sb complete
+    // phase sb mod 2 of tbar.
+    int tma_issued = -1;  // (thread 0's bookkeeping) the last sub-block whose copies were issued
+    auto issue_in = [&](int sb) {
+        mbar_arrive_expect_tx(tbar, 4 * kTile);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            tma_load_3d(uk + 2 * kTile * h, tm_u, 64 * h, sb * kSB, bh, tbar);
+            tma_load_3d(uk + 2 * kTile * h + kTile, tm_k, 64 * h, sb * kSB, bh, tbar);
+        }
+        tma_issued = sb;
+    };
+    if (tid == 0 && nsb > 0) issue_in(0);  // lands while A0 is set up
 
     // ---- A at the start (A0, or I / lambda0): fp32 in TMEM, bf16 hi/lo tiles ----
     {
@@ -280,16 +297,6 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
         tc_fence_before();
     }
 
-    uint4 ru[4], rk[4];  // inputs of the next sub-block (token pt, features 32 pq ..)
-    auto load_in = [&](int sb) {
-        const int t = min(sb * kSB + pt, T - 1);
-        const size_t off = (size_t)t * kD2 + 32 * pq;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            ru[h] = reinterpret_cast<const uint4 *>(gu + off)[h];
-            rk[h] = reinterpret_cast<const uint4 *>(gk + off)[h];
-        }
-    };
     uint32_t phase = 0;
     auto round_wait = [&]() -> bool {
         const bool w = mbar_wait_bounded(bar, phase, a.p.wait_limit_ns, a.p.err);
@@ -299,18 +306,18 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
         tc_fence_after();
         return *abort_flag == 0;
     };
-    // [U; K] of sub-block sb into its two feature tiles, key norms into the sb-parity halves
-    auto stage_in = [&](int sb) {
-        const int nt = min(kSB, T - sb * kSB);
-        if (pt >= nt) {
-#pragma unroll
-            for (int h = 0; h < 4; ++h) ru[h] = rk[h] = make_uint4(0, 0, 0, 0);
-        }
+    // the key norms of sub-block sb, from its K rows once its copies have landed,
+    // into the sb-parity halves
+    auto norms_in = [&](int sb) {
+        if (!mbar_wait_bounded(tbar, (uint32_t)(sb & 1), a.p.wait_limit_ns, a.p.err)) *abort_flag = 1;
+        const unsigned char *tile = uk + 2 * kTile * (pq >> 1);
+        const int k0 = 32 * (pq & 1);
         float ss = 0.f;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
+            const uint4 rk = *reinterpret_cast<const uint4 *>(tile + toff(64 + pt, k0 + 8 * h));
             float kf[8];
-            unpack8(rk[h], kf);
+            unpack8(rk, kf);
 #pragma unroll
             for (int m = 0; m < 8; ++m) ss = fmaf(kf[m], kf[m], ss);
         }
@@ -321,19 +328,10 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
             s_kn[64 * (sb & 1) + pt] = kn;
             s_ks[64 * (sb & 1) + pt] = 1.f / kn;
         }
-        unsigned char *tile = uk + 2 * kTile * (pq >> 1);
-        const int k0 = 32 * (pq & 1);
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            *reinterpret_cast<uint4 *>(tile + toff(pt, k0 + 8 * h)) = ru[h];
-            *reinterpret_cast<uint4 *>(tile + toff(64 + pt, k0 + 8 * h)) = rk[h];
-        }
-        fence_proxy_async_smem();
     };
 
     bool ok = true;
-    load_in(0);
-    if (nsb > 0) stage_in(0);
+    if (nsb > 0) norms_in(0);
     fence_proxy_async_smem();
     __syncthreads();
     constexpr uint32_t id_r1 = idesc_bf16_f32(128, 128);
@@ -393,6 +391,8 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
             ok = false;
             break;
         }
+        // round 2 has read [U; K]: the next sub-block's copies land during the elimination
+        if (tid == 0 && sb + 1 < nsb) issue_in(sb + 1);
         // ---- Y_hat rows s and I + G (fp32) for the elimination ----
         {
             float v[32];
@@ -421,7 +421,6 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
         // ---- elimination: Z^T, P, beta and round 4's tiles ----
         eliminate_rhs128(g32, w32, y32, reinterpret_cast<float *>(work + L::kPub),
                          reinterpret_cast<float *>(work + L::kSrow), s_beta, kn_sb, zt, bz, ep);
-        load_in(sb + 1);
         fence_proxy_async_smem();
         __syncthreads();
         // ---- R4: D1[k rows] += E'^T Z^T (A MN-major, atoms [-(beta Z)^T f0 | E'] 32 KB apart: the
@@ -439,7 +438,7 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
             mma_k64<true, true>(tbase + col_a, smem_u32(bz[2]), smem_u32(zt[0]), id_r1, true, kTile, kTile);
             umma_commit(bar);
         }
-        if (sb + 1 < nsb) stage_in(sb + 1);  // [U; K] was last read by round 2
+        if (sb + 1 < nsb) norms_in(sb + 1);  // its copies have landed by now
         if (!round_wait()) {
             ok = false;
             break;
@@ -484,6 +483,8 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
     }
     if (!ok) {
         if (tid == 0) (void)mbar_wait_bounded(bar, phase ^ 1u, a.p.wait_limit_ns, a.p.err);
+        // copies issued for a sub-block that was never reached land before the CTA ends
+        if (tid == 0 && tma_issued >= 0) (void)mbar_wait_bounded(tbar, (uint32_t)(tma_issued & 1), a.p.wait_limit_ns, a.p.err);
     } else {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -498,7 +499,10 @@ __device__ __forceinline__ void gates_tc128_body(const ChunkArgs &a, int bh, uns
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 512);
-    if (tid == 0) mbar_inval(bar);  // (a later job of this CTA may lay out its memory otherwise)
+    if (tid == 0) {  // (a later job of this CTA may lay out its memory otherwise)
+        mbar_inval(bar);
+        mbar_inval(tbar);
+    }
 }
 
 }  // namespace g128

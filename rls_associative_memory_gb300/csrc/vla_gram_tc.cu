@@ -200,11 +200,11 @@ EncodeTiledFn encode_fn() {
 
 bool tile_maps_available() { return encode_fn() != nullptr; }
 
-bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T) {
+bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T, int d) {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)T, (cuuint64_t)BH};
-    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)T * kD * 2};
+    if (!fn || (d != 64 && d != 128)) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
     const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)kSB, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,

@@ -26,9 +26,10 @@ constexpr size_t kRowsSmem = r128::R2Layout::total + 1024;
 constexpr size_t kQueueSmem = kGatesSmem > kRowsSmem ? kGatesSmem : kRowsSmem;
 static_assert(kQueueSmem <= 227 * 1024, "one CTA per SM");
 
-__global__ void __launch_bounds__(kT128Threads, 1) gates_tc128_kernel(ChunkArgs a) {
+__global__ void __launch_bounds__(kT128Threads, 1) gates_tc128_kernel(ChunkArgs a, const __grid_constant__ CUtensorMap tm_u,
+                                                                   const __grid_constant__ CUtensorMap tm_k) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    g128::gates_tc128_body(a, a.bh_lo + (int)blockIdx.x, smem_raw);
+    g128::gates_tc128_body(a, a.bh_lo + (int)blockIdx.x, smem_raw, &tm_u, &tm_k);
 }
 
 __global__ void __launch_bounds__(kT128Threads, 1) rows_tc128_kernel(ChunkArgs a) {
@@ -63,7 +64,9 @@ __device__ bool wait_flag(const unsigned *flag, long long limit_ns, int *err) {
 
 // ctl[0]: the next job; ctl[1 + j]: unit bh_lo + j's gates are published.  Both
 // zero at launch.
-__global__ void __launch_bounds__(kT128Threads, 1) tc128_queue_kernel(ChunkArgs a, unsigned *ctl) {
+__global__ void __launch_bounds__(kT128Threads, 1) tc128_queue_kernel(ChunkArgs a, unsigned *ctl,
+                                                                   const __grid_constant__ CUtensorMap tm_u,
+                                                                   const __grid_constant__ CUtensorMap tm_k) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the job and the wait's outcome in the last 16 bytes of the allocation, past
     // any job's region (each body aligns its start within the 1024 bytes of slack)
@@ -76,7 +79,7 @@ __global__ void __launch_bounds__(kT128Threads, 1) tc128_queue_kernel(ChunkArgs 
         const int job = *s_job;
         if (job >= 2 * n) break;
         if (job < n) {
-            g128::gates_tc128_body(a, a.bh_lo + job, smem_raw);
+            g128::gates_tc128_body(a, a.bh_lo + job, smem_raw, &tm_u, &tm_k);
             __threadfence();  // this thread's stores of the gates, before the flag
             __syncthreads();
             if (threadIdx.x == 0) st_release_gpu(ctl + 1 + job, 1u);
@@ -96,7 +99,10 @@ cudaError_t launch_gates_tc128(const ChunkArgs &a, cudaStream_t stream) {
                                          (int)kGatesSmem);
     if (e != cudaSuccess) return e;
     const int n = a.bh_n > 0 ? a.bh_n : a.p.BH;
-    gates_tc128_kernel<<<(unsigned)n, kT128Threads, kGatesSmem, stream>>>(a);
+    CUtensorMap tm_u, tm_k;
+    if (!make_tile_map(&tm_u, a.p.u, a.p.BH, a.p.T, 128) || !make_tile_map(&tm_k, a.p.k, a.p.BH, a.p.T, 128))
+        return cudaErrorInvalidValue;
+    gates_tc128_kernel<<<(unsigned)n, kT128Threads, kGatesSmem, stream>>>(a, tm_u, tm_k);
     return cudaGetLastError();
 }
 
@@ -128,7 +134,10 @@ cudaError_t launch_tc128_queue(const ChunkArgs &a0, cudaStream_t stream) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     long long grid = (long long)sms * per_sm;
     if (grid > 2LL * a.p.BH) grid = 2LL * a.p.BH;
-    tc128_queue_kernel<<<(unsigned)grid, kT128Threads, kQueueSmem, stream>>>(a, ctl);
+    CUtensorMap tm_u, tm_k;
+    if (!make_tile_map(&tm_u, a.p.u, a.p.BH, a.p.T, 128) || !make_tile_map(&tm_k, a.p.k, a.p.BH, a.p.T, 128))
+        return cudaErrorInvalidValue;
+    tc128_queue_kernel<<<(unsigned)grid, kT128Threads, kQueueSmem, stream>>>(a, ctl, tm_u, tm_k);
     return cudaGetLastError();
 }
 

@@ -9,10 +9,11 @@
 
 namespace vla {
 
-// Map of a [BH][T][64] bf16 tensor at `base`: boxes of 64 tokens x 64 features
-// of one (b, h), 128-byte swizzle, zeros past T.  False when the driver's
-// encoder is unavailable or rejects the arguments.
-bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T);
+// Map of a [BH][T][d] bf16 tensor at `base` (d = 64 or 128): boxes of 64
+// tokens x 64 features of one (b, h) (feature offset x a multiple of 64),
+// 128-byte swizzle, zeros past T.  False when the driver's encoder is
+// unavailable or rejects the arguments.
+bool make_tile_map(CUtensorMap *m, const void *base, int BH, int T, int d = 64);
 // Whether the driver's tensor-map encoder could be found.
 bool tile_maps_available();
 
