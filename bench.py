@@ -59,8 +59,8 @@ TRAFFIC = {
     # of a unit's two passes do not depend on how many units a launch holds)
     # decode step, state in place: one launch at full size (one ncu pass of the full set)
     ("decode", "decode", "decode_kernel"): {"bytes": 68.699136e6 + 13.662208e6, "src_sha": "fa5b569b82b39c4d"},
-    ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.733312e6 + 126.918144e6),
-                                                    "src_sha": "99228bae6f0f1461"},
+    ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.700800e6 + 127.022336e6),
+                                                    "src_sha": "8e2fc763b85a164a"},
 }
 
 
