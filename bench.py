@@ -53,7 +53,7 @@ TRAFFIC = {
     # sequential kernel at d = 32, recall8 workload: one full-size launch (one ncu pass)
     ("seq", "recall8", "seq32_kernel"): {"bytes": 268.589312e6 + 50.995200e6, "src_sha": "36a8d00592a68bf1"},
     # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.227712e6 + 98.069248e6, "src_sha": "8220b20275eb9b97"},
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.227712e6 + 98.069248e6, "src_sha": "b34d78b4170caf92"},
     ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.107456e6 + 246.773504e6, "src_sha": "348d9146873b85b1"},
     # d = 128 queue launch, batched workload: at B=8 (128 units), scaled x4 to B=32 (the bytes
     # of a unit's two passes do not depend on how many units a launch holds)
