@@ -49,16 +49,16 @@ FP32_PEAK_TFLOPS = N_SM * 128 * 2 * SM_MAX_GHZ / 1e3
 # adds only host declarations re-keys the records without a new capture.)
 TRAFFIC = {
     # sequential kernel, long stream: 135.3 + 18.9 MB at T=16384, scaled x4 to T=65536
-    ("seq", "long", "seq_kernel"): {"bytes": 4 * (135.331840e6 + 18.873600e6), "src_sha": "c7b1da03ef2a882b"},
+    ("seq", "long", "seq_kernel"): {"bytes": 4 * (135.000064e6 + 19.173888e6), "src_sha": "8029d371d74d05f3"},
     # sequential kernel at d = 32, recall8 workload: one full-size launch (one ncu pass)
-    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.589312e6 + 50.995200e6, "src_sha": "36a8d00592a68bf1"},
+    ("seq", "recall8", "seq32_kernel"): {"bytes": 268.476160e6 + 50.967040e6, "src_sha": "c6686e0ee56813b5"},
     # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
     ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.227712e6 + 98.069248e6, "src_sha": "b34d78b4170caf92"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.107456e6 + 246.773504e6, "src_sha": "348d9146873b85b1"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.124096e6 + 249.843200e6, "src_sha": "0e96f5eea2a9d97e"},
     # d = 128 queue launch, batched workload: at B=8 (128 units), scaled x4 to B=32 (the bytes
     # of a unit's two passes do not depend on how many units a launch holds)
     # decode step, state in place: one launch at full size (one ncu pass of the full set)
-    ("decode", "decode", "decode_kernel"): {"bytes": 68.699136e6 + 13.662208e6, "src_sha": "fa5b569b82b39c4d"},
+    ("decode", "decode", "decode_kernel"): {"bytes": 68.697600e6 + 12.946432e6, "src_sha": "377e9a67c43a05a7"},
     ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.700800e6 + 127.022336e6),
                                                     "src_sha": "8e2fc763b85a164a"},
 }
