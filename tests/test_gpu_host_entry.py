@@ -221,21 +221,31 @@ def test_host_entry_sequential_ranges(B, H, T, download):
     compare({"o": ho.numpy(), "S_T": hS.numpy(), "A_T": hA.numpy(), "n_T": hn.numpy()}, oracle_ref(x), "f32")
 
 
-def test_host_entry_halves_with_their_own_chunks():
+@pytest.mark.parametrize("init", [False, True], ids=["default_state", "given_state"])
+def test_host_entry_halves_with_their_own_chunks(init):
     """1 x 16 x 65536 (the long stream's shape): the first half (8 units) at the
     whole problem's chunk length, then two ranges of 4 at the second half's
     own, each bit-identical to vla_forward on its units with its chunk length;
-    the last unit of every range against the oracle."""
-    x = make_inputs(1, 16, 65536, 64, "bf16", seed=77)
+    the last unit of every range against the oracle.  With a given state each
+    half inverts its own A0 before its front."""
+    x = make_inputs(1, 16, 65536, 64, "bf16", seed=77, u_scale=0.5)
     q, k, v, u = to_device(x)
+    S0 = A0 = n0 = None
+    ref0 = {}
+    if init:
+        pre = make_inputs(1, 16, 200, 64, "bf16", seed=78, u_scale=0.5)
+        st = oracle_ref(pre)
+        S0, A0, n0 = (torch.from_numpy(st[nm]).float().cuda().contiguous() for nm in ("S_T", "A_T", "n_T"))
+        ref0 = dict(S0=st["S_T"], A0=st["A_T"], n0=st["n_T"])
     ranges = vla.vla_host_ranges(1, 16, 65536, 64, vla.VLA_BF16, vla.VLA_KERNEL_AUTO)
     assert len({r[2] for r in ranges}) == 2, ranges  # the halves do not share one chunk length
-    o_ref, S_ref, A_ref, n_ref = _device_reference(q, k, v, u, x.lambda0, vla.VLA_KERNEL_AUTO)
+    o_ref, S_ref, A_ref, n_ref = _device_reference(q, k, v, u, x.lambda0, vla.VLA_KERNEL_AUTO, S0=S0, A0=A0, n0=n0)
     torch.cuda.synchronize()
-    got = _host_call(x, vla.VLA_KERNEL_AUTO)
+    got = _host_call(x, vla.VLA_KERNEL_AUTO, S0=S0, A0=A0, n0=n0)
     assert (got["o"] == o_ref.float().cpu().numpy()).all()
     assert (got["S_T"] == S_ref.cpu().numpy()).all() and (got["A_T"] == A_ref.cpu().numpy()).all()
     for lo, n, C, CA in ranges:
         b, h = divmod(lo + n - 1, 16)
-        ref = oracle_ref(x.slice_heads(slice(b, b + 1), slice(h, h + 1)))  # the range's last unit
+        sub0 = {key: val[b:b + 1, h:h + 1] for key, val in ref0.items()}
+        ref = oracle_ref(x.slice_heads(slice(b, b + 1), slice(h, h + 1)), **sub0)  # the range's last unit
         compare({key: val[b:b + 1, h:h + 1] for key, val in got.items()}, ref, "bf16")
