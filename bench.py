@@ -52,13 +52,14 @@ TRAFFIC = {
     ("seq", "long", "seq_kernel"): {"bytes": 4 * (135.000064e6 + 19.173888e6), "src_sha": "8029d371d74d05f3"},
     # sequential kernel at d = 32, recall8 workload: one full-size launch (one ncu pass)
     ("seq", "recall8", "seq32_kernel"): {"bytes": 268.476160e6 + 50.967040e6, "src_sha": "c6686e0ee56813b5"},
-    # tensor-core path, long stream: one full-size launch each (T=65536; one ncu pass)
-    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.227712e6 + 98.069248e6, "src_sha": "b34d78b4170caf92"},
-    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.124096e6 + 249.843200e6, "src_sha": "0e96f5eea2a9d97e"},
+    # tensor-core path at d = 64, long stream (two launches): one full-size launch each
+    # (T=65536; one ncu pass)
+    ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.221824e6 + 101.037824e6, "src_sha": "2bd40b3ddad0f1e0"},
+    ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.165824e6 + 246.693120e6, "src_sha": "9e62ca08836996eb"},
+    # decode step, state in place: one launch at full size (one ncu pass)
+    ("decode", "decode", "decode_kernel"): {"bytes": 68.697600e6 + 12.946432e6, "src_sha": "377e9a67c43a05a7"},
     # d = 128 queue launch, batched workload: at B=8 (128 units), scaled x4 to B=32 (the bytes
     # of a unit's two passes do not depend on how many units a launch holds)
-    # decode step, state in place: one launch at full size (one ncu pass of the full set)
-    ("decode", "decode", "decode_kernel"): {"bytes": 68.697600e6 + 12.946432e6, "src_sha": "377e9a67c43a05a7"},
     ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.700800e6 + 127.022336e6),
                                                     "src_sha": "8e2fc763b85a164a"},
 }
@@ -69,8 +70,10 @@ TRAFFIC = {
 KERNEL_SOURCES = {
     "seq_kernel": ["vla_seq.cu"],
     "seq32_kernel": ["vla_seq32.cu"],
-    "gates_tc_kernel": ["vla_gates_tc.cu", "vla_tc_common.cuh", "vla_tma.cuh"],
-    "rows_tc_kernel": ["vla_chunk_tc.cu", "vla_tc_common.cuh"],
+    "gates_tc_kernel": ["vla_gates_tc.cu", "vla_gates_tc.cuh", "vla_tc_common.cuh", "vla_tma.cuh"],
+    "rows_tc_kernel": ["vla_chunk_tc.cu", "vla_rows_tc.cuh", "vla_tc_common.cuh"],
+    "tc64_queue_kernel": ["vla_tc64_queue.cu", "vla_gates_tc.cuh", "vla_rows_tc.cuh", "vla_tc_common.cuh",
+                          "vla_tma.cuh"],
     "tc128_queue_kernel": ["vla_gates_tc128.cuh", "vla_rows_tc128.cuh", "vla_tc128.cu", "vla_tc_common.cuh", "vla_tma.cuh"],
     "decode_kernel": ["vla_decode.cu"],
 }
@@ -98,9 +101,10 @@ def kernel_src_hash(kernel_name: str) -> str:
 # transitions, the chain - counts zero), and so is every input and output
 # byte.  engine is the pipe the kernel's arithmetic runs on: "alu" (FP32 CUDA
 # cores) or "tensor" (bf16 tcgen05; its roofline takes the bf16 tensor peak).
-def kernel_plan(kname, d, io_dtype="bf16", units=0):
+def kernel_plan(kname, d, io_dtype="bf16", units=0, launches=0):
     """[(kernel, algorithmic flops, algorithmic bytes per token-head, engine)] in launch order
-    (units: the (b, h) units of the batch)."""
+    (units: the (b, h) units of the batch; launches: the launches of one step, which tell
+    the d = 64 tensor-core path's one queue launch of both passes from two launches)."""
     io = 2 if io_dtype == "bf16" else 4
     full = 12 * d * d + 16 * d
     if kname == "seq":
@@ -123,9 +127,15 @@ def kernel_plan(kname, d, io_dtype="bf16", units=0):
         # both passes of every unit in one persistent launch (a job queue)
         return [("tc128_queue_kernel", full, 5 * d * io, "tensor")]
     if kname == "chunk_tc" and io_dtype == "bf16" and d == 64:
-        return [("gram_tma_kernel", 0, 0, "tensor"), ("prefix_kernel", 0, 0, "alu"),
-                ("gates_tc_kernel", half, 2 * d * io, "tensor"), ("rows_tc_kernel", half, 2 * d * io, "tensor"),
-                ("chain_kernel", 0, 0, "alu"), ("out_tc_kernel", 0, d * io, "tensor")]
+        head = [("gram_tma_kernel", 0, 0, "tensor"), ("prefix_kernel", 0, 0, "alu")]
+        tail = [("chain_kernel", 0, 0, "alu"), ("out_tc_kernel", 0, d * io, "tensor")]
+        if launches == 5:
+            # the gates (a0-a2, reading u and k) and the state pass (a3-a4, reading q and
+            # v) in one persistent launch fed by a job queue (when the passes' last waves
+            # would be part full)
+            return head + [("tc64_queue_kernel", full, 4 * d * io, "tensor")] + tail
+        return head + [("gates_tc_kernel", half, 2 * d * io, "tensor"),
+                       ("rows_tc_kernel", half, 2 * d * io, "tensor")] + tail
     return [(gram, 0, 0, gram_e), ("prefix_kernel", 0, 0, "alu"), ("gates_kernel", half, 2 * d * io, "alu"),
             ("rows_kernel<summary>", 0, 0, "alu"), ("chain_kernel", 0, 0, "alu"),
             ("rows_kernel<output>", half, 3 * d * io, "alu")]
@@ -441,18 +451,19 @@ def main():
         vla.vla_forward(q, k, v, u, x.lambda0, S0=st[0], A0=st[1], n0=st[2], o=o, S_T=S_T, A_T=A_T, n_T=n_T,
                         kernel=resolved, workspace=ws if need else None, stream=stream)
 
-    plan = kernel_plan(kname, d, x.dtype, B * H)
-    nb = len(plan) + 1  # launch boundaries per step
-    bounds = [[torch.cuda.Event(enable_timing=True) for _ in range(nb)] for _ in range(args.steps)]
-    for evs in bounds:
-        for ev in evs:
-            ev.record(stream)  # creates the underlying cudaEvent_t
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     st = vla.vla_device_status(stream)
     if st != vla.VLA_OK:
         raise RuntimeError("device status after warm-up: " + vla.vla_status_str(st))
+    plan = kernel_plan(kname, d, x.dtype, B * H, vla.vla_last_launch_count())
+    nb = len(plan) + 1  # launch boundaries per step
+    bounds = [[torch.cuda.Event(enable_timing=True) for _ in range(nb)] for _ in range(args.steps)]
+    for evs in bounds:
+        for ev in evs:
+            ev.record(stream)  # creates the underlying cudaEvent_t
+    torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(bus_id_of(dev.index)) if rank == 0 else None
     if sampler:

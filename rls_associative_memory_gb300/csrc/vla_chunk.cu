@@ -41,6 +41,11 @@ namespace vla {
 // Whether the driver's tensor-map encoder could be found (vla_gram_tc.cu): the
 // tensor-core passes stage their inputs by tiled tensor copies.
 bool tile_maps_available();
+// The gates and the state pass of the tensor-core path at d = 64 in one
+// persistent launch fed by a job queue (vla_tc64_queue.cu).
+cudaError_t launch_tc64_queue(const ChunkArgs &a, cudaStream_t stream);
+// Wave model of one tensor-core pass of `ctas` CTAs of `len` sub-blocks each.
+static double tc_pass_cost(long long ctas, double len);
 namespace {
 
 constexpr int kTT = 16;  // tokens per staged tile
@@ -1191,6 +1196,49 @@ cudaError_t tc_front(const ChunkArgs &a, cudaStream_t st) {
     return cudaSuccess;
 }
 
+// Both passes over resident inputs: the Grams, their prefix, the gates and the
+// state pass as one queue launch, the chain, the output pass.
+cudaError_t tc_fused(const ChunkArgs &a, cudaStream_t st) {
+    constexpr int D = 64;
+    using R = RowCfg<D>;
+    const long long n_units = a.bh_n > 0 ? a.bh_n : a.p.BH;
+    int n = a.p.launches ? *a.p.launches : 0;
+    if (n == 0) mark_launch(a.p, 0, st);
+    cudaError_t e;
+    if (a.p.A0) {
+        invert_a0_kernel<D><<<(unsigned)n_units, R::NT, 0, st>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        mark_launch(a.p, ++n, st);
+    }
+    if ((e = launch_gram_tma(a, st)) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    prefix_kernel<D><<<(unsigned)(((D * D + D + 255) / 256) * n_units), 256, 0, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    if ((e = launch_tc64_queue(a, st)) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    if ((e = set_smem(chain_kernel<D>, ChainSmem<D>::total)) != cudaSuccess) return e;
+    chain_kernel<D><<<(unsigned)((D / chain_rows<D>()) * n_units), 256, ChainSmem<D>::total, st>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    if ((e = launch_rows_tc(a, 1, st)) != cudaSuccess) return e;
+    mark_launch(a.p, ++n, st);
+    return cudaSuccess;
+}
+
+// Whether the gates and the state pass take less time as one queue launch than
+// as two.  Two launches pay each pass's part-full last wave (tc_pass_cost, a
+// gates job taken as long as a state-pass job).  The queue packs both passes'
+// jobs into (G + R) / 304 job times, but a gates job and a state-pass job on
+// one SM run slower than two of a kind: taken as 8 % (6 % measured with every
+// SM holding one of each).  The long stream's two full waves a pass stay two
+// launches; 32 units of 4096 tokens (1.68 waves a pass) take the queue.
+bool tc_queue_pays(const ChunkArgs &a) {
+    const long long n = a.bh_n > 0 ? a.bh_n : a.p.BH;
+    const long long G = n * a.L.NCA, R = n * a.L.NC;
+    return 1.08 * (double)(G + R) / (2.0 * 152) < tc_pass_cost(G, 1.0) + tc_pass_cost(R, 1.0) - 1e-9;
+}
+
 cudaError_t tc_back(const ChunkArgs &a, cudaStream_t st) {
     constexpr int D = 64;
     const long long n_units = a.bh_n > 0 ? a.bh_n : a.p.BH;
@@ -1235,6 +1283,7 @@ cudaError_t launch_chunk_t(const ChunkArgs &a, cudaStream_t st) {
     }
     if constexpr (D == 64 && sizeof(IO) == 2) {
         if (tc_parts_ok(a.p, a.L)) {
+            if (!a.p.wait_qv && tc_queue_pays(a)) return tc_fused(a, st);
             if ((e = tc_front(a, st)) != cudaSuccess) return e;
             // the front reads u and k only; q and v may still be arriving
             if (a.p.wait_qv && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.p.wait_qv), 0)) != cudaSuccess)
@@ -1486,7 +1535,7 @@ static ChunkLayout layout_for(int BH, int T, int d, int C, int CA, bool tc) {
     L.off_yh = off;
     L.yh = tc ? 1 : 0;
     if (L.yh) off = align256(off + bh * nc * (size_t)(L.C / 64) * 16384);
-    L.off_q = off; off = align256(off + (bh + 1) * 4);
+    L.off_q = off; off = align256(off + (bh * nca + 1) * 4);  // job counter and flags of the queue launches
     L.total = off;
     return L;
 }

@@ -106,7 +106,7 @@ struct ChunkLayout {
                          // tiles) of every 64-token sub-block, written by the tensor-core
                          // state pass for the output pass
     int yh;              // 1 when the off_yh region is reserved
-    size_t off_q;        // [BH + 1] u32: the job queue of the d = 128 single-chunk launch
+    size_t off_q;        // [BH NCA + 1] u32: job counter and flags of the queue launches
     size_t total;
 };
 

@@ -108,3 +108,22 @@ def test_recall_exact_after_the_writes(n_pairs):
     vn = np.linalg.norm(x.values, axis=-1)
     assert np.all(ro <= 2e-2 * vn)  # exact recall up to the bf16 rounding of the keys
     assert np.all(np.abs(rg - ro) <= TOL["bf16"] * vn), float(np.max(np.abs(rg - ro) / vn))
+
+
+@pytest.mark.parametrize("B,H,T,chunk,per,launches", [
+    (1, 16, 2048, 128, 1, 5),  # 256 jobs a pass (0.84 of a wave): one queue launch
+    (1, 3, 6000, 0, 2, 5),     # S-chunks of two A-chunks, ragged tail: a state pass waits on two flags
+    (1, 1, 16384, 0, 4, 5),    # S-chunks of four A-chunks
+    (1, 16, 2432, 128, 1, 6),  # 304 jobs a pass, one full wave each: two launches
+])
+def test_launch_form(B, H, T, chunk, per, launches):
+    """The device entry runs the gates and the state pass as one queue launch
+    where a pass's last wave would be part full, else as two launches (the
+    launch count tells them apart: Grams, prefix, passes, chain, output
+    pass); both forms against the oracle."""
+    x = make_inputs(B, H, T, 64, "bf16", seed=83)
+    C, CA = vla.vla_chunk_lengths(B, H, T, 64, vla.VLA_BF16, TC, chunk)
+    assert C // CA == per and C % CA == 0
+    got = run_gpu(x, TC, chunk=chunk)
+    assert vla.vla_last_launch_count() == launches
+    compare(got, oracle_ref(x), "bf16")
