@@ -46,6 +46,16 @@ bool tile_maps_available();
 cudaError_t launch_tc64_queue(const ChunkArgs &a, cudaStream_t stream);
 // Wave model of one tensor-core pass of `ctas` CTAs of `len` sub-blocks each.
 static double tc_pass_cost(long long ctas, double len);
+// Whether G gates jobs and R state-pass jobs take less time as one queue launch
+// than as two.  Two launches pay each pass's part-full last wave (tc_pass_cost,
+// a gates job taken as long as a state-pass job).  The queue packs both
+// passes' jobs into (G + R) / 304 job times, but a gates job and a state-pass
+// job on one SM run slower than two of a kind: taken as 8 % (6 % measured with
+// every SM holding one of each).  The long stream's two full waves a pass stay
+// two launches; 32 units of 4096 tokens (1.68 waves a pass) take the queue.
+static bool tc_queue_pays_jobs(long long G, long long R) {
+    return 1.08 * (double)(G + R) / (2.0 * 152) < tc_pass_cost(G, 1.0) + tc_pass_cost(R, 1.0) - 1e-9;
+}
 namespace {
 
 constexpr int kTT = 16;  // tokens per staged tile
@@ -1226,17 +1236,10 @@ cudaError_t tc_fused(const ChunkArgs &a, cudaStream_t st) {
     return cudaSuccess;
 }
 
-// Whether the gates and the state pass take less time as one queue launch than
-// as two.  Two launches pay each pass's part-full last wave (tc_pass_cost, a
-// gates job taken as long as a state-pass job).  The queue packs both passes'
-// jobs into (G + R) / 304 job times, but a gates job and a state-pass job on
-// one SM run slower than two of a kind: taken as 8 % (6 % measured with every
-// SM holding one of each).  The long stream's two full waves a pass stay two
-// launches; 32 units of 4096 tokens (1.68 waves a pass) take the queue.
+// The device entry's choice between one queue launch and two (tc_queue_pays_jobs).
 bool tc_queue_pays(const ChunkArgs &a) {
     const long long n = a.bh_n > 0 ? a.bh_n : a.p.BH;
-    const long long G = n * a.L.NCA, R = n * a.L.NC;
-    return 1.08 * (double)(G + R) / (2.0 * 152) < tc_pass_cost(G, 1.0) + tc_pass_cost(R, 1.0) - 1e-9;
+    return tc_queue_pays_jobs(n * a.L.NCA, n * a.L.NC);
 }
 
 cudaError_t tc_back(const ChunkArgs &a, cudaStream_t st) {
@@ -1401,10 +1404,16 @@ static double tc_pass_cost(long long ctas, double len) {
 // S-chunk length of the tensor-core path, a multiple of 64 (the long stream,
 // 16 units of 65536 tokens: 1728, two full waves of 27 sub-blocks, where 512
 // took seven waves of 8 with the last one part full). It minimises, in
-// sub-block times, the state pass over all units plus the same pass over each
-// half of the units (the host entry runs the halves one after the other, to
-// overlap the copies), plus the chain along the chunks, about 0.045 of a
-// sub-block per chunk (measured), counted for both.
+// sub-block times, the passes of vla_forward over all units plus the same pass
+// over each half of the units (the host entry runs the halves one after the
+// other, to overlap the copies), plus the chain along the chunks, about 0.045
+// of a sub-block per chunk (measured), counted for both.  A CTA costs its
+// sub-blocks plus kTcCtaCost for its start and end (the chunk start in, the
+// chunk maps out).  Where vla_forward takes the queue launch (tc_queue_pays)
+// its passes cost their packed jobs plus half a job of ragged end.
+constexpr double kTcCtaCost = 0.6;  // fitted: 0.4 .. 1.0 give the same lengths on the
+                                    // five shapes timed (8 x 16 x 1024 tokens: 0.446 ms at
+                                    // C = 64, 0.295 ms at C = 256)
 int chunk_default_tc(int BH, int T) {
     static thread_local int last_BH = -1, last_T = -1, last_C = 64;
     if (BH == last_BH && T == last_T) return last_C;
@@ -1414,8 +1423,11 @@ int chunk_default_tc(int BH, int T) {
     double best_cost = -1;
     for (int m = 1; m <= maxm; ++m) {
         const long long NC = (T + 64LL * m - 1) / (64LL * m);
-        const double full = tc_pass_cost(BH * NC, m);
-        const double halves = h1 > 0 ? tc_pass_cost(h1 * NC, m) + tc_pass_cost(h2 * NC, m) : full;
+        const double len = m + kTcCtaCost;
+        double full = tc_pass_cost(BH * NC, len);
+        if (tc_queue_pays_jobs(BH * NC, BH * NC))  // per pass: half the packed jobs and of the ragged end
+            full = 1.08 * (double)(BH * NC) * len / (2.0 * 152) + 0.25 * len;
+        const double halves = h1 > 0 ? tc_pass_cost(h1 * NC, len) + tc_pass_cost(h2 * NC, len) : full;
         const double cost = full + halves + 2 * 0.045 * (double)NC;
         if (best_cost < 0 || cost < best_cost - 1e-9) {
             best_cost = cost;

@@ -113,7 +113,7 @@ def test_recall_exact_after_the_writes(n_pairs):
 @pytest.mark.parametrize("B,H,T,chunk,per,launches", [
     (1, 16, 2048, 128, 1, 5),  # 256 jobs a pass (0.84 of a wave): one queue launch
     (1, 3, 6000, 0, 2, 5),     # S-chunks of two A-chunks, ragged tail: a state pass waits on two flags
-    (1, 1, 16384, 0, 4, 5),    # S-chunks of four A-chunks
+    (1, 1, 16384, 0, 7, 5),    # S-chunks of seven A-chunks
     (1, 16, 2432, 128, 1, 6),  # 304 jobs a pass, one full wave each: two launches
 ])
 def test_launch_form(B, H, T, chunk, per, launches):
