@@ -56,15 +56,14 @@ TRAFFIC = {
     # (T=65536; one ncu pass)
     ("chunk_tc", "long", "gates_tc_kernel"): {"bytes": 278.221824e6 + 101.037824e6, "src_sha": "2bd40b3ddad0f1e0"},
     ("chunk_tc", "long", "rows_tc_kernel"): {"bytes": 537.165824e6 + 246.693120e6, "src_sha": "9e62ca08836996eb"},
-    # d = 64 queue launch of both passes, 4x8x4096 (heads32): from one full-set capture of a
-    # launch at full size
-    ("chunk_tc", "heads32", "tc64_queue_kernel"): {"bytes": 78.863104e6 + 17.706752e6, "src_sha": "7f16db9cbca9269b"},
+    # d = 64 queue launch of both passes, 4x8x4096 (heads32): one launch at full size (one ncu pass)
+    ("chunk_tc", "heads32", "tc64_queue_kernel"): {"bytes": 78.998784e6 + 17.412352e6, "src_sha": "9bc481f16332c96c"},
     # decode step, state in place: one launch at full size (one ncu pass)
     ("decode", "decode", "decode_kernel"): {"bytes": 68.697600e6 + 12.946432e6, "src_sha": "377e9a67c43a05a7"},
     # d = 128 queue launch, batched workload: at B=8 (128 units), scaled x4 to B=32 (the bytes
     # of a unit's two passes do not depend on how many units a launch holds)
-    ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.700800e6 + 127.022336e6),
-                                                    "src_sha": "8e2fc763b85a164a"},
+    ("chunk_tc", "batched", "tc128_queue_kernel"): {"bytes": 4 * (402.768640e6 + 127.273472e6),
+                                                     "src_sha": "d9e92a2f261757b3"},
 }
 
 

@@ -199,10 +199,12 @@ int vla_device_status(void *stream);
 
 /* Test hook for the failure path: mode 1 makes the next vla_forward launches
  * of the sequential kernel wait for an input tile that is never requested,
- * so that the bounded wait (limit `wait_limit_ns`, clamped to [1e5, 1e10])
- * expires and sets the device error word; mode 0 restores normal operation
- * and the default one-second limit.  Host state only; returns VLA_OK or
- * VLA_ERR_ARG. */
+ * and the gates jobs of the tensor-core queue launches (d_h = 64 and 128)
+ * leave their flags unset, so that the bounded waits (limit `wait_limit_ns`,
+ * clamped to [1e5, 1e10]) expire and set the device error word; the waiting
+ * state passes are then skipped and the launch ends.  Mode 0 restores normal
+ * operation and the default one-second limit.  Host state only; returns
+ * VLA_OK or VLA_ERR_ARG. */
 int vla_debug_inject(int mode, long long wait_limit_ns);
 
 /* Measurement hook.  With n > 0, every later vla_forward (or

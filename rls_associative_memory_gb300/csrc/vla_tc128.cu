@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(kT128Threads, 1) tc128_queue_kernel(ChunkArgs 
             g128::gates_tc128_body(a, a.bh_lo + job, smem_raw, &tm_u, &tm_k);
             __threadfence();  // this thread's stores of the gates, before the flag
             __syncthreads();
-            if (threadIdx.x == 0) st_release_gpu(ctl + 1 + job, 1u);
+            // (test hook: with inject set the flag stays unset, so the state pass's
+            // bounded wait expires and sets the error word)
+            if (threadIdx.x == 0 && !a.p.inject) st_release_gpu(ctl + 1 + job, 1u);
         } else {
             if (threadIdx.x == 0) *s_ok = wait_flag(ctl + 1 + (job - n), a.p.wait_limit_ns, a.p.err) ? 1 : 0;
             __syncthreads();

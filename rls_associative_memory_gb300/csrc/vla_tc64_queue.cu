@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(kQThreads, 2) tc64_queue_kernel(ChunkArgs a, u
             g64::gates_tc_body(a, c, a.bh_lo + u, smem_raw, &tm_u, &tm_k, tbase);
             __threadfence();  // this thread's stores of the gates (and A_T), before the flag
             __syncthreads();
-            if (threadIdx.x == 0) st_release_gpu(ctl + 1 + job, 1u);
+            // (test hook: with inject set the flag stays unset, so the state pass's
+            // bounded wait expires and sets the error word)
+            if (threadIdx.x == 0 && !a.p.inject) st_release_gpu(ctl + 1 + job, 1u);
         } else {
             const int u = (job - G) / NC, c = (job - G) % NC;
             if (threadIdx.x == 0) {

@@ -118,3 +118,21 @@ def test_queue_launch_many_units(T, init):
             kw = dict(S0=S0[b:b + 1, h:h + 1], A0=A0[b:b + 1, h:h + 1], n0=n0[b:b + 1, h:h + 1])
         ref = oracle_ref(sub, **kw)
         compare({k: v[b:b + 1, h:h + 1] for k, v in got.items()}, ref, "bf16")
+
+
+def test_bounded_wait_expiry_in_queue_launch():
+    """Test hook: the gates jobs of the queue launch leave their flags unset,
+    so every state pass's bounded wait expires (1 ms), sets the device error
+    word and skips its job; the launch still ends, and the next call is
+    normal."""
+    x = make_inputs(1, 4, 200, 128, "bf16", seed=521, lambda0=0.5)
+    q, k, v, u = to_device(x)
+    assert vla.vla_debug_inject(1, 1_000_000) == vla.VLA_OK
+    try:
+        vla.vla_forward(q, k, v, u, x.lambda0, kernel=TC, chunk=256)
+        assert vla.vla_last_launch_count() == 1
+        assert vla.vla_device_status() == vla.VLA_ERR_TIMEOUT
+    finally:
+        vla.vla_debug_inject(0)
+    assert vla.vla_device_status() == vla.VLA_OK
+    compare(_run(x), oracle_ref(x), "bf16")

@@ -21,7 +21,7 @@ import pytest
 
 import rls_associative_memory_gb300 as vla
 from synthetic import make_inputs, make_recall_stream
-from vla_testutil import TOL, compare, oracle_ref, run_gpu
+from vla_testutil import TOL, compare, oracle_ref, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -127,3 +127,21 @@ def test_launch_form(B, H, T, chunk, per, launches):
     got = run_gpu(x, TC, chunk=chunk)
     assert vla.vla_last_launch_count() == launches
     compare(got, oracle_ref(x), "bf16")
+
+
+def test_bounded_wait_expiry_in_queue_launch():
+    """Test hook: the gates jobs of the d = 64 queue launch leave their flags
+    unset, so every state pass's bounded wait expires (1 ms), sets the device
+    error word and skips its job; the launch still ends, and the next call is
+    normal."""
+    x = make_inputs(1, 16, 2048, 64, "bf16", seed=522)
+    q, k, v, u = to_device(x)
+    assert vla.vla_debug_inject(1, 1_000_000) == vla.VLA_OK
+    try:
+        vla.vla_forward(q, k, v, u, x.lambda0, kernel=TC, chunk=128)
+        assert vla.vla_last_launch_count() == 5  # the queue form
+        assert vla.vla_device_status() == vla.VLA_ERR_TIMEOUT
+    finally:
+        vla.vla_debug_inject(0)
+    assert vla.vla_device_status() == vla.VLA_OK
+    compare(run_gpu(x, TC, chunk=128), oracle_ref(x), "bf16")
