@@ -538,11 +538,15 @@ def main():
             e2e_step()
             ee[i].record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(es, ee)])), dist, dev)
+        e2e_steps = [s.elapsed_time(e) for s, e in zip(es, ee)]
+        e2e_ms = max_over_ranks(float(np.mean(e2e_steps)), dist, dev)
         h2d = 4 * units * d * io_bytes
         d2h = units * d * io_bytes + (0 if in_place else B * H * (2 * d * d + d) * 4)
         e2e = {"value": job_value(world, units, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               # this rank's spread over the timed steps (the value is the mean)
+               "ms_min": float(np.min(e2e_steps)), "ms_median": float(np.median(e2e_steps)),
+               "ms_max": float(np.max(e2e_steps))}
 
     # ---- roofline of the dominant kernel (and of the whole step) ----
     flops, byts = algorithmic_work(B, H, T, d, io_bytes)

@@ -145,3 +145,15 @@ def test_bounded_wait_expiry_in_queue_launch():
         vla.vla_debug_inject(0)
     assert vla.vla_device_status() == vla.VLA_OK
     compare(run_gpu(x, TC, chunk=128), oracle_ref(x), "bf16")
+
+
+def test_launch_form_queue_from_a_given_state():
+    """The queue form from a given initial state: A0 is inverted first (one
+    more launch); the first A-chunk starts from A0, later ones from the
+    inverse of the prefix."""
+    pre = make_inputs(1, 16, 300, 64, "bf16", seed=84)
+    st = oracle_ref(pre)
+    x = make_inputs(1, 16, 2048, 64, "bf16", seed=85)
+    got = run_gpu(x, TC, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"], chunk=128)
+    assert vla.vla_last_launch_count() == 6
+    compare(got, oracle_ref(x, S0=st["S_T"], A0=st["A_T"], n0=st["n_T"]), "bf16")
