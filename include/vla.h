@@ -218,8 +218,10 @@ int vla_debug_inject(int mode, long long wait_limit_ns);
 int vla_set_launch_events(void *const *events, int n);
 
 /* Number of kernels the last successful vla_forward call on this host
- * thread launched (1 for the sequential and decode paths, 6 or 7 for the
- * chunked one). */
+ * thread launched: 1 for the sequential and decode paths and for the
+ * tensor-core path at d_h = 128; 6 for the chunked one, or 5 on the
+ * tensor-core path at d_h = 64 when its gates and state pass run as one queue
+ * launch; one more on the chunked paths when A0 is given. */
 int vla_last_launch_count(void);
 
 /*
