@@ -221,7 +221,8 @@ int vla_set_launch_events(void *const *events, int n);
  * thread launched: 1 for the sequential and decode paths and for the
  * tensor-core path at d_h = 128; 6 for the chunked one, or 5 on the
  * tensor-core path at d_h = 64 when its gates and state pass run as one queue
- * launch; one more on the chunked paths when A0 is given. */
+ * launch; one more for the inverse of A0, when given, on the chunked path and
+ * the tensor-core path at d_h = 64. */
 int vla_last_launch_count(void);
 
 /*
